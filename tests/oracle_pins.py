@@ -1,0 +1,416 @@
+"""Pins for the CPU oracle: checks against what the pages and mathematics fix.
+
+Every pin takes an ``oracle.Oracle`` handle and raises ``AssertionError`` when
+the oracle disagrees, so the same pins run against the real oracle
+(``test_oracle_pins.py``) and against deliberately broken builds of it
+(``test_oracle_mutants.py``).  None of them re-types the oracle's formulas:
+each compares it with something else --
+
+* values the pages print (``tests/golden/*.json``, each with its citation),
+* a library attention routine (``torch.nn.functional.scaled_dot_product_attention``
+  in fp64 on the un-paged tensors),
+* pure-Python brute force on tiny inputs (naive softmax, ``math.fsum``),
+* closed forms (one key, zero query, constant values),
+* invariants the pages state (output independent of physical placement; shared
+  prefix blocks equal private copies; C=1 prefill equals decode).
+
+Run as ``python -m tests.oracle_pins --library PATH`` to print a JSON list of
+the pins that fail for the oracle built at PATH (exit status 1 if any fail).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+import sys
+from typing import Callable, Dict, List
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+GOLDEN = os.path.join(HERE, "golden")
+ROOT = os.path.dirname(HERE)
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import oracle as oracle_pkg  # noqa: E402
+
+BF16 = torch.bfloat16
+
+
+def golden(name: str) -> dict:
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def from_bits(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(BF16)
+
+
+def randn(shape, gen) -> torch.Tensor:
+    return torch.randn(shape, generator=gen, dtype=torch.float32).to(BF16)
+
+
+def place(K: torch.Tensor, V: torch.Tensor, lens, tables, num_blocks: int, block_size: int,
+          gen) -> torch.Tensor:
+    """Test-side placement of contiguous K/V ([B][Lmax][Hkv][d]) into a fresh
+    pool [NB][2][Hkv][b][d] (slots not covered stay random junk)."""
+    B, _, H, d = K.shape
+    pool = randn((num_blocks, 2, H, block_size, d), gen)
+    for s in range(B):
+        for t in range(int(lens[s])):
+            blk, off = int(tables[s][t // block_size]), t % block_size
+            pool[blk, 0, :, off, :] = K[s, t]
+            pool[blk, 1, :, off, :] = V[s, t]
+    return pool
+
+
+def random_tables(rng, lens, num_blocks: int, block_size: int) -> np.ndarray:
+    counts = [-(-int(L) // block_size) for L in lens]
+    tables = np.full((len(lens), max(1, max(counts))), -1, dtype=np.int32)
+    perm = rng.permutation(num_blocks)
+    c = 0
+    for s, n in enumerate(counts):
+        tables[s, :n] = perm[c:c + n]
+        c += n
+    return tables
+
+
+def sdpa_rows(q_rows: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float,
+              mask=None) -> torch.Tensor:
+    """Library attention in fp64.  q_rows [M][Hq][d], K/V [L][Hkv][d];
+    GQA by repeating each kv-head over its consecutive group of q-heads."""
+    Hq, Hkv = q_rows.shape[1], K.shape[1]
+    G = Hq // Hkv
+    qq = q_rows.double().permute(1, 0, 2).unsqueeze(0)                      # [1][Hq][M][d]
+    kk = K.double().permute(1, 0, 2).repeat_interleave(G, dim=0).unsqueeze(0)  # [1][Hq][L][d]
+    vv = V.double().permute(1, 0, 2).repeat_interleave(G, dim=0).unsqueeze(0)
+    o = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=scale)
+    return o.squeeze(0).permute(1, 0, 2)                                      # [M][Hq][d]
+
+
+# ---------------------------------------------------------------------------
+# capacity arithmetic and address map
+# ---------------------------------------------------------------------------
+
+def pin_block_layout_page_example(orc):
+    g = golden("block_layout_page_example.json")
+    b = g["block_size"]
+    for tokens, expect in g["cases"]:
+        assert orc.block_layout(tokens, b) == tuple(expect), (tokens, expect)
+    assert orc.block_layout(g["printed"]["tokens"], b) == tuple(g["printed"]["layout"])
+    tb = g["tail_bound"]
+    for n in range(tb["tokens_from"], tb["tokens_to_exclusive"]):
+        blocks, unused = orc.block_layout(n, b)
+        assert blocks * b >= n and tb["unused_min"] <= unused < tb["unused_max_exclusive"], n
+    for tokens, bs in g["invalid"]:
+        try:
+            orc.block_layout(tokens, bs)
+        except ValueError:
+            continue
+        raise AssertionError(f"block_layout({tokens}, {bs}) accepted an invalid size")
+
+
+def pin_block_layout_worked_example(orc):
+    g = golden("worked_example_blocks.json")
+    blocks, unused = orc.block_layout(g["tokens"], g["block_size"])
+    assert blocks == g["blocks"], blocks
+    for n in range(1, 2000):
+        _, unused = orc.block_layout(n, g["block_size"])
+        assert 0 <= unused <= g["max_idle_slots"], n
+    # exactly-full sequences leave nothing idle, one more token opens a block
+    assert orc.block_layout(32, 16) == (2, 0) and orc.block_layout(33, 16) == (3, 15)
+
+
+def pin_address_page_example(orc):
+    g = golden("address_page_example.json")
+    phys, off = orc.address(g["table"], g["position"], g["block_size"])
+    assert (phys, off) == (g["physical_block"], g["offset"]), (phys, off)
+    # the first slot of each logical block lands at offset 0 of the next table entry
+    for logical, blk in enumerate(g["table"]):
+        assert orc.address(g["table"], logical * g["block_size"], g["block_size"]) == (blk, 0)
+
+
+def pin_slot_writer_page_example(orc):
+    """Write the page's 10 tokens through the slot writer with table [5,1,7] and
+    b=4: token 9 must be found at physical block 7, offset 1, and the two tail
+    slots of block 7 must stay untouched."""
+    g = golden("address_page_example.json")
+    b, table, T = g["block_size"], g["table"], g["tokens"]
+    H, d, NB = 2, 8, 8
+    gen = torch.Generator().manual_seed(11)
+    geom = oracle_pkg.dense_geom(NB, H, b, d)
+    pool = bits(randn((NB, 2, H, b, d), gen)).copy()
+    before = pool.copy()
+    k, v = bits(randn((T, H, d), gen)), bits(randn((T, H, d), gen))
+    slots = orc.slot_mapping([table], np.zeros(T, np.int32), np.arange(T), b)
+    orc.reshape_and_cache(pool, geom, k, v, slots)
+    assert np.array_equal(pool[g["physical_block"], 0, :, g["offset"]], k[g["position"]])
+    assert np.array_equal(pool[g["physical_block"], 1, :, g["offset"]], v[g["position"]])
+    # tokens 0..3 fill block 5, 4..7 fill block 1, 8..9 the head of block 7
+    for t in range(T):
+        blk, off = table[t // b], t % b
+        assert np.array_equal(pool[blk, 0, :, off], k[t]) and np.array_equal(pool[blk, 1, :, off], v[t])
+    assert np.array_equal(pool[7, :, :, 2:], before[7, :, :, 2:])
+    untouched = [i for i in range(NB) if i not in table]
+    assert np.array_equal(pool[untouched], before[untouched])
+    # a negative slot is padding: nothing is written
+    pool2 = before.copy()
+    orc.reshape_and_cache(pool2, geom, k[:3], v[:3], [-1, -1, -1])
+    assert np.array_equal(pool2, before)
+
+
+# ---------------------------------------------------------------------------
+# attention
+# ---------------------------------------------------------------------------
+
+DECODE_CASES = [
+    # B, Hq, Hkv, d, b, lens, NB, seed
+    (4, 4, 2, 16, 4, [1, 7, 13, 4], 24, 1),
+    (2, 8, 1, 32, 16, [33, 5], 12, 2),
+    (3, 8, 8, 8, 2, [9, 1, 6], 20, 3),
+    (2, 6, 2, 64, 16, [70, 16], 10, 4),
+]
+
+
+def _decode_case(case):
+    B, Hq, Hkv, d, b, lens, NB, seed = case
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator().manual_seed(seed)
+    Lmax = max(lens)
+    K, V = randn((B, Lmax, Hkv, d), gen), randn((B, Lmax, Hkv, d), gen)
+    q = randn((B, Hq, d), gen)
+    tables = random_tables(rng, lens, NB, b)
+    pool = place(K, V, lens, tables, NB, b, gen)
+    geom = oracle_pkg.dense_geom(NB, Hkv, b, d)
+    return q, K, V, tables, pool, geom, np.asarray(lens, np.int32), 1.0 / math.sqrt(d)
+
+
+def pin_decode_vs_sdpa(orc):
+    for case in DECODE_CASES:
+        q, K, V, tables, pool, geom, lens, scale = _decode_case(case)
+        got = orc.paged_decode(bits(q), bits(pool), geom, tables, lens, q.shape[1], scale)
+        for s in range(len(lens)):
+            ref = sdpa_rows(q[s:s + 1], K[s, :lens[s]], V[s, :lens[s]], scale)[0].numpy()
+            err = np.abs(got[s] - ref).max()
+            assert err < 1e-10, (case, s, err)
+        rows = np.asarray([[s, h] for s in range(len(lens)) for h in range(q.shape[1])][::3])
+        sub = orc.paged_decode(bits(q), bits(pool), geom, tables, lens, q.shape[1], scale, rows=rows)
+        assert np.array_equal(sub, got[rows[:, 0], rows[:, 1]])
+
+
+def pin_decode_brute_force(orc):
+    """Naive softmax in pure Python (no max subtraction, math.fsum) on tiny inputs."""
+    B, Hq, Hkv, d, b, lens, NB = 2, 4, 2, 4, 2, [3, 5], 8
+    rng = np.random.default_rng(5)
+    gen = torch.Generator().manual_seed(5)
+    K, V = randn((B, 5, Hkv, d), gen), randn((B, 5, Hkv, d), gen)
+    q = randn((B, Hq, d), gen)
+    tables = random_tables(rng, lens, NB, b)
+    pool = place(K, V, lens, tables, NB, b, gen)
+    scale = 0.37
+    got = orc.paged_decode(bits(q), bits(pool), oracle_pkg.dense_geom(NB, Hkv, b, d), tables,
+                           np.asarray(lens, np.int32), Hq, scale)
+    Kf, Vf, qf = K.double().tolist(), V.double().tolist(), q.double().tolist()
+    for s in range(B):
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            w = [math.exp(scale * math.fsum(qf[s][h][i] * Kf[s][t][g][i] for i in range(d)))
+                 for t in range(lens[s])]
+            z = math.fsum(w)
+            for i in range(d):
+                ref = math.fsum(w[t] * Vf[s][t][g][i] for t in range(lens[s])) / z
+                assert abs(got[s, h, i] - ref) <= 1e-12 * max(1.0, abs(ref)), (s, h, i)
+
+
+def pin_decode_closed_forms(orc):
+    B, Hq, Hkv, d, b, NB = 3, 4, 2, 16, 4, 16
+    rng = np.random.default_rng(6)
+    gen = torch.Generator().manual_seed(6)
+    geom = oracle_pkg.dense_geom(NB, Hkv, b, d)
+    # one key: the output is that key's value row, exactly
+    lens = [1, 1, 1]
+    K, V, q = randn((B, 1, Hkv, d), gen), randn((B, 1, Hkv, d), gen), randn((B, Hq, d), gen)
+    tables = random_tables(rng, lens, NB, b)
+    pool = place(K, V, lens, tables, NB, b, gen)
+    out = orc.paged_decode(bits(q), bits(pool), geom, tables, np.asarray(lens, np.int32), Hq, 0.25)
+    for s in range(B):
+        for h in range(Hq):
+            assert np.array_equal(out[s, h], V[s, 0, h // 2].double().numpy()), (s, h)
+    # zero query: every key weighs the same, the output is the mean of V
+    lens = [5, 9, 12]
+    K, V = randn((B, 12, Hkv, d), gen), randn((B, 12, Hkv, d), gen)
+    q = torch.zeros((B, Hq, d), dtype=BF16)
+    tables = random_tables(rng, lens, NB, b)
+    pool = place(K, V, lens, tables, NB, b, gen)
+    out = orc.paged_decode(bits(q), bits(pool), geom, tables, np.asarray(lens, np.int32), Hq, 0.25)
+    for s in range(B):
+        mean = V[s, :lens[s]].double().mean(dim=0).numpy()
+        for h in range(Hq):
+            assert np.abs(out[s, h] - mean[h // 2]).max() < 1e-13, (s, h)
+    # all value rows equal c: the output is c whatever the scores
+    q = randn((B, Hq, d), gen)
+    c = randn((Hkv, d), gen)
+    V = c.unsqueeze(0).unsqueeze(0).expand(B, 12, Hkv, d).contiguous()
+    pool = place(K, V, lens, tables, NB, b, gen)
+    out = orc.paged_decode(bits(q), bits(pool), geom, tables, np.asarray(lens, np.int32), Hq, 0.25)
+    for s in range(B):
+        for h in range(Hq):
+            assert np.abs(out[s, h] - c[h // 2].double().numpy()).max() < 1e-13, (s, h)
+
+
+def pin_decode_placement_invariance(orc):
+    """Same logical K/V under two random physical placements: identical output."""
+    q, K, V, tables, pool, geom, lens, scale = _decode_case(DECODE_CASES[0])
+    rng = np.random.default_rng(99)
+    gen = torch.Generator().manual_seed(99)
+    tables2 = random_tables(rng, lens, geom.num_blocks, geom.block_size)
+    pool2 = place(K, V, lens, tables2, geom.num_blocks, geom.block_size, gen)
+    a = orc.paged_decode(bits(q), bits(pool), geom, tables, lens, q.shape[1], scale)
+    b = orc.paged_decode(bits(q), bits(pool2), geom, tables2, lens, q.shape[1], scale)
+    assert not np.array_equal(tables, tables2)
+    assert np.array_equal(a, b)
+
+
+def pin_decode_shared_prefix(orc):
+    """Tables sharing physical prefix blocks give the same result as tables
+    holding private copies of the same prefix."""
+    Hq, Hkv, d, b, NB = 4, 2, 8, 4, 40
+    gen = torch.Generator().manual_seed(7)
+    prefix_tokens, lens = 8, [11, 14, 8]
+    B = len(lens)
+    Kp, Vp = randn((prefix_tokens, Hkv, d), gen), randn((prefix_tokens, Hkv, d), gen)
+    K, V = randn((B, 14, Hkv, d), gen), randn((B, 14, Hkv, d), gen)
+    K[:, :prefix_tokens], V[:, :prefix_tokens] = Kp, Vp
+    q = randn((B, Hq, d), gen)
+    # private: every sequence has its own copy of the prefix blocks
+    priv = np.asarray([[0, 1, 2, 3], [4, 5, 6, 7], [8, 9, -1, -1]], np.int32)
+    pool_priv = place(K, V, lens, priv, NB, b, gen)
+    # shared: one copy of the two prefix blocks, every table starts with them
+    shared = np.asarray([[20, 21, 30, -1], [20, 21, 31, 32], [20, 21, -1, -1]], np.int32)
+    pool_sh = place(K, V, lens, shared, NB, b, gen)
+    geom = oracle_pkg.dense_geom(NB, Hkv, b, d)
+    a = orc.paged_decode(bits(q), bits(pool_priv), geom, priv, np.asarray(lens, np.int32), Hq, 0.3)
+    c = orc.paged_decode(bits(q), bits(pool_sh), geom, shared, np.asarray(lens, np.int32), Hq, 0.3)
+    assert np.array_equal(a, c)
+
+
+def pin_decode_layered_pool(orc):
+    """The pages' pool shape [NB][2][layers][Hkv][b][d]: a layer's view through
+    strides equals a dense pool holding only that layer."""
+    B, Hq, Hkv, d, b, NB, layers = 2, 4, 2, 8, 4, 12, 3
+    rng = np.random.default_rng(8)
+    gen = torch.Generator().manual_seed(8)
+    lens = np.asarray([7, 10], np.int32)
+    tables = random_tables(rng, lens, NB, b)
+    pool3 = bits(randn((NB, 2, layers, Hkv, b, d), gen))
+    q = randn((B, Hq, d), gen)
+    for layer in range(layers):
+        dense = np.ascontiguousarray(pool3[:, :, layer])
+        a = orc.paged_decode(bits(q), dense, oracle_pkg.dense_geom(NB, Hkv, b, d), tables, lens, Hq, 0.3)
+        view = pool3.reshape(-1)[layer * Hkv * b * d:]
+        geom = oracle_pkg.dense_geom(NB, Hkv, b, d, num_layers=layers)
+        c = orc.paged_decode(bits(q), view, geom, tables, lens, Hq, 0.3)
+        assert np.array_equal(a, c), layer
+
+
+def pin_prefill_vs_sdpa(orc):
+    """Chunk queries at positions ctx..ctx+C-1 against causal, paged keys."""
+    Hq, Hkv, d, b, NB, C = 4, 2, 16, 4, 24, 5
+    ctx = [0, 7, 3]
+    B = len(ctx)
+    rng = np.random.default_rng(9)
+    gen = torch.Generator().manual_seed(9)
+    total = [c + C for c in ctx]
+    K, V = randn((B, max(total), Hkv, d), gen), randn((B, max(total), Hkv, d), gen)
+    q = randn((B, C, Hq, d), gen)
+    tables = random_tables(rng, total, NB, b)
+    pool = place(K, V, total, tables, NB, b, gen)
+    geom = oracle_pkg.dense_geom(NB, Hkv, b, d)
+    scale = 1.0 / math.sqrt(d)
+    got = orc.prefill(bits(q), bits(pool), geom, tables, np.asarray(ctx, np.int32), Hq, scale)
+    for s in range(B):
+        L = total[s]
+        key_pos = torch.arange(L)
+        mask = key_pos[None, :] <= (ctx[s] + torch.arange(C))[:, None]        # [C][L]
+        ref = sdpa_rows(q[s], K[s, :L], V[s, :L], scale, mask=mask.unsqueeze(0).unsqueeze(0))
+        err = np.abs(got[s] - ref.numpy()).max()
+        assert err < 1e-10, (s, err)
+    rows = np.asarray([[s, j, h] for s in range(B) for j in range(C) for h in range(Hq)][::5])
+    sub = orc.prefill(bits(q), bits(pool), geom, tables, np.asarray(ctx, np.int32), Hq, scale, rows=rows)
+    assert np.array_equal(sub, got[rows[:, 0], rows[:, 1], rows[:, 2]])
+
+
+def pin_prefill_one_query_is_decode(orc):
+    """A chunk of one query at position ctx is a decode step over ctx+1 keys."""
+    q, K, V, tables, pool, geom, lens, scale = _decode_case(DECODE_CASES[3])
+    ctx = lens - 1
+    pre = orc.prefill(bits(q.unsqueeze(1)), bits(pool), geom, tables, ctx, q.shape[1], scale)
+    dec = orc.paged_decode(bits(q), bits(pool), geom, tables, lens, q.shape[1], scale)
+    assert np.array_equal(pre[:, 0], dec)
+
+
+# ---------------------------------------------------------------------------
+# copy-on-write
+# ---------------------------------------------------------------------------
+
+def pin_copy_blocks(orc):
+    """After a fork copy, each dst block holds its src block's K and V; reading
+    a sequence through dst gives what reading it through src gave."""
+    for layers in (1, 2):
+        NB, Hkv, b, d = 10, 2, 4, 8
+        gen = torch.Generator().manual_seed(10 + layers)
+        pool = bits(randn((NB, 2, layers, Hkv, b, d), gen)).copy()
+        before = pool.copy()
+        pairs = np.asarray([[3, 5], [0, 6], [9, 2]], np.int32)
+        geom = oracle_pkg.dense_geom(NB, Hkv, b, d, num_layers=layers)
+        flat = pool.reshape(-1)
+        orc.copy_blocks(flat[(layers - 1) * Hkv * b * d:], geom, pairs)
+        for src, dst in pairs:
+            assert np.array_equal(pool[dst, :, layers - 1], before[src, :, layers - 1]), (src, dst)
+            if layers > 1:
+                assert np.array_equal(pool[dst, :, 0], before[dst, :, 0])
+        others = [i for i in range(NB) if i not in pairs[:, 1]]
+        assert np.array_equal(pool[others], before[others])
+    q = randn((1, 4, d), gen)
+    lens = np.asarray([4 * b], np.int32)
+    pool1 = bits(randn((NB, 2, Hkv, b, d), gen)).copy()
+    g1 = oracle_pkg.dense_geom(NB, Hkv, b, d)
+    t_src = np.asarray([[3, 0, 9, 1]], np.int32)
+    a = orc.paged_decode(bits(q), pool1, g1, t_src, lens, 4, 0.3)
+    orc.copy_blocks(pool1, g1, [[3, 5], [0, 6], [9, 2], [1, 4]])
+    c = orc.paged_decode(bits(q), pool1, g1, np.asarray([[5, 6, 2, 4]], np.int32), lens, 4, 0.3)
+    assert np.array_equal(a, c)
+
+
+PINS: Dict[str, Callable] = {name: fn for name, fn in globals().items() if name.startswith("pin_")}
+
+
+def failing_pins(orc) -> List[str]:
+    bad = []
+    for name, fn in PINS.items():
+        try:
+            fn(orc)
+        except Exception:  # noqa: BLE001 -- any exception means the pin did not hold
+            bad.append(name)
+    return bad
+
+
+def main(argv=None) -> int:
+    import argparse
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--library", default=oracle_pkg.LIBRARY)
+    args = ap.parse_args(argv)
+    bad = failing_pins(oracle_pkg.Oracle(args.library))
+    print(json.dumps(bad))
+    return 1 if bad else 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
