@@ -1,0 +1,415 @@
+"""Benchmark of one paged decode step on GB300.
+
+A step is the whole decode hot path for one batch: the slot writer stores
+each sequence's newest token (pa_reshape_and_cache), then paged GQA decode
+attention (pa_decode: split-context partition kernel plus, when the context
+is split, the partition reduce) attends every cached token.  The default
+workload is the Llama-3.1-70B-shaped single layer: 64 sequences of 600-850
+tokens, 64 query / 8 KV heads, head_dim 128, bf16, 16-token blocks placed at
+random in a 16,384-block pool.
+
+Prints one JSON line.  ``value`` is tokens/s (decoded tokens, i.e. sequences
+per step, over device time with inputs resident in HBM and L2 flushed between
+steps); ``e2e`` is the same metric through the C ABI from pinned host buffers
+(per-step inputs copied in and the output copied back inside the timed
+region; the KV pool is device-resident state).  ``roofline`` reports the
+decode call (partition kernel + reduce) against the measured HBM copy
+bandwidth.  ``cpu_baseline`` times the CPU oracle on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 launch one process per GPU with torch.distributed.run; every rank
+decodes its own batch (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import pa_workloads as wl  # noqa: E402
+
+METRIC = "paged decode attention tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20   # twice the 129 MB L2
+
+
+def log(msg: str) -> None:
+    print(msg, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_bytes(w: wl.Workload) -> int:
+    """Algorithmic bytes of one decode call: every attended K and V row once,
+    q and out once, the table entries used and the lengths."""
+    L = w.seq_lens.astype(np.int64)
+    kv = int(L.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    qo = 2 * w.batch * w.num_q_heads * w.head_dim * 2
+    tables = 4 * int((-(-L // w.block_size)).sum())
+    return kv + qo + tables + 4 * w.batch
+
+
+def traffic_record():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_sha256") != kernel_source_sha():
+        return None
+    return rec
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for name in ("pa_decode_kernel.cuh", "pa_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_167_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class DecodeStep:
+    """Device-resident inputs of one decode step and the calls that run it."""
+
+    def __init__(self, pa, w: wl.Workload, dev: torch.device, tensors):
+        self.pa, self.w, self.dev = pa, w, dev
+        self.pool = tensors["pool"].to(dev)
+        self.q = tensors["q"].to(dev)
+        self.new_k = tensors["new_k"].to(dev)
+        self.new_v = tensors["new_v"].to(dev)
+        self.tables = torch.as_tensor(w.tables, device=dev)
+        self.seq_lens = torch.as_tensor(w.seq_lens, device=dev)
+        self.slots_host = pa.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size, w.num_blocks)
+        self.slots = torch.as_tensor(self.slots_host, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.part = pa.decode_partition_tokens(self.pool, w.batch, w.num_q_heads, w.max_seq_len, w.partition_tokens)
+        nbytes = pa.decode_workspace_size(self.pool, w.batch, w.num_q_heads, w.max_seq_len, self.part)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
+        self.num_parts = -(-w.max_seq_len // self.part)
+        self.launches_per_step = 2 + (1 if self.num_parts > 1 else 0)
+
+    def write(self):
+        self.pa.reshape_and_cache(self.pool, self.new_k, self.new_v, self.slots)
+
+    def decode(self):
+        w = self.w
+        self.pa.decode(self.out, self.q, self.pool, self.tables, self.seq_lens, w.max_seq_len, w.scale,
+                       self.part, self.ws)
+
+
+def run_ours(args, world, rank, local):
+    import paged_kv_cache_167_gb300 as pa
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = wl.CONFIGS[args.config](seed=wl.SEED_BASE + 1 + 1000 * rank) if args.config == "llama70b_decode" \
+        else wl.CONFIGS[args.config]()
+    tensors = wl.make_tensors(w, "cpu")
+    step = DecodeStep(pa, w, dev, tensors)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step.write()
+        step.decode()
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0, "device error during warm-up"
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step.write()
+            ev[i][1].record(stream)
+            step.decode()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    total_ms = sum(step_ms)
+    assert pa.get_device_error() == 0, "device error during the timed steps"
+
+    # ---- end to end through the C ABI from pinned host buffers
+    host_q = tensors["q"].pin_memory()
+    host_k = tensors["new_k"].pin_memory()
+    host_v = tensors["new_v"].pin_memory()
+    host_tables = torch.as_tensor(w.tables).pin_memory()
+    host_lens = torch.as_tensor(w.seq_lens).pin_memory()
+    host_slots = torch.empty(len(step.slots_host), dtype=torch.int64).pin_memory()
+    host_out = torch.empty_like(tensors["q"]).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (host_q, host_k, host_v, host_tables, host_lens, host_slots))
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        host_slots.numpy()[:] = pa.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size,
+                                                w.num_blocks)
+        step.q.copy_(host_q, non_blocking=True)
+        step.new_k.copy_(host_k, non_blocking=True)
+        step.new_v.copy_(host_v, non_blocking=True)
+        step.tables.copy_(host_tables, non_blocking=True)
+        step.seq_lens.copy_(host_lens, non_blocking=True)
+        step.slots.copy_(host_slots, non_blocking=True)
+        step.write()
+        step.decode()
+        host_out.copy_(step.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    e2e_s = 0.0
+    for _ in range(K):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        e2e_s += time.perf_counter() - t0
+    barrier()
+
+    elapsed = torch.tensor([total_ms, e2e_s * 1e3, float(np.mean(decode_ms))], dtype=torch.float64, device=dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms, decode_avg_ms = elapsed.tolist()
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    tokens = world * w.batch * K
+    value = tokens / (total_ms / 1e3)
+    peak, peak_kind = measured_peaks()
+    alg = decode_bytes(w)
+    achieved = alg / (decode_avg_ms / 1e3) / 1e9
+    traffic = traffic_record()
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded bf16 N(0,1) K/V/q, random physical block placement",
+        "config": {"workload": w.name, "global_batch": world * w.batch, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                   "seq_len_min": int(w.seq_lens.min()), "seq_len_max": int(w.seq_lens.max()),
+                   "seq_len_mean": float(w.seq_lens.mean()), "pool_blocks": w.num_blocks,
+                   "partition_tokens": step.part, "partitions": step.num_parts,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "flushed between steps (256 MiB write)"},
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (partition kernel + reduce)",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
+                     "algorithmic_bytes": alg, "decode_ms": round(decode_avg_ms, 5)},
+        "kv_read_gbs": round(achieved, 1),
+        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches_per_step * K,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, tensors, budget_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_pass(orc, w, tensors_bits, seqs):
+    """The oracle's decode step for sequences `seqs`: write their new tokens,
+    then attend every query head."""
+    import oracle
+    pool, q, k, v = tensors_bits
+    geom = oracle.dense_geom(w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    sel = np.isin(w.new_seq_idx, seqs)
+    slots = orc.slot_mapping(w.tables, w.new_seq_idx[sel], w.new_positions[sel], w.block_size)
+    orc.reshape_and_cache(pool, geom, k[sel], v[sel], slots)
+    rows = np.stack(np.meshgrid(seqs, np.arange(w.num_q_heads), indexing="ij"), axis=-1).reshape(-1, 2)
+    orc.paged_decode(q, pool, geom, w.tables, w.seq_lens, w.num_q_heads, w.scale, rows=rows)
+
+
+def cpu_baseline(w, tensors, budget_s: float = 10.0):
+    import oracle
+    orc = oracle.load()
+    tb = (wl.bf16_bits(tensors["pool"]).copy(), wl.bf16_bits(tensors["q"]), wl.bf16_bits(tensors["new_k"]),
+          wl.bf16_bits(tensors["new_v"]))
+    t0 = time.perf_counter()
+    oracle_pass(orc, w, tb, np.arange(w.batch))
+    first = time.perf_counter() - t0
+    passes, elapsed = 1, first
+    while elapsed < budget_s and passes < 50:
+        t0 = time.perf_counter()
+        oracle_pass(orc, w, tb, np.arange(w.batch))
+        elapsed += time.perf_counter() - t0
+        passes += 1
+    return {"value": round(w.batch * passes / elapsed, 2), "unit": "tokens/s", "cores": orc.num_threads(),
+            "kind": "oracle",
+            "sample": f"{passes} full passes over the {w.batch}-sequence batch ({w.batch * w.num_q_heads} "
+                      f"query rows each), fp64, {elapsed:.1f} s"}
+
+
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return
+    import oracle
+    orc = oracle.load()
+    w = wl.CONFIGS[args.config]()
+    tensors = wl.make_tensors(w, "cpu")
+    tb = (wl.bf16_bits(tensors["pool"]).copy(), wl.bf16_bits(tensors["q"]), wl.bf16_bits(tensors["new_k"]),
+          wl.bf16_bits(tensors["new_v"]))
+    # size a step so that warm-up plus timed steps stay near a minute
+    t0 = time.perf_counter()
+    oracle_pass(orc, w, tb, np.arange(1))
+    per_seq = max(time.perf_counter() - t0, 1e-4)
+    per_step = int(max(1, min(w.batch, 60.0 / (args.steps + args.warmup) / per_seq)))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle_pass(orc, w, tb, rng.choice(w.batch, per_step, replace=False))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_pass(orc, w, tb, rng.choice(w.batch, per_step, replace=False))
+    elapsed = time.perf_counter() - t0
+    value = per_step * args.steps / elapsed
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded bf16 N(0,1) K/V/q, random physical block placement",
+        "config": {"workload": w.name, "global_batch": w.batch, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                   "sequences_per_step": per_step},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": orc.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{per_step} random sequences of the batch per step, all query heads"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama70b_decode",
+                    choices=["tiny", "llama70b_decode", "long_context", "shared_prefix", "beam_fork"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if world != args.gpus and rank == 0:
+        log(f"note: --gpus {args.gpus} but WORLD_SIZE={world}; using WORLD_SIZE")
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

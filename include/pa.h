@@ -1,0 +1,268 @@
+/*
+ * pa.h -- C ABI of the paged KV-cache attention library (libpa.so).
+ *
+ * A KV cache held in fixed-size physical blocks, read through per-sequence
+ * block tables, on one GB300 (sm_103a).  Every device call is a hand-written
+ * CUDA kernel launched asynchronously on the caller's stream.
+ *
+ * Conventions for every call below:
+ *  - Device pointers are allocated and owned by the caller.  The library
+ *    never allocates, frees or synchronises device memory, except where a
+ *    function says so (pa_get_device_error synchronises its stream).
+ *  - Arguments are validated on the host before anything is launched; a
+ *    non-PA_OK status means nothing was launched.  A CUDA launch failure is
+ *    reported as PA_ERR_CUDA.
+ *  - Values that only the device can see (table entries, slots, sequence
+ *    lengths, fork pairs) are bounds-checked inside the kernels.  An
+ *    out-of-range value is never dereferenced: the kernel records a bit in a
+ *    per-device error word (PA_DEVERR_*) and leaves the affected output
+ *    undefined.  Read the word with pa_get_device_error.
+ *  - Tensors are bf16, row-major, densely packed unless a stride is given,
+ *    and 16-byte aligned.
+ *
+ * Sources (page, section) for the operations:
+ *  [P1] how-pagedattention-works (aiinfrainterviews.com)
+ *  [P2] attn-paged-attention-mcq-hard (zenaique.com)
+ *  [P3] auto-20261007-1900-en (lihaoran.work)
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, bad stride   */
+    PA_ERR_UNSUPPORTED = 2,   /* head_dim, block_size, group size or dtype not built      */
+    PA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than the *_workspace_size   */
+    PA_ERR_CUDA = 4,          /* the CUDA runtime reported an error                       */
+    PA_ERR_DEVICE = 5,        /* pa_get_device_error found a non-zero device error word   */
+    PA_ERR_NO_BLOCKS = 6,     /* block manager: the pool has no free block left           */
+    PA_ERR_NOT_FOUND = 7      /* block manager: unknown sequence id                       */
+} pa_status;
+
+/* Bits of the per-device error word written by the kernels. */
+#define PA_DEVERR_BLOCK_ID 0x1u /* a table entry or fork pair outside [0, num_blocks)      */
+#define PA_DEVERR_SLOT     0x2u /* a slot >= num_blocks * block_size                       */
+#define PA_DEVERR_SEQ_LEN  0x4u /* a length < 0, beyond the table width or the host bound  */
+#define PA_DEVERR_TIMEOUT  0x8u /* a bounded wait on a shared-memory barrier gave up       */
+
+typedef enum { PA_DTYPE_BF16 = 0 } pa_dtype;
+
+/*
+ * One layer's view of the physical block pool.  [P1] "A strong answer": the
+ * cache is carved into equal blocks of block_size token slots per layer;
+ * [P2] conceptual block-lookup listing: pool shaped
+ * [num_blocks, 2, num_layers, num_kv_heads, block_size, d_head].
+ *
+ * Element (blk, kv, h, off, i) -- kv 0 for K, 1 for V -- is at element offset
+ *     blk*block_stride + kv*kv_stride + (h*block_size + off)*head_dim + i
+ * from base.  block_stride = 0 means 2*Hkv*b*d and kv_stride = 0 means
+ * Hkv*b*d, i.e. the dense one-layer layout [NB][2][Hkv][b][d].  For the
+ * layered layout [NB][2][L][Hkv][b][d] at layer l, point base at layer l's
+ * first slab and set block_stride = 2*L*Hkv*b*d, kv_stride = L*Hkv*b*d.
+ * Every (blk, kv, h) slab of block_size*head_dim elements is contiguous.
+ * base and both strides (in bytes) must be multiples of 16.
+ */
+typedef struct {
+    void *base;           /* device memory, owned by the caller                 */
+    int64_t num_blocks;   /* NB: valid physical block ids are [0, NB)           */
+    int32_t num_kv_heads; /* Hkv                                                */
+    int32_t block_size;   /* b: token slots per block                           */
+    int32_t head_dim;     /* d                                                  */
+    int32_t dtype;        /* PA_DTYPE_BF16                                      */
+    int64_t block_stride; /* elements; 0 = dense                                */
+    int64_t kv_stride;    /* elements; 0 = dense                                */
+} pa_kv_pool;
+
+/* Human-readable name of a status.  Never returns NULL. */
+const char *pa_status_string(pa_status status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int32_t pa_version(void);
+
+/*
+ * Slot writer.  [P1] "A strong answer": a sequence's cache grows by one token
+ * each decode step, into the next free slot of its last block.
+ *   k, v          device, [num_tokens][Hkv][d] bf16 (the new tokens' K and V)
+ *   slot_mapping  device, [num_tokens] int64; slot = phys*block_size + offset
+ *                 (the linear form of [P3]'s (table[t//b], t%b)); a negative
+ *                 slot is padding and is skipped; slot >= NB*b raises
+ *                 PA_DEVERR_SLOT and is skipped
+ * Writes pool[slot/b][0][h][slot%b][:] = k[n][h][:] and the same for V,
+ * bit-exactly.  Two tokens with the same slot race (the result is one of them).
+ */
+pa_status pa_reshape_and_cache(const pa_kv_pool *pool, const void *k, const void *v,
+                               const int64_t *slot_mapping, int64_t num_tokens,
+                               cudaStream_t stream);
+
+/*
+ * Bytes of device workspace pa_decode needs for these shapes (0 when a single
+ * context partition covers max_seq_len).  partition_tokens as in pa_decode;
+ * 0 lets the library choose, from the current device's SM count.
+ */
+size_t pa_decode_workspace_size(const pa_kv_pool *pool, int32_t num_seqs, int32_t num_q_heads,
+                                int32_t max_seq_len, int32_t partition_tokens);
+
+/* The partition length pa_decode will use for these shapes (a multiple of
+ * block_size), or -1 if the shapes are invalid. */
+int32_t pa_decode_partition_tokens(const pa_kv_pool *pool, int32_t num_seqs, int32_t num_q_heads,
+                                   int32_t max_seq_len, int32_t partition_tokens);
+
+/*
+ * Paged GQA decode attention.  [P1] "A strong answer": the kernel takes the
+ * block table and reads each query's K/V from the physical blocks it names;
+ * [P2] conceptual block-lookup listing: position t of sequence s is at
+ * (block_tables[s][t // b], t % b), and attention over the gathered rows is
+ * ordinary scaled dot-product attention; [P3] "A block table maps logical
+ * order to physical storage".
+ *
+ *   out          device, [num_seqs][num_q_heads][d] bf16 (written)
+ *   q            device, [num_seqs][num_q_heads][d] bf16
+ *   block_tables device, [num_seqs][max_blocks_per_seq] int32 physical ids
+ *   seq_lens     device, [num_seqs] int32, tokens to attend (0 gives zeros)
+ *   max_seq_len  host upper bound on every seq_lens[s] (sizes the grid)
+ *   scale        softmax scale, usually 1/sqrt(d)
+ *   partition_tokens  context tokens per split-context partition: 0 = auto,
+ *                else a positive multiple of block_size.  When more than one
+ *                partition covers max_seq_len, the partitions' partial
+ *                results are merged by a second (reduce) kernel.
+ *   workspace    device scratch of pa_decode_workspace_size bytes (may be
+ *                NULL when that size is 0); its contents are overwritten
+ *
+ * q-head h reads kv-head h / (num_q_heads / Hkv).  All query heads of a KV
+ * group are served from one staged copy of each block.  Accumulation is fp32;
+ * out is rounded to bf16 (round to nearest even).
+ * Supported: head_dim 64 or 128; block_size 4, 8, 16 or 32; group size
+ * num_q_heads / Hkv of 1, 2, 4 or 8.
+ */
+pa_status pa_decode(void *out, const void *q, const pa_kv_pool *pool,
+                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                    int32_t max_seq_len, float scale, int32_t partition_tokens,
+                    void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Copy-on-write block copies.  [P1] feature table, beam-search row: forks
+ * share blocks and only the block that diverges is copied; [P2] interviewer
+ * follow-up on beam search: a fresh block receives the diverging block's
+ * content.
+ *   pairs  device, [num_pairs][2] int32 (src, dst)
+ * For each pair, every K and V slot of every kv-head of block src (in this
+ * layer's view) is copied to block dst, bit-exactly.  An id outside
+ * [0, num_blocks) raises PA_DEVERR_BLOCK_ID and that pair is skipped.  Pairs
+ * are copied concurrently: a dst that is also some pair's src, or a repeated
+ * dst, gives an unspecified result.
+ */
+pa_status pa_copy_blocks(const pa_kv_pool *pool, const int32_t *pairs, int32_t num_pairs,
+                         cudaStream_t stream);
+
+/*
+ * Chunked causal prefill against a paged context.  [P3] "A block table maps
+ * logical order to physical storage": paging changes only where K/V live, so
+ * each query still attends its whole visible (causal) history.
+ *   out, q       device, [num_seqs][chunk_len][num_q_heads][d] bf16
+ *   ctx_lens     device, [num_seqs] int32: tokens cached before the chunk
+ *   max_ctx_len  host upper bound on every ctx_lens[s]
+ * Query j of sequence s sits at position ctx_lens[s] + j and attends keys
+ * 0 .. ctx_lens[s] + j.  The chunk's own K/V must already be in the pool
+ * (pa_reshape_and_cache).  QK^T and PV run on the tcgen05 tensor cores with
+ * fp32 accumulation in tensor memory.
+ * Supported: head_dim 128, block_size 16, group size 1, 2, 4 or 8.
+ */
+pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *ctx_lens, int32_t num_seqs, int32_t chunk_len,
+                           int32_t num_q_heads, int32_t max_ctx_len, float scale,
+                           cudaStream_t stream);
+
+/*
+ * Reads (and, if clear != 0, resets) the current device's error word after
+ * synchronising `stream`.  Returns PA_ERR_DEVICE when the word is non-zero.
+ */
+pa_status pa_get_device_error(uint32_t *err_out, int32_t clear, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Host helpers (no GPU work).
+ * ------------------------------------------------------------------------- */
+
+/*
+ * Capacity arithmetic.  [P3] "How many tail slots remain unused?": a sequence
+ * of `tokens` positions needs ceil(tokens/b) blocks and leaves
+ * ceil(tokens/b)*b - tokens slots idle.  tokens < 0 or block_size <= 0 is
+ * PA_ERR_INVALID_ARG.
+ */
+pa_status pa_block_layout(int64_t tokens, int32_t block_size, int64_t *blocks, int64_t *unused);
+
+/*
+ * Slot mapping on the host.  [P3] "A block table maps logical order to
+ * physical storage": position t of sequence s lives in physical block
+ * tables[s][t // b] at offset t % b; its slot is that block * b + offset.
+ *   slots [n] (written), tables [num_seqs][max_blocks], seq_idx [n],
+ *   positions [n]; all host memory.
+ * A position outside the table or an entry outside [0, num_blocks) is
+ * PA_ERR_INVALID_ARG (slots then unspecified).
+ */
+pa_status pa_slot_mapping(int64_t *slots, const int32_t *tables, int32_t num_seqs,
+                          int32_t max_blocks, const int32_t *seq_idx, const int64_t *positions,
+                          int64_t n, int32_t block_size, int64_t num_blocks);
+
+/* ---------------------------------------------------------------------------
+ * Host block manager: free list, per-block reference counts, fork and
+ * copy-on-write planning.  [P1] "A strong answer" (on-demand equal-size
+ * blocks, one table per sequence) and its feature table (shared prefix with a
+ * refcount per block; beam fork sharing blocks with copy-on-write of the
+ * diverging block); [P1] "What interviewers probe next" (admission needs
+ * ceil(prompt/b) + 1 free blocks, plus a watermark reserve).
+ * Not thread-safe: one manager per thread or external locking.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_bm pa_bm;
+
+/* A manager over physical blocks [0, num_blocks) of size block_size. */
+pa_status pa_bm_create(pa_bm **out, int64_t num_blocks, int32_t block_size);
+void pa_bm_destroy(pa_bm *bm);
+
+/* New empty sequence (0 tokens, no blocks). */
+pa_status pa_bm_add_seq(pa_bm *bm, int32_t *seq_out);
+
+/*
+ * Appends n tokens to seq, allocating blocks on demand.  slots_out (may be
+ * NULL) receives the n new slots.  If the sequence's last block is shared
+ * (refcount > 1) and only partly filled, the first append forks it:
+ * a fresh block is allocated, (src, dst) is written to cow_pair_out (may be
+ * NULL) and *n_cow_out is set to 1 -- the caller must run pa_copy_blocks on
+ * that pair before writing the new slots.  PA_ERR_NO_BLOCKS leaves the
+ * sequence unchanged.
+ */
+pa_status pa_bm_append_tokens(pa_bm *bm, int32_t seq, int64_t n, int64_t *slots_out,
+                              int32_t *cow_pair_out, int32_t *n_cow_out);
+
+/* New sequence sharing every block of parent (refcount + 1 on each). */
+pa_status pa_bm_fork(pa_bm *bm, int32_t parent, int32_t *child_out);
+
+/* Releases a sequence; blocks whose refcount drops to 0 return to the pool. */
+pa_status pa_bm_free_seq(pa_bm *bm, int32_t seq);
+
+/* Writes seq's table into table_out[0..cap) (-1 past its blocks). */
+pa_status pa_bm_get_table(const pa_bm *bm, int32_t seq, int32_t *table_out, int32_t cap,
+                          int32_t *num_blocks_out, int64_t *num_tokens_out);
+
+/* Free blocks left; reference count of one block (-1 if out of range). */
+int64_t pa_bm_num_free(const pa_bm *bm);
+int32_t pa_bm_refcount(const pa_bm *bm, int64_t block);
+
+/* *admit = 1 iff free blocks >= ceil(prompt_tokens/b) + 1 + watermark_blocks. */
+pa_status pa_bm_can_admit(const pa_bm *bm, int64_t prompt_tokens, int64_t watermark_blocks,
+                          int32_t *admit);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

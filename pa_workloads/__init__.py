@@ -236,6 +236,24 @@ def prefill_chunk(seed: int = SEED_BASE + 4, batch: int = 16, ctx: int = 4096,
                     new_seq_idx=seq_idx, new_positions=positions, ctx_lens=ctx_lens, chunk=chunk)
 
 
+def custom(lens, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+           num_blocks: Optional[int] = None, seed: int = SEED_BASE + 100, name: str = "custom",
+           partition_tokens: int = 0) -> Workload:
+    """Decode batch with the given sequence lengths (zeros allowed), random
+    placement in a pool with spare blocks, scale 1/sqrt(head_dim)."""
+    rng = np.random.default_rng(seed)
+    b = block_size
+    counts = [_blocks_for(int(L), b) for L in lens]
+    nb = num_blocks if num_blocks is not None else max(8, 2 * sum(counts) + 3)
+    tables = _tables_from_counts(counts, rng.permutation(nb).astype(np.int32))
+    seq = np.asarray(lens, dtype=np.int32)
+    has = seq > 0
+    return Workload(name, "decode", num_q_heads, num_kv_heads, head_dim, b, nb, 1.0 / math.sqrt(head_dim),
+                    seq, tables, _referenced(tables), seed,
+                    new_seq_idx=np.nonzero(has)[0].astype(np.int32),
+                    new_positions=seq[has].astype(np.int64) - 1, partition_tokens=partition_tokens)
+
+
 CONFIGS = {
     "tiny": tiny,
     "tiny_page_example": tiny_page_example,

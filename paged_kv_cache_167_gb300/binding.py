@@ -1,0 +1,244 @@
+"""ctypes binding of ``libpa.so`` (``include/pa.h``), same names as the C ABI.
+
+Argument marshalling only: these functions check that tensors have the
+dtype, device and contiguity the C ABI expects, pass raw pointers, sizes and
+the current CUDA stream, and turn a non-OK status into an exception.  Every
+step of the computation runs in the library's CUDA kernels; there is no
+fallback.  If ``libpa.so`` has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+LIBRARY = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa.so")
+
+PA_OK = 0
+STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
+                4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE", 6: "PA_ERR_NO_BLOCKS", 7: "PA_ERR_NOT_FOUND"}
+DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+PA_DTYPE_BF16 = 0
+
+# Every function declared in include/pa.h with (restype, argtypes).
+_P, _I64, _I32, _U32, _F, _SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32,
+                                  ctypes.c_float, ctypes.c_size_t)
+
+
+class PaKvPool(ctypes.Structure):
+    """``pa_kv_pool``: one layer's view of the block pool (strides in elements)."""
+    _fields_ = [("base", ctypes.c_void_p), ("num_blocks", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("block_stride", ctypes.c_int64), ("kv_stride", ctypes.c_int64)]
+
+
+_POOL = ctypes.POINTER(PaKvPool)
+SIGNATURES = {
+    "pa_status_string": (ctypes.c_char_p, [_I32]),
+    "pa_version": (_I32, []),
+    "pa_reshape_and_cache": (_I32, [_POOL, _P, _P, _P, _I64, _P]),
+    "pa_decode_workspace_size": (_SZ, [_POOL, _I32, _I32, _I32, _I32]),
+    "pa_decode_partition_tokens": (_I32, [_POOL, _I32, _I32, _I32, _I32]),
+    "pa_decode": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _P]),
+    "pa_copy_blocks": (_I32, [_POOL, _P, _I32, _P]),
+    "pa_prefill_chunk": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _I32, _F, _P]),
+    "pa_get_device_error": (_I32, [ctypes.POINTER(_U32), _I32, _P]),
+    "pa_block_layout": (_I32, [_I64, _I32, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
+    "pa_slot_mapping": (_I32, [_P, _P, _I32, _I32, _P, _P, _I64, _I32, _I64]),
+    "pa_bm_create": (_I32, [ctypes.POINTER(_P), _I64, _I32]),
+    "pa_bm_destroy": (None, [_P]),
+    "pa_bm_add_seq": (_I32, [_P, ctypes.POINTER(_I32)]),
+    "pa_bm_append_tokens": (_I32, [_P, _I32, _I64, _P, _P, ctypes.POINTER(_I32)]),
+    "pa_bm_fork": (_I32, [_P, _I32, ctypes.POINTER(_I32)]),
+    "pa_bm_free_seq": (_I32, [_P, _I32]),
+    "pa_bm_get_table": (_I32, [_P, _I32, _P, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I64)]),
+    "pa_bm_num_free": (_I64, [_P]),
+    "pa_bm_refcount": (_I32, [_P, _I64]),
+    "pa_bm_can_admit": (_I32, [_P, _I64, _I64, ctypes.POINTER(_I32)]),
+}
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIBRARY):
+            raise RuntimeError(f"{LIBRARY} is missing: build it with paged_kv_cache_167_gb300.build.build()")
+        handle = ctypes.CDLL(LIBRARY)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PagedAttentionError(status, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return ctypes.c_void_p(handle)
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> ctypes.c_void_p:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# ---------------------------------------------------------------------------
+# pool descriptor
+# ---------------------------------------------------------------------------
+
+def pool_desc(pool: torch.Tensor, layer: Optional[int] = None) -> PaKvPool:
+    """Descriptor of a bf16 pool tensor.
+
+    ``pool`` is [NB][2][Hkv][b][d] (one layer) or the layered
+    [NB][2][L][Hkv][b][d]; for the latter ``layer`` picks the layer's view.
+    """
+    _dev(pool, torch.bfloat16, "pool")
+    if pool.dim() == 5:
+        nb, two, hkv, b, d = pool.shape
+        base, bstride, kvstride = pool.data_ptr(), 0, 0
+    elif pool.dim() == 6:
+        if layer is None:
+            raise ValueError("layer is required for a layered pool")
+        nb, two, nl, hkv, b, d = pool.shape
+        if not 0 <= layer < nl:
+            raise ValueError("layer out of range")
+        slab = hkv * b * d
+        base = pool.data_ptr() + layer * slab * pool.element_size()
+        bstride, kvstride = 2 * nl * slab, nl * slab
+    else:
+        raise ValueError("pool must be [NB][2][Hkv][b][d] or [NB][2][L][Hkv][b][d]")
+    if two != 2:
+        raise ValueError("pool dim 1 must be 2 (K, V)")
+    return PaKvPool(base, nb, hkv, b, d, PA_DTYPE_BF16, bstride, kvstride)
+
+
+# ---------------------------------------------------------------------------
+# device calls
+# ---------------------------------------------------------------------------
+
+def reshape_and_cache(pool: torch.Tensor, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                      layer: Optional[int] = None, stream=None) -> None:
+    desc = pool_desc(pool, layer)
+    n = k.shape[0]
+    if v.shape != k.shape or slot_mapping.numel() != n:
+        raise ValueError("k, v and slot_mapping disagree on the token count")
+    _check(lib().pa_reshape_and_cache(ctypes.byref(desc), _dev(k, torch.bfloat16, "k"),
+                                      _dev(v, torch.bfloat16, "v"),
+                                      _dev(slot_mapping, torch.int64, "slot_mapping"), n, _stream(stream)),
+           "pa_reshape_and_cache")
+
+
+def decode_workspace_size(pool: torch.Tensor, num_seqs: int, num_q_heads: int, max_seq_len: int,
+                          partition_tokens: int = 0, layer: Optional[int] = None) -> int:
+    desc = pool_desc(pool, layer)
+    return int(lib().pa_decode_workspace_size(ctypes.byref(desc), num_seqs, num_q_heads, max_seq_len,
+                                              partition_tokens))
+
+
+def decode_partition_tokens(pool: torch.Tensor, num_seqs: int, num_q_heads: int, max_seq_len: int,
+                            partition_tokens: int = 0, layer: Optional[int] = None) -> int:
+    desc = pool_desc(pool, layer)
+    return int(lib().pa_decode_partition_tokens(ctypes.byref(desc), num_seqs, num_q_heads, max_seq_len,
+                                                partition_tokens))
+
+
+def decode(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_tables: torch.Tensor,
+           seq_lens: torch.Tensor, max_seq_len: int, scale: float, partition_tokens: int = 0,
+           workspace: Optional[torch.Tensor] = None, layer: Optional[int] = None, stream=None) -> None:
+    """pa_decode.  ``workspace`` is a uint8 CUDA tensor of at least
+    decode_workspace_size(...) bytes (None when that size is 0)."""
+    desc = pool_desc(pool, layer)
+    B, Hq, _ = q.shape
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.numel() != B:
+        raise ValueError("block_tables / seq_lens do not match the batch")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, torch.uint8, "workspace"), workspace.numel()
+    _check(lib().pa_decode(_dev(out, torch.bfloat16, "out"), _dev(q, torch.bfloat16, "q"), ctypes.byref(desc),
+                           _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+                           _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, int(max_seq_len), float(scale),
+                           int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)),
+           "pa_decode")
+
+
+def copy_blocks(pool: torch.Tensor, pairs: torch.Tensor, layer: Optional[int] = None, stream=None) -> None:
+    desc = pool_desc(pool, layer)
+    if pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be [n][2]")
+    _check(lib().pa_copy_blocks(ctypes.byref(desc), _dev(pairs, torch.int32, "pairs"), pairs.shape[0],
+                                _stream(stream)), "pa_copy_blocks")
+
+
+def prefill_chunk(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_tables: torch.Tensor,
+                  ctx_lens: torch.Tensor, max_ctx_len: int, scale: float, layer: Optional[int] = None,
+                  stream=None) -> None:
+    desc = pool_desc(pool, layer)
+    B, C, Hq, _ = q.shape
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or ctx_lens.numel() != B:
+        raise ValueError("block_tables / ctx_lens do not match the batch")
+    _check(lib().pa_prefill_chunk(_dev(out, torch.bfloat16, "out"), _dev(q, torch.bfloat16, "q"),
+                                  ctypes.byref(desc), _dev(block_tables, torch.int32, "block_tables"),
+                                  block_tables.shape[1], _dev(ctx_lens, torch.int32, "ctx_lens"), B, C, Hq,
+                                  int(max_ctx_len), float(scale), _stream(stream)), "pa_prefill_chunk")
+
+
+def get_device_error(clear: bool = True, stream=None) -> int:
+    """The current device's error word (PA_DEVERR_* bits); synchronises."""
+    word = ctypes.c_uint32(0)
+    status = lib().pa_get_device_error(ctypes.byref(word), 1 if clear else 0, _stream(stream))
+    if status not in (PA_OK, 5):
+        raise PagedAttentionError(status, "pa_get_device_error")
+    return int(word.value)
+
+
+# ---------------------------------------------------------------------------
+# host helpers
+# ---------------------------------------------------------------------------
+
+def block_layout(tokens: int, block_size: int):
+    blocks, unused = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().pa_block_layout(tokens, block_size, ctypes.byref(blocks), ctypes.byref(unused)),
+           "pa_block_layout")
+    return blocks.value, unused.value
+
+
+def slot_mapping(tables: np.ndarray, seq_idx: Sequence[int], positions: Sequence[int], block_size: int,
+                 num_blocks: int) -> np.ndarray:
+    """Host slot mapping (int64 numpy array) for (sequence, position) pairs."""
+    tables = np.ascontiguousarray(tables, dtype=np.int32)
+    seq_idx = np.ascontiguousarray(seq_idx, dtype=np.int32)
+    positions = np.ascontiguousarray(positions, dtype=np.int64)
+    out = np.empty(len(positions), dtype=np.int64)
+    _check(lib().pa_slot_mapping(out.ctypes.data_as(_P), tables.ctypes.data_as(_P), tables.shape[0],
+                                 tables.shape[1], seq_idx.ctypes.data_as(_P), positions.ctypes.data_as(_P),
+                                 len(positions), block_size, num_blocks), "pa_slot_mapping")
+    return out

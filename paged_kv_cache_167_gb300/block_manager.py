@@ -1,0 +1,84 @@
+"""Python handle on the host block manager (``pa_bm_*`` in ``include/pa.h``).
+
+Marshalling only; the free list, reference counts, forks and copy-on-write
+planning live in ``csrc/pa_block_manager.cpp``.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import numpy as np
+
+from .binding import PagedAttentionError, _check, lib
+
+_I32, _I64 = ctypes.c_int32, ctypes.c_int64
+
+
+class BlockManager:
+    def __init__(self, num_blocks: int, block_size: int):
+        handle = ctypes.c_void_p()
+        _check(lib().pa_bm_create(ctypes.byref(handle), num_blocks, block_size), "pa_bm_create")
+        self._h = handle
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self) -> None:
+        if self._h:
+            lib().pa_bm_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 -- interpreter shutdown
+            pass
+
+    def add_seq(self) -> int:
+        sid = _I32()
+        _check(lib().pa_bm_add_seq(self._h, ctypes.byref(sid)), "pa_bm_add_seq")
+        return sid.value
+
+    def append_tokens(self, seq: int, n: int) -> Tuple[np.ndarray, Optional[Tuple[int, int]]]:
+        """Appends n tokens; returns their slots and the (src, dst) copy-on-write
+        pair to run through copy_blocks first, if any."""
+        slots = np.empty(n, dtype=np.int64)
+        pair = (ctypes.c_int32 * 2)()
+        ncow = _I32()
+        _check(lib().pa_bm_append_tokens(self._h, seq, n, slots.ctypes.data_as(ctypes.c_void_p),
+                                         ctypes.cast(pair, ctypes.c_void_p), ctypes.byref(ncow)),
+               "pa_bm_append_tokens")
+        return slots, ((pair[0], pair[1]) if ncow.value else None)
+
+    def fork(self, parent: int) -> int:
+        child = _I32()
+        _check(lib().pa_bm_fork(self._h, parent, ctypes.byref(child)), "pa_bm_fork")
+        return child.value
+
+    def free_seq(self, seq: int) -> None:
+        _check(lib().pa_bm_free_seq(self._h, seq), "pa_bm_free_seq")
+
+    def table(self, seq: int) -> Tuple[np.ndarray, int]:
+        """(physical block ids, token count) of a sequence."""
+        nb, nt = _I32(), _I64()
+        _check(lib().pa_bm_get_table(self._h, seq, None, 0, ctypes.byref(nb), ctypes.byref(nt)),
+               "pa_bm_get_table")
+        out = np.empty(max(nb.value, 1), dtype=np.int32)
+        _check(lib().pa_bm_get_table(self._h, seq, out.ctypes.data_as(ctypes.c_void_p), nb.value, None, None),
+               "pa_bm_get_table")
+        return out[:nb.value], nt.value
+
+    def num_free(self) -> int:
+        return int(lib().pa_bm_num_free(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(lib().pa_bm_refcount(self._h, block))
+
+    def can_admit(self, prompt_tokens: int, watermark_blocks: int = 0) -> bool:
+        ok = _I32()
+        _check(lib().pa_bm_can_admit(self._h, prompt_tokens, watermark_blocks, ctypes.byref(ok)),
+               "pa_bm_can_admit")
+        return bool(ok.value)
+
+
+__all__ = ["BlockManager", "PagedAttentionError"]

@@ -1,0 +1,282 @@
+// pa_api.cpp -- the C ABI (include/pa.h): argument validation, partition
+// planning and dispatch to the kernels.  Host code only; it allocates no
+// device memory and launches nothing when validation fails.
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+cudaError_t launch_decode_d64(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_decode_d128(const DecodeArgs &a, cudaStream_t stream);
+
+namespace {
+
+constexpr int kDecodeWarps = 4;          // warps per decode CTA (must match the kernel)
+constexpr int kAutoCtasPerSm = 2;        // resident decode CTAs per SM
+constexpr int kAutoWaves = 4;            // CTAs per resident slot the auto partition aims for
+constexpr int kAutoMaxPartition = 1024;  // cap so long sequences still spread over SMs
+constexpr size_t kWsAlign = 256;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Resolves a public pool descriptor into a PoolView; PA_OK or the reason.
+pa_status resolve_pool(const pa_kv_pool *pool, PoolView *out) {
+    if (!pool || !pool->base || !aligned16(pool->base)) return PA_ERR_INVALID_ARG;
+    if (pool->dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
+    if (pool->num_blocks <= 0 || pool->num_kv_heads <= 0 || pool->block_size <= 0 || pool->head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (pool->head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+    const int64_t slab = (int64_t)pool->num_kv_heads * pool->block_size * pool->head_dim;
+    const int64_t kv_stride = pool->kv_stride ? pool->kv_stride : slab;
+    const int64_t block_stride = pool->block_stride ? pool->block_stride : 2 * slab;
+    if (kv_stride < slab || block_stride < kv_stride + slab) return PA_ERR_INVALID_ARG;
+    if ((kv_stride * 2) % 16 != 0 || (block_stride * 2) % 16 != 0) return PA_ERR_INVALID_ARG;
+    out->base = pool->base;
+    out->num_blocks = pool->num_blocks;
+    out->num_kv_heads = pool->num_kv_heads;
+    out->block_size = pool->block_size;
+    out->head_dim = pool->head_dim;
+    out->block_stride = block_stride;
+    out->kv_stride = kv_stride;
+    return PA_OK;
+}
+
+struct DecodePlan {
+    int32_t partition_tokens;
+    int32_t num_partitions;
+    size_t ws_o_bytes;
+    size_t ws_ml_bytes;
+    size_t total_bytes() const { return ws_o_bytes + ws_ml_bytes; }
+};
+
+pa_status plan_decode(const PoolView &pool, int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
+                      int32_t partition_tokens, DecodePlan *plan) {
+    if (num_seqs < 0 || num_q_heads <= 0 || max_seq_len < 0 || partition_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (num_q_heads % pool.num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    const int group = num_q_heads / pool.num_kv_heads;
+    if (!decode_supported(pool.head_dim, group, pool.block_size)) return PA_ERR_UNSUPPORTED;
+    int64_t part = partition_tokens;
+    if (part > 0) {
+        if (part % pool.block_size != 0) return PA_ERR_INVALID_ARG;
+    } else {
+        // Auto: enough partitions that the grid covers every resident CTA slot
+        // several times, each partition a whole number of per-warp stages.
+        const int64_t grain = (int64_t)decode_stage_tokens(pool.block_size) * kDecodeWarps;
+        int sms = device_sm_count();
+        if (sms <= 0) sms = 148;
+        const int64_t units = (int64_t)(num_seqs > 0 ? num_seqs : 1) * pool.num_kv_heads;
+        const int64_t want = ceil_div((int64_t)sms * kAutoCtasPerSm * kAutoWaves, units);
+        part = ceil_div(ceil_div(max_seq_len > 0 ? max_seq_len : 1, want), grain) * grain;
+        const int64_t cap = (kAutoMaxPartition / grain) * grain;
+        if (part > cap) part = cap;
+        if (part < grain) part = grain;
+    }
+    const int64_t parts = max_seq_len > 0 ? ceil_div(max_seq_len, part) : 1;
+    if (parts > 65535) return PA_ERR_INVALID_ARG;
+    plan->partition_tokens = (int32_t)part;
+    plan->num_partitions = (int32_t)parts;
+    plan->ws_o_bytes = 0;
+    plan->ws_ml_bytes = 0;
+    if (parts > 1) {
+        const size_t rows = (size_t)num_seqs * num_q_heads * (size_t)parts;
+        plan->ws_o_bytes = round_up(rows * pool.head_dim * sizeof(float), kWsAlign);
+        plan->ws_ml_bytes = round_up(rows * 2 * sizeof(float), kWsAlign);
+    }
+    return PA_OK;
+}
+
+}  // namespace
+
+int decode_stage_tokens(int block_size) { return block_size >= 16 ? block_size : 16; }
+
+bool decode_supported(int head_dim, int group, int block_size) {
+    const bool d_ok = head_dim == 64 || head_dim == 128;
+    const bool g_ok = group == 1 || group == 2 || group == 4 || group == 8;
+    const bool b_ok = block_size == 4 || block_size == 8 || block_size == 16 || block_size == 32;
+    return d_ok && g_ok && b_ok;
+}
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
+    switch (a.pool.head_dim) {
+        case 64: return launch_decode_d64(a, stream);
+        case 128: return launch_decode_d128(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char *pa_status_string(pa_status status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PA_ERR_WORKSPACE: return "workspace missing or too small";
+        case PA_ERR_CUDA: return "CUDA runtime error";
+        case PA_ERR_DEVICE: return "device error word is set";
+        case PA_ERR_NO_BLOCKS: return "no free block left";
+        case PA_ERR_NOT_FOUND: return "unknown sequence";
+    }
+    return "unknown status";
+}
+
+int32_t pa_version(void) { return 10000; }
+
+pa_status pa_reshape_and_cache(const pa_kv_pool *pool, const void *k, const void *v,
+                               const int64_t *slot_mapping, int64_t num_tokens, cudaStream_t stream) {
+    PoolView view;
+    pa_status st = resolve_pool(pool, &view);
+    if (st != PA_OK) return st;
+    if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !aligned16(k) || !aligned16(v)) return PA_ERR_INVALID_ARG;
+    return launch_reshape_and_cache(view, k, v, slot_mapping, num_tokens, stream) == cudaSuccess ? PA_OK
+                                                                                                 : PA_ERR_CUDA;
+}
+
+size_t pa_decode_workspace_size(const pa_kv_pool *pool, int32_t num_seqs, int32_t num_q_heads,
+                                int32_t max_seq_len, int32_t partition_tokens) {
+    PoolView view;
+    if (resolve_pool(pool, &view) != PA_OK) return 0;
+    DecodePlan plan;
+    if (plan_decode(view, num_seqs, num_q_heads, max_seq_len, partition_tokens, &plan) != PA_OK) return 0;
+    return plan.total_bytes();
+}
+
+int32_t pa_decode_partition_tokens(const pa_kv_pool *pool, int32_t num_seqs, int32_t num_q_heads,
+                                   int32_t max_seq_len, int32_t partition_tokens) {
+    PoolView view;
+    if (resolve_pool(pool, &view) != PA_OK) return -1;
+    DecodePlan plan;
+    if (plan_decode(view, num_seqs, num_q_heads, max_seq_len, partition_tokens, &plan) != PA_OK) return -1;
+    return plan.partition_tokens;
+}
+
+pa_status pa_decode(void *out, const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
+                    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                    int32_t max_seq_len, float scale, int32_t partition_tokens, void *workspace,
+                    size_t workspace_bytes, cudaStream_t stream) {
+    PoolView view;
+    pa_status st = resolve_pool(pool, &view);
+    if (st != PA_OK) return st;
+    DecodePlan plan;
+    st = plan_decode(view, num_seqs, num_q_heads, max_seq_len, partition_tokens, &plan);
+    if (st != PA_OK) return st;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !block_tables || !seq_lens || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (num_seqs > 65535) return PA_ERR_INVALID_ARG;
+    if (plan.total_bytes() > 0) {
+        if (!workspace || workspace_bytes < plan.total_bytes()) return PA_ERR_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(workspace) % kWsAlign) != 0) return PA_ERR_WORKSPACE;
+    }
+    DecodeArgs a;
+    a.out = out;
+    a.q = q;
+    a.pool = view;
+    a.tables = block_tables;
+    a.max_blocks = max_blocks_per_seq;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.max_seq_len = max_seq_len;
+    a.scale = scale;
+    a.partition_tokens = plan.partition_tokens;
+    a.num_partitions = plan.num_partitions;
+    a.ws_o = plan.total_bytes() ? static_cast<float *>(workspace) : nullptr;
+    a.ws_ml = plan.total_bytes() ? reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_o_bytes)
+                                 : nullptr;
+    return launch_decode(a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_copy_blocks(const pa_kv_pool *pool, const int32_t *pairs, int32_t num_pairs, cudaStream_t stream) {
+    PoolView view;
+    pa_status st = resolve_pool(pool, &view);
+    if (st != PA_OK) return st;
+    if (num_pairs < 0) return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!pairs || num_pairs > (1 << 30)) return PA_ERR_INVALID_ARG;
+    return launch_copy_blocks(view, pairs, num_pairs, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *ctx_lens, int32_t num_seqs,
+                           int32_t chunk_len, int32_t num_q_heads, int32_t max_ctx_len, float scale,
+                           cudaStream_t stream) {
+    PoolView view;
+    pa_status st = resolve_pool(pool, &view);
+    if (st != PA_OK) return st;
+    if (num_seqs < 0 || chunk_len < 0 || num_q_heads <= 0 || max_ctx_len < 0) return PA_ERR_INVALID_ARG;
+    if (num_q_heads % view.num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (!prefill_supported(view.head_dim, num_q_heads / view.num_kv_heads, view.block_size))
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || chunk_len == 0) return PA_OK;
+    if (!out || !q || !block_tables || !ctx_lens || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if ((int64_t)max_ctx_len + chunk_len > (int64_t)max_blocks_per_seq * view.block_size) return PA_ERR_INVALID_ARG;
+    PrefillArgs a;
+    a.out = out;
+    a.q = q;
+    a.pool = view;
+    a.tables = block_tables;
+    a.max_blocks = max_blocks_per_seq;
+    a.ctx_lens = ctx_lens;
+    a.num_seqs = num_seqs;
+    a.chunk_len = chunk_len;
+    a.num_q_heads = num_q_heads;
+    a.max_ctx_len = max_ctx_len;
+    a.scale = scale;
+    return launch_prefill(a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_get_device_error(uint32_t *err_out, int32_t clear, cudaStream_t stream) {
+    if (!err_out) return PA_ERR_INVALID_ARG;
+    unsigned int *word = device_error_word();
+    if (!word) return PA_ERR_CUDA;
+    uint32_t value = 0;
+    if (cudaMemcpyAsync(&value, word, sizeof(value), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (clear && value) {
+        if (cudaMemsetAsync(word, 0, sizeof(value), stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    *err_out = value;
+    return value ? PA_ERR_DEVICE : PA_OK;
+}
+
+pa_status pa_block_layout(int64_t tokens, int32_t block_size, int64_t *blocks, int64_t *unused) {
+    if (tokens < 0 || block_size <= 0 || !blocks || !unused) return PA_ERR_INVALID_ARG;
+    const int64_t n = ceil_div(tokens, block_size);
+    *blocks = n;
+    *unused = n * block_size - tokens;
+    return PA_OK;
+}
+
+pa_status pa_slot_mapping(int64_t *slots, const int32_t *tables, int32_t num_seqs, int32_t max_blocks,
+                          const int32_t *seq_idx, const int64_t *positions, int64_t n, int32_t block_size,
+                          int64_t num_blocks) {
+    if (n < 0 || num_seqs < 0 || max_blocks <= 0 || block_size <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (n == 0) return PA_OK;
+    if (!slots || !tables || !seq_idx || !positions) return PA_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < n; ++i) {
+        const int32_t s = seq_idx[i];
+        const int64_t t = positions[i];
+        if (s < 0 || s >= num_seqs || t < 0 || t / block_size >= max_blocks) return PA_ERR_INVALID_ARG;
+        const int32_t phys = tables[(int64_t)s * max_blocks + t / block_size];
+        if (phys < 0 || phys >= num_blocks) return PA_ERR_INVALID_ARG;
+        slots[i] = (int64_t)phys * block_size + t % block_size;
+    }
+    return PA_OK;
+}
+
+}  // extern "C"

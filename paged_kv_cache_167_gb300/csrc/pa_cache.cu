@@ -1,0 +1,188 @@
+// pa_cache.cu -- slot writer (reshape_and_cache), copy-on-write block copies,
+// and the per-device error word.
+//
+// Slot writer: how-pagedattention-works (aiinfrainterviews.com), "A strong
+// answer" -- the cache grows by one token per decode step, stored in the next
+// slot of the sequence's last block; the slot is the linear form of the
+// (table[t // b], t % b) address of auto-20261007-1900-en (lihaoran.work), "A
+// block table maps logical order to physical storage".
+// Block copies: how-pagedattention-works, feature table (beam-search row) and
+// attn-paged-attention-mcq-hard (zenaique.com), the beam-search follow-up --
+// forks share blocks and a diverging block is copied into a fresh one.
+//
+// Both kernels move 16-byte vectors (8 bf16): a (block, K/V, head) slab is
+// contiguous, so each token row of d elements is d/8 coalesced 16-B accesses.
+#include <mutex>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+__device__ unsigned int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned int *g_error_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+// ---- reshape_and_cache ------------------------------------------------------
+
+struct CacheParams {
+    uint4 *pool;                 // pool base as 16-B vectors
+    int64_t num_blocks;
+    int64_t block_stride_v;      // in 16-B vectors
+    int64_t kv_stride_v;
+    int32_t num_kv_heads;
+    int32_t block_size;
+    int32_t row_vecs;            // head_dim / 8
+    const uint4 *k;
+    const uint4 *v;
+    const int64_t *slots;
+    int64_t num_tokens;
+    unsigned int *err;
+};
+
+// One thread per 16-B vector of a (token, K/V, head) row.
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheParams p) {
+    const int64_t per_token = 2ll * p.num_kv_heads * p.row_vecs;
+    const int64_t total = p.num_tokens * per_token;
+    const int64_t slot_limit = p.num_blocks * p.block_size;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = idx / per_token;
+        int64_t r = idx - n * per_token;
+        const int kv = (int)(r / ((int64_t)p.num_kv_heads * p.row_vecs));
+        r -= (int64_t)kv * p.num_kv_heads * p.row_vecs;
+        const int h = (int)(r / p.row_vecs);
+        const int c = (int)(r - (int64_t)h * p.row_vecs);
+        const int64_t slot = __ldg(p.slots + n);
+        if (slot < 0) continue;  // padding
+        if (slot >= slot_limit) {
+            if (kv == 0 && h == 0 && c == 0) raise_error(p.err, PA_DEVERR_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / p.block_size;
+        const int off = (int)(slot - blk * p.block_size);
+        const uint4 *src = (kv ? p.v : p.k) + (n * p.num_kv_heads + h) * p.row_vecs + c;
+        uint4 *dst = p.pool + blk * p.block_stride_v + kv * p.kv_stride_v +
+                     ((int64_t)h * p.block_size + off) * p.row_vecs + c;
+        *dst = __ldg(src);
+    }
+}
+
+// ---- copy_blocks --------------------------------------------------------------
+
+struct CopyParams {
+    uint4 *pool;
+    int64_t num_blocks;
+    int64_t block_stride_v;
+    int64_t kv_stride_v;
+    int64_t half_vecs;           // Hkv * b * d / 8: one K (or V) half of a block
+    const int32_t *pairs;
+    int32_t num_pairs;
+    unsigned int *err;
+};
+
+// grid (num_pairs, 2): one CTA per (pair, K/V half); the half is contiguous.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyParams p) {
+    const int pair = blockIdx.x, kv = blockIdx.y;
+    const int32_t src = __ldg(p.pairs + 2 * pair), dst = __ldg(p.pairs + 2 * pair + 1);
+    if (src < 0 || src >= p.num_blocks || dst < 0 || dst >= p.num_blocks) {
+        if (kv == 0 && threadIdx.x == 0) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+        return;
+    }
+    const uint4 *s = p.pool + src * p.block_stride_v + kv * p.kv_stride_v;
+    uint4 *d = p.pool + dst * p.block_stride_v + kv * p.kv_stride_v;
+    constexpr int kUnroll = 4;
+    int64_t i = threadIdx.x;
+    for (; i + (kUnroll - 1) * blockDim.x < p.half_vecs; i += kUnroll * blockDim.x) {
+        uint4 t[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) t[u] = s[i + u * blockDim.x];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) d[i + u * blockDim.x] = t[u];
+    }
+    for (; i < p.half_vecs; i += blockDim.x) d[i] = s[i];
+}
+
+}  // namespace
+
+unsigned int *device_error_word() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_error_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+        g_error_ptr[dev] = static_cast<unsigned int *>(ptr);
+    }
+    return g_error_ptr[dev];
+}
+
+int device_sm_count() {
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+cudaError_t launch_reshape_and_cache(const PoolView &pool, const void *k, const void *v,
+                                     const int64_t *slots, int64_t num_tokens, cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    unsigned int *err = device_error_word();
+    if (!err) return cudaErrorUnknown;
+    CacheParams p;
+    p.pool = reinterpret_cast<uint4 *>(const_cast<void *>(pool.base));
+    p.num_blocks = pool.num_blocks;
+    p.block_stride_v = pool.block_stride / 8;
+    p.kv_stride_v = pool.kv_stride / 8;
+    p.num_kv_heads = pool.num_kv_heads;
+    p.block_size = pool.block_size;
+    p.row_vecs = pool.head_dim / 8;
+    p.k = static_cast<const uint4 *>(k);
+    p.v = static_cast<const uint4 *>(v);
+    p.slots = slots;
+    p.num_tokens = num_tokens;
+    p.err = err;
+    const int64_t total = num_tokens * 2 * pool.num_kv_heads * p.row_vecs;
+    const int threads = 256;
+    const int64_t max_blocks = (int64_t)device_sm_count() * 8;
+    int64_t blocks = (total + threads - 1) / threads;
+    if (max_blocks > 0 && blocks > max_blocks) blocks = max_blocks;
+    reshape_and_cache_kernel<<<(unsigned)blocks, threads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(const PoolView &pool, const int32_t *pairs, int32_t num_pairs,
+                               cudaStream_t stream) {
+    if (num_pairs == 0) return cudaSuccess;
+    unsigned int *err = device_error_word();
+    if (!err) return cudaErrorUnknown;
+    CopyParams p;
+    p.pool = reinterpret_cast<uint4 *>(const_cast<void *>(pool.base));
+    p.num_blocks = pool.num_blocks;
+    p.block_stride_v = pool.block_stride / 8;
+    p.kv_stride_v = pool.kv_stride / 8;
+    p.half_vecs = (int64_t)pool.num_kv_heads * pool.block_size * pool.head_dim / 8;
+    p.pairs = pairs;
+    p.num_pairs = num_pairs;
+    p.err = err;
+    copy_blocks_kernel<<<dim3(num_pairs, 2), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

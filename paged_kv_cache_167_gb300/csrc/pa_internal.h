@@ -1,0 +1,78 @@
+// pa_internal.h -- host-side interface between the C ABI layer (pa_api.cpp)
+// and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// A validated, stride-resolved view of one layer of the block pool.
+struct PoolView {
+    const void *base;
+    int64_t num_blocks;
+    int32_t num_kv_heads;
+    int32_t block_size;
+    int32_t head_dim;
+    int64_t block_stride;  // elements
+    int64_t kv_stride;     // elements
+};
+
+// Device address of the current device's error word (set up once per device);
+// nullptr if the CUDA runtime failed.
+unsigned int *device_error_word();
+
+// Number of SMs of the current device (cached per device); 0 on failure.
+int device_sm_count();
+
+// ---- slot writer and block copies (pa_cache.cu) ---------------------------
+cudaError_t launch_reshape_and_cache(const PoolView &pool, const void *k, const void *v,
+                                     const int64_t *slots, int64_t num_tokens, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const PoolView &pool, const int32_t *pairs, int32_t num_pairs,
+                               cudaStream_t stream);
+
+// ---- decode (pa_decode_*.cu) -----------------------------------------------
+struct DecodeArgs {
+    void *out;
+    const void *q;
+    PoolView pool;
+    const int32_t *tables;
+    int32_t max_blocks;
+    const int32_t *seq_lens;
+    int32_t num_seqs;
+    int32_t num_q_heads;
+    int32_t max_seq_len;
+    float scale;
+    int32_t partition_tokens;  // resolved (> 0, multiple of block_size)
+    int32_t num_partitions;    // ceil(max_seq_len / partition_tokens), >= 1
+    float *ws_o;               // [B][Hq][P][d] when num_partitions > 1
+    float *ws_ml;              // [B][Hq][P][2]
+};
+
+// Tokens per pipeline stage of the decode kernel for a block size (the
+// granularity a partition length is rounded to).
+int decode_stage_tokens(int block_size);
+bool decode_supported(int head_dim, int group, int block_size);
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+
+// ---- prefill (pa_prefill.cu) -----------------------------------------------
+struct PrefillArgs {
+    void *out;
+    const void *q;
+    PoolView pool;
+    const int32_t *tables;
+    int32_t max_blocks;
+    const int32_t *ctx_lens;
+    int32_t num_seqs;
+    int32_t chunk_len;
+    int32_t num_q_heads;
+    int32_t max_ctx_len;
+    float scale;
+};
+bool prefill_supported(int head_dim, int group, int block_size);
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,130 @@
+"""The C-ABI library loads, exports every function include/pa.h declares, and
+rejects bad arguments on the host without launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_cache_167_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(B):
+    names = declared_functions()
+    assert len(names) >= 20
+    lib = ctypes.CDLL(B.LIBRARY)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the binding knows a signature for each of them
+    assert set(names) <= set(B.SIGNATURES), set(names) - set(B.SIGNATURES)
+
+
+def test_status_strings(B):
+    for s in range(8):
+        assert B.lib().pa_status_string(s)
+    assert B.lib().pa_status_string(99) == b"unknown status"
+
+
+def _pool(B, base=0x10000, nb=64, hkv=8, b=16, d=128, bstride=0, kvstride=0, dtype=0):
+    return B.PaKvPool(base, nb, hkv, b, d, dtype, bstride, kvstride)
+
+
+def test_host_validation(B):
+    L = B.lib()
+    P = ctypes.c_void_p
+    good = _pool(B)
+    ok_ptr = P(0x20000)
+    args = lambda pool, out=ok_ptr, q=ok_ptr, hq=64, part=0, ws=P(0), wsb=0: (
+        out, q, ctypes.byref(pool), ok_ptr, 8, ok_ptr, 4, hq, 100, 0.1, part, ws, wsb, P(0))
+    assert L.pa_decode(*args(good, out=P(0))) == 1                     # null out
+    assert L.pa_decode(*args(_pool(B, base=0x10001))) == 1              # misaligned pool
+    assert L.pa_decode(*args(_pool(B, d=96))) == 2                      # head_dim not built
+    assert L.pa_decode(*args(_pool(B, dtype=7))) == 2                   # dtype
+    assert L.pa_decode(*args(good, hq=60)) == 1                         # Hq % Hkv
+    assert L.pa_decode(*args(good, hq=8 * 16)) == 2                     # group 16 not built
+    assert L.pa_decode(*args(good, part=24)) == 1                       # partition % b
+    assert L.pa_decode(*args(good, part=16)) == 3                       # workspace missing
+    assert L.pa_decode(*args(_pool(B, kvstride=100))) == 1              # overlapping halves
+    assert L.pa_reshape_and_cache(ctypes.byref(good), P(0), P(0), P(0), 0, P(0)) == 0  # nothing to do
+    assert L.pa_reshape_and_cache(ctypes.byref(good), P(0x20008), ok_ptr, ok_ptr, 4, P(0)) == 1
+    assert L.pa_copy_blocks(ctypes.byref(good), P(0), -1, P(0)) == 1
+    assert L.pa_copy_blocks(ctypes.byref(good), P(0), 0, P(0)) == 0
+    assert L.pa_prefill_chunk(ok_ptr, ok_ptr, ctypes.byref(_pool(B, d=64)), ok_ptr, 8, ok_ptr, 1, 4, 64, 10,
+                              0.1, P(0)) == 2
+    err = ctypes.c_uint32()
+    assert L.pa_get_device_error(None, 0, P(0)) == 1
+
+
+def test_workspace_size(B):
+    L = B.lib()
+    pool = _pool(B, nb=16384)
+    # 64 sequences, 64 q-heads, two 512-token partitions over 851 tokens
+    n = L.pa_decode_workspace_size(ctypes.byref(pool), 64, 64, 851, 512)
+    assert n == 64 * 64 * 2 * 128 * 4 + 64 * 64 * 2 * 2 * 4
+    assert L.pa_decode_workspace_size(ctypes.byref(pool), 64, 64, 512, 512) == 0
+    assert L.pa_decode_partition_tokens(ctypes.byref(pool), 64, 64, 851, 512) == 512
+    auto = L.pa_decode_partition_tokens(ctypes.byref(pool), 64, 64, 851, 0)
+    assert auto > 0 and auto % 16 == 0
+
+
+def test_block_layout_matches_oracle(B):
+    orc = oracle.load()
+    for b in (1, 4, 16, 32):
+        for t in range(0, 300):
+            assert B.block_layout(t, b) == orc.block_layout(t, b)
+    for bad in ((-1, 4), (4, 0)):
+        with pytest.raises(B.PagedAttentionError):
+            B.block_layout(*bad)
+
+
+def test_slot_mapping_matches_oracle(B):
+    import pa_workloads as wl
+    orc = oracle.load()
+    for w in (wl.tiny(), wl.tiny_page_example(), wl.llama70b_decode(), wl.beam_fork()):
+        got = B.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size, w.num_blocks)
+        ref = orc.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size)
+        assert np.array_equal(got, ref), w.name
+    # every position of every sequence of the long-context batch
+    w = wl.long_context()
+    seq = np.repeat(np.arange(w.batch, dtype=np.int32), w.seq_lens)
+    pos = np.concatenate([np.arange(L) for L in w.seq_lens]).astype(np.int64)
+    assert np.array_equal(B.slot_mapping(w.tables, seq, pos, 16, w.num_blocks),
+                          orc.slot_mapping(w.tables, seq, pos, 16))
+    with pytest.raises(B.PagedAttentionError):
+        B.slot_mapping(w.tables, [0], [w.max_blocks * 16], 16, w.num_blocks)   # past the table
+    with pytest.raises(B.PagedAttentionError):
+        B.slot_mapping(np.asarray([[5, 1, 7]]), [0], [9], 4, 7)                # block 7 outside an NB=7 pool
+
+
+def test_product_does_not_touch_the_oracle():
+    """The product package never imports or loads the oracle, and the oracle
+    never imports the product."""
+    pkg = os.path.join(ROOT, "paged_kv_cache_167_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle", text, re.M), f
+                assert "pa_oracle" not in text and "orc_" not in text, f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c")):
+            text = open(os.path.join(ROOT, "oracle", f)).read()
+            assert not re.search(r"^\s*(import|from)\s+paged_kv_cache_167_gb300", text, re.M), f
+            assert "libpa.so" not in text and "pa_decode" not in text, f

@@ -1,0 +1,257 @@
+"""GPU parity of the decode path (slot writer, paged decode, split-context
+reduce, copy-on-write copies) against the oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import pa_workloads as wl
+from tests.parity import Case, assert_close
+
+pytestmark = pytest.mark.gpu
+
+bits = wl.bf16_bits
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_167_gb300 as pa
+    assert torch.cuda.is_available(), "a CUDA device is required"
+    pa.get_device_error(clear=True)
+    return pa
+
+
+def write_new_tokens(pa, c: Case):
+    w = c.w
+    if w.new_positions is None or len(w.new_positions) == 0:
+        return
+    slots = pa.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size, w.num_blocks)
+    oslots = c.orc.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size)
+    assert np.array_equal(slots, oslots), "host slot mapping differs from the oracle"
+    pa.reshape_and_cache(c.pool, c.new_k, c.new_v, torch.as_tensor(slots, device=c.dev))
+    c.orc.reshape_and_cache(c.pool_ref, c.geom, bits(c.cpu["new_k"]), bits(c.cpu["new_v"]), oslots)
+
+
+def run_decode(pa, c: Case, partition_tokens=None):
+    w = c.w
+    part = w.partition_tokens if partition_tokens is None else partition_tokens
+    out = torch.empty_like(c.q)
+    nbytes = pa.decode_workspace_size(c.pool, w.batch, w.num_q_heads, w.max_seq_len, part)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=c.dev) if nbytes else None
+    pa.decode(out, c.q, c.pool, c.tables, c.seq_lens, w.max_seq_len, w.scale, part, ws)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    return out
+
+
+def oracle_decode(c: Case, rows=None):
+    return c.orc.paged_decode(bits(c.cpu["q"]), c.pool_ref, c.geom, c.w.tables, c.w.seq_lens,
+                              c.w.num_q_heads, c.w.scale, rows=rows)
+
+
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_page_example"])
+@pytest.mark.parametrize("part_blocks", [0, 1, 2])
+def test_tiny_configs(pa, name, part_blocks):
+    w = wl.CONFIGS[name]()
+    c = Case(w)
+    write_new_tokens(pa, c)
+    assert np.array_equal(bits(c.pool), c.pool_ref), "slot writer is not bit-exact"
+    out = run_decode(pa, c, part_blocks * w.block_size)
+    assert_close(out, oracle_decode(c), f"{name} part={part_blocks}")
+
+
+def test_page_example_slot(pa):
+    """Token 9 of the page example lands in physical block 7, offset 1."""
+    w = wl.tiny_page_example()
+    c = Case(w)
+    write_new_tokens(pa, c)
+    pool = bits(c.pool)
+    assert np.array_equal(pool[7, 0, :, 1], bits(c.cpu["new_k"])[9])
+    assert np.array_equal(pool[7, 1, :, 1], bits(c.cpu["new_v"])[9])
+
+
+SWEEP_LENS = [1, 3, 16, 17, 63, 64, 65, 200, 331]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+@pytest.mark.parametrize("bs", [4, 8, 16, 32])
+def test_shape_sweep(pa, d, group, bs):
+    hkv = 2
+    w = wl.custom(SWEEP_LENS, hkv * group, hkv, d, bs, seed=1000 + d + group * 10 + bs)
+    c = Case(w)
+    write_new_tokens(pa, c)
+    assert np.array_equal(bits(c.pool), c.pool_ref)
+    ref = oracle_decode(c)
+    for part in (0, bs, 4 * bs, 64 if 64 % bs == 0 else bs):
+        assert_close(run_decode(pa, c, part), ref, f"d={d} G={group} b={bs} part={part}")
+
+
+@pytest.mark.parametrize("name,sample", [("llama70b_decode", None), ("long_context", None),
+                                         ("shared_prefix", 2048), ("beam_fork", 2048)])
+def test_full_size(pa, name, sample):
+    """BASELINE-sized workloads in the launch configuration the bench times."""
+    w = wl.CONFIGS[name]()
+    c = Case(w)
+    if w.copy_pairs is not None and len(w.copy_pairs):
+        pa.copy_blocks(c.pool, torch.as_tensor(w.copy_pairs, device=c.dev))
+        c.orc.copy_blocks(c.pool_ref, c.geom, w.copy_pairs)
+    write_new_tokens(pa, c)
+    assert np.array_equal(bits(c.pool), c.pool_ref), "pool after copies and writes is not bit-exact"
+    out = run_decode(pa, c)
+    if sample is None:
+        assert_close(out, oracle_decode(c), name)
+    else:
+        rng = np.random.default_rng(5)
+        flat = rng.choice(w.batch * w.num_q_heads, size=sample, replace=False)
+        rows = np.stack([flat // w.num_q_heads, flat % w.num_q_heads], axis=1)
+        ref = oracle_decode(c, rows)
+        assert_close(out[rows[:, 0], rows[:, 1]], ref, name)
+
+
+def test_partitions_agree(pa):
+    """P = 1 and many partitions both match the oracle on the same inputs."""
+    w = wl.llama70b_decode(batch=16)
+    c = Case(w)
+    write_new_tokens(pa, c)
+    ref = oracle_decode(c)
+    outs = [run_decode(pa, c, part) for part in (16, 64, 256, 1024)]
+    for part, o in zip((16, 64, 256, 1024), outs):
+        assert_close(o, ref, f"part={part}")
+
+
+def _move_blocks(c: Case, rng):
+    """Same logical content under a new random placement (test-side)."""
+    w = c.w
+    perm = rng.permutation(w.num_blocks).astype(np.int32)
+    tables2 = np.where(w.tables >= 0, perm[np.maximum(w.tables, 0)], -1).astype(np.int32)
+    pool2 = torch.zeros_like(c.pool)
+    valid = w.tables >= 0
+    src = torch.as_tensor(w.tables[valid].astype(np.int64), device=c.dev)
+    dst = torch.as_tensor(tables2[valid].astype(np.int64), device=c.dev)
+    pool2[dst] = c.pool[src]
+    return tables2, pool2
+
+
+def test_placement_invariance(pa):
+    """Permuting physical placement leaves the output bit-identical."""
+    w = wl.custom([5, 40, 333, 700, 1], 64, 8, 128, 16, num_blocks=512)
+    c = Case(w)
+    out1 = run_decode(pa, c, 64)
+    tables2, pool2 = _move_blocks(c, np.random.default_rng(3))
+    c.pool, c.tables = pool2, torch.as_tensor(tables2, device=c.dev)
+    out2 = run_decode(pa, c, 64)
+    assert torch.equal(out1, out2)
+
+
+def test_shared_prefix_equals_private_copies(pa):
+    w = wl.shared_prefix(batch=8)
+    c = Case(w)
+    out_shared = run_decode(pa, c)
+    # give every sequence private copies of the shared prefix blocks
+    shared = w.notes["shared_ids"]
+    used = set(np.unique(w.tables[w.tables >= 0]).tolist())
+    free = [i for i in range(w.num_blocks) if i not in used]
+    tables = w.tables.copy()
+    pool = c.pool.clone()
+    k = 0
+    for s in range(1, w.batch):
+        fresh = np.asarray(free[k:k + len(shared)], np.int32)
+        k += len(shared)
+        pool[torch.as_tensor(fresh, device=c.dev).long()] = c.pool[torch.as_tensor(shared, device=c.dev).long()]
+        tables[s, :len(shared)] = fresh
+    c.pool, c.tables = pool, torch.as_tensor(tables, device=c.dev)
+    out_private = run_decode(pa, c)
+    assert torch.equal(out_shared, out_private)
+
+
+def test_empty_sequences_and_junk_tails(pa):
+    """seq_len 0 gives zeros; NaN junk in unused tail slots is never used."""
+    w = wl.custom([0, 5, 0, 17, 33, 1], 8, 2, 128, 16, num_blocks=64)
+    c = Case(w)
+    nan = torch.full((w.head_dim,), float("nan"), dtype=torch.bfloat16, device=c.dev)
+    for s, L in enumerate(w.seq_lens):
+        if L % w.block_size:
+            blk = int(w.tables[s, (L - 1) // w.block_size])
+            c.pool[blk, :, :, L % w.block_size:, :] = nan
+    for part in (0, 16):
+        out = run_decode(pa, c, part)
+        assert not torch.isnan(out).any()
+        assert torch.count_nonzero(out[0]) == 0 and torch.count_nonzero(out[2]) == 0
+        ref = oracle_decode(c)
+        assert_close(out, ref, f"part={part}")
+
+
+def test_layered_pool(pa):
+    """The pages' layered pool shape [NB][2][L][Hkv][b][d], read one layer at a time."""
+    w = wl.custom([20, 77, 130], 16, 4, 64, 16, num_blocks=40)
+    layers = 3
+    gen = torch.Generator(device="cpu").manual_seed(4)
+    pool6 = wl.randn_bf16((w.num_blocks, 2, layers, w.num_kv_heads, w.block_size, w.head_dim), gen)
+    q = wl.randn_bf16((w.batch, w.num_q_heads, w.head_dim), gen)
+    dev = torch.device("cuda")
+    pool6_d, q_d = pool6.to(dev), q.to(dev)
+    tables, lens = torch.as_tensor(w.tables, device=dev), torch.as_tensor(w.seq_lens, device=dev)
+    import oracle
+    orc = oracle.load()
+    geom = oracle.dense_geom(w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim, num_layers=layers)
+    flat = bits(pool6).reshape(-1)
+    slab = w.num_kv_heads * w.block_size * w.head_dim
+    for layer in range(layers):
+        out = torch.empty_like(q_d)
+        nbytes = pa.decode_workspace_size(pool6_d, w.batch, w.num_q_heads, w.max_seq_len, 32, layer=layer)
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+        pa.decode(out, q_d, pool6_d, tables, lens, w.max_seq_len, w.scale, 32, ws, layer=layer)
+        ref = orc.paged_decode(bits(q), flat[layer * slab:], geom, w.tables, w.seq_lens, w.num_q_heads, w.scale)
+        assert_close(out, ref, f"layer {layer}")
+    # copy-on-write copies through a layer view touch only that layer
+    pairs = np.asarray([[int(w.tables[0, 0]), 39]], np.int32)
+    before = bits(pool6_d).copy()
+    pa.copy_blocks(pool6_d, torch.as_tensor(pairs, device=dev), layer=1)
+    ref = before.reshape(-1).copy()
+    orc.copy_blocks(ref[slab:], geom, pairs)
+    assert np.array_equal(bits(pool6_d).reshape(-1), ref)
+
+
+def test_copy_blocks_bit_exact(pa):
+    w = wl.custom([100, 60], 8, 8, 128, 16, num_blocks=64)
+    c = Case(w)
+    pairs = np.asarray([[int(w.tables[0, 0]), 50], [int(w.tables[1, 3]), 51], [int(w.tables[0, 6]), 63]], np.int32)
+    pa.copy_blocks(c.pool, torch.as_tensor(pairs, device=c.dev))
+    c.orc.copy_blocks(c.pool_ref, c.geom, pairs)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(c.pool), c.pool_ref)
+    assert pa.get_device_error() == 0
+
+
+def test_device_errors_are_reported_not_faulted(pa):
+    """Out-of-range table entries, slots, pairs and lengths set error bits and
+    are never dereferenced; the context stays usable."""
+    from paged_kv_cache_167_gb300 import binding as B
+    w = wl.custom([40, 9], 8, 2, 64, 16, num_blocks=16)
+    c = Case(w)
+    pa.get_device_error(clear=True)
+    bad_tables = c.tables.clone()
+    bad_tables[0, 1] = w.num_blocks + 5
+    c_tables = c.tables
+    c.tables = bad_tables
+    out = torch.empty_like(c.q)
+    pa.decode(out, c.q, c.pool, c.tables, c.seq_lens, w.max_seq_len, w.scale, 0, None)
+    assert pa.get_device_error() & B.DEVERR_BLOCK_ID
+    c.tables = c_tables
+    slots = torch.as_tensor([w.num_blocks * w.block_size + 3, -1], device=c.dev, dtype=torch.int64)
+    before = c.pool.clone()
+    pa.reshape_and_cache(c.pool, c.new_k[:2], c.new_v[:2], slots)
+    assert pa.get_device_error() & B.DEVERR_SLOT
+    assert torch.equal(before, c.pool)
+    pa.copy_blocks(c.pool, torch.as_tensor([[0, w.num_blocks]], device=c.dev, dtype=torch.int32))
+    assert pa.get_device_error() & B.DEVERR_BLOCK_ID
+    assert torch.equal(before, c.pool)
+    long_lens = torch.as_tensor([w.max_blocks * w.block_size + 1, 9], device=c.dev, dtype=torch.int32)
+    pa.decode(out, c.q, c.pool, c.tables, long_lens, w.max_seq_len, w.scale, 0, None)
+    assert pa.get_device_error() & B.DEVERR_SEQ_LEN
+    # still healthy afterwards
+    assert_close(run_decode(pa, c, 0), oracle_decode(c), "after errors")
