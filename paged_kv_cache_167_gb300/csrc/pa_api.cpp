@@ -14,7 +14,10 @@ cudaError_t launch_decode_d128(const DecodeArgs &a, cudaStream_t stream);
 
 namespace {
 
-constexpr int kDecodeWarps = 4;          // warps per decode CTA (must match the kernel)
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 4
+#endif
+constexpr int kDecodeWarps = PA_DECODE_WARPS;  // warps per decode CTA (must match the kernel)
 constexpr int kAutoCtasPerSm = 2;        // resident decode CTAs per SM
 constexpr int kAutoWaves = 4;            // CTAs per resident slot the auto partition aims for
 constexpr int kAutoMaxPartition = 1024;  // cap so long sequences still spread over SMs

@@ -28,6 +28,23 @@ std::mutex g_mutex;
 unsigned int *g_error_ptr[kMaxDevices];
 int g_sm_count[kMaxDevices];
 
+// Launch with programmatic stream serialisation: the kernel's launch overlaps
+// the previous kernel's tail; its griddepcontrol.wait orders the data.
+template <typename Kernel, typename Arg>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, cudaStream_t stream, const Arg &arg) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
+
 int current_device() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
@@ -53,6 +70,7 @@ struct CacheParams {
 
 // One thread per 16-B vector of a (token, K/V, head) row.
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // inputs may come from the previous kernel
     const int64_t per_token = 2ll * p.num_kv_heads * p.row_vecs;
     const int64_t total = p.num_tokens * per_token;
     const int64_t slot_limit = p.num_blocks * p.block_size;
@@ -94,6 +112,7 @@ struct CopyParams {
 
 // grid (num_pairs, 2): one CTA per (pair, K/V half); the half is contiguous.
 __global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int pair = blockIdx.x, kv = blockIdx.y;
     const int32_t src = __ldg(p.pairs + 2 * pair), dst = __ldg(p.pairs + 2 * pair + 1);
     if (src < 0 || src >= p.num_blocks || dst < 0 || dst >= p.num_blocks) {
@@ -163,8 +182,7 @@ cudaError_t launch_reshape_and_cache(const PoolView &pool, const void *k, const 
     const int64_t max_blocks = (int64_t)device_sm_count() * 8;
     int64_t blocks = (total + threads - 1) / threads;
     if (max_blocks > 0 && blocks > max_blocks) blocks = max_blocks;
-    reshape_and_cache_kernel<<<(unsigned)blocks, threads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(reshape_and_cache_kernel, dim3((unsigned)blocks), dim3(threads), stream, p);
 }
 
 cudaError_t launch_copy_blocks(const PoolView &pool, const int32_t *pairs, int32_t num_pairs,
@@ -181,8 +199,7 @@ cudaError_t launch_copy_blocks(const PoolView &pool, const int32_t *pairs, int32
     p.pairs = pairs;
     p.num_pairs = num_pairs;
     p.err = err;
-    copy_blocks_kernel<<<dim3(num_pairs, 2), 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(copy_blocks_kernel, dim3(num_pairs, 2), dim3(256), stream, p);
 }
 
 }  // namespace pa

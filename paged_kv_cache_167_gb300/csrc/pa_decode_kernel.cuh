@@ -10,11 +10,11 @@
 // the kernel's inner loop); auto-20261007-1900-en (lihaoran.work), "A block
 // table maps logical order to physical storage".
 //
-// Design (one GB300 SM runs two 4-warp CTAs):
+// Design:
 //  * grid (partition, kv-head, sequence); a partition is a run of
 //    partition_tokens context positions of one (sequence, kv-head).
 //  * Each warp owns every W-th pipeline stage of the partition and a private
-//    ring of kStages shared-memory slots.  A stage is 16 token slots (one
+//    ring of STAGES shared-memory slots.  A stage is 16 token slots (one
 //    16-token block, or several smaller blocks).  Lane 0 fetches a stage's K
 //    and V slabs (b*d bf16 each, contiguous in the pool) with bulk TMA copies
 //    that complete on the slot's mbarrier; block ids come from a per-warp
@@ -22,23 +22,28 @@
 //    dependent table load.  No data is multicast.
 //  * All G query heads of the group are served from one staged copy of the
 //    block.  A lane owns 8 of the d dimensions of one token row (16 B) and
-//    keeps q for all G heads on those dimensions in registers (pre-scaled by
-//    scale * log2 e), so each K element is widened once and used G times.
-//    Partial dot products are combined across the row's lanes with a
-//    transposing butterfly: at each shuffle step a lane keeps half of its
-//    head values and receives the other half from its partner, so G heads
-//    over 16 lanes cost 8 shuffles per token instead of 32.  Query slots are
-//    stored in a lane-dependent order (slot j holds head j ^ hl) which makes
-//    every register index of that butterfly static.
-//  * Online softmax in the log2 domain per warp; probabilities and the
-//    running-max correction are broadcast through shared memory; P.V
-//    accumulates fp32 pairs with packed f32x2 FMAs.
+//    keeps q for all G heads on those dimensions in registers, pre-scaled by
+//    scale * log2 e and packed as head pairs, so one packed f32x2 FMA
+//    advances two heads' dot products.  Partial dot products are combined
+//    across the row's lanes with a transposing butterfly: at each shuffle step
+//    a lane keeps half of its head values and receives the other half from its
+//    partner (8 shuffles per token for 8 heads over 16 lanes instead of 32).
+//    Query slots are stored in a lane-dependent order (slot j holds head
+//    j ^ hl) which makes every register index of that butterfly static.
+//  * Online softmax in the log2 domain per warp.  Probabilities and the
+//    running-max correction are broadcast through shared memory, stored
+//    duplicated so each is a ready f32x2 operand; P.V accumulates with packed
+//    f32x2 FMAs; the correction multiply is skipped when no head's running
+//    maximum moved.
 //  * At the end the warps' (m, l, o) are merged in shared memory.  With one
 //    partition the CTA writes bf16 output; otherwise it writes fp32 partials
 //    (o normalised by l, m, l) and the reduce kernel merges partitions.
 //  * Every table entry and length is bounds-checked; an out-of-range value is
 //    reported in the error word and never dereferenced.  Every barrier wait
 //    is bounded.
+//  * Launched with programmatic stream serialisation: set-up that reads no
+//    global memory overlaps the previous kernel's tail, and every global read
+//    waits on griddepcontrol.wait.
 #pragma once
 
 #include <cfloat>
@@ -47,11 +52,22 @@
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 3
+#endif
+#ifndef PA_DECODE_MIN_CTAS
+#define PA_DECODE_MIN_CTAS 2
+#endif
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 4
+#endif
+
 namespace pa {
 namespace decode {
 
-constexpr int kWarps = 4;
-constexpr int kStages = 3;   // ring depth per warp
+constexpr int kWarps = PA_DECODE_WARPS;        // warps per CTA, each owning every kWarps-th stage
+constexpr int kStages = PA_DECODE_STAGES;      // ring depth per warp
+constexpr int kMinCtas = PA_DECODE_MIN_CTAS;   // resident CTAs per SM the register budget targets
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
@@ -67,6 +83,7 @@ struct Shape {
     static constexpr int LOG_LPR = ilog2(LPR);
     static constexpr int NT = ilog2(G);               // transposing butterfly steps
     static constexpr int DUP = LPR / G;               // lanes holding the same head's score
+    static constexpr int QS = G >= 2 ? G / 2 : 4;     // q register pairs: head pairs, or dim pairs if G == 1
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group");
     static_assert(TPS % TPI == 0 && TPS % BS == 0, "stage shape");
@@ -78,8 +95,8 @@ struct alignas(16) WarpSmem {
     using S = Shape<D, G, BS>;
     __nv_bfloat16 k[kStages][S::TPS * D];
     __nv_bfloat16 v[kStages][S::TPS * D];
-    float p[S::TPS][G < 4 ? 4 : G];    // probabilities by (token, head)
-    float alpha[G < 4 ? 4 : G];        // running-max correction by head
+    float2 p[S::TPS][G < 2 ? 2 : G];   // (p, p) by (token, head)
+    float2 alpha[G < 2 ? 2 : G];       // (a, a) running-max correction by head
     uint64_t bar[kStages + (kStages & 1)];
 };
 
@@ -103,6 +120,9 @@ struct Params {
     unsigned int *err;
 };
 
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // Length actually processed for a sequence: negative lengths count as 0 and
 // lengths beyond the table or the host bound are clipped (both reported).
 __device__ __forceinline__ int effective_len(const Params &p, int s, int block_size, bool report) {
@@ -117,14 +137,71 @@ __device__ __forceinline__ int effective_len(const Params &p, int s, int block_s
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+
+__device__ __forceinline__ float2 shfl_xor2(float2 v, int dist) {
+    return make_float2(__shfl_xor_sync(0xffffffffu, v.x, dist), __shfl_xor_sync(0xffffffffu, v.y, dist));
+}
+
+// Score of head hl for the token row at `krow` (this lane's 8 dims), summed
+// over the row's LPR lanes.
+template <int D, int G, int BS>
+__device__ __forceinline__ float qk_score(const float2 (&q2)[Shape<D, G, BS>::QS][8], const uint4 kw) {
+    using S = Shape<D, G, BS>;
+    const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
+    float s;
+    if constexpr (G >= 2) {
+        // dims duplicated into both halves: q2[p][i] = (q[2p^hl][i], q[(2p+1)^hl][i])
+        float2 kd[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float lo = __uint_as_float(w4[c] << 16), hi = __uint_as_float(w4[c] & 0xffff0000u);
+            kd[2 * c] = make_float2(lo, lo);
+            kd[2 * c + 1] = make_float2(hi, hi);
+        }
+        float2 acc[S::QS];
+#pragma unroll
+        for (int pp = 0; pp < S::QS; ++pp) {
+            acc[pp] = fmul2(q2[pp][0], kd[0]);
+#pragma unroll
+            for (int i = 1; i < 8; ++i) acc[pp] = ffma2(q2[pp][i], kd[i], acc[pp]);
+        }
+        // pair steps: halve the head-pair set
+#pragma unroll
+        for (int st = 0; st < S::NT - 1; ++st) {
+            const int half = S::QS >> (st + 1);
+            const int dist = S::LPR >> (st + 1);
+#pragma unroll
+            for (int pp = 0; pp < half; ++pp) acc[pp] = fadd2(acc[pp], shfl_xor2(acc[pp + half], dist));
+        }
+        // split step: keep .x, take the partner's .y
+        s = acc[0].x + __shfl_xor_sync(0xffffffffu, acc[0].y, S::LPR >> S::NT);
+    } else {
+        // one head: q2[c] holds dim pairs; fold the pair, then reduce
+        float2 a = fmul2(q2[0][0], bf16x2_to_float2(w4[0]));
+#pragma unroll
+        for (int c = 1; c < 4; ++c) a = ffma2(q2[c][0], bf16x2_to_float2(w4[c]), a);
+        s = a.x + a.y;
+    }
+#pragma unroll
+    for (int dist = S::LPR >> (S::NT + 1); dist >= 1; dist >>= 1) s += __shfl_xor_sync(0xffffffffu, s, dist);
+    return s;
+}
 
 template <int D, int G, int BS>
-__global__ void __launch_bounds__(kWarps * 32, 2) paged_decode_kernel(const Params p) {
+__global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(const Params p) {
     using S = Shape<D, G, BS>;
     using WS = WarpSmem<D, G, BS>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     WS *ws = reinterpret_cast<WS *>(smem_raw) + warp;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int st = 0; st < kStages; ++st) mbar_init(&ws->bar[st], 1);
+        fence_barrier_init();
+    }
+    grid_dependency_wait();   // inputs may come from the previous kernel in the stream
 
     const int part = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
     const int L = effective_len(p, s, BS, part == 0 && g == 0 && threadIdx.x == 0);
@@ -147,23 +224,27 @@ __global__ void __launch_bounds__(kWarps * 32, 2) paged_decode_kernel(const Para
     const int tsub = lane / S::LPR;                       // token within a warp iteration
     const int hl = row >> (S::LOG_LPR - S::NT);           // head whose score this lane ends with
 
-    // q for all G heads on this lane's dims, slot j holding head j ^ hl.
-    float2 q2[G][4];
+    // q on this lane's dims, pre-scaled; slot j holds head j ^ hl
+    float2 q2[S::QS][8];
 #pragma unroll
     for (int j = 0; j < G; ++j) {
         const uint4 w = __ldg(reinterpret_cast<const uint4 *>(p.q + (head0 + (j ^ hl)) * D + row * 8));
-        const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const float2 f = bf16x2_to_float2(ws4[c]);
-            q2[j][c] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+            const float2 f = bf16x2_to_float2(w4[c]);
+            if constexpr (G >= 2) {
+                if ((j & 1) == 0) {
+                    q2[j / 2][2 * c].x = f.x * p.scale_log2;
+                    q2[j / 2][2 * c + 1].x = f.y * p.scale_log2;
+                } else {
+                    q2[j / 2][2 * c].y = f.x * p.scale_log2;
+                    q2[j / 2][2 * c + 1].y = f.y * p.scale_log2;
+                }
+            } else {
+                q2[c][0] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+            }
         }
-    }
-
-    if (lane == 0) {
-#pragma unroll
-        for (int st = 0; st < kStages; ++st) mbar_init(&ws->bar[st], 1);
-        fence_barrier_init();
     }
     __syncwarp();
 
@@ -245,35 +326,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2) paged_decode_kernel(const Para
         const __nv_bfloat16 *ks = ws->k[slot];
         const __nv_bfloat16 *vs = ws->v[slot];
 
-        // ---- scores: q . K for all G heads, one token per (iteration, tsub)
+        // ---- scores for head hl, one token per (iteration, tsub)
         float sc[S::ITERS];
 #pragma unroll
         for (int it = 0; it < S::ITERS; ++it) {
             const int t = it * S::TPI + tsub;
             const uint4 kw = *reinterpret_cast<const uint4 *>(ks + t * D + row * 8);
-            const float2 k2[4] = {bf16x2_to_float2(kw.x), bf16x2_to_float2(kw.y), bf16x2_to_float2(kw.z),
-                                  bf16x2_to_float2(kw.w)};
-            float acc[G];
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-                float2 a = fmul2(q2[j][0], k2[0]);
-                a = ffma2(q2[j][1], k2[1], a);
-                a = ffma2(q2[j][2], k2[2], a);
-                a = ffma2(q2[j][3], k2[3], a);
-                acc[j] = a.x + a.y;
-            }
-            // transposing butterfly: halve the head set at each step
-#pragma unroll
-            for (int st = 0; st < S::NT; ++st) {
-                const int half = G >> (st + 1);
-                const int dist = S::LPR >> (st + 1);
-#pragma unroll
-                for (int j = 0; j < half; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j + half], dist);
-            }
-#pragma unroll
-            for (int dist = S::LPR >> (S::NT + 1); dist >= 1; dist >>= 1)
-                acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], dist);
-            sc[it] = acc[0];
+            sc[it] = qk_score<D, G, BS>(q2, kw);
             if (tail && tok0 + t >= tok_end) sc[it] = -INFINITY;
         }
 
@@ -293,21 +352,23 @@ __global__ void __launch_bounds__(kWarps * 32, 2) paged_decode_kernel(const Para
             psum += sc[it];
         }
         l_run = l_run * alpha + psum;
+        const bool moved = m_new != m_run;
         m_run = m_new;
         if ((row & (S::DUP - 1)) == 0) {
 #pragma unroll
-            for (int it = 0; it < S::ITERS; ++it) ws->p[it * S::TPI + tsub][hl] = sc[it];
-            if (tsub == 0) ws->alpha[hl] = alpha;
+            for (int it = 0; it < S::ITERS; ++it) ws->p[it * S::TPI + tsub][hl] = make_float2(sc[it], sc[it]);
+            if (tsub == 0) ws->alpha[hl] = make_float2(alpha, alpha);
         }
         __syncwarp();
 
-        // ---- rescale and accumulate P . V
+        // ---- rescale (only if some head's maximum moved) and accumulate P . V
+        if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float a = ws->alpha[h];
-            const float2 a2 = make_float2(a, a);
+            for (int h = 0; h < G; ++h) {
+                const float2 a2 = ws->alpha[h];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) o2[h][c] = fmul2(o2[h][c], a2);
+                for (int c = 0; c < 4; ++c) o2[h][c] = fmul2(o2[h][c], a2);
+            }
         }
 #pragma unroll
         for (int it = 0; it < S::ITERS; ++it) {
@@ -321,8 +382,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) paged_decode_kernel(const Para
             }
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const float ph = ws->p[t][h];
-                const float2 p2 = make_float2(ph, ph);
+                const float2 p2 = ws->p[t][h];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) o2[h][c] = ffma2(p2, v2[c], o2[h][c]);
             }
@@ -345,10 +405,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) paged_decode_kernel(const Para
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                o2[h][c].x += __shfl_xor_sync(0xffffffffu, o2[h][c].x, dist);
-                o2[h][c].y += __shfl_xor_sync(0xffffffffu, o2[h][c].y, dist);
-            }
+            for (int c = 0; c < 4; ++c) o2[h][c] = fadd2(o2[h][c], shfl_xor2(o2[h][c], dist));
         l_run += __shfl_xor_sync(0xffffffffu, l_run, dist);
     }
 
@@ -369,6 +426,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) paged_decode_kernel(const Para
         }
     }
     __syncthreads();
+    grid_launch_dependents();
 
     for (int idx = threadIdx.x; idx < G * D / 2; idx += blockDim.x) {
         const int h = idx / (D / 2);
@@ -398,30 +456,54 @@ __global__ void __launch_bounds__(kWarps * 32, 2) paged_decode_kernel(const Para
     }
 }
 
-// Merge the partitions of one (sequence, q-head): weights l_p * 2^(m_p - M).
-// grid (Hq, B), D/2 threads, two dims each.
-template <int D, int BS>
-__global__ void __launch_bounds__(D / 2) paged_decode_reduce_kernel(const Params p) {
-    const int h = blockIdx.x, s = blockIdx.y;
+// Merge the partitions of the G query heads of one (sequence, kv-head):
+// weights l_p * 2^(m_p - M).  grid (Hkv, B), G * D / 4 threads, 4 dims each.
+template <int D, int G, int BS>
+__global__ void __launch_bounds__(G *D / 4) paged_decode_reduce_kernel(const Params p) {
+    grid_dependency_wait();   // partials come from the partition kernel
+    const int g = blockIdx.x, s = blockIdx.y;
+    const int h = threadIdx.x / (D / 4);
+    const int i = (threadIdx.x % (D / 4)) * 4;
     const int L = effective_len(p, s, BS, false);
     const int np = (L + p.part_tokens - 1) / p.part_tokens;
-    const size_t row = (size_t)s * p.num_q_heads + h;
-    const int i = threadIdx.x * 2;
-    const float *ml = p.ws_ml + row * p.num_parts * 2;
+    const size_t row = (size_t)s * p.num_q_heads + (size_t)g * G + h;
+    const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + row * p.num_parts;
     float M = -INFINITY;
-    for (int q = 0; q < np; ++q) M = fmaxf(M, ml[2 * q]);
-    float wsum = 0.f, ox = 0.f, oy = 0.f;
+    for (int q = 0; q < np; ++q) M = fmaxf(M, ml[q].x);
+    float wsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
         for (int q = 0; q < np; ++q) {
-            const float w = ml[2 * q + 1] * fast_exp2(ml[2 * q] - M);
-            const float2 o = *reinterpret_cast<const float2 *>(p.ws_o + (row * p.num_parts + q) * D + i);
+            const float2 mlq = ml[q];
+            const float w = mlq.y * fast_exp2(mlq.x - M);
+            const float4 o = *reinterpret_cast<const float4 *>(p.ws_o + (row * p.num_parts + q) * D + i);
             wsum += w;
-            ox += w * o.x;
-            oy += w * o.y;
+            acc.x += w * o.x;
+            acc.y += w * o.y;
+            acc.z += w * o.z;
+            acc.w += w * o.w;
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    reinterpret_cast<uint32_t *>(p.out + row * D + i)[0] = pack_bf16x2(ox * inv, oy * inv);
+    uint2 packed = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    *reinterpret_cast<uint2 *>(p.out + row * D + i) = packed;
+}
+
+// Launch with programmatic stream serialisation (the kernel waits on
+// griddepcontrol.wait before touching global memory).
+template <typename Kernel>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Params &prm) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, prm);
 }
 
 template <int D, int G, int BS>
@@ -438,12 +520,11 @@ cudaError_t launch_shape(const Params &prm, int num_kv_heads, int num_seqs, cuda
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    dim3 grid(prm.num_parts, num_kv_heads, num_seqs);
-    paged_decode_kernel<D, G, BS><<<grid, kWarps * 32, smem, stream>>>(prm);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(paged_decode_kernel<D, G, BS>, dim3(prm.num_parts, num_kv_heads, num_seqs),
+                               dim3(kWarps * 32), smem, stream, prm);
     if (e != cudaSuccess || prm.num_parts == 1) return e;
-    paged_decode_reduce_kernel<D, BS><<<dim3(prm.num_q_heads, num_seqs), D / 2, 0, stream>>>(prm);
-    return cudaGetLastError();
+    return launch_pdl(paged_decode_reduce_kernel<D, G, BS>, dim3(num_kv_heads, num_seqs), dim3(G * D / 4), 0,
+                      stream, prm);
 }
 
 template <int D, int G>
