@@ -84,10 +84,15 @@ struct Shape {
     static constexpr int NT = ilog2(G);               // transposing butterfly steps
     static constexpr int DUP = LPR / G;               // lanes holding the same head's score
     static constexpr int QS = G >= 2 ? G / 2 : 4;     // q register pairs: head pairs, or dim pairs if G == 1
+    // Two token rows are reduced jointly when a row's lanes number exactly 2G:
+    // the butterfly then ends with every lane owning one (row, head) score.
+    static constexpr bool JOINT = LPR == 2 * G;
+    static constexpr int QK_ITERS = JOINT ? TPS / (2 * TPI) : ITERS;
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group");
     static_assert(TPS % TPI == 0 && TPS % BS == 0, "stage shape");
     static_assert(BPS <= 32, "table cache");
+    static_assert(!JOINT || TPS % (2 * TPI) == 0, "joint rows");
 };
 
 template <int D, int G, int BS>
@@ -188,6 +193,51 @@ __device__ __forceinline__ float qk_score(const float2 (&q2)[Shape<D, G, BS>::QS
     return s;
 }
 
+// Joint scores of two token rows (own = this lane's row, other = the row its
+// partners own) for all G heads, reduced over the row's 2G lanes.  Slot j of a
+// lane holds value j ^ rl (value = row * G + head, rl = lane % LPR), so each
+// butterfly step keeps half of the slots and receives the other half from
+// its partner; the lane ends with the score of (row rl / G, head rl % G).
+template <int D, int G, int BS>
+__device__ __forceinline__ float qk_score_joint(const float2 (&q2)[Shape<D, G, BS>::QS][8], const uint4 kown,
+                                                const uint4 koth) {
+    using S = Shape<D, G, BS>;
+    static_assert(S::JOINT, "joint rows");
+    float2 ko[8], kt[8];
+    const uint32_t wo[4] = {kown.x, kown.y, kown.z, kown.w};
+    const uint32_t wt[4] = {koth.x, koth.y, koth.z, koth.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        // each dim duplicated into both halves of a pair, built by two different
+        // ops so no register move is needed
+        ko[2 * c] = make_float2(__uint_as_float(wo[c] << 16), __uint_as_float(__byte_perm(wo[c], 0u, 0x1044)));
+        ko[2 * c + 1] = make_float2(__uint_as_float(wo[c] & 0xffff0000u), __uint_as_float(__byte_perm(wo[c], 0u, 0x3244)));
+        kt[2 * c] = make_float2(__uint_as_float(wt[c] << 16), __uint_as_float(__byte_perm(wt[c], 0u, 0x1044)));
+        kt[2 * c + 1] = make_float2(__uint_as_float(wt[c] & 0xffff0000u), __uint_as_float(__byte_perm(wt[c], 0u, 0x3244)));
+    }
+    float2 acc[G];
+#pragma unroll
+    for (int pp = 0; pp < G / 2; ++pp) {
+        acc[pp] = fmul2(q2[pp][0], ko[0]);
+        acc[pp + G / 2] = fmul2(q2[pp][0], kt[0]);
+    }
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+#pragma unroll
+        for (int pp = 0; pp < G / 2; ++pp) {
+            acc[pp] = ffma2(q2[pp][i], ko[i], acc[pp]);
+            acc[pp + G / 2] = ffma2(q2[pp][i], kt[i], acc[pp + G / 2]);
+        }
+#pragma unroll
+    for (int st = 0; st < S::NT; ++st) {
+        const int half = G >> (st + 1);
+        const int dist = S::LPR >> (st + 1);
+#pragma unroll
+        for (int pp = 0; pp < half; ++pp) acc[pp] = fadd2(acc[pp], shfl_xor2(acc[pp + half], dist));
+    }
+    return acc[0].x + __shfl_xor_sync(0xffffffffu, acc[0].y, 1);
+}
+
 template <int D, int G, int BS>
 __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(const Params p) {
     using S = Shape<D, G, BS>;
@@ -222,7 +272,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
 
     const int row = lane % S::LPR;                        // this lane's 8-dim chunk of a token row
     const int tsub = lane / S::LPR;                       // token within a warp iteration
-    const int hl = row >> (S::LOG_LPR - S::NT);           // head whose score this lane ends with
+    // head whose score this lane ends with, and (joint rows) which of the two rows
+    const int hl = S::JOINT ? (row & (G - 1)) : (row >> (S::LOG_LPR - S::NT));
+    const int rsel = S::JOINT ? (row >> S::NT) : 0;
 
     // q on this lane's dims, pre-scaled; slot j holds head j ^ hl
     float2 q2[S::QS][8];
@@ -326,20 +378,30 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
         const __nv_bfloat16 *ks = ws->k[slot];
         const __nv_bfloat16 *vs = ws->v[slot];
 
-        // ---- scores for head hl, one token per (iteration, tsub)
-        float sc[S::ITERS];
+        // ---- scores for head hl
+        float sc[S::QK_ITERS];
 #pragma unroll
-        for (int it = 0; it < S::ITERS; ++it) {
-            const int t = it * S::TPI + tsub;
-            const uint4 kw = *reinterpret_cast<const uint4 *>(ks + t * D + row * 8);
-            sc[it] = qk_score<D, G, BS>(q2, kw);
+        for (int it = 0; it < S::QK_ITERS; ++it) {
+            int t;
+            if constexpr (S::JOINT) {
+                const int t0 = it * 2 * S::TPI + tsub * 2;   // rows t0 (0) and t0 + 1 (1)
+                t = t0 + rsel;
+                const uint4 kown = *reinterpret_cast<const uint4 *>(ks + t * D + row * 8);
+                const uint4 koth = *reinterpret_cast<const uint4 *>(ks + (t0 + 1 - rsel) * D + row * 8);
+                sc[it] = qk_score_joint<D, G, BS>(q2, kown, koth);
+            } else {
+                t = it * S::TPI + tsub;
+                const uint4 kw = *reinterpret_cast<const uint4 *>(ks + t * D + row * 8);
+                sc[it] = qk_score<D, G, BS>(q2, kw);
+            }
             if (tail && tok0 + t >= tok_end) sc[it] = -INFINITY;
         }
 
         // ---- online softmax for head hl over this stage
         float mb = sc[0];
 #pragma unroll
-        for (int it = 1; it < S::ITERS; ++it) mb = fmaxf(mb, sc[it]);
+        for (int it = 1; it < S::QK_ITERS; ++it) mb = fmaxf(mb, sc[it]);
+        if constexpr (S::JOINT) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, G));
 #pragma unroll
         for (int dist = S::LPR; dist < 32; dist <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, dist));
         const float m_new = fmaxf(m_run, mb);
@@ -347,14 +409,19 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
         const float alpha = fast_exp2(m_run - m_use);
         float psum = 0.f;
 #pragma unroll
-        for (int it = 0; it < S::ITERS; ++it) {
+        for (int it = 0; it < S::QK_ITERS; ++it) {
             sc[it] = fast_exp2(sc[it] - m_use);
             psum += sc[it];
         }
         l_run = l_run * alpha + psum;
         const bool moved = m_new != m_run;
         m_run = m_new;
-        if ((row & (S::DUP - 1)) == 0) {
+        if constexpr (S::JOINT) {
+#pragma unroll
+            for (int it = 0; it < S::QK_ITERS; ++it)
+                ws->p[it * 2 * S::TPI + tsub * 2 + rsel][hl] = make_float2(sc[it], sc[it]);
+            if (tsub == 0 && rsel == 0) ws->alpha[hl] = make_float2(alpha, alpha);
+        } else if ((row & (S::DUP - 1)) == 0) {
 #pragma unroll
             for (int it = 0; it < S::ITERS; ++it) ws->p[it * S::TPI + tsub][hl] = make_float2(sc[it], sc[it]);
             if (tsub == 0) ws->alpha[hl] = make_float2(alpha, alpha);
@@ -400,6 +467,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
     }
 
     // ---- merge the lanes of different tokens (same dims, same running max)
+    if constexpr (S::JOINT) l_run += __shfl_xor_sync(0xffffffffu, l_run, G);
 #pragma unroll
     for (int dist = S::LPR; dist < 32; dist <<= 1) {
 #pragma unroll
@@ -420,7 +488,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
 #pragma unroll
             for (int c = 0; c < 4; ++c)
                 *reinterpret_cast<float2 *>(co + (warp * G + h) * D + row * 8 + 2 * c) = o2[h][c];
-        if ((row & (S::DUP - 1)) == 0) {
+        if (S::JOINT ? rsel == 0 : (row & (S::DUP - 1)) == 0) {
             cm[warp * G + hl] = my_stages > 0 ? m_run : -INFINITY;
             cl[warp * G + hl] = my_stages > 0 ? l_run : 0.f;
         }
