@@ -149,6 +149,33 @@ pa_status pa_decode(void *out, const void *q, const pa_kv_pool *pool,
                     void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * pa_decode without a caller workspace, for callers that cannot allocate
+ * device memory: e.g. a plugin that its host framework hands only input and
+ * output buffers (the framework's allocator owns all device memory), or a
+ * serving loop that must not call cudaMalloc (which can synchronise the
+ * device) once it is running.  The pages have no counterpart to this call;
+ * it is a library convenience.
+ *
+ * Same arguments, semantics and results as pa_decode, minus the workspace.
+ * The split-context partials go to a fixed 8 MiB array in the library's own
+ * device memory (a file-scope __device__ array that every GPU loading the
+ * library holds until the process exits).  Shapes whose
+ * pa_decode_workspace_size exceeds 8 MiB return PA_ERR_WORKSPACE and launch
+ * nothing.  The call allocates and frees nothing.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture begins.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents (nothing in it needs to start at zero).  Calls whose kernels
+ *    overlap on the GPU, e.g. on two streams, race on it: serialise them.
+ */
+pa_status pa_decode_noalloc(void *out, const void *q, const pa_kv_pool *pool,
+                            const int32_t *block_tables, int32_t max_blocks_per_seq,
+                            const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t max_seq_len, float scale, int32_t partition_tokens,
+                            cudaStream_t stream);
+
+/*
  * Copy-on-write block copies.  [P1] feature table, beam-search row: forks
  * share blocks and only the block that diverges is copied; [P2] interviewer
  * follow-up on beam search: a fresh block receives the diverging block's

@@ -43,6 +43,7 @@ SIGNATURES = {
     "pa_decode_workspace_size": (_SZ, [_POOL, _I32, _I32, _I32, _I32]),
     "pa_decode_partition_tokens": (_I32, [_POOL, _I32, _I32, _I32, _I32]),
     "pa_decode": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _P]),
+    "pa_decode_noalloc": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P]),
     "pa_copy_blocks": (_I32, [_POOL, _P, _I32, _P]),
     "pa_prefill_chunk": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _I32, _F, _P]),
     "pa_get_device_error": (_I32, [ctypes.POINTER(_U32), _I32, _P]),
@@ -186,6 +187,24 @@ def decode(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_tables:
                            _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, int(max_seq_len), float(scale),
                            int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)),
            "pa_decode")
+
+
+def decode_noalloc(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_tables: torch.Tensor,
+                   seq_lens: torch.Tensor, max_seq_len: int, scale: float, partition_tokens: int = 0,
+                   layer: Optional[int] = None, stream=None) -> None:
+    """pa_decode_noalloc: pa_decode with its partials in the library's fixed
+    8 MiB device array, for callers that cannot allocate a workspace."""
+    desc = pool_desc(pool, layer)
+    B, Hq, _ = q.shape
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.numel() != B:
+        raise ValueError("block_tables / seq_lens do not match the batch")
+    _check(lib().pa_decode_noalloc(_dev(out, torch.bfloat16, "out"), _dev(q, torch.bfloat16, "q"),
+                                   ctypes.byref(desc), _dev(block_tables, torch.int32, "block_tables"),
+                                   block_tables.shape[1], _dev(seq_lens, torch.int32, "seq_lens"), B, Hq,
+                                   int(max_seq_len), float(scale), int(partition_tokens), _stream(stream)),
+           "pa_decode_noalloc")
 
 
 def copy_blocks(pool: torch.Tensor, pairs: torch.Tensor, layer: Optional[int] = None, stream=None) -> None:
