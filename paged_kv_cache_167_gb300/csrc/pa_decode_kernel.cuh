@@ -21,20 +21,24 @@
 //    register cache of the table row, so address generation never waits on a
 //    dependent table load.  No data is multicast.
 //  * All G query heads of the group are served from one staged copy of the
-//    block.  A lane owns 8 of the d dimensions of one token row (16 B) and
-//    keeps q for all G heads on those dimensions in registers, pre-scaled by
-//    scale * log2 e and packed as head pairs, so one packed f32x2 FMA
-//    advances two heads' dot products.  Partial dot products are combined
-//    across the row's lanes with a transposing butterfly: at each shuffle step
-//    a lane keeps half of its head values and receives the other half from its
-//    partner (8 shuffles per token for 8 heads over 16 lanes instead of 32).
-//    Query slots are stored in a lane-dependent order (slot j holds head
-//    j ^ hl) which makes every register index of that butterfly static.
-//  * Online softmax in the log2 domain per warp.  Probabilities and the
-//    running-max correction are broadcast through shared memory, stored
-//    duplicated so each is a ready f32x2 operand; P.V accumulates with packed
-//    f32x2 FMAs; the correction multiply is skipped when no head's running
+//    block.  The arithmetic is the fp32-accumulating bf16 FMA of sm_100-class
+//    SMs (fma.rn.f32.bf16): K, V and q are used as stored, each product is
+//    exact in fp32, and no operand needs converting.
+//  * Q.K: a lane owns 8 of the d dimensions of a token row (16 B) and keeps q
+//    for all G heads on those dimensions in registers (packed bf16).  Partial
+//    dot products are combined across the row's lanes with a transposing
+//    butterfly: at each shuffle step a lane keeps half of its values and
+//    receives the other half from its partner.  When a row has exactly 2G
+//    lanes, two token rows are reduced together and every lane ends with one
+//    (row, head) score.  Query slots are stored in a lane-dependent order so
+//    that every register index of the butterfly is static.
+//  * Online softmax in the log2 domain per warp.  Probabilities are rounded
+//    to bf16 once and broadcast through shared memory (one 16-byte load gives
+//    a token's 8 heads); the softmax denominator sums the same rounded values,
+//    so the output is an exact weighted average with those weights.  The
+//    running-max correction of the accumulators is skipped when no head's
 //    maximum moved.
+//  * P.V: a lane owns 8 dims x G heads of fp32 accumulators.
 //  * At the end the warps' (m, l, o) are merged in shared memory.  With one
 //    partition the CTA writes bf16 output; otherwise it writes fp32 partials
 //    (o normalised by l, m, l) and the reduce kernel merges partitions.
@@ -78,21 +82,20 @@ struct Shape {
     static constexpr int TPI = 32 / LPR;              // tokens per warp iteration
     static constexpr int TPS = BS >= 16 ? BS : 16;    // tokens per pipeline stage
     static constexpr int BPS = TPS / BS;              // blocks per stage
-    static constexpr int ITERS = TPS / TPI;
+    static constexpr int ITERS = TPS / TPI;           // P.V iterations per stage
     static constexpr int SLAB = BS * D;               // elements of one (block, K|V, head) slab
     static constexpr int LOG_LPR = ilog2(LPR);
     static constexpr int NT = ilog2(G);               // transposing butterfly steps
-    static constexpr int DUP = LPR / G;               // lanes holding the same head's score
-    static constexpr int QS = G >= 2 ? G / 2 : 4;     // q register pairs: head pairs, or dim pairs if G == 1
-    // Two token rows are reduced jointly when a row's lanes number exactly 2G:
-    // the butterfly then ends with every lane owning one (row, head) score.
+    static constexpr int DUP = LPR / G;               // lanes holding the same head's score (one row)
+    // Two token rows are reduced jointly when a row's lanes number exactly 2G.
     static constexpr bool JOINT = LPR == 2 * G;
-    static constexpr int QK_ITERS = JOINT ? TPS / (2 * TPI) : ITERS;
+    static constexpr int ROWS = JOINT ? 2 : 1;        // token rows per Q.K butterfly
+    static constexpr int QK_ITERS = TPS / (ROWS * TPI);
+    static constexpr int PW = G < 2 ? 1 : G / 2;      // 32-bit words of one token's bf16 probabilities
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group");
-    static_assert(TPS % TPI == 0 && TPS % BS == 0, "stage shape");
+    static_assert(TPS % (ROWS * TPI) == 0 && TPS % BS == 0, "stage shape");
     static_assert(BPS <= 32, "table cache");
-    static_assert(!JOINT || TPS % (2 * TPI) == 0, "joint rows");
 };
 
 template <int D, int G, int BS>
@@ -100,8 +103,8 @@ struct alignas(16) WarpSmem {
     using S = Shape<D, G, BS>;
     __nv_bfloat16 k[kStages][S::TPS * D];
     __nv_bfloat16 v[kStages][S::TPS * D];
-    float2 p[S::TPS][G < 2 ? 2 : G];   // (p, p) by (token, head)
-    float2 alpha[G < 2 ? 2 : G];       // (a, a) running-max correction by head
+    uint32_t p[S::TPS][S::PW];        // bf16 probabilities by (token, head), packed in pairs
+    float alpha[G < 4 ? 4 : G];       // running-max correction by head
     uint64_t bar[kStages + (kStages & 1)];
 };
 
@@ -140,102 +143,66 @@ __device__ __forceinline__ int effective_len(const Params &p, int s, int block_s
     return L;
 }
 
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-
-__device__ __forceinline__ float2 shfl_xor2(float2 v, int dist) {
-    return make_float2(__shfl_xor_sync(0xffffffffu, v.x, dist), __shfl_xor_sync(0xffffffffu, v.y, dist));
+// acc += (bf16 half HA of a) * (bf16 half HB of b), fp32 accumulate; 0 = low half.
+template <int HA, int HB>
+__device__ __forceinline__ void bf16_fma(float &acc, uint32_t a, uint32_t b) {
+    if constexpr (HA == 0 && HB == 0)
+        asm("{ .reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, al, bl, %0; }" : "+f"(acc) : "r"(a), "r"(b));
+    else if constexpr (HA == 0 && HB == 1)
+        asm("{ .reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, al, bh, %0; }" : "+f"(acc) : "r"(a), "r"(b));
+    else if constexpr (HA == 1 && HB == 0)
+        asm("{ .reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, ah, bl, %0; }" : "+f"(acc) : "r"(a), "r"(b));
+    else
+        asm("{ .reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, ah, bh, %0; }" : "+f"(acc) : "r"(a), "r"(b));
 }
 
-// Score of head hl for the token row at `krow` (this lane's 8 dims), summed
-// over the row's LPR lanes.
-template <int D, int G, int BS>
-__device__ __forceinline__ float qk_score(const float2 (&q2)[Shape<D, G, BS>::QS][8], const uint4 kw) {
-    using S = Shape<D, G, BS>;
-    const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
-    float s;
-    if constexpr (G >= 2) {
-        // dims duplicated into both halves: q2[p][i] = (q[2p^hl][i], q[(2p+1)^hl][i])
-        float2 kd[8];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const float lo = __uint_as_float(w4[c] << 16), hi = __uint_as_float(w4[c] & 0xffff0000u);
-            kd[2 * c] = make_float2(lo, lo);
-            kd[2 * c + 1] = make_float2(hi, hi);
-        }
-        float2 acc[S::QS];
-#pragma unroll
-        for (int pp = 0; pp < S::QS; ++pp) {
-            acc[pp] = fmul2(q2[pp][0], kd[0]);
-#pragma unroll
-            for (int i = 1; i < 8; ++i) acc[pp] = ffma2(q2[pp][i], kd[i], acc[pp]);
-        }
-        // pair steps: halve the head-pair set
-#pragma unroll
-        for (int st = 0; st < S::NT - 1; ++st) {
-            const int half = S::QS >> (st + 1);
-            const int dist = S::LPR >> (st + 1);
-#pragma unroll
-            for (int pp = 0; pp < half; ++pp) acc[pp] = fadd2(acc[pp], shfl_xor2(acc[pp + half], dist));
-        }
-        // split step: keep .x, take the partner's .y
-        s = acc[0].x + __shfl_xor_sync(0xffffffffu, acc[0].y, S::LPR >> S::NT);
-    } else {
-        // one head: q2[c] holds dim pairs; fold the pair, then reduce
-        float2 a = fmul2(q2[0][0], bf16x2_to_float2(w4[0]));
-#pragma unroll
-        for (int c = 1; c < 4; ++c) a = ffma2(q2[c][0], bf16x2_to_float2(w4[c]), a);
-        s = a.x + a.y;
-    }
-#pragma unroll
-    for (int dist = S::LPR >> (S::NT + 1); dist >= 1; dist >>= 1) s += __shfl_xor_sync(0xffffffffu, s, dist);
-    return s;
-}
-
-// Joint scores of two token rows (own = this lane's row, other = the row its
-// partners own) for all G heads, reduced over the row's 2G lanes.  Slot j of a
-// lane holds value j ^ rl (value = row * G + head, rl = lane % LPR), so each
-// butterfly step keeps half of the slots and receives the other half from
-// its partner; the lane ends with the score of (row rl / G, head rl % G).
-template <int D, int G, int BS>
-__device__ __forceinline__ float qk_score_joint(const float2 (&q2)[Shape<D, G, BS>::QS][8], const uint4 kown,
-                                                const uint4 koth) {
-    using S = Shape<D, G, BS>;
-    static_assert(S::JOINT, "joint rows");
-    float2 ko[8], kt[8];
-    const uint32_t wo[4] = {kown.x, kown.y, kown.z, kown.w};
-    const uint32_t wt[4] = {koth.x, koth.y, koth.z, koth.w};
+// 8-dim partial dot product of a packed bf16 q chunk with a packed bf16 K chunk.
+__device__ __forceinline__ float dot8(const uint32_t (&q)[4], const uint32_t (&k)[4]) {
+    float a = 0.f, b = 0.f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        // each dim duplicated into both halves of a pair, built by two different
-        // ops so no register move is needed
-        ko[2 * c] = make_float2(__uint_as_float(wo[c] << 16), __uint_as_float(__byte_perm(wo[c], 0u, 0x1044)));
-        ko[2 * c + 1] = make_float2(__uint_as_float(wo[c] & 0xffff0000u), __uint_as_float(__byte_perm(wo[c], 0u, 0x3244)));
-        kt[2 * c] = make_float2(__uint_as_float(wt[c] << 16), __uint_as_float(__byte_perm(wt[c], 0u, 0x1044)));
-        kt[2 * c + 1] = make_float2(__uint_as_float(wt[c] & 0xffff0000u), __uint_as_float(__byte_perm(wt[c], 0u, 0x3244)));
+        bf16_fma<0, 0>(a, q[c], k[c]);
+        bf16_fma<1, 1>(b, q[c], k[c]);
     }
-    float2 acc[G];
+    return a + b;
+}
+
+// Q.K for ROWS token rows, summed over the row's LPR lanes.
+//  * one row: slot j (< G) holds head j ^ hl; NT transposing steps leave the
+//    lane with head hl, plain steps finish the sum.
+//  * two rows (JOINT): slot j (< 2G) holds value j ^ rl, value = row * G +
+//    head; the first G slots use this lane's own row.  NT + 1 transposing
+//    steps leave the lane with (row rl / G, head rl % G).
+// Returns the raw dot product (scale applied by the caller).
+template <int D, int G, int BS>
+__device__ __forceinline__ float qk_dot(const uint32_t (&q)[G][4], const uint4 kown, const uint4 koth) {
+    using S = Shape<D, G, BS>;
+    const uint32_t ko[4] = {kown.x, kown.y, kown.z, kown.w};
+    constexpr int NV = G * S::ROWS;
+    float a[NV];
 #pragma unroll
-    for (int pp = 0; pp < G / 2; ++pp) {
-        acc[pp] = fmul2(q2[pp][0], ko[0]);
-        acc[pp + G / 2] = fmul2(q2[pp][0], kt[0]);
+    for (int j = 0; j < G; ++j) a[j] = dot8(q[j], ko);
+    if constexpr (S::JOINT) {
+        const uint32_t kt[4] = {koth.x, koth.y, koth.z, koth.w};
+#pragma unroll
+        for (int j = 0; j < G; ++j) a[G + j] = dot8(q[j], kt);
     }
+    constexpr int NTR = S::JOINT ? S::NT + 1 : S::NT;  // transposing steps
 #pragma unroll
-    for (int i = 1; i < 8; ++i)
-#pragma unroll
-        for (int pp = 0; pp < G / 2; ++pp) {
-            acc[pp] = ffma2(q2[pp][i], ko[i], acc[pp]);
-            acc[pp + G / 2] = ffma2(q2[pp][i], kt[i], acc[pp + G / 2]);
-        }
-#pragma unroll
-    for (int st = 0; st < S::NT; ++st) {
-        const int half = G >> (st + 1);
+    for (int st = 0; st < NTR; ++st) {
+        const int half = NV >> (st + 1);
         const int dist = S::LPR >> (st + 1);
 #pragma unroll
-        for (int pp = 0; pp < half; ++pp) acc[pp] = fadd2(acc[pp], shfl_xor2(acc[pp + half], dist));
+        for (int j = 0; j < half; ++j) a[j] += __shfl_xor_sync(0xffffffffu, a[j + half], dist);
     }
-    return acc[0].x + __shfl_xor_sync(0xffffffffu, acc[0].y, 1);
+    float s = a[0];
+#pragma unroll
+    for (int dist = S::LPR >> (NTR + 1); dist >= 1; dist >>= 1) s += __shfl_xor_sync(0xffffffffu, s, dist);
+    return s;
 }
 
 template <int D, int G, int BS>
@@ -276,27 +243,15 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
     const int hl = S::JOINT ? (row & (G - 1)) : (row >> (S::LOG_LPR - S::NT));
     const int rsel = S::JOINT ? (row >> S::NT) : 0;
 
-    // q on this lane's dims, pre-scaled; slot j holds head j ^ hl
-    float2 q2[S::QS][8];
+    // q on this lane's 8 dims, packed bf16; slot j holds head j ^ hl
+    uint32_t qw[G][4];
 #pragma unroll
     for (int j = 0; j < G; ++j) {
         const uint4 w = __ldg(reinterpret_cast<const uint4 *>(p.q + (head0 + (j ^ hl)) * D + row * 8));
-        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const float2 f = bf16x2_to_float2(w4[c]);
-            if constexpr (G >= 2) {
-                if ((j & 1) == 0) {
-                    q2[j / 2][2 * c].x = f.x * p.scale_log2;
-                    q2[j / 2][2 * c + 1].x = f.y * p.scale_log2;
-                } else {
-                    q2[j / 2][2 * c].y = f.x * p.scale_log2;
-                    q2[j / 2][2 * c + 1].y = f.y * p.scale_log2;
-                }
-            } else {
-                q2[c][0] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
-            }
-        }
+        qw[j][0] = w.x;
+        qw[j][1] = w.y;
+        qw[j][2] = w.z;
+        qw[j][3] = w.w;
     }
     __syncwarp();
 
@@ -357,11 +312,11 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
 
     float m_run = -INFINITY;   // running max (log2 domain) of head hl
     float l_run = 0.f;         // this lane's share of the softmax denominator of head hl
-    float2 o2[G][4];
+    float o[G][8];             // numerators: head x this lane's 8 dims
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) o2[h][c] = make_float2(0.f, 0.f);
+        for (int i = 0; i < 8; ++i) o[h][i] = 0.f;
 
     int consumed = 0;
     bool ok = true;
@@ -378,22 +333,16 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
         const __nv_bfloat16 *ks = ws->k[slot];
         const __nv_bfloat16 *vs = ws->v[slot];
 
-        // ---- scores for head hl
+        // ---- scores (log2 domain) for head hl
         float sc[S::QK_ITERS];
 #pragma unroll
         for (int it = 0; it < S::QK_ITERS; ++it) {
-            int t;
-            if constexpr (S::JOINT) {
-                const int t0 = it * 2 * S::TPI + tsub * 2;   // rows t0 (0) and t0 + 1 (1)
-                t = t0 + rsel;
-                const uint4 kown = *reinterpret_cast<const uint4 *>(ks + t * D + row * 8);
-                const uint4 koth = *reinterpret_cast<const uint4 *>(ks + (t0 + 1 - rsel) * D + row * 8);
-                sc[it] = qk_score_joint<D, G, BS>(q2, kown, koth);
-            } else {
-                t = it * S::TPI + tsub;
-                const uint4 kw = *reinterpret_cast<const uint4 *>(ks + t * D + row * 8);
-                sc[it] = qk_score<D, G, BS>(q2, kw);
-            }
+            const int t0 = it * S::ROWS * S::TPI + tsub * S::ROWS;   // first row of this lane's group
+            const int t = t0 + rsel;                                 // the row whose score this lane keeps
+            const uint4 kown = *reinterpret_cast<const uint4 *>(ks + t * D + row * 8);
+            uint4 koth = kown;
+            if constexpr (S::JOINT) koth = *reinterpret_cast<const uint4 *>(ks + (t0 + 1 - rsel) * D + row * 8);
+            sc[it] = qk_dot<D, G, BS>(qw, kown, koth) * p.scale_log2;
             if (tail && tok0 + t >= tok_end) sc[it] = -INFINITY;
         }
 
@@ -408,23 +357,21 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = fast_exp2(m_run - m_use);
         float psum = 0.f;
+        __nv_bfloat16 pb[S::QK_ITERS];
 #pragma unroll
         for (int it = 0; it < S::QK_ITERS; ++it) {
-            sc[it] = fast_exp2(sc[it] - m_use);
-            psum += sc[it];
+            pb[it] = __float2bfloat16_rn(fast_exp2(sc[it] - m_use));
+            psum += __bfloat162float(pb[it]);
         }
         l_run = l_run * alpha + psum;
         const bool moved = m_new != m_run;
         m_run = m_new;
-        if constexpr (S::JOINT) {
+        if (S::JOINT || (row & (S::DUP - 1)) == 0) {
+            __nv_bfloat16 *pt = reinterpret_cast<__nv_bfloat16 *>(&ws->p[0][0]);
 #pragma unroll
             for (int it = 0; it < S::QK_ITERS; ++it)
-                ws->p[it * 2 * S::TPI + tsub * 2 + rsel][hl] = make_float2(sc[it], sc[it]);
-            if (tsub == 0 && rsel == 0) ws->alpha[hl] = make_float2(alpha, alpha);
-        } else if ((row & (S::DUP - 1)) == 0) {
-#pragma unroll
-            for (int it = 0; it < S::ITERS; ++it) ws->p[it * S::TPI + tsub][hl] = make_float2(sc[it], sc[it]);
-            if (tsub == 0) ws->alpha[hl] = make_float2(alpha, alpha);
+                pt[(it * S::ROWS * S::TPI + tsub * S::ROWS + rsel) * (2 * S::PW) + hl] = pb[it];
+            if (tsub == 0 && rsel == 0) ws->alpha[hl] = alpha;
         }
         __syncwarp();
 
@@ -432,27 +379,42 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
         if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const float2 a2 = ws->alpha[h];
+                const float a = ws->alpha[h];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) o2[h][c] = fmul2(o2[h][c], a2);
+                for (int i = 0; i < 8; ++i) o[h][i] *= a;
             }
         }
 #pragma unroll
         for (int it = 0; it < S::ITERS; ++it) {
             const int t = it * S::TPI + tsub;
-            const uint4 vw = *reinterpret_cast<const uint4 *>(vs + t * D + row * 8);
-            float2 v2[4] = {bf16x2_to_float2(vw.x), bf16x2_to_float2(vw.y), bf16x2_to_float2(vw.z),
-                            bf16x2_to_float2(vw.w)};
-            if (tail && tok0 + t >= tok_end) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) v2[c] = make_float2(0.f, 0.f);  // slot may hold stale data
+            uint4 vw = *reinterpret_cast<const uint4 *>(vs + t * D + row * 8);
+            if (tail && tok0 + t >= tok_end) vw = make_uint4(0u, 0u, 0u, 0u);  // slot may hold stale data
+            const uint32_t v4[4] = {vw.x, vw.y, vw.z, vw.w};
+            uint32_t pw[S::PW];
+            if constexpr (S::PW == 4) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(&ws->p[t][0]);
+                pw[0] = w.x;
+                pw[1] = w.y;
+                pw[2] = w.z;
+                pw[3] = w.w;
+            } else if constexpr (S::PW == 2) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(&ws->p[t][0]);
+                pw[0] = w.x;
+                pw[1] = w.y;
+            } else {
+                pw[0] = ws->p[t][0];
             }
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float2 p2 = ws->p[t][h];
+            for (int hp = 0; hp < S::PW; ++hp)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) o2[h][c] = ffma2(p2, v2[c], o2[h][c]);
-            }
+                for (int c = 0; c < 4; ++c) {
+                    bf16_fma<0, 0>(o[2 * hp][2 * c], pw[hp], v4[c]);
+                    bf16_fma<0, 1>(o[2 * hp][2 * c + 1], pw[hp], v4[c]);
+                    if constexpr (G >= 2) {
+                        bf16_fma<1, 0>(o[2 * hp + 1][2 * c], pw[hp], v4[c]);
+                        bf16_fma<1, 1>(o[2 * hp + 1][2 * c + 1], pw[hp], v4[c]);
+                    }
+                }
         }
         __syncwarp();
         issue(k + kStages);
@@ -473,7 +435,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) o2[h][c] = fadd2(o2[h][c], shfl_xor2(o2[h][c], dist));
+            for (int i = 0; i < 8; ++i) o[h][i] += __shfl_xor_sync(0xffffffffu, o[h][i], dist);
         l_run += __shfl_xor_sync(0xffffffffu, l_run, dist);
     }
 
@@ -484,10 +446,11 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
     float *co = cl + kWarps * G;                       // [W][G][D] numerators
     if (tsub == 0) {
 #pragma unroll
-        for (int h = 0; h < G; ++h)
+        for (int h = 0; h < G; ++h) {
+            float *dst = co + (warp * G + h) * D + row * 8;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                *reinterpret_cast<float2 *>(co + (warp * G + h) * D + row * 8 + 2 * c) = o2[h][c];
+            for (int i = 0; i < 8; i += 2) *reinterpret_cast<float2 *>(dst + i) = make_float2(o[h][i], o[h][i + 1]);
+        }
         if (S::JOINT ? rsel == 0 : (row & (S::DUP - 1)) == 0) {
             cm[warp * G + hl] = my_stages > 0 ? m_run : -INFINITY;
             cl[warp * G + hl] = my_stages > 0 ? l_run : 0.f;
@@ -508,9 +471,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
             for (int w = 0; w < kWarps; ++w) {
                 const float f = fast_exp2(cm[w * G + h] - M);
                 lsum += cl[w * G + h] * f;
-                const float2 o = *reinterpret_cast<const float2 *>(co + (w * G + h) * D + i);
-                ox += o.x * f;
-                oy += o.y * f;
+                const float2 ov = *reinterpret_cast<const float2 *>(co + (w * G + h) * D + i);
+                ox += ov.x * f;
+                oy += ov.y * f;
             }
         }
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
@@ -544,12 +507,12 @@ __global__ void __launch_bounds__(G *D / 4) paged_decode_reduce_kernel(const Par
         for (int q = 0; q < np; ++q) {
             const float2 mlq = ml[q];
             const float w = mlq.y * fast_exp2(mlq.x - M);
-            const float4 o = *reinterpret_cast<const float4 *>(p.ws_o + (row * p.num_parts + q) * D + i);
+            const float4 ov = *reinterpret_cast<const float4 *>(p.ws_o + (row * p.num_parts + q) * D + i);
             wsum += w;
-            acc.x += w * o.x;
-            acc.y += w * o.y;
-            acc.z += w * o.z;
-            acc.w += w * o.w;
+            acc.x += w * ov.x;
+            acc.y += w * ov.y;
+            acc.z += w * ov.z;
+            acc.w += w * ov.w;
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
