@@ -218,11 +218,12 @@ def beam_fork(seed: int = SEED_BASE + 4, prompts: int = 32, beams: int = 4) -> W
                     notes={"prompt_lens": plen, "beams": beams})
 
 
-def prefill_chunk(seed: int = SEED_BASE + 4, batch: int = 16, ctx: int = 4096,
-                  chunk: int = 512, num_blocks: int = 8192) -> Workload:
-    """16 sequences, each with `ctx` cached tokens and a `chunk`-token causal
-    query chunk at positions ctx .. ctx+chunk-1 whose K/V are first written
-    by the slot writer; 64/8 heads, d=128, b=16, random placement."""
+def prefill_chunk(seed: int = SEED_BASE + 4, batch: int = 16, ctx=4096, chunk: int = 512,
+                  num_blocks: int = 8192, num_q_heads: int = 64, num_kv_heads: int = 8) -> Workload:
+    """16 sequences, each with `ctx` cached tokens (a number, or one per
+    sequence) and a `chunk`-token causal query chunk at positions
+    ctx .. ctx+chunk-1 whose K/V are first written by the slot writer;
+    64/8 heads, d=128, b=16, random placement."""
     rng = np.random.default_rng(seed + 1000)
     b = 16
     ctx_lens = np.full(batch, ctx, dtype=np.int32) if np.isscalar(ctx) else np.asarray(ctx, np.int32)
@@ -231,7 +232,7 @@ def prefill_chunk(seed: int = SEED_BASE + 4, batch: int = 16, ctx: int = 4096,
     tables = _tables_from_counts(counts, rng.permutation(num_blocks).astype(np.int32))
     seq_idx = np.repeat(np.arange(batch, dtype=np.int32), chunk)
     positions = (ctx_lens.astype(np.int64)[:, None] + np.arange(chunk, dtype=np.int64)[None, :]).ravel()
-    return Workload("prefill_chunk", "prefill", 64, 8, 128, b, num_blocks, 1.0 / math.sqrt(128),
+    return Workload("prefill_chunk", "prefill", num_q_heads, num_kv_heads, 128, b, num_blocks, 1.0 / math.sqrt(128),
                     total.astype(np.int32), tables, _referenced(tables), seed,
                     new_seq_idx=seq_idx, new_positions=positions, ctx_lens=ctx_lens, chunk=chunk)
 

@@ -19,7 +19,9 @@ namespace {
 #endif
 constexpr int kDecodeWarps = PA_DECODE_WARPS;  // warps per decode CTA (must match the kernel)
 constexpr int kAutoCtasPerSm = 2;        // resident decode CTAs per SM
-constexpr int kAutoWaves = 4;            // CTAs per resident slot the auto partition aims for
+constexpr int kAutoWaves = 1;            // CTAs per resident slot the auto partition aims for: split
+                                         // only when (sequence, kv-head) units cannot fill the SMs,
+                                         // since partials and the reduce cost more than waves gain
 constexpr int kAutoMaxPartition = 1024;  // cap so long sequences still spread over SMs
 constexpr size_t kWsAlign = 256;
 
@@ -67,8 +69,8 @@ pa_status plan_decode(const PoolView &pool, int32_t num_seqs, int32_t num_q_head
     if (part > 0) {
         if (part % pool.block_size != 0) return PA_ERR_INVALID_ARG;
     } else {
-        // Auto: enough partitions that the grid covers every resident CTA slot
-        // several times, each partition a whole number of per-warp stages.
+        // Auto: enough partitions that the grid covers every resident CTA
+        // slot, each partition a whole number of per-warp stages.
         const int64_t grain = (int64_t)decode_stage_tokens(pool.block_size) * kDecodeWarps;
         int sms = device_sm_count();
         if (sms <= 0) sms = 148;

@@ -1,11 +1,532 @@
-// pa_prefill.cu -- chunked causal prefill against a paged context.
+// pa_prefill.cu -- chunked causal prefill against a paged context on the
+// tcgen05 tensor cores (sm_103a).
+//
+// What it computes: for sequence s with ctx cached tokens and a chunk of C new
+// query tokens at positions ctx .. ctx + C - 1 (whose K/V are already in the
+// pool), query j of head h attends keys 0 .. ctx + j of kv-head h / G, read
+// through the block table (table[s][t / b], t % b).  Sources:
+// auto-20261007-1900-en (lihaoran.work), "A block table maps logical order to
+// physical storage" (paging changes where K/V live, not what a causal query
+// sees); attn-paged-attention-mcq-hard (zenaique.com), conceptual block-lookup
+// listing (the gather belongs inside the kernel's tiling loop).
+//
+// Design:
+//  * One CTA (4 warps) per 128-row M-tile of one (sequence, kv-head): row r is
+//    query j0 + r / G of head g*G + r % G, so every K/V tile staged in shared
+//    memory serves the whole query group.
+//  * TMA (cp.async.bulk.tensor, 128-byte swizzle) brings Q and the K/V tiles:
+//    a K or V tile of 128 keys is 8 blocks x 2 halves of d, one box of
+//    16 rows x 64 dims per (block, half), addressed through a 5-D tensor map of
+//    the pool's (d, slot, head, K|V, block) view.  Blocks past the sequence
+//    end, or with an out-of-range table entry, are fetched from an
+//    out-of-bounds coordinate, which TMA fills with zeros.  No multicast.
+//  * S = Q.K^T and O += P.V are tcgen05.mma kind::f16 (bf16 in, fp32 out)
+//    with M = N = 128, K = 16 per instruction, accumulators in tensor memory
+//    (S in columns 0..127, O in 128..255), issued by one thread and tracked
+//    with tcgen05.commit on mbarriers.
+//  * Softmax: thread r owns row r (tensor-memory lane r).  It reads S with
+//    tcgen05.ld, applies the scale and the causal mask, keeps a reference
+//    maximum in the log2 domain that only moves when a tile's maximum exceeds
+//    it by more than 8 (so p <= 2^8 and O needs rescaling rarely; the result
+//    is exact because l and O share the reference), writes P as bf16 into
+//    the swizzled shared-memory layout the next MMA reads, and sums the same
+//    rounded values into l.
+//  * K and V rings of two stages each; a K slot is refilled once its Q.K MMA
+//    has completed, a V slot once its P.V MMA has.
+//  * Every wait is bounded; on expiry the kernel records PA_DEVERR_TIMEOUT,
+//    waits (bounded) for its outstanding work and frees its tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pa {
+namespace prefill {
 
-bool prefill_supported(int, int, int) { return false; }
+constexpr int kThreads = 128;
+constexpr int kRows = 128;                  // M tile
+constexpr int kKeys = 128;                  // N tile of Q.K (keys per iteration)
+constexpr int kD = 128;                     // head_dim
+constexpr int kBS = 16;                     // block_size
+constexpr uint32_t kHalf = 128u * 128u;     // one [128 rows][64 bf16] swizzled half tile, bytes
+constexpr uint32_t kTile = 2u * kHalf;      // [2 halves][128 rows][128 B]
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kTile;   // 2 stages
+constexpr uint32_t kOffV = kOffK + 2 * kTile;
+constexpr uint32_t kOffP = kOffV + 2 * kTile;
+constexpr uint32_t kOffBar = kOffP + kTile;
+constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;   // + alignment slack
+constexpr uint32_t kTmemCols = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 domain
 
-cudaError_t launch_prefill(const PrefillArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+struct Params {
+    __nv_bfloat16 *out;          // [B][C][Hq][D]
+    const int32_t *tables;
+    int32_t max_blocks;
+    const int32_t *ctx_lens;
+    int32_t max_ctx_len;
+    int32_t chunk;
+    int32_t num_q_heads;
+    int64_t num_blocks;
+    float scale_log2;
+    unsigned int *err;
+};
+
+// ---- PTX wrappers -----------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5}], [%6];" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                            int c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5, %6}], [%7];" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int *err) {
+    return mbar_wait_bounded(reinterpret_cast<uint64_t *>(__cvta_shared_to_generic(bar)), parity, err);
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: 128-byte swizzle, descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+#define PA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
+                 "=r"(r[i + 6]), "=r"(r[i + 7])
+#define PA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
+                 "r"(r[i + 6]), "r"(r[i + 7])
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : PA_R8(0), PA_R8(8), PA_R8(16), PA_R8(24)
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        PA_W8(0), PA_W8(8), PA_W8(16), PA_W8(24)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---- the kernel ---------------------------------------------------------------
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
+                   const Params p) {
+    constexpr int QPT = kRows / G;   // queries per M-tile
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+    unsigned char *gbase = smem_raw + (base - smem_addr(smem_raw));
+    const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sP = base + kOffP;
+    const uint32_t barQ = base + kOffBar, barK = barQ + 8, barV = barQ + 24, barS = barQ + 40, barO = barQ + 48;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 64);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int mt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+    const int j0 = mt * QPT;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 7; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(barQ + 8 * i) : "memory");
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tO = tmem + 128;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    int ctx = __ldg(p.ctx_lens + s);
+    if (ctx < 0 || ctx > p.max_ctx_len) {
+        if (tid == 0 && mt == 0 && g == 0) raise_error(p.err, PA_DEVERR_SEQ_LEN);
+        ctx = ctx < 0 ? 0 : p.max_ctx_len;
+    }
+    const int seq_end = ctx + p.chunk;                         // keys 0 .. seq_end - 1 exist
+    const int nblk_seq = (seq_end + kBS - 1) / kBS;
+    const int last_q = min(j0 + QPT, p.chunk) - 1;             // last valid query of this tile
+    const int n_tiles = (ctx + last_q + 1 + kKeys - 1) / kKeys;
+    const int32_t *table_row = p.tables + (size_t)s * p.max_blocks;
+
+    // physical block of logical block bi, or the out-of-bounds coordinate (zero fill)
+    auto phys = [&](int bi) -> int {
+        if (bi >= nblk_seq) return (int)p.num_blocks;
+        const int id = __ldg(table_row + bi);
+        if (id < 0 || id >= p.num_blocks) {
+            raise_error(p.err, PA_DEVERR_BLOCK_ID);
+            return (int)p.num_blocks;
+        }
+        return id;
+    };
+    int issued_tiles[2] = {0, 0};   // K, V tiles whose copies thread 0 has issued
+    int waited_tiles[2] = {0, 0};   // K, V tiles whose arrival thread 0 has seen
+    auto load_kv = [&](int t, int kv) {   // thread 0 only
+        issued_tiles[kv] = t + 1;
+        const int st = t & 1;
+        const uint32_t dst = (kv ? sV : sK) + st * kTile;
+        const uint32_t bar = (kv ? barV : barK) + 8 * st;
+        mbar_expect(bar, kTile);
+#pragma unroll
+        for (int i = 0; i < kKeys / kBS; ++i) {
+            const int blk = phys(t * (kKeys / kBS) + i);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) tma_load_5d(dst + h * kHalf + i * 2048, &tmap_kv, h * 64, 0, g, kv, blk, bar);
+        }
+    };
+
+    if (tid == 0) {
+        mbar_expect(barQ, kTile);
+        const int qrow = s * p.chunk + j0;
+        tma_load_4d(sQ, &tmap_q, 0, 0, g, qrow, barQ);
+        tma_load_4d(sQ + kHalf, &tmap_q, 64, 0, g, qrow, barQ);
+        for (int t = 0; t < 2 && t < n_tiles; ++t) {
+            load_kv(t, 0);
+            load_kv(t, 1);
+        }
+    }
+
+    const int r = tid;                                   // this thread's row
+    const int jr = j0 + r / G;
+    const int pos = min(ctx + jr, seq_end - 1);          // last key this row may attend
+    constexpr uint32_t idesc_qk = idesc_bf16(kRows, kKeys, false);
+    constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, true);
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    int issued_o = 0;                                    // P.V commits issued
+
+    for (int t = 0; t < n_tiles && ok; ++t) {
+        const int st = t & 1;
+        const uint32_t ph2 = (uint32_t)((t >> 1) & 1);
+        // ---- S = Q . K^T
+        if (tid == 0) {
+            bool w = (t > 0 || mbar_wait(barQ, 0, p.err)) && mbar_wait(barK + 8 * st, ph2, p.err);
+            if (w) {
+                waited_tiles[0] = t + 1;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    umma(tS, smem_desc(sQ + off, 16, 1024), smem_desc(sK + st * kTile + off, 16, 1024), idesc_qk,
+                         kk > 0);
+                }
+            }
+            umma_commit(barS);   // arrives even if nothing was issued
+            if (!w) ok = false;
+        }
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+        if (!mbar_wait(barS, (uint32_t)(t & 1), p.err)) ok = false;
+        // P smem and O are still read/written by the previous P.V until it completes
+        if (ok && t > 0 && !mbar_wait(barO, (uint32_t)((t - 1) & 1), p.err)) ok = false;
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0) {
+            if (t + 2 < n_tiles) load_kv(t + 2, 0);          // K slot st is free: its Q.K completed
+            if (t >= 1 && t + 1 < n_tiles) load_kv(t + 1, 1); // V slot of tile t-1 is free
+        }
+
+        // ---- softmax of row r over this tile's 128 keys
+        uint32_t sraw[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, sraw[c]);
+        tmem_ld_wait();
+        const int key0 = t * kKeys;
+        float mt_ = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float x = key0 + c * 32 + i <= pos ? __uint_as_float(sraw[c][i]) * p.scale_log2 : -INFINITY;
+                sraw[c][i] = __float_as_uint(x);
+                mt_ = fmaxf(mt_, x);
+            }
+        float alpha = 1.f;
+        if (mt_ > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt_ != -INFINITY)) {
+            alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - mt_);
+            m_ref = mt_;
+        }
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        float psum = 0.f;
+        const uint32_t prow = sP + (uint32_t)r * 128u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {        // 8 keys = one 16-byte chunk
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = fast_exp2(__uint_as_float(sraw[c][q4 * 8 + 2 * e]) - m_use);
+                    const float b = fast_exp2(__uint_as_float(sraw[c][q4 * 8 + 2 * e + 1]) - m_use);
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(a, b);
+                    psum += __low2float(pr) + __high2float(pr);
+                    w[e] = *reinterpret_cast<const uint32_t *>(&pr);
+                }
+                const int key = c * 32 + q4 * 8;                // 0..127
+                const uint32_t half = (uint32_t)(key >> 6);
+                const uint32_t chunk = (uint32_t)((key & 63) >> 3);
+                const uint32_t addr = prow + half * kHalf + ((chunk ^ (uint32_t)(r & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                             "r"(w[3])
+                             : "memory");
+            }
+        }
+        l = l * alpha + psum;
+        // rescale O (only warps where some row's reference moved)
+        if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + lane_off + c * 32, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                tmem_st32(tO + lane_off + c * 32, o);
+            }
+            tmem_st_wait();
+        }
+        // keys past the sequence end inside the last block: zero their V rows
+        // (their p is 0, but the slots may hold non-finite junk)
+        const int tail_lo = seq_end - key0, blk_end = ((seq_end + kBS - 1) / kBS) * kBS - key0;
+        if (tail_lo > 0 && tail_lo < kKeys && (seq_end % kBS) != 0) {
+            if (!mbar_wait(barV + 8 * st, ph2, p.err)) ok = false;
+            const int nrows = min(blk_end, kKeys) - tail_lo;
+            for (int idx = tid; idx < nrows * 2 * 8; idx += kThreads) {
+                const int rr = tail_lo + idx / 16, h = (idx / 8) & 1, c16 = idx & 7;
+                const uint32_t addr = sV + st * kTile + h * kHalf + (uint32_t)rr * 128u + (uint32_t)c16 * 16u;
+                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+        // ---- O += P . V
+        if (tid == 0) {
+            tc_fence_after();
+            const bool w = mbar_wait(barV + 8 * st, ph2, p.err);
+            if (w) {
+                waited_tiles[1] = t + 1;
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; ++kk) {
+                    const uint32_t a_off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    umma(tO, smem_desc(sP + a_off, 16, 1024), smem_desc(sV + st * kTile + kk * 2048, kHalf, 1024),
+                         idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                }
+            }
+            umma_commit(barO);
+            if (!w) ok = false;
+        }
+        ++issued_o;
+    }
+
+    // ---- epilogue: O / l to bf16
+    const bool fin = ok && issued_o > 0 && mbar_wait(barO, (uint32_t)((issued_o - 1) & 1), p.err);
+    tc_fence_after();
+    const bool row_ok = jr < p.chunk;
+    if (__syncthreads_and(fin)) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16 *dst = p.out + (((size_t)s * p.chunk + jr) * p.num_q_heads + (size_t)g * G + (r % G)) * kD;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + lane_off + c * 32, o);
+            tmem_ld_wait();
+            if (row_ok) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint4 v;
+                    v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
+                    v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
+                    v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
+                    v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
+                    *reinterpret_cast<uint4 *>(dst + c * 32 + q4 * 8) = v;
+                }
+            }
+        }
+    } else if (tid == 0) {
+        // A wait gave up.  Before the shared and tensor memory are released,
+        // wait (bounded) for every copy still in flight and, through one more
+        // commit on the Q barrier (its second phase), for every issued MMA.
+        for (int kv = 0; kv < 2; ++kv)
+            for (int tt = waited_tiles[kv]; tt < issued_tiles[kv]; ++tt)
+                mbar_wait((kv ? barV : barK) + 8 * (tt & 1), (uint32_t)((tt >> 1) & 1), p.err);
+        umma_commit(barQ);
+        mbar_wait(barQ, 1, p.err);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// ---- host side --------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qres) ==
+                cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+template <int G>
+cudaError_t launch_group(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mkv, const Params &prm,
+                         cudaStream_t stream) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    constexpr int QPT = kRows / G;
+    dim3 grid((a.chunk_len + QPT - 1) / QPT, a.pool.num_kv_heads, a.num_seqs);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<G>, mq, mkv, prm);
+}
+
+}  // namespace prefill
+
+bool prefill_supported(int head_dim, int group, int block_size) {
+    return head_dim == prefill::kD && block_size == prefill::kBS &&
+           (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
+    using namespace prefill;
+    unsigned int *err = device_error_word();
+    if (!err) return cudaErrorUnknown;
+    auto encode = encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    const int G = a.num_q_heads / a.pool.num_kv_heads;
+    const int Hkv = a.pool.num_kv_heads;
+
+    // q viewed as (d, head in group, kv-head, row = s * C + j); box 64 x G x 1 x (128 / G)
+    CUtensorMap mq, mkv;
+    {
+        cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)G, (cuuint64_t)Hkv,
+                              (cuuint64_t)a.num_seqs * (cuuint64_t)a.chunk_len};
+        cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)G * kD * 2, (cuuint64_t)a.num_q_heads * kD * 2};
+        cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)(kRows / G)};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (encode(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(a.q), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    // pool viewed as (d, slot, kv-head, K|V, block); box 64 x 16 x 1 x 1 x 1
+    {
+        cuuint64_t dims[5] = {(cuuint64_t)kD, (cuuint64_t)kBS, (cuuint64_t)Hkv, 2, (cuuint64_t)a.pool.num_blocks};
+        cuuint64_t strides[4] = {(cuuint64_t)kD * 2, (cuuint64_t)kBS * kD * 2, (cuuint64_t)a.pool.kv_stride * 2,
+                                 (cuuint64_t)a.pool.block_stride * 2};
+        cuuint32_t box[5] = {64, (cuuint32_t)kBS, 1, 1, 1};
+        cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        if (encode(&mkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(a.pool.base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    Params prm;
+    prm.out = static_cast<__nv_bfloat16 *>(a.out);
+    prm.tables = a.tables;
+    prm.max_blocks = a.max_blocks;
+    prm.ctx_lens = a.ctx_lens;
+    prm.max_ctx_len = a.max_ctx_len;
+    prm.chunk = a.chunk_len;
+    prm.num_q_heads = a.num_q_heads;
+    prm.num_blocks = a.pool.num_blocks;
+    prm.scale_log2 = a.scale * kLog2e;
+    prm.err = err;
+    switch (G) {
+        case 1: return launch_group<1>(a, mq, mkv, prm, stream);
+        case 2: return launch_group<2>(a, mq, mkv, prm, stream);
+        case 4: return launch_group<4>(a, mq, mkv, prm, stream);
+        case 8: return launch_group<8>(a, mq, mkv, prm, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 }  // namespace pa

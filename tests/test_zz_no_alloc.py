@@ -30,7 +30,7 @@ def _inputs(w, dev):
             torch.as_tensor(w.seq_lens, device=dev))
 
 
-@pytest.mark.parametrize("name,part", [("llama70b_decode", 0), ("long_context", 512), ("tiny", 16)])
+@pytest.mark.parametrize("name,part", [("llama70b_decode", 320), ("long_context", 512), ("tiny", 16)])
 def test_noalloc_matches_workspace_decode(pa, name, part):
     w = wl.CONFIGS[name]()
     dev = torch.device("cuda")
