@@ -9,12 +9,17 @@ tokens, 64 query / 8 KV heads, head_dim 128, bf16, 16-token blocks placed at
 random in a 16,384-block pool.
 
 Prints one JSON line.  ``value`` is tokens/s (decoded tokens, i.e. sequences
-per step, over device time with inputs resident in HBM and L2 flushed between
-steps); ``e2e`` is the same metric through the C ABI from pinned host buffers
-(per-step inputs copied in and the output copied back inside the timed
-region; the KV pool is device-resident state).  ``roofline`` reports the
-decode call (partition kernel + reduce) against the measured HBM copy
-bandwidth.  ``cpu_baseline`` times the CPU oracle on the host cores.
+per step, over device time with inputs resident in HBM).  Between timed
+steps the L2 cache is flushed by reading a 256 MiB buffer: that evicts every
+line the previous step touched without leaving dirty lines, whose write-back
+would otherwise land inside the next timed step (the same steps timed after
+a 256 MiB write flush are reported too).  ``e2e`` is the same metric through
+the C ABI from pinned host buffers (per-step inputs copied in and the output
+copied back inside the timed region; the KV pool is device-resident state).
+``roofline`` reports the decode call against the measured HBM copy
+bandwidth.  ``prefill`` times chunked prefill (16 sequences x 4,096 cached +
+512 new tokens) against the measured bf16 tensor peak.  ``cpu_baseline``
+times the CPU oracle on the host cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -56,13 +61,49 @@ def dist_env():
     return world, rank, local
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
 def measured_peaks():
+    """(HBM GB/s, bf16 dense TFLOP/s burst, 'measured' | 'fallback')."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(p["hbm_gbs"]), float(p.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def prefill_flops(w: wl.Workload) -> int:
+    """Algorithmic FLOPs of chunked causal prefill: for every (sequence, query,
+    head) 2*d multiply-adds per visible key in Q.K and again in P.V."""
+    visible = w.ctx_lens.astype(np.int64)[:, None] + np.arange(w.chunk, dtype=np.int64)[None, :] + 1
+    return 4 * w.head_dim * int(visible.sum()) * w.num_q_heads
+
+
+def measure_prefill(pa, dev, flush_fn, iters: int = 10):
+    """Median device time of pa_prefill_chunk on the 16 x (4096 + 512) chunk."""
+    w = wl.prefill_chunk()
+    t = wl.make_tensors(w, dev)
+    tables = torch.as_tensor(w.tables, device=dev)
+    ctx = torch.as_tensor(w.ctx_lens, device=dev)
+    out = torch.empty_like(t["q"])
+    run = lambda: pa.prefill_chunk(out, t["q"], t["pool"], tables, ctx, int(w.ctx_lens.max()), w.scale)
+    for _ in range(3):
+        run()
+    ts = []
+    stream = torch.cuda.current_stream()
+    for _ in range(iters):
+        flush_fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    assert pa.get_device_error() == 0, "device error during prefill"
+    ms = float(np.median(ts))
+    return w, ms, prefill_flops(w)
 
 
 def decode_bytes(w: wl.Workload) -> int:
@@ -194,7 +235,9 @@ def run_ours(args, world, rank, local):
     tensors = wl.make_tensors(w, "cpu")
     step = DecodeStep(pa, w, dev, tensors)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_read = lambda: flush.view(torch.int32).sum()     # evicts L2, leaves no dirty lines
+    flush_write = lambda: flush.fill_(1)
 
     def barrier():
         if world > 1:
@@ -202,29 +245,34 @@ def run_ours(args, world, rank, local):
             dist.barrier()
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_read()
         step.write()
         step.decode()
     torch.cuda.synchronize()
     assert pa.get_device_error() == 0, "device error during warm-up"
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
+
+    def timed_steps(flush_fn):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        barrier()
+        torch.cuda.synchronize()
         for i in range(K):
-            flush.zero_()
+            flush_fn()
             ev[i][0].record(stream)
             step.write()
             ev[i][1].record(stream)
             step.decode()
             ev[i][2].record(stream)
         torch.cuda.synchronize()
-    barrier()
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
-    decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+        barrier()
+        return ([ev[i][0].elapsed_time(ev[i][2]) for i in range(K)],
+                [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)])
+
+    with ClockSampler(local) as clocks:
+        step_ms, decode_ms = timed_steps(flush_read)
     total_ms = sum(step_ms)
+    wstep_ms, _ = timed_steps(flush_write)
     assert pa.get_device_error() == 0, "device error during the timed steps"
 
     # ---- end to end through the C ABI from pinned host buffers
@@ -257,18 +305,21 @@ def run_ours(args, world, rank, local):
     barrier()
     e2e_s = 0.0
     for _ in range(K):
-        flush.zero_()
+        flush_read()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_step()
         e2e_s += time.perf_counter() - t0
     barrier()
 
-    elapsed = torch.tensor([total_ms, e2e_s * 1e3, float(np.mean(decode_ms))], dtype=torch.float64, device=dev)
+    prefill = None if args.no_prefill else measure_prefill(pa, dev, flush_read)
+
+    elapsed = torch.tensor([total_ms, e2e_s * 1e3, float(np.mean(decode_ms)), sum(wstep_ms)], dtype=torch.float64,
+                           device=dev)
     if world > 1:
         import torch.distributed as dist
         dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms, decode_avg_ms = elapsed.tolist()
+    total_ms, e2e_ms, decode_avg_ms, wtotal_ms = elapsed.tolist()
 
     if rank != 0:
         if world > 1:
@@ -277,7 +328,7 @@ def run_ours(args, world, rank, local):
         return
     tokens = world * w.batch * K
     value = tokens / (total_ms / 1e3)
-    peak, peak_kind = measured_peaks()
+    peak, bf16_peak, peak_kind = measured_peaks()
     alg = decode_bytes(w)
     achieved = alg / (decode_avg_ms / 1e3) / 1e9
     traffic = traffic_record()
@@ -293,7 +344,8 @@ def run_ours(args, world, rank, local):
                    "seq_len_mean": float(w.seq_lens.mean()), "pool_blocks": w.num_blocks,
                    "partition_tokens": step.part, "partitions": step.num_parts,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "flushed between steps (256 MiB write)"},
+                   "l2": "flushed between steps by reading a 256 MiB buffer (clean eviction)"},
+        "value_after_write_flush": round(tokens / (wtotal_ms / 1e3), 1),
         "roofline": {"bound": "hbm", "kernel": "pa_decode (partition kernel + reduce)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
@@ -305,6 +357,15 @@ def run_ours(args, world, rank, local):
         "gpu_launches": step.launches_per_step * K,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
     }
+    if prefill is not None:
+        pw, pms, pflop = prefill
+        line["prefill"] = {"workload": f"{pw.batch} seqs x ({int(pw.ctx_lens[0])} cached + {pw.chunk} chunk) tokens, "
+                                       f"{pw.num_q_heads}/{pw.num_kv_heads} heads, d={pw.head_dim}",
+                           "ms": round(pms, 4), "tflops": round(pflop / (pms / 1e3) / 1e12, 1),
+                           "roofline": {"bound": "tensor", "achieved": round(pflop / (pms / 1e3) / 1e12, 1),
+                                        "peak": bf16_peak, "peak_kind": peak_kind, "unit": "TFLOP/s",
+                                        "frac": round(pflop / (pms / 1e3) / 1e12 / bf16_peak, 4),
+                                        "flops": pflop}}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, tensors, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -339,7 +400,7 @@ def cpu_baseline(w, tensors, budget_s: float = 10.0):
     oracle_pass(orc, w, tb, np.arange(w.batch))
     first = time.perf_counter() - t0
     passes, elapsed = 1, first
-    while elapsed < budget_s and passes < 50:
+    while elapsed < budget_s and passes < 1000:
         t0 = time.perf_counter()
         oracle_pass(orc, w, tb, np.arange(w.batch))
         elapsed += time.perf_counter() - t0
@@ -398,6 +459,7 @@ def main(argv=None):
     ap.add_argument("--config", default="llama70b_decode",
                     choices=["tiny", "llama70b_decode", "long_context", "shared_prefix", "beam_fork"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
