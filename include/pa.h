@@ -103,15 +103,18 @@ pa_status pa_reshape_and_cache(const pa_kv_pool *pool, const void *k, const void
                                cudaStream_t stream);
 
 /*
- * Bytes of device workspace pa_decode needs for these shapes (0 when a single
- * context partition covers max_seq_len).  partition_tokens as in pa_decode;
- * 0 lets the library choose, from the current device's SM count.
+ * Bytes of device workspace pa_decode needs for these shapes.  With an
+ * explicit partition_tokens it is 0 when one partition covers max_seq_len;
+ * with partition_tokens = 0 (the balanced schedule) it is a few MB at most:
+ * (num_seqs + 1) ints plus two partial records per CTA of a grid sized from
+ * the current device's SM count.
  */
 size_t pa_decode_workspace_size(const pa_kv_pool *pool, int32_t num_seqs, int32_t num_q_heads,
                                 int32_t max_seq_len, int32_t partition_tokens);
 
 /* The partition length pa_decode will use for these shapes (a multiple of
- * block_size), or -1 if the shapes are invalid. */
+ * block_size); 0 when partition_tokens = 0 selects the balanced schedule;
+ * -1 if the shapes are invalid. */
 int32_t pa_decode_partition_tokens(const pa_kv_pool *pool, int32_t num_seqs, int32_t num_q_heads,
                                    int32_t max_seq_len, int32_t partition_tokens);
 
@@ -129,10 +132,14 @@ int32_t pa_decode_partition_tokens(const pa_kv_pool *pool, int32_t num_seqs, int
  *   seq_lens     device, [num_seqs] int32, tokens to attend (0 gives zeros)
  *   max_seq_len  host upper bound on every seq_lens[s] (sizes the grid)
  *   scale        softmax scale, usually 1/sqrt(d)
- *   partition_tokens  context tokens per split-context partition: 0 = auto,
- *                else a positive multiple of block_size.  When more than one
- *                partition covers max_seq_len, the partitions' partial
- *                results are merged by a second (reduce) kernel.
+ *   partition_tokens  0 (recommended): the balanced schedule -- a persistent
+ *                grid in which every CTA takes an equal contiguous share of
+ *                all (sequence, kv-head, 16-token stage) work, units cut
+ *                between two CTAs being merged by a second kernel.  Else a
+ *                positive multiple of block_size: split-context partitions
+ *                of that many tokens, grid (partition, kv-head, sequence),
+ *                merged by a reduce kernel when more than one covers
+ *                max_seq_len.
  *   workspace    device scratch of pa_decode_workspace_size bytes (may be
  *                NULL when that size is 0); its contents are overwritten
  *

@@ -18,11 +18,7 @@ namespace {
 #define PA_DECODE_WARPS 4
 #endif
 constexpr int kDecodeWarps = PA_DECODE_WARPS;  // warps per decode CTA (must match the kernel)
-constexpr int kAutoCtasPerSm = 2;        // resident decode CTAs per SM
-constexpr int kAutoWaves = 1;            // CTAs per resident slot the auto partition aims for: split
-                                         // only when (sequence, kv-head) units cannot fill the SMs,
-                                         // since partials and the reduce cost more than waves gain
-constexpr int kAutoMaxPartition = 1024;  // cap so long sequences still spread over SMs
+constexpr int kStreamKCtasPerSm = 2;     // resident decode CTAs per SM (persistent stream-K grid)
 constexpr size_t kWsAlign = 256;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -52,11 +48,14 @@ pa_status resolve_pool(const pa_kv_pool *pool, PoolView *out) {
 }
 
 struct DecodePlan {
-    int32_t partition_tokens;
+    bool stream_k;            // automatic plan: persistent balanced schedule
+    int32_t partition_tokens; // split-context plan
     int32_t num_partitions;
+    int32_t num_ctas;         // stream-K grid
+    size_t ws_cum_bytes;
     size_t ws_o_bytes;
     size_t ws_ml_bytes;
-    size_t total_bytes() const { return ws_o_bytes + ws_ml_bytes; }
+    size_t total_bytes() const { return ws_cum_bytes + ws_o_bytes + ws_ml_bytes; }
 };
 
 pa_status plan_decode(const PoolView &pool, int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
@@ -65,28 +64,31 @@ pa_status plan_decode(const PoolView &pool, int32_t num_seqs, int32_t num_q_head
     if (num_q_heads % pool.num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     const int group = num_q_heads / pool.num_kv_heads;
     if (!decode_supported(pool.head_dim, group, pool.block_size)) return PA_ERR_UNSUPPORTED;
-    int64_t part = partition_tokens;
-    if (part > 0) {
-        if (part % pool.block_size != 0) return PA_ERR_INVALID_ARG;
-    } else {
-        // Auto: enough partitions that the grid covers every resident CTA
-        // slot, each partition a whole number of per-warp stages.
-        const int64_t grain = (int64_t)decode_stage_tokens(pool.block_size) * kDecodeWarps;
+    *plan = DecodePlan{};
+    if (partition_tokens == 0) {
+        // Persistent stream-K: two CTAs per SM share all (sequence, kv-head,
+        // stage) work equally; at most two partial records per CTA.
+        const int64_t stage = decode_stage_tokens(pool.block_size);
+        const int64_t max_stages = (int64_t)num_seqs * pool.num_kv_heads * ceil_div(max_seq_len, stage);
         int sms = device_sm_count();
         if (sms <= 0) sms = 148;
-        const int64_t units = (int64_t)(num_seqs > 0 ? num_seqs : 1) * pool.num_kv_heads;
-        const int64_t want = ceil_div((int64_t)sms * kAutoCtasPerSm * kAutoWaves, units);
-        part = ceil_div(ceil_div(max_seq_len > 0 ? max_seq_len : 1, want), grain) * grain;
-        const int64_t cap = (kAutoMaxPartition / grain) * grain;
-        if (part > cap) part = cap;
-        if (part < grain) part = grain;
+        int64_t ctas = (int64_t)sms * kStreamKCtasPerSm;
+        if (ctas > max_stages) ctas = max_stages;
+        if (ctas < 1) ctas = 1;
+        plan->stream_k = true;
+        plan->partition_tokens = max_seq_len > 0 ? max_seq_len : 1;   // length bound used by the kernel
+        plan->num_partitions = 1;
+        plan->num_ctas = (int32_t)ctas;
+        plan->ws_cum_bytes = round_up(((size_t)num_seqs + 1) * sizeof(int32_t), kWsAlign);
+        plan->ws_o_bytes = round_up((size_t)2 * ctas * group * pool.head_dim * sizeof(float), kWsAlign);
+        plan->ws_ml_bytes = round_up((size_t)2 * ctas * group * 2 * sizeof(float), kWsAlign);
+        return PA_OK;
     }
-    const int64_t parts = max_seq_len > 0 ? ceil_div(max_seq_len, part) : 1;
+    if (partition_tokens % pool.block_size != 0) return PA_ERR_INVALID_ARG;
+    const int64_t parts = max_seq_len > 0 ? ceil_div(max_seq_len, partition_tokens) : 1;
     if (parts > 65535) return PA_ERR_INVALID_ARG;
-    plan->partition_tokens = (int32_t)part;
+    plan->partition_tokens = partition_tokens;
     plan->num_partitions = (int32_t)parts;
-    plan->ws_o_bytes = 0;
-    plan->ws_ml_bytes = 0;
     if (parts > 1) {
         const size_t rows = (size_t)num_seqs * num_q_heads * (size_t)parts;
         plan->ws_o_bytes = round_up(rows * pool.head_dim * sizeof(float), kWsAlign);
@@ -163,7 +165,7 @@ int32_t pa_decode_partition_tokens(const pa_kv_pool *pool, int32_t num_seqs, int
     if (resolve_pool(pool, &view) != PA_OK) return -1;
     DecodePlan plan;
     if (plan_decode(view, num_seqs, num_q_heads, max_seq_len, partition_tokens, &plan) != PA_OK) return -1;
-    return plan.partition_tokens;
+    return plan.stream_k ? 0 : plan.partition_tokens;
 }
 
 pa_status pa_decode(void *out, const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
@@ -197,9 +199,12 @@ pa_status pa_decode(void *out, const void *q, const pa_kv_pool *pool, const int3
     a.scale = scale;
     a.partition_tokens = plan.partition_tokens;
     a.num_partitions = plan.num_partitions;
-    a.ws_o = plan.total_bytes() ? static_cast<float *>(workspace) : nullptr;
-    a.ws_ml = plan.total_bytes() ? reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_o_bytes)
-                                 : nullptr;
+    char *ws = static_cast<char *>(workspace);
+    a.ws_cum = plan.ws_cum_bytes ? reinterpret_cast<int32_t *>(ws) : nullptr;
+    a.ws_o = plan.ws_o_bytes ? reinterpret_cast<float *>(ws + plan.ws_cum_bytes) : nullptr;
+    a.ws_ml = plan.ws_ml_bytes ? reinterpret_cast<float *>(ws + plan.ws_cum_bytes + plan.ws_o_bytes) : nullptr;
+    a.stream_k = plan.stream_k;
+    a.num_ctas = plan.num_ctas;
     return launch_decode(a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -48,8 +48,11 @@ struct DecodeArgs {
     float scale;
     int32_t partition_tokens;  // resolved (> 0, multiple of block_size)
     int32_t num_partitions;    // ceil(max_seq_len / partition_tokens), >= 1
-    float *ws_o;               // [B][Hq][P][d] when num_partitions > 1
-    float *ws_ml;              // [B][Hq][P][2]
+    float *ws_o;               // split: [B][Hq][P][d] when num_partitions > 1; stream-K: [2C][G][d]
+    float *ws_ml;              // split: [B][Hq][P][2]; stream-K: [2C][G][2]
+    bool stream_k;             // persistent balanced schedule (automatic plan)
+    int32_t *ws_cum;           // stream-K: [B + 1] stage prefix
+    int32_t num_ctas;          // stream-K grid size C
 };
 
 // Tokens per pipeline stage of the decode kernel for a block size (the

@@ -80,8 +80,14 @@ def test_workspace_size(B):
     assert n == 64 * 64 * 2 * 128 * 4 + 64 * 64 * 2 * 2 * 4
     assert L.pa_decode_workspace_size(ctypes.byref(pool), 64, 64, 512, 512) == 0
     assert L.pa_decode_partition_tokens(ctypes.byref(pool), 64, 64, 851, 512) == 512
-    auto = L.pa_decode_partition_tokens(ctypes.byref(pool), 64, 64, 851, 0)
-    assert auto > 0 and auto % 16 == 0
+    # partition_tokens = 0 selects the balanced (stream-K) schedule: a stage
+    # prefix of B + 1 ints and two partial records of G heads per CTA
+    assert L.pa_decode_partition_tokens(ctypes.byref(pool), 64, 64, 851, 0) == 0
+    ws = L.pa_decode_workspace_size(ctypes.byref(pool), 64, 64, 851, 0)
+    rup = lambda x: -(-x // 256) * 256
+    ctas = ws and next(c for c in range(1, 4097)
+                       if rup(65 * 4) + rup(2 * c * 8 * 128 * 4) + rup(2 * c * 8 * 2 * 4) == ws)
+    assert ctas and ctas % 2 == 0
 
 
 def test_block_layout_matches_oracle(B):

@@ -239,7 +239,9 @@ def test_device_errors_are_reported_not_faulted(pa):
     c_tables = c.tables
     c.tables = bad_tables
     out = torch.empty_like(c.q)
-    pa.decode(out, c.q, c.pool, c.tables, c.seq_lens, w.max_seq_len, w.scale, 0, None)
+    nbytes = pa.decode_workspace_size(c.pool, w.batch, w.num_q_heads, w.max_seq_len, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=c.dev)
+    pa.decode(out, c.q, c.pool, c.tables, c.seq_lens, w.max_seq_len, w.scale, 0, ws)
     assert pa.get_device_error() & B.DEVERR_BLOCK_ID
     c.tables = c_tables
     slots = torch.as_tensor([w.num_blocks * w.block_size + 3, -1], device=c.dev, dtype=torch.int64)
@@ -251,7 +253,7 @@ def test_device_errors_are_reported_not_faulted(pa):
     assert pa.get_device_error() & B.DEVERR_BLOCK_ID
     assert torch.equal(before, c.pool)
     long_lens = torch.as_tensor([w.max_blocks * w.block_size + 1, 9], device=c.dev, dtype=torch.int32)
-    pa.decode(out, c.q, c.pool, c.tables, long_lens, w.max_seq_len, w.scale, 0, None)
+    pa.decode(out, c.q, c.pool, c.tables, long_lens, w.max_seq_len, w.scale, 0, ws)
     assert pa.get_device_error() & B.DEVERR_SEQ_LEN
     # still healthy afterwards
     assert_close(run_decode(pa, c, 0), oracle_decode(c), "after errors")
