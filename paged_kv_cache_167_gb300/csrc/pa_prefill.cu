@@ -11,9 +11,11 @@
 // listing (the gather belongs inside the kernel's tiling loop).
 //
 // Design:
-//  * One CTA (4 warps) per 128-row M-tile of one (sequence, kv-head): row r is
-//    query j0 + r / G of head g*G + r % G, so every K/V tile staged in shared
-//    memory serves the whole query group.
+//  * One CTA per 128-row M-tile of one (sequence, kv-head): row r is query
+//    j0 + r / G of head g*G + r % G, so every K/V tile staged in shared memory
+//    serves the whole query group.  Nine warps: one producer lane issues every
+//    copy and MMA; eight softmax warps in two warpgroups each own 64 of a
+//    row's 128 keys (tensor-memory lanes follow warp % 4).
 //  * TMA (cp.async.bulk.tensor, 128-byte swizzle) brings Q and the K/V tiles:
 //    a K or V tile of 128 keys is 8 blocks x 2 halves of d, one box of
 //    16 rows x 64 dims per (block, half), addressed through a 5-D tensor map of
@@ -22,14 +24,17 @@
 //    out-of-bounds coordinate, which TMA fills with zeros.  No multicast.
 //  * S = Q.K^T and O += P.V are tcgen05.mma kind::f16 (bf16 in, fp32 out)
 //    with M = N = 128, K = 16 per instruction, accumulators in tensor memory
-//    (S in columns 0..127, O in 128..255), issued by one thread and tracked
-//    with tcgen05.commit on mbarriers.
-//  * Softmax: thread r owns row r (tensor-memory lane r).  It reads S with
-//    tcgen05.ld, applies the scale and the causal mask, keeps a reference
-//    maximum in the log2 domain that only moves when a tile's maximum exceeds
-//    it by more than 8 (so p <= 2^8 and O needs rescaling rarely; the result
-//    is exact because l and O share the reference), writes P as bf16 into
-//    the swizzled shared-memory layout the next MMA reads, and sums the same
+//    (two S buffers in columns 0..255, O in 256..383), tracked with
+//    tcgen05.commit on mbarriers.  The producer issues Q.K(t+1) into the
+//    other S buffer before P.V(t), so the tensor pipe works on the next tile
+//    while the softmax warps process this one.
+//  * Softmax: each thread owns half of one row.  It reads S with tcgen05.ld,
+//    applies the scale and the causal mask, agrees with the other half on the
+//    tile maximum through shared memory, keeps a reference maximum in the
+//    log2 domain that only moves when a tile's maximum exceeds it by more
+//    than 8 (so p <= 2^8 and O needs rescaling rarely; the result is exact
+//    because l and O share the reference), writes P as bf16 into one of two
+//    swizzled shared-memory buffers the next MMA reads, and sums the same
 //    rounded values into l.
 //  * K and V rings of two stages each; a K slot is refilled once its Q.K MMA
 //    has completed, a V slot once its P.V MMA has.
@@ -46,7 +51,9 @@
 namespace pa {
 namespace prefill {
 
-constexpr int kThreads = 128;
+constexpr int kSoftWarps = 8;               // two warpgroups, each owning 64 of a row's 128 keys
+constexpr int kProducerWarp = kSoftWarps;   // one more warp issues every copy and MMA
+constexpr int kThreads = (kSoftWarps + 1) * 32;
 constexpr int kRows = 128;                  // M tile
 constexpr int kKeys = 128;                  // N tile of Q.K (keys per iteration)
 constexpr int kD = 128;                     // head_dim
@@ -56,12 +63,14 @@ constexpr uint32_t kTile = 2u * kHalf;      // [2 halves][128 rows][128 B]
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTile;   // 2 stages
 constexpr uint32_t kOffV = kOffK + 2 * kTile;
-constexpr uint32_t kOffP = kOffV + 2 * kTile;
-constexpr uint32_t kOffBar = kOffP + kTile;
-constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;   // + alignment slack
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kOffP = kOffV + 2 * kTile; // 2 buffers
+constexpr uint32_t kOffX = kOffP + 2 * kTile; // [2 halves][128 rows] fp32 exchange
+constexpr uint32_t kOffBar = kOffX + 1024;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // + alignment slack
+constexpr uint32_t kTmemCols = 512;         // S0, S1, O (128 columns each)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 domain
+static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct Params {
     __nv_bfloat16 *out;          // [B][C][Hq][D]
@@ -164,6 +173,20 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // ---- the kernel ---------------------------------------------------------------
 
+__device__ __forceinline__ void mbar_arrive_u32(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void pair_sync(int warp) {   // warps w and w + 4 own the same rows
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + (warp & 3)), "r"(64) : "memory");
+}
+
+// Timeline of tile t (the producer runs one tile ahead):
+//   producer : Q.K(t+1) -> S[(t+1)%2] ; refill K(t+2), V(t+1) ; P.V(t) once P(t) is ready
+//   softmax  : S[t%2] -> registers (frees S) ; row max over both halves ; P(t) ;
+//              O rescale when the reference moved ; signal P(t)
+// Barriers: S ready (MMA commit), S free (256 arrivals), P ready (256 arrivals),
+// P.V done per P buffer (MMA commit), K / V / Q landed (TMA).
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
@@ -173,30 +196,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     unsigned char *gbase = smem_raw + (base - smem_addr(smem_raw));
     const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sP = base + kOffP;
-    const uint32_t barQ = base + kOffBar, barK = barQ + 8, barV = barQ + 24, barS = barQ + 40, barO = barQ + 48;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 64);
+    float *xch = reinterpret_cast<float *>(gbase + kOffX);
+    const uint32_t barQ = base + kOffBar;
+    const uint32_t barK = barQ + 8, barV = barQ + 24, barS = barQ + 40, barSfree = barQ + 56, barP = barQ + 72,
+                   barOP = barQ + 88;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 128);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffBar + 132);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
     const int j0 = mt * QPT;
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
                      "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        for (int i = 0; i < 7; ++i)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(barQ + 8 * i) : "memory");
+        const uint32_t counts[13] = {1, 1, 1, 1, 1, 1, 1, 256, 256, 256, 256, 1, 1};
+        for (int i = 0; i < 13; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(barQ + 8 * i), "r"(counts[i]) : "memory");
+        *abort_flag = 0;
         fence_barrier_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + 128;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tO = tmem + 256;
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -209,217 +237,258 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nblk_seq = (seq_end + kBS - 1) / kBS;
     const int last_q = min(j0 + QPT, p.chunk) - 1;             // last valid query of this tile
     const int n_tiles = (ctx + last_q + 1 + kKeys - 1) / kKeys;
-    const int32_t *table_row = p.tables + (size_t)s * p.max_blocks;
-
-    // physical block of logical block bi, or the out-of-bounds coordinate (zero fill)
-    auto phys = [&](int bi) -> int {
-        if (bi >= nblk_seq) return (int)p.num_blocks;
-        const int id = __ldg(table_row + bi);
-        if (id < 0 || id >= p.num_blocks) {
-            raise_error(p.err, PA_DEVERR_BLOCK_ID);
-            return (int)p.num_blocks;
-        }
-        return id;
-    };
-    int issued_tiles[2] = {0, 0};   // K, V tiles whose copies thread 0 has issued
-    int waited_tiles[2] = {0, 0};   // K, V tiles whose arrival thread 0 has seen
-    auto load_kv = [&](int t, int kv) {   // thread 0 only
-        issued_tiles[kv] = t + 1;
-        const int st = t & 1;
-        const uint32_t dst = (kv ? sV : sK) + st * kTile;
-        const uint32_t bar = (kv ? barV : barK) + 8 * st;
-        mbar_expect(bar, kTile);
-#pragma unroll
-        for (int i = 0; i < kKeys / kBS; ++i) {
-            const int blk = phys(t * (kKeys / kBS) + i);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) tma_load_5d(dst + h * kHalf + i * 2048, &tmap_kv, h * 64, 0, g, kv, blk, bar);
-        }
-    };
-
-    if (tid == 0) {
-        mbar_expect(barQ, kTile);
-        const int qrow = s * p.chunk + j0;
-        tma_load_4d(sQ, &tmap_q, 0, 0, g, qrow, barQ);
-        tma_load_4d(sQ + kHalf, &tmap_q, 64, 0, g, qrow, barQ);
-        for (int t = 0; t < 2 && t < n_tiles; ++t) {
-            load_kv(t, 0);
-            load_kv(t, 1);
-        }
-    }
-
-    const int r = tid;                                   // this thread's row
-    const int jr = j0 + r / G;
-    const int pos = min(ctx + jr, seq_end - 1);          // last key this row may attend
     constexpr uint32_t idesc_qk = idesc_bf16(kRows, kKeys, false);
     constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, true);
-    float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-    int issued_o = 0;                                    // P.V commits issued
 
-    for (int t = 0; t < n_tiles && ok; ++t) {
-        const int st = t & 1;
-        const uint32_t ph2 = (uint32_t)((t >> 1) & 1);
-        // ---- S = Q . K^T
-        if (tid == 0) {
-            bool w = (t > 0 || mbar_wait(barQ, 0, p.err)) && mbar_wait(barK + 8 * st, ph2, p.err);
-            if (w) {
-                waited_tiles[0] = t + 1;
-                tc_fence_after();
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            const int32_t *table_row = p.tables + (size_t)s * p.max_blocks;
+            auto phys = [&](int bi) -> int {   // physical block, or the out-of-bounds coordinate (zero fill)
+                if (bi >= nblk_seq) return (int)p.num_blocks;
+                const int id = __ldg(table_row + bi);
+                if (id < 0 || id >= p.num_blocks) {
+                    raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                    return (int)p.num_blocks;
+                }
+                return id;
+            };
+            int issued[2] = {0, 0}, waited[2] = {0, 0};   // K, V tiles issued / seen landed
+            auto load_kv = [&](int t, int kv) {
+                issued[kv] = t + 1;
+                const int st = t & 1;
+                const uint32_t dst = (kv ? sV : sK) + st * kTile;
+                const uint32_t bar = (kv ? barV : barK) + 8 * st;
+                mbar_expect(bar, kTile);
+#pragma unroll
+                for (int i = 0; i < kKeys / kBS; ++i) {
+                    const int blk = phys(t * (kKeys / kBS) + i);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_5d(dst + h * kHalf + i * 2048, &tmap_kv, h * 64, 0, g, kv, blk, bar);
+                }
+            };
+            auto qk = [&](int t) {
+                const int st = t & 1;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    umma(tS, smem_desc(sQ + off, 16, 1024), smem_desc(sK + st * kTile + off, 16, 1024), idesc_qk,
-                         kk > 0);
+                    umma(tmem + st * 128, smem_desc(sQ + off, 16, 1024), smem_desc(sK + st * kTile + off, 16, 1024),
+                         idesc_qk, kk > 0);
                 }
-            }
-            umma_commit(barS);   // arrives even if nothing was issued
-            if (!w) ok = false;
-        }
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        if (!mbar_wait(barS, (uint32_t)(t & 1), p.err)) ok = false;
-        // P smem and O are still read/written by the previous P.V until it completes
-        if (ok && t > 0 && !mbar_wait(barO, (uint32_t)((t - 1) & 1), p.err)) ok = false;
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        tc_fence_after();
-        if (tid == 0) {
-            if (t + 2 < n_tiles) load_kv(t + 2, 0);          // K slot st is free: its Q.K completed
-            if (t >= 1 && t + 1 < n_tiles) load_kv(t + 1, 1); // V slot of tile t-1 is free
-        }
-
-        // ---- softmax of row r over this tile's 128 keys
-        uint32_t sraw[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, sraw[c]);
-        tmem_ld_wait();
-        const int key0 = t * kKeys;
-        float mt_ = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float x = key0 + c * 32 + i <= pos ? __uint_as_float(sraw[c][i]) * p.scale_log2 : -INFINITY;
-                sraw[c][i] = __float_as_uint(x);
-                mt_ = fmaxf(mt_, x);
-            }
-        float alpha = 1.f;
-        if (mt_ > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt_ != -INFINITY)) {
-            alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - mt_);
-            m_ref = mt_;
-        }
-        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        float psum = 0.f;
-        const uint32_t prow = sP + (uint32_t)r * 128u;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {        // 8 keys = one 16-byte chunk
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a = fast_exp2(__uint_as_float(sraw[c][q4 * 8 + 2 * e]) - m_use);
-                    const float b = fast_exp2(__uint_as_float(sraw[c][q4 * 8 + 2 * e + 1]) - m_use);
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(a, b);
-                    psum += __low2float(pr) + __high2float(pr);
-                    w[e] = *reinterpret_cast<const uint32_t *>(&pr);
+                umma_commit(barS + 8 * st);
+            };
+            bool ok = true;
+            auto wait = [&](uint32_t bar, uint32_t parity) {
+                if (ok && !mbar_wait(bar, parity, p.err)) {
+                    ok = false;
+                    *abort_flag = 1;
                 }
-                const int key = c * 32 + q4 * 8;                // 0..127
-                const uint32_t half = (uint32_t)(key >> 6);
-                const uint32_t chunk = (uint32_t)((key & 63) >> 3);
-                const uint32_t addr = prow + half * kHalf + ((chunk ^ (uint32_t)(r & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                             "r"(w[3])
-                             : "memory");
+                return ok;
+            };
+            mbar_expect(barQ, kTile);
+            const int qrow = s * p.chunk + j0;
+            tma_load_4d(sQ, &tmap_q, 0, 0, g, qrow, barQ);
+            tma_load_4d(sQ + kHalf, &tmap_q, 64, 0, g, qrow, barQ);
+            for (int t = 0; t < 2 && t < n_tiles; ++t) {
+                load_kv(t, 0);
+                load_kv(t, 1);
             }
-        }
-        l = l * alpha + psum;
-        // rescale O (only warps where some row's reference moved)
-        if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tO + lane_off + c * 32, o);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                tmem_st32(tO + lane_off + c * 32, o);
+            int committed_pv = 0;
+            if (wait(barQ, 0) && wait(barK, 0)) {
+                waited[0] = 1;
+                tc_fence_after();
+                qk(0);
             }
-            tmem_st_wait();
-        }
-        // keys past the sequence end inside the last block: zero their V rows
-        // (their p is 0, but the slots may hold non-finite junk)
-        const int tail_lo = seq_end - key0, blk_end = ((seq_end + kBS - 1) / kBS) * kBS - key0;
-        if (tail_lo > 0 && tail_lo < kKeys && (seq_end % kBS) != 0) {
-            if (!mbar_wait(barV + 8 * st, ph2, p.err)) ok = false;
-            const int nrows = min(blk_end, kKeys) - tail_lo;
-            for (int idx = tid; idx < nrows * 2 * 8; idx += kThreads) {
-                const int rr = tail_lo + idx / 16, h = (idx / 8) & 1, c16 = idx & 7;
-                const uint32_t addr = sV + st * kTile + h * kHalf + (uint32_t)rr * 128u + (uint32_t)c16 * 16u;
-                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
-            }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        // ---- O += P . V
-        if (tid == 0) {
-            tc_fence_after();
-            const bool w = mbar_wait(barV + 8 * st, ph2, p.err);
-            if (w) {
-                waited_tiles[1] = t + 1;
+            for (int t = 0; t < n_tiles && ok && !*abort_flag; ++t) {
+                const int st = t & 1, st1 = (t + 1) & 1;
+                if (t + 1 < n_tiles) {
+                    if (!wait(barK + 8 * st1, (uint32_t)(((t + 1) >> 1) & 1))) break;
+                    waited[0] = t + 2;
+                    if (t >= 1 && !wait(barSfree + 8 * st1, (uint32_t)(((t - 1) >> 1) & 1))) break;
+                    tc_fence_after();
+                    qk(t + 1);
+                }
+                if (t + 2 < n_tiles) {   // K slot st is free once Q.K(t) completed
+                    if (!wait(barS + 8 * st, (uint32_t)((t >> 1) & 1))) break;
+                    load_kv(t + 2, 0);
+                }
+                if (t >= 1 && t + 1 < n_tiles) {   // V slot st1 is free once P.V(t-1) completed
+                    if (!wait(barOP + 8 * st1, (uint32_t)(((t - 1) >> 1) & 1))) break;
+                    load_kv(t + 1, 1);
+                }
+                if (!wait(barP + 8 * st, (uint32_t)((t >> 1) & 1))) break;
+                if (!wait(barV + 8 * st, (uint32_t)((t >> 1) & 1))) break;
+                waited[1] = t + 1;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
                     const uint32_t a_off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    umma(tO, smem_desc(sP + a_off, 16, 1024), smem_desc(sV + st * kTile + kk * 2048, kHalf, 1024),
-                         idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                    umma(tO, smem_desc(sP + st * kTile + a_off, 16, 1024),
+                         smem_desc(sV + st * kTile + kk * 2048, kHalf, 1024), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
                 }
+                umma_commit(barOP + 8 * st);
+                committed_pv = t + 1;
             }
-            umma_commit(barO);
-            if (!w) ok = false;
-        }
-        ++issued_o;
-    }
-
-    // ---- epilogue: O / l to bf16
-    const bool fin = ok && issued_o > 0 && mbar_wait(barO, (uint32_t)((issued_o - 1) & 1), p.err);
-    tc_fence_after();
-    const bool row_ok = jr < p.chunk;
-    if (__syncthreads_and(fin)) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16 *dst = p.out + (((size_t)s * p.chunk + jr) * p.num_q_heads + (size_t)g * G + (r % G)) * kD;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + lane_off + c * 32, o);
-            tmem_ld_wait();
-            if (row_ok) {
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint4 v;
-                    v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
-                    v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
-                    v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
-                    v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
-                    *reinterpret_cast<uint4 *>(dst + c * 32 + q4 * 8) = v;
-                }
+            if (!ok || *abort_flag) {
+                // Give up: wait (bounded) for every copy still in flight and,
+                // through one more commit on the Q barrier, for every issued MMA.
+                *abort_flag = 1;
+                for (int kv = 0; kv < 2; ++kv)
+                    for (int tt = waited[kv]; tt < issued[kv]; ++tt)
+                        mbar_wait((kv ? barV : barK) + 8 * (tt & 1), (uint32_t)((tt >> 1) & 1), p.err);
+                umma_commit(barQ);
+                mbar_wait(barQ, 1, p.err);
+            } else if (committed_pv > 0) {
+                const int t = committed_pv - 1;   // all MMAs done before the memory is released
+                mbar_wait(barOP + 8 * (t & 1), (uint32_t)((t >> 1) & 1), p.err);
             }
         }
-    } else if (tid == 0) {
-        // A wait gave up.  Before the shared and tensor memory are released,
-        // wait (bounded) for every copy still in flight and, through one more
-        // commit on the Q barrier (its second phase), for every issued MMA.
-        for (int kv = 0; kv < 2; ++kv)
-            for (int tt = waited_tiles[kv]; tt < issued_tiles[kv]; ++tt)
-                mbar_wait((kv ? barV : barK) + 8 * (tt & 1), (uint32_t)((tt >> 1) & 1), p.err);
-        umma_commit(barQ);
-        mbar_wait(barQ, 1, p.err);
+        __syncwarp();
+    } else {
+        // ---- softmax warps: row r, key half hf
+        const int r = (warp & 3) * 32 + lane, hf = warp >> 2;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const int jr = j0 + r / G;
+        const int pos = min(ctx + jr, seq_end - 1);   // last key this row may attend
+        float m_ref = -INFINITY, l = 0.f;
+        int done = 0;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t & 1;
+            bool ok = mbar_wait(barS + 8 * st, (uint32_t)((t >> 1) & 1), p.err);
+            uint32_t sr[2][32];
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+                tmem_ld32(tmem + st * 128 + lane_off + hf * 64, sr[0]);
+                tmem_ld32(tmem + st * 128 + lane_off + hf * 64 + 32, sr[1]);
+                tmem_ld_wait();
+            } else {
+                ok = false;
+            }
+            tc_fence_before();
+            mbar_arrive_u32(barSfree + 8 * st);
+            const int key0 = t * kKeys + hf * 64;
+            float mh = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float x = key0 + c * 32 + i <= pos ? __uint_as_float(sr[c][i]) * p.scale_log2 : -INFINITY;
+                    sr[c][i] = __float_as_uint(x);
+                    mh = fmaxf(mh, x);
+                }
+            // both halves of the row agree on the tile maximum and on giving up
+            xch[hf * 128 + r] = (ok && !*abort_flag) ? mh : __int_as_float(0x7fc00001);
+            pair_sync(warp);
+            const float other = xch[(1 - hf) * 128 + r];
+            const float mine = xch[hf * 128 + r];
+            pair_sync(warp);
+            const bool stop = __any_sync(0xffffffffu, __float_as_int(other) == 0x7fc00001 ||
+                                                          __float_as_int(mine) == 0x7fc00001);
+            if (stop) {
+                *abort_flag = 1;
+                mbar_arrive_u32(barP + 8 * st);   // keep the arrival count balanced
+                break;
+            }
+            const float mt_ = fmaxf(mh, other);
+            float alpha = 1.f;
+            if (mt_ > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt_ != -INFINITY)) {
+                alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - mt_);
+                m_ref = mt_;
+            }
+            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+            // P buffer st was last read by P.V(t-2)
+            if (t >= 2) mbar_wait(barOP + 8 * st, (uint32_t)(((t - 2) >> 1) & 1), p.err);
+            float psum = 0.f;
+            const uint32_t prow = sP + st * kTile + hf * kHalf + (uint32_t)r * 128u;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {        // 8 keys = one 16-byte chunk
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a = fast_exp2(__uint_as_float(sr[c][q4 * 8 + 2 * e]) - m_use);
+                        const float b = fast_exp2(__uint_as_float(sr[c][q4 * 8 + 2 * e + 1]) - m_use);
+                        const __nv_bfloat162 pr = __floats2bfloat162_rn(a, b);
+                        psum += __low2float(pr) + __high2float(pr);
+                        w[e] = *reinterpret_cast<const uint32_t *>(&pr);
+                    }
+                    const uint32_t chunk = (uint32_t)(c * 4 + q4);
+                    const uint32_t addr = prow + ((chunk ^ (uint32_t)(r & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                                 "r"(w[2]), "r"(w[3])
+                                 : "memory");
+                }
+            }
+            l = l * alpha + psum;
+            // rescale this half of O once P.V(t-1) has completed
+            if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                const int tp = t - 1;
+                mbar_wait(barOP + 8 * (tp & 1), (uint32_t)((tp >> 1) & 1), p.err);
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + lane_off + hf * 64 + c * 32, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(tO + lane_off + hf * 64 + c * 32, o);
+                }
+                tmem_st_wait();
+            }
+            // keys past the sequence end inside its last block: zero their V rows
+            // (their p is 0, but the slots may hold non-finite junk)
+            const int tile0 = t * kKeys;
+            const int tail_lo = seq_end - tile0, blk_end = ((seq_end + kBS - 1) / kBS) * kBS - tile0;
+            if (tail_lo > 0 && tail_lo < kKeys && (seq_end % kBS) != 0) {
+                mbar_wait(barV + 8 * st, (uint32_t)((t >> 1) & 1), p.err);
+                const int nrows = min(blk_end, kKeys) - tail_lo;
+                for (int idx = tid; idx < nrows * 2 * 8; idx += kSoftWarps * 32) {
+                    const int rr = tail_lo + idx / 16, h = (idx / 8) & 1, c16 = idx & 7;
+                    const uint32_t addr = sV + st * kTile + h * kHalf + (uint32_t)rr * 128u + (uint32_t)c16 * 16u;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive_u32(barP + 8 * st);
+            done = t + 1;
+        }
+        // ---- epilogue: O / l to bf16, this thread's row and key half
+        const bool fin = done == n_tiles && !*abort_flag &&
+                         mbar_wait(barOP + 8 * ((n_tiles - 1) & 1), (uint32_t)(((n_tiles - 1) >> 1) & 1), p.err);
+        xch[hf * 128 + r] = l;
+        pair_sync(warp);
+        const float lt = l + xch[(1 - hf) * 128 + r];
+        tc_fence_after();
+        if (__all_sync(0xffffffffu, fin)) {
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const bool row_ok = jr < p.chunk;
+            __nv_bfloat16 *dst =
+                p.out + (((size_t)s * p.chunk + jr) * p.num_q_heads + (size_t)g * G + (r % G)) * kD + hf * 64;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + lane_off + hf * 64 + c * 32, o);
+                tmem_ld_wait();
+                if (row_ok) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
+                        v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
+                        v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
+                        v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(dst + c * 32 + q4 * 8) = v;
+                    }
+                }
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
