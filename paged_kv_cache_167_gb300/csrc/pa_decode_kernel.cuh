@@ -25,30 +25,26 @@
 //        removes the partly filled last wave and the per-CTA start-up of a
 //        unit-per-CTA grid.
 //  * Each warp owns every W-th stage of its CTA's work and a private ring of
-//    STAGES shared-memory slots.  Lane 0 fetches a stage's K and V slabs (b*d
-//    bf16 each, contiguous in the pool) with bulk TMA copies that complete on
-//    the slot's mbarrier; block ids come from a per-warp register cache filled
-//    by all lanes, so address generation never waits on a dependent table
-//    load.  No data is multicast.
+//    STAGES shared-memory slots.  Lane 0 fetches a stage's K and V blocks with
+//    tensor copies (one box of b tokens x d per block and K|V, 128-byte
+//    swizzle) that complete on the slot's mbarrier; block ids come from a
+//    per-warp register cache filled by all lanes, so address generation never
+//    waits on a dependent table load.  No data is multicast.
 //  * All G query heads of the group are served from one staged copy of the
-//    block.  The arithmetic is the fp32-accumulating bf16 FMA of sm_100-class
-//    SMs (fma.rn.f32.bf16): K, V and q are used as stored, each product is
-//    exact in fp32, and no operand needs converting.
-//  * Q.K: a lane owns 8 of the d dimensions of a token row (16 B) and keeps q
-//    for all G heads on those dimensions in registers (packed bf16).  Partial
-//    dot products are combined across the row's lanes with a transposing
-//    butterfly: at each shuffle step a lane keeps half of its values and
-//    receives the other half from its partner.  When a row has exactly 2G
-//    lanes, two token rows are reduced together and every lane ends with one
-//    (row, head) score.  Query slots are stored in a lane-dependent order so
-//    that every register index of the butterfly is static.
-//  * Online softmax in the log2 domain per warp.  Probabilities are rounded
-//    to bf16 once and broadcast through shared memory (one 16-byte load gives
-//    a token's 8 heads); the softmax denominator sums the same rounded values,
-//    so the output is an exact weighted average with those weights.  The
-//    running-max correction of the accumulators is skipped when no head's
-//    maximum moved.
-//  * P.V: a lane owns 8 dims x G heads of fp32 accumulators.
+//    block, on the tensor cores: per 16 tokens, S^T = K . Q^T is an
+//    m16n8k16 bf16 MMA with fp32 accumulation (tokens on M, the group's
+//    heads on N, d on K), and O^T += V^T . P^T another (d on M, heads on N,
+//    tokens on K).  A lane reads whole 16-byte chunks of K and V rows from
+//    shared memory; which d a chunk element stands for is a fixed
+//    permutation that q (loaded once in the same order) and the output
+//    write-back follow, and the 128-byte swizzle makes every read
+//    bank-conflict free.  P^T is formed from the S^T accumulators with one
+//    register transpose (movmatrix) per 8 x 8 tile.
+//  * Online softmax in the log2 domain per warp: a head's running maximum
+//    is reduced across the 8 lanes holding its tokens.  Probabilities are
+//    rounded to bf16 once; the softmax denominator sums the same rounded
+//    values, so the output is an exact weighted average with those weights.
+//    The accumulators are rescaled only when some head's maximum moved.
 //  * The warps' (m, l, o) are merged in shared memory; bf16 output or fp32
 //    partials (o normalised by l, m in the log2 domain, l) are written.
 //  * Every table entry and length is bounds-checked; an out-of-range value is
@@ -90,36 +86,28 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
-template <int D, int G, int BS>
+template <int D, int BS>
 struct Shape {
-    static constexpr int LPR = D / 8;                 // lanes per token row (8 dims each)
-    static constexpr int TPI = 32 / LPR;              // tokens per warp iteration
     static constexpr int TPS = BS >= 16 ? BS : 16;    // tokens per pipeline stage
     static constexpr int BPS = TPS / BS;              // blocks per stage
-    static constexpr int ITERS = TPS / TPI;           // P.V iterations per stage
-    static constexpr int SLAB = BS * D;               // elements of one (block, K|V, head) slab
-    static constexpr int LOG_LPR = ilog2(LPR);
-    static constexpr int NT = ilog2(G);               // transposing butterfly steps
-    static constexpr int DUP = LPR / G;               // lanes holding the same head's score (one row)
-    // Two token rows are reduced jointly when a row's lanes number exactly 2G.
-    static constexpr bool JOINT = LPR == 2 * G;
-    static constexpr int ROWS = JOINT ? 2 : 1;        // token rows per Q.K butterfly
-    static constexpr int QK_ITERS = TPS / (ROWS * TPI);
-    static constexpr int PW = G < 2 ? 1 : G / 2;      // 32-bit words of one token's bf16 probabilities
+    static constexpr int KS = TPS / 16;               // 16-token MMA steps per stage
+    static constexpr int HALVES = D / 64;             // 128-byte halves of a token row
+    static constexpr int BOX = BS * D * 2;            // bytes of one (block, K|V, head) copy
+    static constexpr int REGION = BOX < 1024 ? 1024 : BOX;   // its place in a slot (swizzle-atom aligned)
+    static constexpr int SLOT = BPS * REGION;         // bytes of a stage's K (or V) slot
+    static constexpr int NCH = D / 32;                // 16-byte chunks of a K row that one lane reads
+    static constexpr int DK = D / 16;                 // Q.K steps over d = P.V tiles of d
     static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group");
-    static_assert(TPS % (ROWS * TPI) == 0 && TPS % BS == 0, "stage shape");
-    static_assert(BPS <= 32, "table cache");
+    static_assert(BS == 4 || BS == 8 || BS == 16 || BS == 32, "block size");
 };
 
-template <int D, int G, int BS, int NS>
-struct alignas(16) WarpSmem {
-    using S = Shape<D, G, BS>;
-    __nv_bfloat16 k[NS][S::TPS * D];
-    __nv_bfloat16 v[NS][S::TPS * D];
-    uint32_t p[S::TPS][S::PW];        // bf16 probabilities by (token, head), packed in pairs
-    float alpha[G < 4 ? 4 : G];       // running-max correction by head
-    uint64_t bar[NS + (NS & 1)];
+// Per-warp ring of NS stage slots, K slots then V slots.  A block's box starts
+// on a 1024-byte boundary, so its 128-byte swizzle pattern follows from the
+// offset inside the box.
+template <int D, int BS, int NS>
+struct alignas(1024) WarpRing {
+    unsigned char k[NS][Shape<D, BS>::SLOT];
+    unsigned char v[NS][Shape<D, BS>::SLOT];
 };
 
 // CTA-level scratch of the stream-K kernel (after the warps' rings).
@@ -135,13 +123,23 @@ struct alignas(16) SkSmem {
     uint64_t qbar[2];
 };
 
+// Dynamic shared memory: [slack to 1024][rings][ring barriers][extra].
+template <int D, int BS, int NS>
+struct SmemPlan {
+    static constexpr size_t kRings = sizeof(WarpRing<D, BS, NS>) * kWarps;
+    static constexpr size_t kBars = ((kWarps * NS * sizeof(uint64_t) + 127) / 128) * 128;
+    static constexpr size_t bytes(size_t extra) { return 1024 + kRings + kBars + extra; }
+};
+
+__device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
+    const uint32_t a = smem_addr(p);
+    return p + (((a + 1023u) & ~1023u) - a);
+}
+
 struct Params {
     __nv_bfloat16 *out;
     const __nv_bfloat16 *q;
-    const __nv_bfloat16 *pool;
     int64_t num_blocks;
-    int64_t block_stride;
-    int64_t kv_stride;
     const int32_t *tables;
     int32_t max_blocks;
     const int32_t *seq_lens;
@@ -174,234 +172,234 @@ __device__ __forceinline__ int effective_len(const Params &p, int s, int block_s
     return L;
 }
 
-// acc += (bf16 half HA of a) * (bf16 half HB of b), fp32 accumulate; 0 = low half.
-template <int HA, int HB>
-__device__ __forceinline__ void bf16_fma(float &acc, uint32_t a, uint32_t b) {
-    if constexpr (HA == 0 && HB == 0)
-        asm("{ .reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-            "fma.rn.f32.bf16 %0, al, bl, %0; }" : "+f"(acc) : "r"(a), "r"(b));
-    else if constexpr (HA == 0 && HB == 1)
-        asm("{ .reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-            "fma.rn.f32.bf16 %0, al, bh, %0; }" : "+f"(acc) : "r"(a), "r"(b));
-    else if constexpr (HA == 1 && HB == 0)
-        asm("{ .reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-            "fma.rn.f32.bf16 %0, ah, bl, %0; }" : "+f"(acc) : "r"(a), "r"(b));
-    else
-        asm("{ .reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-            "fma.rn.f32.bf16 %0, ah, bh, %0; }" : "+f"(acc) : "r"(a), "r"(b));
+// ---- tensor-core fragments -----------------------------------------------------
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
 }
 
-// 8-dim partial dot product of a packed bf16 q chunk with a packed bf16 K chunk.
-__device__ __forceinline__ float dot8(const uint32_t (&q)[4], const uint32_t (&k)[4]) {
-    float a = 0.f, b = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        bf16_fma<0, 0>(a, q[c], k[c]);
-        bf16_fma<1, 1>(b, q[c], k[c]);
-    }
-    return a + b;
+// c += A . B, m16n8k16, bf16 in, fp32 accumulate (A row-major 16 x 16, B 16 x 8).
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Q.K for ROWS token rows, summed over the row's LPR lanes.
-//  * one row: slot j (< G) holds head j ^ hl; NT transposing steps leave the
-//    lane with head hl, plain steps finish the sum.
-//  * two rows (JOINT): slot j (< 2G) holds value j ^ rl, value = row * G +
-//    head; the first G slots use this lane's own row.  NT + 1 transposing
-//    steps leave the lane with (row rl / G, head rl % G).
-// Returns the raw dot product (scale applied by the caller).
-template <int D, int G, int BS>
-__device__ __forceinline__ float qk_dot(const uint32_t (&q)[G][4], const uint4 kown, const uint4 koth) {
-    using S = Shape<D, G, BS>;
-    const uint32_t ko[4] = {kown.x, kown.y, kown.z, kown.w};
-    constexpr int NV = G * S::ROWS;
-    float a[NV];
-#pragma unroll
-    for (int j = 0; j < G; ++j) a[j] = dot8(q[j], ko);
-    if constexpr (S::JOINT) {
-        const uint32_t kt[4] = {koth.x, koth.y, koth.z, koth.w};
-#pragma unroll
-        for (int j = 0; j < G; ++j) a[G + j] = dot8(q[j], kt);
-    }
-    constexpr int NTR = S::JOINT ? S::NT + 1 : S::NT;  // transposing steps
-#pragma unroll
-    for (int st = 0; st < NTR; ++st) {
-        const int half = NV >> (st + 1);
-        const int dist = S::LPR >> (st + 1);
-#pragma unroll
-        for (int j = 0; j < half; ++j) a[j] += __shfl_xor_sync(0xffffffffu, a[j + half], dist);
-    }
-    float s = a[0];
-#pragma unroll
-    for (int dist = S::LPR >> (NTR + 1); dist >= 1; dist >>= 1) s += __shfl_xor_sync(0xffffffffu, s, dist);
-    return s;
+// Transpose of an 8 x 8 bf16 tile held one row pair per lane.
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t a) {
+    uint32_t d;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
 }
 
-// ---- per-lane roles and per-warp online-softmax state ------------------------
+// Byte offset, inside a slot, of the 128-byte half row hh of the stage's
+// token j, and of its 16-byte chunk c after the 128-byte swizzle.
+template <int D, int BS>
+__device__ __forceinline__ uint32_t row_off(int j, int hh) {
+    using S = Shape<D, BS>;
+    return (uint32_t)((j / BS) * S::REGION + (hh * BS + j % BS) * 128);
+}
+__device__ __forceinline__ uint32_t chunk_at(uint32_t row, int c) {
+    return row + ((((uint32_t)c) ^ ((row >> 7) & 7u)) << 4);
+}
 
-template <int D, int G, int BS>
-struct Lanes {
-    using S = Shape<D, G, BS>;
-    int row, tsub, hl, rsel;
-    __device__ __forceinline__ explicit Lanes(int lane) {
-        row = lane % S::LPR;                        // this lane's 8-dim chunk of a token row
-        tsub = lane / S::LPR;                       // token within a warp iteration
-        // head whose score this lane ends with, and (joint rows) which of the two rows
-        hl = S::JOINT ? (row & (G - 1)) : (row >> (S::LOG_LPR - S::NT));
-        rsel = S::JOINT ? (row >> S::NT) : 0;
+// Lane roles: g = lane / 4 is a token row of an S^T tile / the head of a
+// P^T column; t = lane % 4 picks K chunks and the head pair (2t, 2t + 1).
+// K chunk idx of a lane (idx < NCH) is chunk 2t + (idx & 1) of half idx / 2;
+// its 4 words are Q.K MMA operands 4 idx .. 4 idx + 3, two per d step.
+
+// q of one (sequence, kv-head) group as the B operand of S^T = K . Q^T:
+// head g (zero for g >= G), d in the lane's K chunk order.
+template <int D, int G, bool kShared>
+__device__ __forceinline__ void load_qf(uint32_t (&qf)[D / 8], const __nv_bfloat16 *qrows, int lane) {
+    using S = Shape<D, 16>;
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int idx = 0; idx < S::NCH; ++idx) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (g < G) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(qrows + g * D + (idx >> 1) * 64 + (2 * t + (idx & 1)) * 8);
+            w = kShared ? *src : __ldg(src);
+        }
+        qf[4 * idx + 0] = w.x;
+        qf[4 * idx + 1] = w.y;
+        qf[4 * idx + 2] = w.z;
+        qf[4 * idx + 3] = w.w;
     }
-};
+}
 
-template <int G>
+template <int D>
 struct WarpState {
-    float m;          // running max (log2 domain) of head hl
-    float l;          // this lane's share of the softmax denominator of head hl
-    float o[G][8];    // numerators: head x this lane's 8 dims
+    float m[2];          // running max (log2 domain) of heads 2t, 2t + 1
+    float l[2];          // this lane's share of their denominators
+    float o[D / 16][4];  // O^T tiles: rows d (g, g + 8 of tile), columns heads (2t, 2t + 1)
     __device__ __forceinline__ void reset() {
-        m = -INFINITY;
-        l = 0.f;
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
 #pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[h][i] = 0.f;
+        for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     }
 };
 
-// q of one (sequence, kv-head) group on this lane's 8 dims, packed bf16; slot
-// j holds head j ^ hl.  `qrows` points at the group's first head row.
-template <int D, int G, int BS, bool kShared>
-__device__ __forceinline__ void load_q(uint32_t (&qw)[G][4], const __nv_bfloat16 *qrows, const Lanes<D, G, BS> &ln) {
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(qrows + (j ^ ln.hl) * D + ln.row * 8);
-        const uint4 w = kShared ? *src : __ldg(src);
-        qw[j][0] = w.x;
-        qw[j][1] = w.y;
-        qw[j][2] = w.z;
-        qw[j][3] = w.w;
-    }
-}
+// d held by row r (0 = g, 1 = g + 8) of P.V tile mt, as (half, element) of the
+// lane's V chunk g: for d = 128 half r, element mt; for d = 64 element mt + 4r.
+template <int D>
+__host__ __device__ constexpr int pv_half(int r) { return D == 128 ? r : 0; }
+template <int D>
+__host__ __device__ constexpr int pv_elem(int mt, int r) { return D == 128 ? mt : mt + 4 * r; }
 
-// One pipeline stage: this warp's K and V slabs of TPS tokens are in (ks, vs);
-// token index tok0 + t is valid while < tok_end.
-template <int D, int G, int BS, typename WS>
-__device__ __forceinline__ void stage_compute(WS *ws, const __nv_bfloat16 *ks, const __nv_bfloat16 *vs,
-                                              const uint32_t (&qw)[G][4], int tok0, int tok_end, float scale_log2,
-                                              const Lanes<D, G, BS> &ln, WarpState<G> &st) {
-    using S = Shape<D, G, BS>;
-    const bool tail = tok0 + S::TPS > tok_end;
-    const int row = ln.row, tsub = ln.tsub, hl = ln.hl, rsel = ln.rsel;
+// One pipeline stage: this warp's K and V slots (shared-memory addresses)
+// hold TPS tokens; token tok0 + j is valid while < tok_end.
+template <int D, int G, int BS>
+__device__ __forceinline__ void stage_compute(uint32_t kslot, uint32_t vslot, const uint32_t (&qf)[D / 8], int tok0,
+                                              int tok_end, float scale_log2, int lane, WarpState<D> &st) {
+    using S = Shape<D, BS>;
+    const int g = lane >> 2, t = lane & 3;
+    const int nvalid = tok_end - tok0;
+    const bool tail = nvalid < S::TPS;
 
-    // ---- scores (log2 domain) for head hl
-    float sc[S::QK_ITERS];
+    // ---- scores (log2 domain): x[ks] = S^T of tokens 16ks + (g, g + 8), heads (2t, 2t + 1)
+    float x[S::KS][4];
 #pragma unroll
-    for (int it = 0; it < S::QK_ITERS; ++it) {
-        const int t0 = it * S::ROWS * S::TPI + tsub * S::ROWS;   // first row of this lane's group
-        const int t = t0 + rsel;                                 // the row whose score this lane keeps
-        const uint4 kown = *reinterpret_cast<const uint4 *>(ks + t * D + row * 8);
-        uint4 koth = kown;
-        if constexpr (S::JOINT) koth = *reinterpret_cast<const uint4 *>(ks + (t0 + 1 - rsel) * D + row * 8);
-        sc[it] = qk_dot<D, G, BS>(qw, kown, koth) * scale_log2;
-        if (tail && tok0 + t >= tok_end) sc[it] = -INFINITY;
+    for (int ks = 0; ks < S::KS; ++ks) {
+        const int j0 = ks * 16 + g, j1 = j0 + 8;
+        uint32_t k0[4 * S::NCH], k1[4 * S::NCH];
+#pragma unroll
+        for (int idx = 0; idx < S::NCH; ++idx) {
+            const int hh = idx >> 1, ch = 2 * t + (idx & 1);
+            const uint4 a = lds128(kslot + chunk_at(row_off<D, BS>(j0, hh), ch));
+            const uint4 b = lds128(kslot + chunk_at(row_off<D, BS>(j1, hh), ch));
+            k0[4 * idx + 0] = a.x;
+            k0[4 * idx + 1] = a.y;
+            k0[4 * idx + 2] = a.z;
+            k0[4 * idx + 3] = a.w;
+            k1[4 * idx + 0] = b.x;
+            k1[4 * idx + 1] = b.y;
+            k1[4 * idx + 2] = b.z;
+            k1[4 * idx + 3] = b.w;
+        }
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < S::DK; ++s) mma_bf16(c, k0[2 * s], k1[2 * s], k0[2 * s + 1], k1[2 * s + 1], qf[2 * s], qf[2 * s + 1]);
+        const bool v0 = !tail || j0 < nvalid, v1 = !tail || j1 < nvalid;
+        x[ks][0] = v0 ? c[0] * scale_log2 : -INFINITY;
+        x[ks][1] = v0 ? c[1] * scale_log2 : -INFINITY;
+        x[ks][2] = v1 ? c[2] * scale_log2 : -INFINITY;
+        x[ks][3] = v1 ? c[3] * scale_log2 : -INFINITY;
     }
 
-    // ---- online softmax for head hl over this stage
-    float mb = sc[0];
+    // ---- online softmax for heads 2t, 2t + 1 (maxima reduced over the 8 lanes g)
+    float mh0 = -INFINITY, mh1 = -INFINITY;
 #pragma unroll
-    for (int it = 1; it < S::QK_ITERS; ++it) mb = fmaxf(mb, sc[it]);
-    if constexpr (S::JOINT) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, G));
-#pragma unroll
-    for (int dist = S::LPR; dist < 32; dist <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, dist));
-    const float m_new = fmaxf(st.m, mb);
-    const float m_use = m_new == -INFINITY ? 0.f : m_new;
-    const float alpha = fast_exp2(st.m - m_use);
-    float psum = 0.f;
-    __nv_bfloat16 pb[S::QK_ITERS];
-#pragma unroll
-    for (int it = 0; it < S::QK_ITERS; ++it) {
-        pb[it] = __float2bfloat16_rn(fast_exp2(sc[it] - m_use));
-        psum += __bfloat162float(pb[it]);
+    for (int ks = 0; ks < S::KS; ++ks) {
+        mh0 = fmaxf(mh0, fmaxf(x[ks][0], x[ks][2]));
+        mh1 = fmaxf(mh1, fmaxf(x[ks][1], x[ks][3]));
     }
-    st.l = st.l * alpha + psum;
-    const bool moved = m_new != st.m;
-    st.m = m_new;
-    if (S::JOINT || (row & (S::DUP - 1)) == 0) {
-        __nv_bfloat16 *pt = reinterpret_cast<__nv_bfloat16 *>(&ws->p[0][0]);
 #pragma unroll
-        for (int it = 0; it < S::QK_ITERS; ++it)
-            pt[(it * S::ROWS * S::TPI + tsub * S::ROWS + rsel) * (2 * S::PW) + hl] = pb[it];
-        if (tsub == 0 && rsel == 0) ws->alpha[hl] = alpha;
+    for (int dist = 4; dist < 32; dist <<= 1) {
+        mh0 = fmaxf(mh0, __shfl_xor_sync(0xffffffffu, mh0, dist));
+        mh1 = fmaxf(mh1, __shfl_xor_sync(0xffffffffu, mh1, dist));
     }
-    __syncwarp();
-
-    // ---- rescale (only if some head's maximum moved) and accumulate P . V
+    const float mn0 = fmaxf(st.m[0], mh0), mn1 = fmaxf(st.m[1], mh1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = fast_exp2(st.m[0] - mu0), al1 = fast_exp2(st.m[1] - mu1);
+    const bool moved = mn0 != st.m[0] || mn1 != st.m[1];
+    uint32_t pb[S::KS][2];   // bf16 pairs (head 2t, 2t + 1) of tokens 16ks + g and 16ks + g + 8
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < S::KS; ++ks) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(fast_exp2(x[ks][0] - mu0), fast_exp2(x[ks][1] - mu1));
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(fast_exp2(x[ks][2] - mu0), fast_exp2(x[ks][3] - mu1));
+        ps0 += __low2float(lo) + __low2float(hi);
+        ps1 += __high2float(lo) + __high2float(hi);
+        pb[ks][0] = *reinterpret_cast<const uint32_t *>(&lo);
+        pb[ks][1] = *reinterpret_cast<const uint32_t *>(&hi);
+    }
+    st.l[0] = st.l[0] * al0 + ps0;
+    st.l[1] = st.l[1] * al1 + ps1;
+    st.m[0] = mn0;
+    st.m[1] = mn1;
     if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float a = ws->alpha[h];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) st.o[h][i] *= a;
+        for (int mt = 0; mt < S::DK; ++mt) {
+            st.o[mt][0] *= al0;
+            st.o[mt][1] *= al1;
+            st.o[mt][2] *= al0;
+            st.o[mt][3] *= al1;
         }
     }
+
+    // ---- O^T += V^T . P^T per 16 tokens
 #pragma unroll
-    for (int it = 0; it < S::ITERS; ++it) {
-        const int t = it * S::TPI + tsub;
-        uint4 vw = *reinterpret_cast<const uint4 *>(vs + t * D + row * 8);
-        if (tail && tok0 + t >= tok_end) vw = make_uint4(0u, 0u, 0u, 0u);  // slot may hold stale data
-        const uint32_t v4[4] = {vw.x, vw.y, vw.z, vw.w};
-        uint32_t pw[S::PW];
-        if constexpr (S::PW == 4) {
-            const uint4 w = *reinterpret_cast<const uint4 *>(&ws->p[t][0]);
-            pw[0] = w.x;
-            pw[1] = w.y;
-            pw[2] = w.z;
-            pw[3] = w.w;
-        } else if constexpr (S::PW == 2) {
-            const uint2 w = *reinterpret_cast<const uint2 *>(&ws->p[t][0]);
-            pw[0] = w.x;
-            pw[1] = w.y;
-        } else {
-            pw[0] = ws->p[t][0];
-        }
+    for (int ks = 0; ks < S::KS; ++ks) {
+        const uint32_t b0 = transpose8x8(pb[ks][0]), b1 = transpose8x8(pb[ks][1]);
+        // V chunk g (each half) of tokens 16ks + 2t, +1, +8, +9; tokens past the
+        // end read as zero (their slots may hold stale or non-finite data)
+        uint32_t vw[4][S::HALVES][4];
 #pragma unroll
-        for (int hp = 0; hp < S::PW; ++hp)
+        for (int kk = 0; kk < 4; ++kk) {
+            const int j = ks * 16 + 2 * t + (kk & 1) + 8 * (kk >> 1);
+            const bool valid = !tail || j < nvalid;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                bf16_fma<0, 0>(st.o[2 * hp][2 * c], pw[hp], v4[c]);
-                bf16_fma<0, 1>(st.o[2 * hp][2 * c + 1], pw[hp], v4[c]);
-                if constexpr (G >= 2) {
-                    bf16_fma<1, 0>(st.o[2 * hp + 1][2 * c], pw[hp], v4[c]);
-                    bf16_fma<1, 1>(st.o[2 * hp + 1][2 * c + 1], pw[hp], v4[c]);
-                }
+            for (int hh = 0; hh < S::HALVES; ++hh) {
+                uint4 w = lds128(vslot + chunk_at(row_off<D, BS>(j, hh), g));
+                if (!valid) w = make_uint4(0u, 0u, 0u, 0u);
+                vw[kk][hh][0] = w.x;
+                vw[kk][hh][1] = w.y;
+                vw[kk][hh][2] = w.z;
+                vw[kk][hh][3] = w.w;
             }
+        }
+#pragma unroll
+        for (int mt = 0; mt < S::DK; ++mt) {
+            const int hA = pv_half<D>(0), eA = pv_elem<D>(mt, 0);
+            const int hB = pv_half<D>(1), eB = pv_elem<D>(mt, 1);
+            const uint32_t sA = (eA & 1) ? 0x7632u : 0x5410u, sB = (eB & 1) ? 0x7632u : 0x5410u;
+            const uint32_t a0 = __byte_perm(vw[0][hA][eA >> 1], vw[1][hA][eA >> 1], sA);
+            const uint32_t a1 = __byte_perm(vw[0][hB][eB >> 1], vw[1][hB][eB >> 1], sB);
+            const uint32_t a2 = __byte_perm(vw[2][hA][eA >> 1], vw[3][hA][eA >> 1], sA);
+            const uint32_t a3 = __byte_perm(vw[2][hB][eB >> 1], vw[3][hB][eB >> 1], sB);
+            mma_bf16(st.o[mt], a0, a1, a2, a3, b0, b1);
+        }
     }
-    __syncwarp();
 }
 
-// Merge the lanes that held different tokens (same dims, same running max),
-// then publish this warp's (m, l, o) for the G heads into CTA scratch.
-template <int D, int G, int BS>
-__device__ __forceinline__ void warp_publish(WarpState<G> &st, bool has_work, const Lanes<D, G, BS> &ln, int warp,
-                                             float *cm, float *cl, float *co) {
-    using S = Shape<D, G, BS>;
-    if constexpr (S::JOINT) st.l += __shfl_xor_sync(0xffffffffu, st.l, G);
+// Reduce the denominators over the lanes of a head pair, then publish this
+// warp's (m, l, o) for the G heads into CTA scratch.
+template <int D, int G>
+__device__ __forceinline__ void warp_publish(WarpState<D> &st, bool has_work, int lane, int warp, float *cm,
+                                             float *cl, float *co) {
+    const int g = lane >> 2, t = lane & 3;
+    float l[2] = {st.l[0], st.l[1]};
 #pragma unroll
-    for (int dist = S::LPR; dist < 32; dist <<= 1) {
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) st.o[h][i] += __shfl_xor_sync(0xffffffffu, st.o[h][i], dist);
-        st.l += __shfl_xor_sync(0xffffffffu, st.l, dist);
+    for (int dist = 4; dist < 32; dist <<= 1) {
+        l[0] += __shfl_xor_sync(0xffffffffu, l[0], dist);
+        l[1] += __shfl_xor_sync(0xffffffffu, l[1], dist);
     }
-    if (ln.tsub == 0) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float *dst = co + (warp * G + h) * D + ln.row * 8;
+    for (int hi = 0; hi < 2; ++hi) {
+        const int h = 2 * t + hi;
+        if (h < G) {
+            float *dst = co + (warp * G + h) * D;
+            float r[2][8];
 #pragma unroll
-            for (int i = 0; i < 8; i += 2) *reinterpret_cast<float2 *>(dst + i) = make_float2(st.o[h][i], st.o[h][i + 1]);
-        }
-        if (S::JOINT ? ln.rsel == 0 : (ln.row & (S::DUP - 1)) == 0) {
-            cm[warp * G + ln.hl] = has_work ? st.m : -INFINITY;
-            cl[warp * G + ln.hl] = has_work ? st.l : 0.f;
+            for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) r[pv_half<D>(rr)][pv_elem<D>(mt, rr)] = st.o[mt][2 * rr + hi];
+#pragma unroll
+            for (int hh = 0; hh < D / 64; ++hh) {
+                float4 *d4 = reinterpret_cast<float4 *>(dst + hh * 64 + g * 8);
+                d4[0] = make_float4(r[hh][0], r[hh][1], r[hh][2], r[hh][3]);
+                d4[1] = make_float4(r[hh][4], r[hh][5], r[hh][6], r[hh][7]);
+            }
+            if (g == 0) {
+                cm[warp * G + h] = has_work ? st.m[hi] : -INFINITY;
+                cl[warp * G + h] = has_work ? l[hi] : 0.f;
+            }
         }
     }
 }
@@ -443,16 +441,21 @@ __device__ __forceinline__ void cta_combine_store(const float *cm, const float *
 // ---- split-context partition kernel --------------------------------------------
 
 template <int D, int G, int BS>
-__global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(const Params p) {
-    using S = Shape<D, G, BS>;
-    using WS = WarpSmem<D, G, BS, kStages>;
-    extern __shared__ __align__(128) unsigned char smem_raw[];
+__global__ void __launch_bounds__(kWarps * 32, kMinCtas)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                        const Params p) {
+    using S = Shape<D, BS>;
+    using WR = WarpRing<D, BS, kStages>;
+    using SP = SmemPlan<D, BS, kStages>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = align1024(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    WS *ws = reinterpret_cast<WS *>(smem_raw) + warp;
+    const uint32_t ring = smem_addr(smem) + warp * (uint32_t)sizeof(WR);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + SP::kRings) + warp * kStages;
 
     if (lane == 0) {
 #pragma unroll
-        for (int st = 0; st < kStages; ++st) mbar_init(&ws->bar[st], 1);
+        for (int st = 0; st < kStages; ++st) mbar_init(&bar[st], 1);
         fence_barrier_init();
     }
     grid_dependency_wait();   // inputs may come from the previous kernel in the stream
@@ -474,9 +477,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
         return;
     }
 
-    const Lanes<D, G, BS> ln(lane);
-    uint32_t qw[G][4];
-    load_q<D, G, BS, false>(qw, p.q + head0 * D, ln);
+    uint32_t qf[D / 8];
+    load_qf<D, G, false>(qf, p.q + head0 * D, lane);
     __syncwarp();
 
     const int nblk_seq = (L + BS - 1) / BS;
@@ -484,7 +486,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
     const int nstages = (ntok + S::TPS - 1) / S::TPS;
     const int my_stages = nstages > warp ? (nstages - warp + kWarps - 1) / kWarps : 0;
     const int32_t *table_row = p.tables + (size_t)s * p.max_blocks;
-    const __nv_bfloat16 *pool_g = p.pool + (size_t)g * S::SLAB;
 
     // Register cache of block ids: lane i holds warp-local block kb_base + i,
     // where warp-local block kb = k * BPS + ib is block ib of the warp's k-th stage.
@@ -519,13 +520,13 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
 #pragma unroll
         for (int ib = 0; ib < S::BPS; ++ib) ids[ib] = __shfl_sync(0xffffffffu, id_cache, k * S::BPS + ib - kb_base);
         if (lane == 0) {
-            mbar_arrive_expect_tx(&ws->bar[slot], (uint32_t)(nvalid * S::SLAB * 2 * 2));
+            mbar_arrive_expect_tx(&bar[slot], (uint32_t)(nvalid * S::BOX * 2));
+            const uint32_t kslot = ring + slot * S::SLOT, vslot = ring + (kStages + slot) * S::SLOT;
 #pragma unroll
             for (int ib = 0; ib < S::BPS; ++ib) {
                 if (ib < nvalid) {
-                    const __nv_bfloat16 *src = pool_g + (size_t)ids[ib] * p.block_stride;
-                    bulk_g2s(ws->k[slot] + ib * S::SLAB, src, S::SLAB * 2, &ws->bar[slot]);
-                    bulk_g2s(ws->v[slot] + ib * S::SLAB, src + p.kv_stride, S::SLAB * 2, &ws->bar[slot]);
+                    tensor_copy_5d(kslot + ib * S::REGION, &tmk, 0, 0, 0, g, ids[ib], &bar[slot]);
+                    tensor_copy_5d(vslot + ib * S::REGION, &tmv, 0, 0, 0, g, ids[ib], &bar[slot]);
                 }
             }
         }
@@ -534,20 +535,22 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
 #pragma unroll
     for (int k = 0; k < kStages; ++k) issue(k);
 
-    WarpState<G> st;
+    WarpState<D> st;
     st.reset();
     int consumed = 0;
     bool ok = true;
     for (int k = 0; k < my_stages; ++k) {
         const int slot = k % kStages;
-        const bool arrived = mbar_wait_bounded(&ws->bar[slot], (uint32_t)((k / kStages) & 1), p.err);
+        const bool arrived = mbar_wait_bounded(&bar[slot], (uint32_t)((k / kStages) & 1), p.err);
         if (!__all_sync(0xffffffffu, arrived)) {
             ok = false;
             break;
         }
         consumed = k + 1;
         const int tok0 = tok_begin + (warp + k * kWarps) * S::TPS;
-        stage_compute<D, G, BS>(ws, ws->k[slot], ws->v[slot], qw, tok0, tok_end, p.scale_log2, ln, st);
+        stage_compute<D, G, BS>(ring + slot * S::SLOT, ring + (kStages + slot) * S::SLOT, qf, tok0, tok_end,
+                                p.scale_log2, lane, st);
+        __syncwarp();   // every lane is done with the slot before it is refilled
         issue(k + kStages);
     }
 
@@ -556,15 +559,15 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_kernel(con
         // this warp's slots before the shared memory is reused.
         const int issued = min(my_stages, consumed + kStages);
         for (int k = consumed; k < issued; ++k)
-            mbar_wait_bounded(&ws->bar[k % kStages], (uint32_t)((k / kStages) & 1), p.err);
+            mbar_wait_bounded(&bar[k % kStages], (uint32_t)((k / kStages) & 1), p.err);
     }
 
     // ---- merge the warps in shared memory (stage buffers are free now)
     __syncthreads();
-    float *cm = reinterpret_cast<float *>(smem_raw);   // [W][G] running max
+    float *cm = reinterpret_cast<float *>(smem);       // [W][G] running max
     float *cl = cm + kWarps * G;                       // [W][G] denominators
     float *co = cl + kWarps * G;                       // [W][G][D] numerators
-    warp_publish<D, G, BS>(st, my_stages > 0, ln, warp, cm, cl, co);
+    warp_publish<D, G>(st, my_stages > 0, lane, warp, cm, cl, co);
     __syncthreads();
     grid_launch_dependents();
     const size_t rowp = head0 * p.num_parts + part;
@@ -639,20 +642,25 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int *scratch, int &to
 }
 
 template <int D, int G, int BS>
-__global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_sk_kernel(const Params p) {
-    using S = Shape<D, G, BS>;
-    using WS = WarpSmem<D, G, BS, kSkStages>;
+__global__ void __launch_bounds__(kWarps * 32, kMinCtas)
+    paged_decode_sk_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                           const Params p) {
+    using S = Shape<D, BS>;
+    using WR = WarpRing<D, BS, kSkStages>;
+    using SP = SmemPlan<D, BS, kSkStages>;
     using SK = SkSmem<D, G>;
-    extern __shared__ __align__(128) unsigned char smem_raw[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = align1024(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    WS *ws = reinterpret_cast<WS *>(smem_raw) + warp;
-    SK *sk = reinterpret_cast<SK *>(smem_raw + sizeof(WS) * kWarps);
+    const uint32_t ring = smem_addr(smem) + warp * (uint32_t)sizeof(WR);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + SP::kRings) + warp * kSkStages;
+    SK *sk = reinterpret_cast<SK *>(smem + SP::kRings + SP::kBars);
     constexpr int NT = kWarps * 32;
     const int Hkv = p.num_kv_heads, B = p.num_seqs, c = blockIdx.x;
 
     if (lane == 0) {
 #pragma unroll
-        for (int st = 0; st < kSkStages; ++st) mbar_init(&ws->bar[st], 1);
+        for (int st = 0; st < kSkStages; ++st) mbar_init(&bar[st], 1);
         if (warp == 0) {
             mbar_init(&sk->qbar[0], 1);
             mbar_init(&sk->qbar[1], 1);
@@ -695,7 +703,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_sk_kernel(
     }
     int cur_s = sk->found_s, cur_rem = gs - sk->found_base;   // position of the next segment to list
     int pos = gs;                                              // global stage the next segment starts at
-    const Lanes<D, G, BS> ln(lane);
     int kq = 0;                  // stages this warp has consumed (ring parity counter)
     int jbase = 0;               // segments of earlier listings (q buffer parity counter)
     bool ok = true;
@@ -801,14 +808,13 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_sk_kernel(
                 int nvalid = 0;
 #pragma unroll
                 for (int ib = 0; ib < S::BPS; ++ib) nvalid += ids[ib] >= 0 ? 1 : 0;
-                mbar_arrive_expect_tx(&ws->bar[slot], (uint32_t)(nvalid * S::SLAB * 2 * 2));
-                const __nv_bfloat16 *pool_g = p.pool + (size_t)g * S::SLAB;
+                mbar_arrive_expect_tx(&bar[slot], (uint32_t)(nvalid * S::BOX * 2));
+                const uint32_t kslot = ring + slot * S::SLOT, vslot = ring + (kSkStages + slot) * S::SLOT;
 #pragma unroll
                 for (int ib = 0; ib < S::BPS; ++ib) {
                     if (ids[ib] >= 0) {
-                        const __nv_bfloat16 *src = pool_g + (size_t)ids[ib] * p.block_stride;
-                        bulk_g2s(ws->k[slot] + ib * S::SLAB, src, S::SLAB * 2, &ws->bar[slot]);
-                        bulk_g2s(ws->v[slot] + ib * S::SLAB, src + p.kv_stride, S::SLAB * 2, &ws->bar[slot]);
+                        tensor_copy_5d(kslot + ib * S::REGION, &tmk, 0, 0, 0, g, ids[ib], &bar[slot]);
+                        tensor_copy_5d(vslot + ib * S::REGION, &tmv, 0, 0, 0, g, ids[ib], &bar[slot]);
                     }
                 }
             }
@@ -827,9 +833,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_sk_kernel(
                 ok = false;
                 break;
             }
-            uint32_t qw[G][4];
-            load_q<D, G, BS, true>(qw, sk->q[jg & 1], ln);
-            WarpState<G> st;
+            uint32_t qf[D / 8];
+            load_qf<D, G, true>(qf, sk->q[jg & 1], lane);
+            WarpState<D> st;
             st.reset();
             const int lend = sk->seg_lb[j + 1];
             int done = 0;
@@ -837,18 +843,20 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_sk_kernel(
                 const int i = warp + k * kWarps;
                 const int slot = (kq + k) % kSkStages;
                 const bool arrived =
-                    mbar_wait_bounded(&ws->bar[slot], (uint32_t)(((kq + k) / kSkStages) & 1), p.err);
+                    mbar_wait_bounded(&bar[slot], (uint32_t)(((kq + k) / kSkStages) & 1), p.err);
                 if (!__all_sync(0xffffffffu, arrived)) {
                     ok = false;
                     break;
                 }
                 const int tok0 = (sk->seg_kb[j] + i - sk->seg_lb[j]) * S::TPS;
-                stage_compute<D, G, BS>(ws, ws->k[slot], ws->v[slot], qw, tok0, L, p.scale_log2, ln, st);
+                stage_compute<D, G, BS>(ring + slot * S::SLOT, ring + (kSkStages + slot) * S::SLOT, qf, tok0, L,
+                                        p.scale_log2, lane, st);
+                __syncwarp();   // every lane is done with the slot before it is refilled
                 issue(k + kSkStages);
                 ++k;
                 ++done;
             }
-            warp_publish<D, G, BS>(st, done > 0, ln, warp, sk->cm, sk->cl, sk->co);
+            warp_publish<D, G>(st, done > 0, lane, warp, sk->cm, sk->cl, sk->co);
             if (!__syncthreads_and(ok)) {
                 ok = false;
                 break;
@@ -866,7 +874,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas) paged_decode_sk_kernel(
             // A wait gave up: bounded waits for this warp's copies still in flight.
             const int issued = min(my_n, k + kSkStages);
             for (int kk = k; kk < issued; ++kk)
-                mbar_wait_bounded(&ws->bar[(kq + kk) % kSkStages], (uint32_t)(((kq + kk) / kSkStages) & 1), p.err);
+                mbar_wait_bounded(&bar[(kq + kk) % kSkStages], (uint32_t)(((kq + kk) / kSkStages) & 1), p.err);
             break;
         }
         kq += my_n;
@@ -928,8 +936,8 @@ __global__ void __launch_bounds__(G *D / 4) paged_decode_sk_merge_kernel(const P
 
 // Launch with programmatic stream serialisation (the kernel waits on
 // griddepcontrol.wait before touching global memory).
-template <typename Kernel>
-cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Params &prm) {
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Args &...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -940,7 +948,7 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, prm);
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <typename Kernel>
@@ -957,57 +965,82 @@ cudaError_t ensure_smem(Kernel kernel, size_t smem, bool *configured) {
 
 template <int D, int G, int BS>
 constexpr size_t sk_smem_bytes() {
-    return sizeof(WarpSmem<D, G, BS, kSkStages>) * kWarps + sizeof(SkSmem<D, G>);
+    return SmemPlan<D, BS, kSkStages>::bytes(sizeof(SkSmem<D, G>));
 }
 
 template <int D, int G, int BS>
-cudaError_t launch_shape(const Params &prm, int num_kv_heads, int num_seqs, bool stream_k, cudaStream_t stream) {
+cudaError_t launch_shape(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &prm, int num_kv_heads,
+                         int num_seqs, bool stream_k, cudaStream_t stream) {
     if (stream_k) {
         constexpr size_t smem = sk_smem_bytes<D, G, BS>();
         static bool configured[64] = {};
         cudaError_t e = ensure_smem(paged_decode_sk_kernel<D, G, BS>, smem, configured);
         if (e != cudaSuccess) return e;
-        e = launch_pdl(paged_decode_sk_kernel<D, G, BS>, dim3(prm.num_ctas), dim3(kWarps * 32), smem, stream, prm);
+        e = launch_pdl(paged_decode_sk_kernel<D, G, BS>, dim3(prm.num_ctas), dim3(kWarps * 32), smem, stream, tmk,
+                       tmv, prm);
         if (e != cudaSuccess) return e;
         return launch_pdl(paged_decode_sk_merge_kernel<D, G, BS>, dim3(num_kv_heads, num_seqs), dim3(G * D / 4), 0,
                           stream, prm);
     }
-    using WS = WarpSmem<D, G, BS, kStages>;
-    constexpr size_t smem = sizeof(WS) * kWarps;
-    static_assert(smem >= sizeof(float) * kWarps * G * (D + 2), "combine scratch");
+    using SP = SmemPlan<D, BS, kStages>;
+    constexpr size_t smem = SP::bytes(0);
+    static_assert(SP::kRings >= sizeof(float) * kWarps * G * (D + 2), "combine scratch");
     static bool configured[64] = {};
     cudaError_t e = ensure_smem(paged_decode_kernel<D, G, BS>, smem, configured);
     if (e != cudaSuccess) return e;
     e = launch_pdl(paged_decode_kernel<D, G, BS>, dim3(prm.num_parts, num_kv_heads, num_seqs), dim3(kWarps * 32),
-                   smem, stream, prm);
+                   smem, stream, tmk, tmv, prm);
     if (e != cudaSuccess || prm.num_parts == 1) return e;
     return launch_pdl(paged_decode_reduce_kernel<D, G, BS>, dim3(num_kv_heads, num_seqs), dim3(G * D / 4), 0,
                       stream, prm);
 }
 
 template <int D, int G>
-cudaError_t launch_group(const Params &prm, int bs, int num_kv_heads, int num_seqs, bool stream_k,
-                         cudaStream_t stream) {
+cudaError_t launch_group(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &prm, int bs, int num_kv_heads,
+                         int num_seqs, bool stream_k, cudaStream_t stream) {
     switch (bs) {
-        case 4: return launch_shape<D, G, 4>(prm, num_kv_heads, num_seqs, stream_k, stream);
-        case 8: return launch_shape<D, G, 8>(prm, num_kv_heads, num_seqs, stream_k, stream);
-        case 16: return launch_shape<D, G, 16>(prm, num_kv_heads, num_seqs, stream_k, stream);
-        case 32: return launch_shape<D, G, 32>(prm, num_kv_heads, num_seqs, stream_k, stream);
+        case 4: return launch_shape<D, G, 4>(tmk, tmv, prm, num_kv_heads, num_seqs, stream_k, stream);
+        case 8: return launch_shape<D, G, 8>(tmk, tmv, prm, num_kv_heads, num_seqs, stream_k, stream);
+        case 16: return launch_shape<D, G, 16>(tmk, tmv, prm, num_kv_heads, num_seqs, stream_k, stream);
+        case 32: return launch_shape<D, G, 32>(tmk, tmv, prm, num_kv_heads, num_seqs, stream_k, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// Tensor map of the K (kv = 0) or V (kv = 1) half of the pool as
+// (d within a 64-wide half, slot, half of d, kv-head, block); one box is a
+// whole (block, K|V, kv-head) slab, laid out [half][slot][64] with 128-byte
+// swizzle.
+inline cudaError_t encode_pool_map(CUtensorMap *map, const PoolView &pool, int kv) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const int D = pool.head_dim, BS = pool.block_size;
+    const char *base = static_cast<const char *>(pool.base) + (size_t)kv * pool.kv_stride * 2;
+    cuuint64_t dims[5] = {64, (cuuint64_t)BS, (cuuint64_t)(D / 64), (cuuint64_t)pool.num_kv_heads,
+                          (cuuint64_t)pool.num_blocks};
+    cuuint64_t strides[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)BS * D * 2, (cuuint64_t)pool.block_stride * 2};
+    cuuint32_t box[5] = {64, (cuuint32_t)BS, (cuuint32_t)(D / 64), 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    if (encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<char *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
 }
 
 template <int D>
 cudaError_t launch_for_dim(const DecodeArgs &a, cudaStream_t stream) {
     unsigned int *err = device_error_word();
     if (!err) return cudaErrorUnknown;
+    CUtensorMap tmk, tmv;
+    cudaError_t e = encode_pool_map(&tmk, a.pool, 0);
+    if (e != cudaSuccess) return e;
+    e = encode_pool_map(&tmv, a.pool, 1);
+    if (e != cudaSuccess) return e;
     Params prm;
     prm.out = static_cast<__nv_bfloat16 *>(a.out);
     prm.q = static_cast<const __nv_bfloat16 *>(a.q);
-    prm.pool = static_cast<const __nv_bfloat16 *>(a.pool.base);
     prm.num_blocks = a.pool.num_blocks;
-    prm.block_stride = a.pool.block_stride;
-    prm.kv_stride = a.pool.kv_stride;
     prm.tables = a.tables;
     prm.max_blocks = a.max_blocks;
     prm.seq_lens = a.seq_lens;
@@ -1027,10 +1060,10 @@ cudaError_t launch_for_dim(const DecodeArgs &a, cudaStream_t stream) {
     const int bs = a.pool.block_size, H = a.pool.num_kv_heads, B = a.num_seqs;
     const bool sk = a.stream_k;
     switch (G) {
-        case 1: return launch_group<D, 1>(prm, bs, H, B, sk, stream);
-        case 2: return launch_group<D, 2>(prm, bs, H, B, sk, stream);
-        case 4: return launch_group<D, 4>(prm, bs, H, B, sk, stream);
-        case 8: return launch_group<D, 8>(prm, bs, H, B, sk, stream);
+        case 1: return launch_group<D, 1>(tmk, tmv, prm, bs, H, B, sk, stream);
+        case 2: return launch_group<D, 2>(tmk, tmv, prm, bs, H, B, sk, stream);
+        case 4: return launch_group<D, 4>(tmk, tmv, prm, bs, H, B, sk, stream);
+        case 8: return launch_group<D, 8>(tmk, tmv, prm, bs, H, B, sk, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -75,6 +76,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
             return false;
         }
     }
+}
+
+// ---- tensor copies (TMA) -----------------------------------------------------
+
+// Global -> shared copy of one box of a 5-D tensor map at coordinates
+// (c0 .. c4), completing its bytes on `bar`.  The destination must be aligned
+// to the map's swizzle span (1024 B for 128-byte swizzle) and c0 * element
+// size must be a multiple of 16 B.
+__device__ __forceinline__ void tensor_copy_5d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                               int c4, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5, %6}], [%7];" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_addr(bar))
+        : "memory");
 }
 
 // ---- bulk copies (TMA, non-tensor) ----------------------------------------

@@ -4,6 +4,8 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime_api.h>
 
 #include "pa.h"
@@ -27,6 +29,10 @@ unsigned int *device_error_word();
 
 // Number of SMs of the current device (cached per device); 0 on failure.
 int device_sm_count();
+
+// The driver's cuTensorMapEncodeTiled, resolved once through the runtime;
+// nullptr if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // ---- slot writer and block copies (pa_cache.cu) ---------------------------
 cudaError_t launch_reshape_and_cache(const PoolView &pool, const void *k, const void *v,

@@ -43,8 +43,6 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <mutex>
-
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -496,20 +494,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side --------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult qres;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qres) ==
-                cudaSuccess &&
-            qres == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
 template <int G>
 cudaError_t launch_group(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mkv, const Params &prm,
                          cudaStream_t stream) {
@@ -548,7 +532,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     using namespace prefill;
     unsigned int *err = device_error_word();
     if (!err) return cudaErrorUnknown;
-    auto encode = encode_fn();
+    auto encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const int G = a.num_q_heads / a.pool.num_kv_heads;
     const int Hkv = a.pool.num_kv_heads;
