@@ -9,17 +9,21 @@ tokens, 64 query / 8 KV heads, head_dim 128, bf16, 16-token blocks placed at
 random in a 16,384-block pool.
 
 Prints one JSON line.  ``value`` is tokens/s (decoded tokens, i.e. sequences
-per step, over device time with inputs resident in HBM).  Between timed
-steps the L2 cache is flushed by reading a 256 MiB buffer: that evicts every
-line the previous step touched without leaving dirty lines, whose write-back
-would otherwise land inside the next timed step (the same steps timed after
-a 256 MiB write flush are reported too).  ``e2e`` is the same metric through
-the C ABI from pinned host buffers (per-step inputs copied in and the output
-copied back inside the timed region; the KV pool is device-resident state).
-``roofline`` reports the decode call against the measured HBM copy
-bandwidth.  ``prefill`` times chunked prefill (16 sequences x 4,096 cached +
-512 new tokens) against the measured bf16 tensor peak.  ``cpu_baseline``
-times the CPU oracle on the host cores.
+per step, over device time with inputs resident in HBM).  A model runs one
+such step per layer, each on its own slice of the KV cache, so the timed
+loop runs K steps back to back over 8 layers' pools (and q), layer i % 8 at
+step i: a layer's K/V are touched again only after the other seven layers'
+(over 1.5 GB for the default workload, far beyond the 129 MB L2) have passed
+through, so every step reads its K/V from HBM; no flush kernel sits between
+steps.  The older per-step measurement -- one step between CUDA events after
+an L2 flush by a 256 MiB read -- is reported as ``per_step_flushed``; it adds
+a fixed ~5 us of event and launch latency to every step.  ``e2e`` is the
+same metric through the C ABI from pinned host buffers (per-step inputs
+copied in and the output copied back inside the timed region; the KV pool
+is device-resident state).  ``roofline`` reports the decode call against the
+measured HBM copy bandwidth.  ``prefill`` times chunked prefill (16
+sequences x 4,096 cached + 512 new tokens) against the measured bf16 tensor
+peak.  ``cpu_baseline`` times the CPU oracle on the host cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -194,12 +198,24 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 class DecodeStep:
-    """Device-resident inputs of one decode step and the calls that run it."""
+    """Device-resident inputs of one decode step per layer and the calls that
+    run it.  Every layer has its own pool and q (copies of the workload's);
+    tables, lengths and slots are shared, as in a model."""
 
-    def __init__(self, pa, w: wl.Workload, dev: torch.device, tensors):
-        self.pa, self.w, self.dev = pa, w, dev
-        self.pool = tensors["pool"].to(dev)
-        self.q = tensors["q"].to(dev)
+    LAYERS = 8
+
+    def __init__(self, pa, w: wl.Workload, dev: torch.device, tensors, layers: int = LAYERS):
+        self.pa, self.w, self.dev, self.layers = pa, w, dev, layers
+        pool0 = tensors["pool"].to(dev)
+        self.pools = torch.empty((layers,) + tuple(pool0.shape), dtype=pool0.dtype, device=dev)
+        for layer in range(layers):
+            self.pools[layer].copy_(pool0)
+        del pool0
+        q0 = tensors["q"].to(dev)
+        self.qs = torch.empty((layers,) + tuple(q0.shape), dtype=q0.dtype, device=dev)
+        for layer in range(layers):
+            self.qs[layer].copy_(q0)
+        self.pool, self.q = self.pools[0], self.qs[0]
         self.new_k = tensors["new_k"].to(dev)
         self.new_v = tensors["new_v"].to(dev)
         self.tables = torch.as_tensor(w.tables, device=dev)
@@ -214,13 +230,13 @@ class DecodeStep:
         self.num_parts = -(-w.max_seq_len // self.part) if self.part > 0 else 1
         self.launches_per_step = 1 + (2 if self.part == 0 or self.num_parts > 1 else 1)
 
-    def write(self):
-        self.pa.reshape_and_cache(self.pool, self.new_k, self.new_v, self.slots)
+    def write(self, layer: int = 0):
+        self.pa.reshape_and_cache(self.pools[layer], self.new_k, self.new_v, self.slots)
 
-    def decode(self):
+    def decode(self, layer: int = 0):
         w = self.w
-        self.pa.decode(self.out, self.q, self.pool, self.tables, self.seq_lens, w.max_seq_len, w.scale,
-                       w.partition_tokens, self.ws)
+        self.pa.decode(self.out, self.qs[layer], self.pools[layer], self.tables, self.seq_lens, w.max_seq_len,
+                       w.scale, w.partition_tokens, self.ws)
 
 
 def run_ours(args, world, rank, local):
@@ -245,18 +261,36 @@ def run_ours(args, world, rank, local):
             import torch.distributed as dist
             dist.barrier()
 
-    for _ in range(args.warmup):
-        flush_read()
-        step.write()
-        step.decode()
+    for i in range(args.warmup):
+        step.write(i % step.layers)
+        step.decode(i % step.layers)
     torch.cuda.synchronize()
     assert pa.get_device_error() == 0, "device error during warm-up"
 
     K = args.steps
 
-    def timed_steps(flush_fn, write=True):
-        # no event between the two calls: it would serialise the decode
-        # kernel's programmatic launch behind the slot writer
+    def timed_layers(write=True):
+        # K steps back to back, layer i % L at step i (see the module docstring)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        # The GPU idles (untimed) while the host queues all K steps, so the
+        # timed steps run back to back at device speed rather than at the
+        # rate Python issues calls (that rate is what e2e measures).
+        torch.cuda._sleep(int(max(2e7, 4e5 * K)))
+        e0.record(stream)
+        for i in range(K):
+            if write:
+                step.write(i % step.layers)
+            step.decode(i % step.layers)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return e0.elapsed_time(e1)
+
+    def timed_flushed(flush_fn, write=True):
+        # one step between events after an L2 flush; no event between the two
+        # calls: it would serialise the decode kernel's programmatic launch
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
         barrier()
         torch.cuda.synchronize()
@@ -272,10 +306,11 @@ def run_ours(args, world, rank, local):
         return [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
 
     with ClockSampler(local) as clocks:
-        step_ms = timed_steps(flush_read)
-    total_ms = sum(step_ms)
-    decode_ms = timed_steps(flush_read, write=False)   # the decode call alone, for the roofline
-    wstep_ms = timed_steps(flush_write)
+        total_ms = timed_layers()
+    decode_total_ms = timed_layers(write=False)   # the decode call alone, for the roofline
+    flushed_ms = timed_flushed(flush_read)
+    flushed_decode_ms = timed_flushed(flush_read, write=False)
+    wstep_ms = timed_flushed(flush_write)
     assert pa.get_device_error() == 0, "device error during the timed steps"
 
     # ---- end to end through the C ABI from pinned host buffers
@@ -317,12 +352,12 @@ def run_ours(args, world, rank, local):
 
     prefill = None if args.no_prefill else measure_prefill(pa, dev, flush_read)
 
-    elapsed = torch.tensor([total_ms, e2e_s * 1e3, float(np.mean(decode_ms)), sum(wstep_ms)], dtype=torch.float64,
-                           device=dev)
+    elapsed = torch.tensor([total_ms, e2e_s * 1e3, decode_total_ms / K, sum(wstep_ms), sum(flushed_ms),
+                            float(np.mean(flushed_decode_ms))], dtype=torch.float64, device=dev)
     if world > 1:
         import torch.distributed as dist
         dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms, decode_avg_ms, wtotal_ms = elapsed.tolist()
+    total_ms, e2e_ms, decode_avg_ms, wtotal_ms, ftotal_ms, fdecode_ms = elapsed.tolist()
 
     if rank != 0:
         if world > 1:
@@ -331,8 +366,8 @@ def run_ours(args, world, rank, local):
         return
     tokens = world * w.batch * K
     value = tokens / (total_ms / 1e3)
-    peak, bf16_peak, peak_kind = measured_peaks()
     alg = decode_bytes(w)
+    peak, bf16_peak, peak_kind = measured_peaks()
     achieved = alg / (decode_avg_ms / 1e3) / 1e9
     traffic = traffic_record()
     clk = clocks.summary()
@@ -348,8 +383,13 @@ def run_ours(args, world, rank, local):
                    "schedule": "balanced stream-K (persistent, 2 CTAs/SM)" if step.part == 0
                    else f"split-context, {step.part}-token partitions x {step.num_parts}",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "flushed between steps by reading a 256 MiB buffer (clean eviction)"},
-        "value_after_write_flush": round(tokens / (wtotal_ms / 1e3), 1),
+                   "layers": step.layers,
+                   "l2": f"inputs larger than L2: steps rotate over {step.layers} layers' pools and q, "
+                         f"{(step.layers - 1) * alg / 1e9:.2f} GB of other layers' K/V between reuses of a layer; no flush"},
+        "per_step_flushed": {"ms_per_step": round(ftotal_ms / K, 5), "tokens_per_s": round(tokens / (ftotal_ms / 1e3), 1),
+                             "decode_ms": round(fdecode_ms, 5),
+                             "tokens_per_s_after_write_flush": round(tokens / (wtotal_ms / 1e3), 1),
+                             "l2": "flushed before each step by reading a 256 MiB buffer; one event pair per step"},
         "roofline": {"bound": "hbm", "kernel": "pa_decode (decode kernel + merge kernel)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),

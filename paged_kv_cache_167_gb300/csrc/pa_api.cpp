@@ -18,7 +18,10 @@ namespace {
 #define PA_DECODE_WARPS 4
 #endif
 constexpr int kDecodeWarps = PA_DECODE_WARPS;  // warps per decode CTA (must match the kernel)
-constexpr int kStreamKCtasPerSm = 2;     // resident decode CTAs per SM (persistent stream-K grid)
+#ifndef PA_DECODE_SK_CTAS_PER_SM
+#define PA_DECODE_SK_CTAS_PER_SM 2
+#endif
+constexpr int kStreamKCtasPerSm = PA_DECODE_SK_CTAS_PER_SM;     // resident decode CTAs per SM (persistent stream-K grid)
 constexpr size_t kWsAlign = 256;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
