@@ -41,10 +41,12 @@
 //    bank-conflict free.  P^T is formed from the S^T accumulators with one
 //    register transpose (movmatrix) per 8 x 8 tile.
 //  * Online softmax in the log2 domain per warp: a head's running maximum
-//    is reduced across the 8 lanes holding its tokens.  Probabilities are
-//    rounded to bf16 once; the softmax denominator sums the same rounded
-//    values, so the output is an exact weighted average with those weights.
-//    The accumulators are rescaled only when some head's maximum moved.
+//    is reduced across the 8 lanes holding its tokens.  A probability enters
+//    P.V as the sum of two bf16 terms (its bf16 rounding and the rounding of
+//    the remainder), i.e. two MMAs per tile, so the weights carry ~16
+//    significant bits; a single bf16 rounding of p alone can move an output
+//    by ~2^-9 of the spread of the V values it averages.  The accumulators
+//    are rescaled only when some head's maximum moved.
 //  * The warps' (m, l, o) are merged in shared memory; bf16 output or fp32
 //    partials (o normalised by l, m in the log2 domain, l) are written.
 //  * Every table entry and length is bounds-checked; an out-of-range value is
@@ -308,16 +310,23 @@ __device__ __forceinline__ void stage_compute(uint32_t kslot, uint32_t vslot, co
     const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
     const float al0 = fast_exp2(st.m[0] - mu0), al1 = fast_exp2(st.m[1] - mu1);
     const bool moved = mn0 != st.m[0] || mn1 != st.m[1];
-    uint32_t pb[S::KS][2];   // bf16 pairs (head 2t, 2t + 1) of tokens 16ks + g and 16ks + g + 8
+    // p as the sum of two bf16 terms, hi = bf16(p) and lo = bf16(p - hi): the
+    // weights the P.V MMAs apply then agree with the fp32 probabilities to
+    // about 2^-17 instead of bf16's 2^-9, and the denominator sums the fp32 p.
+    uint32_t pb[S::KS][2][2];   // [ks][token row g | g + 8][hi | lo]: bf16 pairs of heads (2t, 2t + 1)
     float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
     for (int ks = 0; ks < S::KS; ++ks) {
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(fast_exp2(x[ks][0] - mu0), fast_exp2(x[ks][1] - mu1));
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(fast_exp2(x[ks][2] - mu0), fast_exp2(x[ks][3] - mu1));
-        ps0 += __low2float(lo) + __low2float(hi);
-        ps1 += __high2float(lo) + __high2float(hi);
-        pb[ks][0] = *reinterpret_cast<const uint32_t *>(&lo);
-        pb[ks][1] = *reinterpret_cast<const uint32_t *>(&hi);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const float pa = fast_exp2(x[ks][2 * r] - mu0), pc = fast_exp2(x[ks][2 * r + 1] - mu1);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(pa, pc);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(pa - __low2float(hi), pc - __high2float(hi));
+            ps0 += pa;
+            ps1 += pc;
+            pb[ks][r][0] = *reinterpret_cast<const uint32_t *>(&hi);
+            pb[ks][r][1] = *reinterpret_cast<const uint32_t *>(&lo);
+        }
     }
     st.l[0] = st.l[0] * al0 + ps0;
     st.l[1] = st.l[1] * al1 + ps1;
@@ -336,7 +345,8 @@ __device__ __forceinline__ void stage_compute(uint32_t kslot, uint32_t vslot, co
     // ---- O^T += V^T . P^T per 16 tokens
 #pragma unroll
     for (int ks = 0; ks < S::KS; ++ks) {
-        const uint32_t b0 = transpose8x8(pb[ks][0]), b1 = transpose8x8(pb[ks][1]);
+        const uint32_t b0 = transpose8x8(pb[ks][0][0]), b1 = transpose8x8(pb[ks][1][0]);
+        const uint32_t c0 = transpose8x8(pb[ks][0][1]), c1 = transpose8x8(pb[ks][1][1]);
         // V chunk g (each half) of tokens 16ks + 2t, +1, +8, +9; tokens past the
         // end read as zero (their slots may hold stale or non-finite data)
         uint32_t vw[4][S::HALVES][4];
@@ -364,6 +374,7 @@ __device__ __forceinline__ void stage_compute(uint32_t kslot, uint32_t vslot, co
             const uint32_t a2 = __byte_perm(vw[2][hA][eA >> 1], vw[3][hA][eA >> 1], sA);
             const uint32_t a3 = __byte_perm(vw[2][hB][eB >> 1], vw[3][hB][eB >> 1], sB);
             mma_bf16(st.o[mt], a0, a1, a2, a3, b0, b1);
+            mma_bf16(st.o[mt], a0, a1, a2, a3, c0, c1);
         }
     }
 }
@@ -670,13 +681,20 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
     grid_dependency_wait();
 
     // ---- total work W (stages over all units) and this CTA's range [gs, ge)
+    // With at most NT sequences (one per thread) each thread keeps its
+    // sequence's stage count and first global stage for the listing below.
+    const bool one_pass = B <= NT;
+    int my_ns = 0, my_first = 0;
     int total = 0;
     for (int base = 0; base < B; base += NT) {
         const int s = base + tid;
-        const int v = s < B ? Hkv * seq_stages<BS>(p, s, c == 0) : 0;
+        const int ns = s < B ? seq_stages<BS>(p, s, c == 0) : 0;
+        const int v = Hkv * ns;
         int chunk;
         const int inc = block_inclusive_scan(v, sk->scan, chunk);
         if (c == 0 && s < B) p.ws_cum[s] = total + inc - v;
+        my_ns = ns;
+        my_first = total + inc - v;
         total += chunk;
     }
     if (c == 0 && tid == 0) p.ws_cum[B] = total;
@@ -684,8 +702,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
     const int gs = min(total, c * per), ge = min(total, gs + per);
     if (gs >= ge) return;    // nothing issued, nothing to wait for
 
-    // ---- the sequence whose units contain gs
-    {
+    // ---- the sequence whose units contain gs (the serial listing's start)
+    if (!one_pass) {
         int run = 0;
         for (int base = 0; base < B; base += NT) {
             const int s = base + tid;
@@ -709,8 +727,40 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
     bool first_seg = true;
 
     while (pos < ge && ok) {
-        // ---- list up to kMaxSegs segments of units, starting at (cur_s, cur_rem)
-        if (tid == 0) {
+        // ---- list up to kMaxSegs segments of units covering [pos, ge)
+        if (one_pass) {
+            // every thread lists the units of its own sequence that meet
+            // [pos, ge); a block scan of their counts gives the slots
+            const int v = Hkv * my_ns;
+            int g_lo = 0, n = 0;
+            if (my_ns > 0 && my_first < ge && my_first + v > pos) {
+                g_lo = (max(pos, my_first) - my_first) / my_ns;
+                const int g_hi = (min(ge, my_first + v) - 1 - my_first) / my_ns;
+                n = g_hi - g_lo + 1;
+            }
+            int nall;
+            const int base = block_inclusive_scan(n, sk->scan, nall) - n;
+            for (int k = 0; k < n; ++k) {
+                const int idx = base + k;
+                if (idx > kMaxSegs) break;
+                const int u0 = my_first + (g_lo + k) * my_ns;   // global stage of the unit's start
+                const int a = max(pos, u0), b = min(ge, u0 + my_ns);
+                if (idx == kMaxSegs) {        // first unit of the next listing
+                    sk->seg_lb[kMaxSegs] = a - pos;
+                    break;
+                }
+                sk->seg_s[idx] = tid;   // one pass: thread tid holds sequence tid
+                sk->seg_g[idx] = g_lo + k;
+                sk->seg_kb[idx] = a - u0;
+                sk->seg_ke[idx] = b - u0;
+                sk->seg_lb[idx] = a - pos;
+            }
+            if (tid == 0) {
+                sk->nseg = min(nall, kMaxSegs);
+                sk->more = nall > kMaxSegs ? 1 : 0;
+                if (nall <= kMaxSegs) sk->seg_lb[nall] = ge - pos;
+            }
+        } else if (tid == 0) {
             int n = 0, s = cur_s, rem = cur_rem, local = 0;
             const int len = ge - pos;
             while (local < len && n < kMaxSegs && s < B) {

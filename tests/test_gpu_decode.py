@@ -93,7 +93,7 @@ def test_shape_sweep(pa, d, group, bs):
 @pytest.mark.parametrize("name,sample", [("llama70b_decode", None), ("long_context", None),
                                          ("shared_prefix", 2048), ("beam_fork", 2048)])
 def test_full_size(pa, name, sample):
-    """BASELINE-sized workloads in the launch configuration the bench times."""
+    """The full-size workloads, in the launch configuration the bench times."""
     w = wl.CONFIGS[name]()
     c = Case(w)
     if w.copy_pairs is not None and len(w.copy_pairs):
@@ -110,6 +110,20 @@ def test_full_size(pa, name, sample):
         rows = np.stack([flat // w.num_q_heads, flat % w.num_q_heads], axis=1)
         ref = oracle_decode(c, rows)
         assert_close(out[rows[:, 0], rows[:, 1]], ref, name)
+
+
+@pytest.mark.parametrize("batch,hkv", [(100, 128), (300, 64)])
+def test_many_short_units_per_cta(pa, batch, hkv):
+    """Thousands of one-stage units, more per CTA of the balanced schedule
+    than one listing holds: exercises the repeated listings of a CTA's range
+    (one pass per thread's sequence for up to 128 sequences, the sequential
+    listing beyond)."""
+    rng = np.random.default_rng(batch + hkv)
+    lens = rng.integers(1, 17, size=batch)
+    w = wl.custom(list(lens), hkv, hkv, 64, 16, seed=77 + batch)
+    c = Case(w)
+    write_new_tokens(pa, c)
+    assert_close(run_decode(pa, c, 0), oracle_decode(c), f"B={batch} Hkv={hkv}")
 
 
 def test_partitions_agree(pa):
