@@ -250,7 +250,7 @@ def run_ours(args, world, rank, local):
     w = wl.CONFIGS[args.config](seed=wl.SEED_BASE + 1 + 1000 * rank) if args.config == "llama70b_decode" \
         else wl.CONFIGS[args.config]()
     tensors = wl.make_tensors(w, "cpu")
-    step = DecodeStep(pa, w, dev, tensors)
+    step = DecodeStep(pa, w, dev, tensors, layers=args.layers)
     stream = torch.cuda.current_stream()
     flush = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_read = lambda: flush.view(torch.int32).sum()     # evicts L2, leaves no dirty lines
@@ -505,6 +505,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=DecodeStep.LAYERS,
+                    help="layers' pools the timed steps rotate over (1 keeps one pool, e.g. for profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
