@@ -204,6 +204,8 @@ pa_status pa_copy_blocks(const pa_kv_pool *pool, const int32_t *pairs, int32_t n
  *   out, q       device, [num_seqs][chunk_len][num_q_heads][d] bf16
  *   ctx_lens     device, [num_seqs] int32: tokens cached before the chunk
  *   max_ctx_len  host upper bound on every ctx_lens[s]
+ *   scale        softmax scale, finite and > 0 (usually 1/sqrt(d)); else
+ *                PA_ERR_INVALID_ARG
  * Query j of sequence s sits at position ctx_lens[s] + j and attends keys
  * 0 .. ctx_lens[s] + j.  The chunk's own K/V must already be in the pool
  * (pa_reshape_and_cache).  QK^T and PV run on the tcgen05 tensor cores with

@@ -234,7 +234,7 @@ pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool, con
         return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0 || chunk_len == 0) return PA_OK;
     if (!out || !q || !block_tables || !ctx_lens || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(q) || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
     if ((int64_t)max_ctx_len + chunk_len > (int64_t)max_blocks_per_seq * view.block_size) return PA_ERR_INVALID_ARG;
     PrefillArgs a;
     a.out = out;

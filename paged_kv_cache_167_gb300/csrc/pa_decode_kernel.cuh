@@ -1057,35 +1057,14 @@ cudaError_t launch_group(const CUtensorMap &tmk, const CUtensorMap &tmv, const P
     }
 }
 
-// Tensor map of the K (kv = 0) or V (kv = 1) half of the pool as
-// (d within a 64-wide half, slot, half of d, kv-head, block); one box is a
-// whole (block, K|V, kv-head) slab, laid out [half][slot][64] with 128-byte
-// swizzle.
-inline cudaError_t encode_pool_map(CUtensorMap *map, const PoolView &pool, int kv) {
-    auto encode = tensor_map_encoder();
-    if (!encode) return cudaErrorNotSupported;
-    const int D = pool.head_dim, BS = pool.block_size;
-    const char *base = static_cast<const char *>(pool.base) + (size_t)kv * pool.kv_stride * 2;
-    cuuint64_t dims[5] = {64, (cuuint64_t)BS, (cuuint64_t)(D / 64), (cuuint64_t)pool.num_kv_heads,
-                          (cuuint64_t)pool.num_blocks};
-    cuuint64_t strides[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)BS * D * 2, (cuuint64_t)pool.block_stride * 2};
-    cuuint32_t box[5] = {64, (cuuint32_t)BS, (cuuint32_t)(D / 64), 1, 1};
-    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    if (encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<char *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    return cudaSuccess;
-}
-
 template <int D>
 cudaError_t launch_for_dim(const DecodeArgs &a, cudaStream_t stream) {
     unsigned int *err = device_error_word();
     if (!err) return cudaErrorUnknown;
     CUtensorMap tmk, tmv;
-    cudaError_t e = encode_pool_map(&tmk, a.pool, 0);
+    cudaError_t e = encode_pool_block_map(&tmk, a.pool, 0);
     if (e != cudaSuccess) return e;
-    e = encode_pool_map(&tmv, a.pool, 1);
+    e = encode_pool_block_map(&tmv, a.pool, 1);
     if (e != cudaSuccess) return e;
     Params prm;
     prm.out = static_cast<__nv_bfloat16 *>(a.out);

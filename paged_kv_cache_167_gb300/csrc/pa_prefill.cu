@@ -50,8 +50,10 @@ namespace pa {
 namespace prefill {
 
 constexpr int kSoftWarps = 8;               // two warpgroups, each owning 64 of a row's 128 keys
-constexpr int kProducerWarp = kSoftWarps;   // one more warp issues every copy and MMA
-constexpr int kThreads = (kSoftWarps + 1) * 32;
+constexpr int kMmaWarp = kSoftWarps;        // lane 0 issues every MMA
+constexpr int kKWarp = kSoftWarps + 1;      // copies Q and the K tiles
+constexpr int kVWarp = kSoftWarps + 2;      // copies the V tiles
+constexpr int kThreads = (kSoftWarps + 3) * 32;
 constexpr int kRows = 128;                  // M tile
 constexpr int kKeys = 128;                  // N tile of Q.K (keys per iteration)
 constexpr int kD = 128;                     // head_dim
@@ -59,13 +61,14 @@ constexpr int kBS = 16;                     // block_size
 constexpr uint32_t kHalf = 128u * 128u;     // one [128 rows][64 bf16] swizzled half tile, bytes
 constexpr uint32_t kTile = 2u * kHalf;      // [2 halves][128 rows][128 B]
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTile;   // 2 stages
-constexpr uint32_t kOffV = kOffK + 2 * kTile;
+constexpr uint32_t kOffK = kOffQ + kTile;   // 2 stages, [half][128 keys][128 B]
+constexpr uint32_t kOffV = kOffK + 2 * kTile; // 2 stages, [block][half][16 keys][128 B]
 constexpr uint32_t kOffP = kOffV + 2 * kTile; // 2 buffers
 constexpr uint32_t kOffX = kOffP + 2 * kTile; // [2 halves][128 rows] fp32 exchange
 constexpr uint32_t kOffBar = kOffX + 1024;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // + alignment slack
 constexpr uint32_t kTmemCols = 512;         // S0, S1, O (128 columns each)
+constexpr uint32_t kVBlock = 2u * kBS * 128u; // one block's V box, bytes
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 domain
 static_assert(kSmemBytes <= 232448, "shared memory");
@@ -179,16 +182,29 @@ __device__ __forceinline__ void pair_sync(int warp) {   // warps w and w + 4 own
     asm volatile("bar.sync %0, %1;" ::"r"(1 + (warp & 3)), "r"(64) : "memory");
 }
 
-// Timeline of tile t (the producer runs one tile ahead):
-//   producer : Q.K(t+1) -> S[(t+1)%2] ; refill K(t+2), V(t+1) ; P.V(t) once P(t) is ready
+__device__ __forceinline__ float max_tree64(const uint32_t (&a)[32], const uint32_t (&b)[32]) {
+    float m[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m[i] = fmaxf(__uint_as_float(a[i]), __uint_as_float(b[i]));
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    return m[0];
+}
+
+// Timeline of tile t (the MMA lane runs one tile ahead on Q.K):
+//   K warp   : K(t) -> K slot t % 2 once Q.K(t-2) has completed
+//   V warp   : V(t) -> V slot t % 2 once P.V(t-2) has completed
+//   MMA lane : Q.K(t+1) -> S[(t+1)%2] ; P.V(t) once P(t) is ready
 //   softmax  : S[t%2] -> registers (frees S) ; row max over both halves ; P(t) ;
 //              O rescale when the reference moved ; signal P(t)
 // Barriers: S ready (MMA commit), S free (256 arrivals), P ready (256 arrivals),
-// P.V done per P buffer (MMA commit), K / V / Q landed (TMA).
+// P.V done per P buffer (MMA commit), K / V / Q landed (TMA), drain (MMA commit).
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
-                   const Params p) {
+    prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
     constexpr int QPT = kRows / G;   // queries per M-tile
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -197,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *xch = reinterpret_cast<float *>(gbase + kOffX);
     const uint32_t barQ = base + kOffBar;
     const uint32_t barK = barQ + 8, barV = barQ + 24, barS = barQ + 40, barSfree = barQ + 56, barP = barQ + 72,
-                   barOP = barQ + 88;
+                   barOP = barQ + 88, barEnd = barQ + 104;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 128);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffBar + 132);
 
@@ -205,15 +221,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int mt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
     const int j0 = mt * QPT;
 
-    if (warp == kProducerWarp) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
                      "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        const uint32_t counts[13] = {1, 1, 1, 1, 1, 1, 1, 256, 256, 256, 256, 1, 1};
-        for (int i = 0; i < 13; ++i)
+        const uint32_t counts[14] = {1, 1, 1, 1, 1, 1, 1, 256, 256, 256, 256, 1, 1, 1};
+        for (int i = 0; i < 14; ++i)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(barQ + 8 * i), "r"(counts[i]) : "memory");
         *abort_flag = 0;
         fence_barrier_init();
@@ -238,33 +254,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_qk = idesc_bf16(kRows, kKeys, false);
     constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, true);
 
-    if (warp == kProducerWarp) {
+    if (warp == kKWarp || warp == kVWarp) {
+        // ---- copy warps: a lane per box, block ids fetched a tile at a time
+        const bool is_k = warp == kKWarp;
+        const int32_t *table_row = p.tables + (size_t)s * p.max_blocks;
+        const uint32_t bar0 = is_k ? barK : barV;
+        const uint32_t slot0 = is_k ? sK : sV;
+        if (is_k) {
+            if (lane == 0) mbar_expect(barQ, kTile);
+            __syncwarp();
+            if (lane < 2) tma_load_4d(sQ + lane * kHalf, &tmap_q, lane * 64, 0, g, s * p.chunk + j0, barQ);
+        }
+        int issued = 0;
+        bool ok = true;
+        for (int t = 0; t < n_tiles; ++t) {
+            if (*abort_flag) break;
+            const int st = t & 1;
+            int id = (int)p.num_blocks;   // out-of-bounds coordinate: zero fill
+            if (lane < kKeys / kBS) {
+                const int bi = t * (kKeys / kBS) + lane;
+                if (bi < nblk_seq) {
+                    const int v = __ldg(table_row + bi);
+                    if (v < 0 || v >= p.num_blocks) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                    else id = v;
+                }
+            }
+            if (t >= 2) {   // the slot's previous tile has been consumed by its MMA
+                const uint32_t free_bar = (is_k ? barS : barOP) + 8 * st;
+                ok = __all_sync(0xffffffffu, mbar_wait(free_bar, (uint32_t)(((t - 2) >> 1) & 1), p.err));
+                if (!ok) {
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+            if (lane == 0) mbar_expect(bar0 + 8 * st, kTile);
+            __syncwarp();
+            const uint32_t dst = slot0 + st * kTile;
+            if (is_k) {
+                const int blk = __shfl_sync(0xffffffffu, id, lane >> 1);
+                if (lane < 2 * (kKeys / kBS))
+                    tma_load_5d(dst + (lane & 1) * kHalf + (lane >> 1) * 2048, &tmap_k, (lane & 1) * 64, 0, g, 0,
+                                blk, bar0 + 8 * st);
+            } else if (lane < kKeys / kBS) {
+                tma_load_5d(dst + lane * kVBlock, &tmap_v, 0, 0, 0, g, id, bar0 + 8 * st);
+            }
+            issued = t + 1;
+        }
+        if (!ok || *abort_flag) {
+            // wait (bounded) for this warp's last two copies before the memory is released
+            for (int t = max(0, issued - 2); t < issued; ++t) mbar_wait(bar0 + 8 * (t & 1), (uint32_t)((t >> 1) & 1), p.err);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            const int32_t *table_row = p.tables + (size_t)s * p.max_blocks;
-            auto phys = [&](int bi) -> int {   // physical block, or the out-of-bounds coordinate (zero fill)
-                if (bi >= nblk_seq) return (int)p.num_blocks;
-                const int id = __ldg(table_row + bi);
-                if (id < 0 || id >= p.num_blocks) {
-                    raise_error(p.err, PA_DEVERR_BLOCK_ID);
-                    return (int)p.num_blocks;
-                }
-                return id;
-            };
-            int issued[2] = {0, 0}, waited[2] = {0, 0};   // K, V tiles issued / seen landed
-            auto load_kv = [&](int t, int kv) {
-                issued[kv] = t + 1;
-                const int st = t & 1;
-                const uint32_t dst = (kv ? sV : sK) + st * kTile;
-                const uint32_t bar = (kv ? barV : barK) + 8 * st;
-                mbar_expect(bar, kTile);
-#pragma unroll
-                for (int i = 0; i < kKeys / kBS; ++i) {
-                    const int blk = phys(t * (kKeys / kBS) + i);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_5d(dst + h * kHalf + i * 2048, &tmap_kv, h * 64, 0, g, kv, blk, bar);
-                }
-            };
             auto qk = [&](int t) {
                 const int st = t & 1;
 #pragma unroll
@@ -283,17 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return ok;
             };
-            mbar_expect(barQ, kTile);
-            const int qrow = s * p.chunk + j0;
-            tma_load_4d(sQ, &tmap_q, 0, 0, g, qrow, barQ);
-            tma_load_4d(sQ + kHalf, &tmap_q, 64, 0, g, qrow, barQ);
-            for (int t = 0; t < 2 && t < n_tiles; ++t) {
-                load_kv(t, 0);
-                load_kv(t, 1);
-            }
             int committed_pv = 0;
             if (wait(barQ, 0) && wait(barK, 0)) {
-                waited[0] = 1;
                 tc_fence_after();
                 qk(0);
             }
@@ -301,41 +334,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = t & 1, st1 = (t + 1) & 1;
                 if (t + 1 < n_tiles) {
                     if (!wait(barK + 8 * st1, (uint32_t)(((t + 1) >> 1) & 1))) break;
-                    waited[0] = t + 2;
                     if (t >= 1 && !wait(barSfree + 8 * st1, (uint32_t)(((t - 1) >> 1) & 1))) break;
                     tc_fence_after();
                     qk(t + 1);
                 }
-                if (t + 2 < n_tiles) {   // K slot st is free once Q.K(t) completed
-                    if (!wait(barS + 8 * st, (uint32_t)((t >> 1) & 1))) break;
-                    load_kv(t + 2, 0);
-                }
-                if (t >= 1 && t + 1 < n_tiles) {   // V slot st1 is free once P.V(t-1) completed
-                    if (!wait(barOP + 8 * st1, (uint32_t)(((t - 1) >> 1) & 1))) break;
-                    load_kv(t + 1, 1);
-                }
                 if (!wait(barP + 8 * st, (uint32_t)((t >> 1) & 1))) break;
                 if (!wait(barV + 8 * st, (uint32_t)((t >> 1) & 1))) break;
-                waited[1] = t + 1;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk) {
+                for (int kk = 0; kk < kKeys / 16; ++kk) {   // 16 keys = one block's V box
                     const uint32_t a_off = (kk >> 2) * kHalf + (kk & 3) * 32;
                     umma(tO, smem_desc(sP + st * kTile + a_off, 16, 1024),
-                         smem_desc(sV + st * kTile + kk * 2048, kHalf, 1024), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                         smem_desc(sV + st * kTile + kk * kVBlock, kVBlock / 2, 1024), idesc_pv,
+                         (t > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(barOP + 8 * st);
                 committed_pv = t + 1;
             }
             if (!ok || *abort_flag) {
-                // Give up: wait (bounded) for every copy still in flight and,
-                // through one more commit on the Q barrier, for every issued MMA.
+                // give up: one more commit tracks every MMA issued so far
                 *abort_flag = 1;
-                for (int kv = 0; kv < 2; ++kv)
-                    for (int tt = waited[kv]; tt < issued[kv]; ++tt)
-                        mbar_wait((kv ? barV : barK) + 8 * (tt & 1), (uint32_t)((tt >> 1) & 1), p.err);
-                umma_commit(barQ);
-                mbar_wait(barQ, 1, p.err);
+                umma_commit(barEnd);
+                mbar_wait(barEnd, 0, p.err);
             } else if (committed_pv > 0) {
                 const int t = committed_pv - 1;   // all MMAs done before the memory is released
                 mbar_wait(barOP + 8 * (t & 1), (uint32_t)((t >> 1) & 1), p.err);
@@ -343,12 +363,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---- softmax warps: row r, key half hf
+        // ---- softmax warps: row r, key half hf (scale_log2 > 0: maxima of raw scores)
         const int r = (warp & 3) * 32 + lane, hf = warp >> 2;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const int jr = j0 + r / G;
         const int pos = min(ctx + jr, seq_end - 1);   // last key this row may attend
-        float m_ref = -INFINITY, l = 0.f;
+        const float c = p.scale_log2;
+        float m_ref = -INFINITY;                       // reference maximum, log2 domain
+        float2 l2 = make_float2(0.f, 0.f);
         int done = 0;
         for (int t = 0; t < n_tiles; ++t) {
             const int st = t & 1;
@@ -365,15 +387,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive_u32(barSfree + 8 * st);
             const int key0 = t * kKeys + hf * 64;
-            float mh = -INFINITY;
+            if (!__all_sync(0xffffffffu, key0 + 63 <= pos)) {   // tile crosses some row's causal edge
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+                for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float x = key0 + c * 32 + i <= pos ? __uint_as_float(sr[c][i]) * p.scale_log2 : -INFINITY;
-                    sr[c][i] = __float_as_uint(x);
-                    mh = fmaxf(mh, x);
-                }
+                    for (int i = 0; i < 32; ++i)
+                        if (key0 + cc * 32 + i > pos) sr[cc][i] = __float_as_uint(-INFINITY);
+            }
+            const float mh = max_tree64(sr[0], sr[1]);
             // both halves of the row agree on the tile maximum and on giving up
             xch[hf * 128 + r] = (ok && !*abort_flag) ? mh : __int_as_float(0x7fc00001);
             pair_sync(warp);
@@ -387,51 +408,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_u32(barP + 8 * st);   // keep the arrival count balanced
                 break;
             }
-            const float mt_ = fmaxf(mh, other);
+            const float mt_ = fmaxf(mh, other) * c;
             float alpha = 1.f;
             if (mt_ > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt_ != -INFINITY)) {
                 alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - mt_);
                 m_ref = mt_;
             }
-            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+            const float2 c2 = make_float2(c, c);
+            const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
+            const float2 nm2 = make_float2(nm, nm);
             // P buffer st was last read by P.V(t-2)
             if (t >= 2) mbar_wait(barOP + 8 * st, (uint32_t)(((t - 2) >> 1) & 1), p.err);
-            float psum = 0.f;
+            float2 ps2 = make_float2(0.f, 0.f);
             const uint32_t prow = sP + st * kTile + hf * kHalf + (uint32_t)r * 128u;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {        // 8 keys = one 16-byte chunk
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float a = fast_exp2(__uint_as_float(sr[c][q4 * 8 + 2 * e]) - m_use);
-                        const float b = fast_exp2(__uint_as_float(sr[c][q4 * 8 + 2 * e + 1]) - m_use);
-                        const __nv_bfloat162 pr = __floats2bfloat162_rn(a, b);
-                        psum += __low2float(pr) + __high2float(pr);
-                        w[e] = *reinterpret_cast<const uint32_t *>(&pr);
+                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cc][q4 * 8 + 2 * e]),
+                                                                __uint_as_float(sr[cc][q4 * 8 + 2 * e + 1])),
+                                                    c2, nm2);
+                        const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        ps2 = __fadd2_rn(ps2, pe);
+                        w[e] = pack_bf16x2(pe.x, pe.y);
                     }
-                    const uint32_t chunk = (uint32_t)(c * 4 + q4);
+                    const uint32_t chunk = (uint32_t)(cc * 4 + q4);
                     const uint32_t addr = prow + ((chunk ^ (uint32_t)(r & 7)) << 4);
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
                                  "r"(w[2]), "r"(w[3])
                                  : "memory");
                 }
             }
-            l = l * alpha + psum;
+            l2.x = l2.x * alpha + (ps2.x + ps2.y);
             // rescale this half of O once P.V(t-1) has completed
             if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 const int tp = t - 1;
                 mbar_wait(barOP + 8 * (tp & 1), (uint32_t)((tp >> 1) & 1), p.err);
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int cc = 0; cc < 2; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(tO + lane_off + hf * 64 + c * 32, o);
+                    tmem_ld32(tO + lane_off + hf * 64 + cc * 32, o);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(tO + lane_off + hf * 64 + c * 32, o);
+                    tmem_st32(tO + lane_off + hf * 64 + cc * 32, o);
                 }
                 tmem_st_wait();
             }
@@ -444,7 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nrows = min(blk_end, kKeys) - tail_lo;
                 for (int idx = tid; idx < nrows * 2 * 8; idx += kSoftWarps * 32) {
                     const int rr = tail_lo + idx / 16, h = (idx / 8) & 1, c16 = idx & 7;
-                    const uint32_t addr = sV + st * kTile + h * kHalf + (uint32_t)rr * 128u + (uint32_t)c16 * 16u;
+                    const uint32_t addr = sV + st * kTile + (uint32_t)(rr / kBS) * kVBlock + h * (kVBlock / 2) +
+                                          (uint32_t)(rr % kBS) * 128u + (uint32_t)c16 * 16u;
                     asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
                 }
             }
@@ -454,6 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             done = t + 1;
         }
         // ---- epilogue: O / l to bf16, this thread's row and key half
+        const float l = l2.x;
         const bool fin = done == n_tiles && !*abort_flag &&
                          mbar_wait(barOP + 8 * ((n_tiles - 1) & 1), (uint32_t)(((n_tiles - 1) >> 1) & 1), p.err);
         xch[hf * 128 + r] = l;
@@ -466,9 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __nv_bfloat16 *dst =
                 p.out + (((size_t)s * p.chunk + jr) * p.num_q_heads + (size_t)g * G + (r % G)) * kD + hf * 64;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(tO + lane_off + hf * 64 + c * 32, o);
+                tmem_ld32(tO + lane_off + hf * 64 + cc * 32, o);
                 tmem_ld_wait();
                 if (row_ok) {
 #pragma unroll
@@ -478,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
                         v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
                         v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(dst + c * 32 + q4 * 8) = v;
+                        *reinterpret_cast<uint4 *>(dst + cc * 32 + q4 * 8) = v;
                     }
                 }
             }
@@ -486,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kProducerWarp) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
@@ -495,8 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---- host side --------------------------------------------------------------
 
 template <int G>
-cudaError_t launch_group(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mkv, const Params &prm,
-                         cudaStream_t stream) {
+cudaError_t launch_group(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mkv, const CUtensorMap &mv,
+                         const Params &prm, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -518,7 +544,7 @@ cudaError_t launch_group(const PrefillArgs &a, const CUtensorMap &mq, const CUte
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<G>, mq, mkv, prm);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<G>, mq, mkv, mv, prm);
 }
 
 }  // namespace prefill
@@ -562,6 +588,8 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    CUtensorMap mv;   // V: one box per block (both halves of d)
+    if (encode_pool_block_map(&mv, a.pool, 1) != cudaSuccess) return cudaErrorInvalidValue;
     Params prm;
     prm.out = static_cast<__nv_bfloat16 *>(a.out);
     prm.tables = a.tables;
@@ -574,10 +602,10 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     prm.scale_log2 = a.scale * kLog2e;
     prm.err = err;
     switch (G) {
-        case 1: return launch_group<1>(a, mq, mkv, prm, stream);
-        case 2: return launch_group<2>(a, mq, mkv, prm, stream);
-        case 4: return launch_group<4>(a, mq, mkv, prm, stream);
-        case 8: return launch_group<8>(a, mq, mkv, prm, stream);
+        case 1: return launch_group<1>(a, mq, mkv, mv, prm, stream);
+        case 2: return launch_group<2>(a, mq, mkv, mv, prm, stream);
+        case 4: return launch_group<4>(a, mq, mkv, mv, prm, stream);
+        case 8: return launch_group<8>(a, mq, mkv, mv, prm, stream);
         default: return cudaErrorInvalidValue;
     }
 }

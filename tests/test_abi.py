@@ -68,6 +68,9 @@ def test_host_validation(B):
     assert L.pa_copy_blocks(ctypes.byref(good), P(0), 0, P(0)) == 0
     assert L.pa_prefill_chunk(ok_ptr, ok_ptr, ctypes.byref(_pool(B, d=64)), ok_ptr, 8, ok_ptr, 1, 4, 64, 10,
                               0.1, P(0)) == 2
+    for bad_scale in (0.0, -0.1, float("nan")):                          # scale must be finite and > 0
+        assert L.pa_prefill_chunk(ok_ptr, ok_ptr, ctypes.byref(good), ok_ptr, 8, ok_ptr, 1, 4, 64, 10,
+                                  bad_scale, P(0)) == 1
     err = ctypes.c_uint32()
     assert L.pa_get_device_error(None, 0, P(0)) == 1
 
