@@ -110,6 +110,31 @@ def measure_prefill(pa, dev, flush_fn, iters: int = 10):
     return w, ms, prefill_flops(w)
 
 
+def measure_swap(pa, step, iters: int = 5):
+    """Median device time of pa_swap_blocks moving 1,024 blocks of the decode
+    pool (64 MiB) to pinned host memory and back."""
+    n = min(1024, step.w.num_blocks)
+    w = step.w
+    host = torch.empty((n, 2, w.num_kv_heads, w.block_size, w.head_dim), dtype=torch.bfloat16, pin_memory=True)
+    pairs = torch.stack([torch.arange(n, dtype=torch.int32), torch.arange(n, dtype=torch.int32)], 1).to(step.dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name, direction in (("out", pa.PA_SWAP_OUT), ("in", pa.PA_SWAP_IN)):
+        pa.swap_blocks(step.pool, host, pairs, direction)
+        ts = []
+        for _ in range(iters):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            pa.swap_blocks(step.pool, host, pairs, direction)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = float(np.median(ts))
+        res[name] = {"ms": round(ms, 4), "gbs": round(host.numel() * 2 / (ms / 1e3) / 1e9, 1)}
+    assert pa.get_device_error() == 0, "device error during swap"
+    return {"blocks": n, "bytes": host.numel() * 2, **res}
+
+
 def decode_bytes(w: wl.Workload) -> int:
     """Algorithmic bytes of one decode call: every attended K and V row once,
     q and out once, the table entries used and the lengths."""
@@ -351,6 +376,7 @@ def run_ours(args, world, rank, local):
     barrier()
 
     prefill = None if args.no_prefill else measure_prefill(pa, dev, flush_read)
+    swap = measure_swap(pa, step)
 
     elapsed = torch.tensor([total_ms, e2e_s * 1e3, decode_total_ms / K, sum(wstep_ms), sum(flushed_ms),
                             float(np.mean(flushed_decode_ms))], dtype=torch.float64, device=dev)
@@ -410,6 +436,8 @@ def run_ours(args, world, rank, local):
                                         "peak": bf16_peak, "peak_kind": peak_kind, "unit": "TFLOP/s",
                                         "frac": round(pflop / (pms / 1e3) / 1e12 / bf16_peak, 4),
                                         "flops": pflop}}
+    line["swap"] = dict(swap, note="pa_swap_blocks between the decode pool and pinned host memory, one kernel "
+                                   "over the CPU-GPU link")
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, tensors, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)

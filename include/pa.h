@@ -44,7 +44,8 @@ typedef enum {
     PA_ERR_CUDA = 4,          /* the CUDA runtime reported an error                       */
     PA_ERR_DEVICE = 5,        /* pa_get_device_error found a non-zero device error word   */
     PA_ERR_NO_BLOCKS = 6,     /* block manager: the pool has no free block left           */
-    PA_ERR_NOT_FOUND = 7      /* block manager: unknown sequence id                       */
+    PA_ERR_NOT_FOUND = 7,     /* block manager: unknown sequence id                       */
+    PA_ERR_SWAPPED = 8        /* block manager: the sequence's blocks are on the host     */
 } pa_status;
 
 /* Bits of the per-device error word written by the kernels. */
@@ -194,6 +195,34 @@ pa_status pa_decode_noalloc(void *out, const void *q, const pa_kv_pool *pool,
  * are copied concurrently: a dst that is also some pair's src, or a repeated
  * dst, gives an unspecified result.
  */
+/*
+ * Block-granular swap between one layer of the pool and pinned host memory.
+ * [P1] feature table, preemption row: under memory pressure a sequence's
+ * blocks are swapped to host memory at block granularity; [P1] "What
+ * interviewers probe next": when the pool runs dry mid-decode, the preempted
+ * sequence's blocks go to pinned host memory.
+ *   host         host memory the GPU can address -- pinned and mapped
+ *                (cudaHostAlloc, or cudaHostRegister with
+ *                cudaHostRegisterMapped), or any host memory where the GPU
+ *                walks the host's page tables (NVLink-C2C systems) --
+ *                16-byte aligned, holding host_blocks
+ *                blocks as [host_blocks][2][Hkv][b][d] bf16: one block's K and
+ *                V slabs for every kv-head (64 KiB at Hkv 8, b 16, d 128)
+ *   pairs        device, [num_pairs][2] int32 (device block, host block)
+ *   direction    PA_SWAP_OUT: host[hb] = pool[dev]; PA_SWAP_IN: pool[dev] = host[hb]
+ * One kernel reads or writes the host buffer directly through its device
+ * mapping (no staging copy, no per-block copy call), so it can run on its own
+ * stream beside compute.  A host pointer the GPU cannot address
+ * (cudaHostGetDevicePointer fails) gives PA_ERR_INVALID_ARG and nothing is
+ * launched.  An id out of range raises
+ * PA_DEVERR_BLOCK_ID and that pair is skipped; repeated destinations give an
+ * unspecified result.  Bit-exact copies.
+ */
+#define PA_SWAP_OUT 0
+#define PA_SWAP_IN 1
+pa_status pa_swap_blocks(const pa_kv_pool *pool, void *host, int64_t host_blocks, const int32_t *pairs,
+                         int32_t num_pairs, int32_t direction, cudaStream_t stream);
+
 pa_status pa_copy_blocks(const pa_kv_pool *pool, const int32_t *pairs, int32_t num_pairs,
                          cudaStream_t stream);
 
@@ -296,6 +325,33 @@ int32_t pa_bm_refcount(const pa_bm *bm, int64_t block);
 /* *admit = 1 iff free blocks >= ceil(prompt_tokens/b) + 1 + watermark_blocks. */
 pa_status pa_bm_can_admit(const pa_bm *bm, int64_t prompt_tokens, int64_t watermark_blocks,
                           int32_t *admit);
+
+/*
+ * Swapping ([P1] feature table, preemption row; "What interviewers probe
+ * next").  pa_bm_set_host_pool gives the manager host_blocks host slots (the
+ * blocks of the pinned buffer pa_swap_blocks uses); it fails with
+ * PA_ERR_INVALID_ARG while any slot is in use.
+ * pa_bm_swap_out moves every block of seq to a fresh host slot: it writes one
+ * (device block, host block) pair per table entry, in table order, to
+ * pairs_out ([cap][2]) and *n_pairs_out; the caller runs
+ * pa_swap_blocks(PA_SWAP_OUT) on them before reusing the device blocks, whose
+ * references the sequence drops (a block shared with another sequence stays
+ * on the device for it).  pa_bm_swap_in takes fresh device blocks from the
+ * free list and writes the pairs for pa_swap_blocks(PA_SWAP_IN); the host slots
+ * are free once that copy has run.  PA_ERR_NO_BLOCKS (too few free host
+ * slots, or device blocks) and PA_ERR_INVALID_ARG (cap too small) leave the
+ * sequence unchanged.  While swapped out, a sequence cannot be appended to,
+ * forked or read as a table (PA_ERR_SWAPPED); freeing it releases its host
+ * slots.  Swapping in a sequence that is not swapped out, or out one that is,
+ * gives PA_ERR_SWAPPED.
+ */
+pa_status pa_bm_set_host_pool(pa_bm *bm, int64_t host_blocks);
+pa_status pa_bm_swap_out(pa_bm *bm, int32_t seq, int32_t *pairs_out, int32_t cap, int32_t *n_pairs_out);
+pa_status pa_bm_swap_in(pa_bm *bm, int32_t seq, int32_t *pairs_out, int32_t cap, int32_t *n_pairs_out);
+/* Free host slots (-1 for a NULL manager); 1 if seq is swapped out, 0 if it
+ * is on the device, -1 if it does not exist. */
+int64_t pa_bm_num_free_host(const pa_bm *bm);
+int32_t pa_bm_is_swapped(const pa_bm *bm, int32_t seq);
 
 #ifdef __cplusplus
 }

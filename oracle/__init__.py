@@ -102,6 +102,7 @@ class Oracle:
             "orc_slot_mapping": (None, [P, P, I64, P, P, I64, I64]),
             "orc_reshape_and_cache": (None, [P, G, P, P, P, I64]),
             "orc_copy_blocks": (None, [P, G, P, I64]),
+            "orc_swap_blocks": (None, [P, G, P, P, I64, I32]),
             "orc_paged_decode_rows": (None, [P, P, P, G, P, I64, P, I64, D, P, I64]),
             "orc_paged_decode": (None, [P, P, P, G, P, I64, P, I64, I64, D]),
             "orc_prefill_rows": (None, [P, P, P, G, P, I64, P, I64, I64, D, P, I64]),
@@ -153,6 +154,16 @@ class Oracle:
             raise TypeError("pool must be a C-contiguous uint16 array")
         pairs = _i32(pairs).reshape(-1, 2)
         self._lib.orc_copy_blocks(_ptr(pool), ctypes.byref(geom), _ptr(pairs), pairs.shape[0])
+
+    def swap_blocks(self, pool: np.ndarray, geom: PoolGeom, host: np.ndarray, pairs, direction: int) -> None:
+        """Block copies between pool and host ([hb][2][Hkv][b][d]); pairs are
+        (pool block, host block); direction 0 = pool -> host, 1 = host -> pool."""
+        for name, a in (("pool", pool), ("host", host)):
+            if a.dtype != np.uint16 or not a.flags.c_contiguous:
+                raise TypeError(f"{name} must be a C-contiguous uint16 array")
+        pairs = _i32(pairs).reshape(-1, 2)
+        self._lib.orc_swap_blocks(_ptr(pool), ctypes.byref(geom), _ptr(host), _ptr(pairs), pairs.shape[0],
+                                  int(direction))
 
     # -- attention -------------------------------------------------------------
     def paged_decode(self, q: np.ndarray, pool: np.ndarray, geom: PoolGeom, tables, seq_lens,

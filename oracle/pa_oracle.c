@@ -157,6 +157,32 @@ void orc_copy_blocks(uint16_t *pool, const orc_pool *p, const int32_t *pairs, in
     }
 }
 
+/* Preemption by swapping (how-pagedattention-works, feature table, preemption
+ * row; "What interviewers probe next": a preempted sequence's blocks go to
+ * pinned host memory): block-granular copies between the pool and a host
+ * array of host_blocks blocks laid out [hb][2][Hkv][b][d].  pairs is [n][2] =
+ * (pool block, host block); direction 0 copies pool -> host, 1 host -> pool. */
+void orc_swap_blocks(uint16_t *pool, const orc_pool *p, uint16_t *host, const int32_t *pairs, int64_t n_pairs,
+                     int32_t direction)
+{
+    const int64_t H = p->num_kv_heads, d = p->head_dim, b = p->block_size;
+    for (int64_t j = 0; j < n_pairs; ++j) {
+        int64_t blk = pairs[2 * j], hb = pairs[2 * j + 1];
+        for (int64_t half = 0; half < 2; ++half)
+            for (int64_t h = 0; h < H; ++h)
+                for (int64_t off = 0; off < b; ++off) {
+                    uint16_t *pr = pool + pool_elem(p, blk, half, h, off);
+                    uint16_t *hr = host + (((hb * 2 + half) * H + h) * b + off) * d;
+                    for (int64_t i = 0; i < d; ++i) {
+                        if (direction == 0)
+                            hr[i] = pr[i];
+                        else
+                            pr[i] = hr[i];
+                    }
+                }
+    }
+}
+
 /* Attention of one query row over the first n_keys positions of one
  * sequence, kv-head kvh.  Step 1 gathers K and V position by position
  * through the table (the conceptual lookup code); step 2 is standard scaled

@@ -19,7 +19,9 @@ LIBRARY = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa.so")
 
 PA_OK = 0
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
-                4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE", 6: "PA_ERR_NO_BLOCKS", 7: "PA_ERR_NOT_FOUND"}
+                4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE", 6: "PA_ERR_NO_BLOCKS", 7: "PA_ERR_NOT_FOUND",
+                8: "PA_ERR_SWAPPED"}
+PA_SWAP_OUT, PA_SWAP_IN = 0, 1
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 PA_DTYPE_BF16 = 0
 
@@ -45,6 +47,7 @@ SIGNATURES = {
     "pa_decode": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _P]),
     "pa_decode_noalloc": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P]),
     "pa_copy_blocks": (_I32, [_POOL, _P, _I32, _P]),
+    "pa_swap_blocks": (_I32, [_POOL, _P, _I64, _P, _I32, _I32, _P]),
     "pa_prefill_chunk": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _I32, _F, _P]),
     "pa_get_device_error": (_I32, [ctypes.POINTER(_U32), _I32, _P]),
     "pa_block_layout": (_I32, [_I64, _I32, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
@@ -59,6 +62,11 @@ SIGNATURES = {
     "pa_bm_num_free": (_I64, [_P]),
     "pa_bm_refcount": (_I32, [_P, _I64]),
     "pa_bm_can_admit": (_I32, [_P, _I64, _I64, ctypes.POINTER(_I32)]),
+    "pa_bm_set_host_pool": (_I32, [_P, _I64]),
+    "pa_bm_swap_out": (_I32, [_P, _I32, _P, _I32, ctypes.POINTER(_I32)]),
+    "pa_bm_swap_in": (_I32, [_P, _I32, _P, _I32, ctypes.POINTER(_I32)]),
+    "pa_bm_num_free_host": (_I64, [_P]),
+    "pa_bm_is_swapped": (_I32, [_P, _I32]),
 }
 
 
@@ -213,6 +221,23 @@ def copy_blocks(pool: torch.Tensor, pairs: torch.Tensor, layer: Optional[int] = 
         raise ValueError("pairs must be [n][2]")
     _check(lib().pa_copy_blocks(ctypes.byref(desc), _dev(pairs, torch.int32, "pairs"), pairs.shape[0],
                                 _stream(stream)), "pa_copy_blocks")
+
+
+def swap_blocks(pool: torch.Tensor, host: torch.Tensor, pairs: torch.Tensor, direction: int,
+                layer: Optional[int] = None, stream=None) -> None:
+    """pa_swap_blocks.  ``host`` is a pinned CPU bf16 tensor of
+    [host_blocks][2][Hkv][b][d]; ``pairs`` a CUDA int32 [n][2] of
+    (device block, host block); ``direction`` PA_SWAP_OUT or PA_SWAP_IN."""
+    desc = pool_desc(pool, layer)
+    if pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be [n][2]")
+    if host.device.type != "cpu" or host.dtype != torch.bfloat16 or not host.is_contiguous():
+        raise ValueError("host must be a contiguous bf16 CPU tensor")
+    if host.dim() != 5 or tuple(host.shape[1:]) != (2, desc.num_kv_heads, desc.block_size, desc.head_dim):
+        raise ValueError("host must be [host_blocks][2][Hkv][b][d]")
+    _check(lib().pa_swap_blocks(ctypes.byref(desc), ctypes.c_void_p(host.data_ptr()), host.shape[0],
+                                _dev(pairs, torch.int32, "pairs"), pairs.shape[0], int(direction),
+                                _stream(stream)), "pa_swap_blocks")
 
 
 def prefill_chunk(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_tables: torch.Tensor,

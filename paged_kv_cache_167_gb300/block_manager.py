@@ -80,5 +80,36 @@ class BlockManager:
                "pa_bm_can_admit")
         return bool(ok.value)
 
+    # ---- swapping to a pinned host buffer (see pa_bm_swap_out / pa_bm_swap_in)
+
+    def set_host_pool(self, host_blocks: int) -> None:
+        _check(lib().pa_bm_set_host_pool(self._h, host_blocks), "pa_bm_set_host_pool")
+
+    def _swap(self, fn, name: str, seq: int) -> np.ndarray:
+        cap = self.num_blocks   # a sequence never holds more blocks than the pool
+        pairs = np.empty((cap, 2), dtype=np.int32)
+        n = _I32()
+        _check(fn(self._h, seq, pairs.ctypes.data_as(ctypes.c_void_p), cap, ctypes.byref(n)), name)
+        return pairs[:n.value]
+
+    def swap_out(self, seq: int) -> np.ndarray:
+        """Moves seq's blocks to host slots; returns the (device block, host
+        block) pairs to run through swap_blocks(PA_SWAP_OUT)."""
+        return self._swap(lib().pa_bm_swap_out, "pa_bm_swap_out", seq)
+
+    def swap_in(self, seq: int) -> np.ndarray:
+        """Gives seq fresh device blocks; returns the (device block, host block)
+        pairs to run through swap_blocks(PA_SWAP_IN)."""
+        return self._swap(lib().pa_bm_swap_in, "pa_bm_swap_in", seq)
+
+    def num_free_host(self) -> int:
+        return int(lib().pa_bm_num_free_host(self._h))
+
+    def is_swapped(self, seq: int) -> bool:
+        r = int(lib().pa_bm_is_swapped(self._h, seq))
+        if r < 0:
+            raise PagedAttentionError(7, "pa_bm_is_swapped")
+        return r == 1
+
 
 __all__ = ["BlockManager", "PagedAttentionError"]

@@ -135,6 +135,7 @@ const char *pa_status_string(pa_status status) {
         case PA_ERR_DEVICE: return "device error word is set";
         case PA_ERR_NO_BLOCKS: return "no free block left";
         case PA_ERR_NOT_FOUND: return "unknown sequence";
+        case PA_ERR_SWAPPED: return "sequence is swapped out";
     }
     return "unknown status";
 }
@@ -219,6 +220,27 @@ pa_status pa_copy_blocks(const pa_kv_pool *pool, const int32_t *pairs, int32_t n
     if (num_pairs == 0) return PA_OK;
     if (!pairs || num_pairs > (1 << 30)) return PA_ERR_INVALID_ARG;
     return launch_copy_blocks(view, pairs, num_pairs, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_swap_blocks(const pa_kv_pool *pool, void *host, int64_t host_blocks, const int32_t *pairs,
+                         int32_t num_pairs, int32_t direction, cudaStream_t stream) {
+    PoolView view;
+    pa_status st = resolve_pool(pool, &view);
+    if (st != PA_OK) return st;
+    if (num_pairs < 0 || host_blocks <= 0 || (direction != PA_SWAP_OUT && direction != PA_SWAP_IN))
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!pairs || !host || !aligned16(host) || num_pairs > (1 << 30)) return PA_ERR_INVALID_ARG;
+    // The kernel reaches the host buffer through its device mapping: pinned
+    // (page-locked, mapped) memory only.
+    void *host_dev = nullptr;
+    if (cudaHostGetDevicePointer(&host_dev, host, 0) != cudaSuccess || !host_dev) {
+        cudaGetLastError();   // clear the sticky-free error this query leaves
+        return PA_ERR_INVALID_ARG;
+    }
+    return launch_swap_blocks(view, host_dev, host_blocks, pairs, num_pairs, direction, stream) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool, const int32_t *block_tables,

@@ -9,7 +9,9 @@
 //    only the block it diverges in (copy-on-write).
 //  * "What interviewers probe next": a request is admitted when
 //    ceil(prompt / b) blocks plus one to grow into are free, above a small
-//    reserved watermark.
+//    reserved watermark; when the pool runs dry mid-decode a preempted
+//    sequence's blocks are swapped to pinned host memory (feature table,
+//    preemption row: swap at block granularity).
 // auto-20261007-1900-en (lihaoran.work), "How many tail slots remain unused?":
 // a sequence of T tokens holds ceil(T / b) blocks.
 //
@@ -24,9 +26,10 @@
 
 struct pa_bm {
     struct Seq {
-        std::vector<int32_t> blocks;
+        std::vector<int32_t> blocks;   // device blocks, or host slots while swapped out
         int64_t tokens = 0;
         bool live = false;
+        bool swapped = false;
     };
     int64_t num_blocks = 0;
     int32_t block_size = 0;
@@ -34,6 +37,8 @@ struct pa_bm {
     std::vector<int32_t> free_stack;
     std::vector<Seq> seqs;
     std::vector<int32_t> free_seq_ids;
+    int64_t host_blocks = 0;
+    std::vector<int32_t> host_free;   // free host slots, lowest first
 
     bool valid_seq(int32_t s) const { return s >= 0 && (size_t)s < seqs.size() && seqs[s].live; }
     int32_t pop_block() {
@@ -44,6 +49,11 @@ struct pa_bm {
     }
     void release_block(int32_t b) {
         if (--refcount[b] == 0) free_stack.push_back(b);
+    }
+    int32_t pop_host() {
+        const int32_t h = host_free.back();
+        host_free.pop_back();
+        return h;
     }
 };
 
@@ -92,6 +102,7 @@ pa_status pa_bm_append_tokens(pa_bm *bm, int32_t seq, int64_t n, int64_t *slots_
     if (!bm || n < 0) return PA_ERR_INVALID_ARG;
     if (!bm->valid_seq(seq)) return PA_ERR_NOT_FOUND;
     pa_bm::Seq &s = bm->seqs[seq];
+    if (s.swapped) return PA_ERR_SWAPPED;
     const int32_t b = bm->block_size;
     if (n_cow_out) *n_cow_out = 0;
     if (n == 0) return PA_OK;
@@ -123,6 +134,7 @@ pa_status pa_bm_append_tokens(pa_bm *bm, int32_t seq, int64_t n, int64_t *slots_
 pa_status pa_bm_fork(pa_bm *bm, int32_t parent, int32_t *child_out) {
     if (!bm || !child_out) return PA_ERR_INVALID_ARG;
     if (!bm->valid_seq(parent)) return PA_ERR_NOT_FOUND;
+    if (bm->seqs[parent].swapped) return PA_ERR_SWAPPED;
     int32_t child;
     pa_status st = pa_bm_add_seq(bm, &child);
     if (st != PA_OK) return st;
@@ -139,10 +151,14 @@ pa_status pa_bm_free_seq(pa_bm *bm, int32_t seq) {
     if (!bm) return PA_ERR_INVALID_ARG;
     if (!bm->valid_seq(seq)) return PA_ERR_NOT_FOUND;
     pa_bm::Seq &s = bm->seqs[seq];
-    for (int32_t blk : s.blocks) bm->release_block(blk);
+    if (s.swapped)
+        for (int32_t h : s.blocks) bm->host_free.push_back(h);
+    else
+        for (int32_t blk : s.blocks) bm->release_block(blk);
     s.blocks.clear();
     s.tokens = 0;
     s.live = false;
+    s.swapped = false;
     bm->free_seq_ids.push_back(seq);
     return PA_OK;
 }
@@ -152,6 +168,7 @@ pa_status pa_bm_get_table(const pa_bm *bm, int32_t seq, int32_t *table_out, int3
     if (!bm || cap < 0 || (cap > 0 && !table_out)) return PA_ERR_INVALID_ARG;
     if (!bm->valid_seq(seq)) return PA_ERR_NOT_FOUND;
     const pa_bm::Seq &s = bm->seqs[seq];
+    if (s.swapped) return PA_ERR_SWAPPED;
     if ((int64_t)s.blocks.size() > cap && table_out) return PA_ERR_INVALID_ARG;
     for (int32_t i = 0; i < cap; ++i) table_out[i] = (size_t)i < s.blocks.size() ? s.blocks[i] : -1;
     if (num_blocks_out) *num_blocks_out = (int32_t)s.blocks.size();
@@ -171,6 +188,63 @@ pa_status pa_bm_can_admit(const pa_bm *bm, int64_t prompt_tokens, int64_t waterm
     const int64_t need = blocks_for(prompt_tokens, bm->block_size) + 1 + watermark_blocks;
     *admit = (int64_t)bm->free_stack.size() >= need ? 1 : 0;
     return PA_OK;
+}
+
+pa_status pa_bm_set_host_pool(pa_bm *bm, int64_t host_blocks) {
+    if (!bm || host_blocks < 0 || host_blocks > INT32_MAX) return PA_ERR_INVALID_ARG;
+    if ((int64_t)bm->host_free.size() != bm->host_blocks) return PA_ERR_INVALID_ARG;   // slots in use
+    bm->host_blocks = host_blocks;
+    bm->host_free.clear();
+    bm->host_free.reserve((size_t)host_blocks);
+    for (int64_t h = host_blocks - 1; h >= 0; --h) bm->host_free.push_back((int32_t)h);
+    return PA_OK;
+}
+
+pa_status pa_bm_swap_out(pa_bm *bm, int32_t seq, int32_t *pairs_out, int32_t cap, int32_t *n_pairs_out) {
+    if (!bm || !n_pairs_out || cap < 0) return PA_ERR_INVALID_ARG;
+    if (!bm->valid_seq(seq)) return PA_ERR_NOT_FOUND;
+    pa_bm::Seq &s = bm->seqs[seq];
+    if (s.swapped) return PA_ERR_SWAPPED;
+    const size_t n = s.blocks.size();
+    if ((int64_t)n > cap || (n > 0 && !pairs_out)) return PA_ERR_INVALID_ARG;
+    if (bm->host_free.size() < n) return PA_ERR_NO_BLOCKS;
+    for (size_t i = 0; i < n; ++i) {
+        const int32_t dev = s.blocks[i], h = bm->pop_host();
+        pairs_out[2 * i] = dev;
+        pairs_out[2 * i + 1] = h;
+        bm->release_block(dev);
+        s.blocks[i] = h;
+    }
+    s.swapped = true;
+    *n_pairs_out = (int32_t)n;
+    return PA_OK;
+}
+
+pa_status pa_bm_swap_in(pa_bm *bm, int32_t seq, int32_t *pairs_out, int32_t cap, int32_t *n_pairs_out) {
+    if (!bm || !n_pairs_out || cap < 0) return PA_ERR_INVALID_ARG;
+    if (!bm->valid_seq(seq)) return PA_ERR_NOT_FOUND;
+    pa_bm::Seq &s = bm->seqs[seq];
+    if (!s.swapped) return PA_ERR_SWAPPED;
+    const size_t n = s.blocks.size();
+    if ((int64_t)n > cap || (n > 0 && !pairs_out)) return PA_ERR_INVALID_ARG;
+    if (bm->free_stack.size() < n) return PA_ERR_NO_BLOCKS;
+    for (size_t i = 0; i < n; ++i) {
+        const int32_t h = s.blocks[i], dev = bm->pop_block();
+        pairs_out[2 * i] = dev;
+        pairs_out[2 * i + 1] = h;
+        bm->host_free.push_back(h);
+        s.blocks[i] = dev;
+    }
+    s.swapped = false;
+    *n_pairs_out = (int32_t)n;
+    return PA_OK;
+}
+
+int64_t pa_bm_num_free_host(const pa_bm *bm) { return bm ? (int64_t)bm->host_free.size() : -1; }
+
+int32_t pa_bm_is_swapped(const pa_bm *bm, int32_t seq) {
+    if (!bm || !bm->valid_seq(seq)) return -1;
+    return bm->seqs[seq].swapped ? 1 : 0;
 }
 
 }  // extern "C"

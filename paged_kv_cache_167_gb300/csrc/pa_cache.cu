@@ -133,6 +133,45 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyParams p) {
     for (; i < p.half_vecs; i += blockDim.x) d[i] = s[i];
 }
 
+struct SwapParams {
+    uint4 *pool;
+    int64_t num_blocks;
+    int64_t block_stride_v;
+    int64_t kv_stride_v;
+    int64_t half_vecs;           // Hkv * b * d / 8: one K (or V) half of a block
+    uint4 *host;                 // device view of the pinned host buffer [host_blocks][2][half]
+    int64_t host_blocks;
+    const int32_t *pairs;        // [n][2] (device block, host block)
+    int32_t direction;           // PA_SWAP_OUT: pool -> host; PA_SWAP_IN: host -> pool
+    unsigned int *err;
+};
+
+// grid (num_pairs, 2): one CTA per (pair, K/V half).  The host side is read or
+// written directly through its device mapping, over the CPU-GPU link.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(const SwapParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int pair = blockIdx.x, kv = blockIdx.y;
+    const int32_t dev = __ldg(p.pairs + 2 * pair), hb = __ldg(p.pairs + 2 * pair + 1);
+    if (dev < 0 || dev >= p.num_blocks || hb < 0 || hb >= p.host_blocks) {
+        if (kv == 0 && threadIdx.x == 0) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+        return;
+    }
+    uint4 *pool_half = p.pool + dev * p.block_stride_v + kv * p.kv_stride_v;
+    uint4 *host_half = p.host + ((int64_t)hb * 2 + kv) * p.half_vecs;
+    const uint4 *s = p.direction == PA_SWAP_OUT ? pool_half : host_half;
+    uint4 *d = p.direction == PA_SWAP_OUT ? host_half : pool_half;
+    constexpr int kUnroll = 4;
+    int64_t i = threadIdx.x;
+    for (; i + (kUnroll - 1) * blockDim.x < p.half_vecs; i += kUnroll * blockDim.x) {
+        uint4 t[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) t[u] = s[i + u * blockDim.x];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) d[i + u * blockDim.x] = t[u];
+    }
+    for (; i < p.half_vecs; i += blockDim.x) d[i] = s[i];
+}
+
 }  // namespace
 
 unsigned int *device_error_word() {
@@ -231,6 +270,25 @@ cudaError_t launch_copy_blocks(const PoolView &pool, const int32_t *pairs, int32
     p.num_pairs = num_pairs;
     p.err = err;
     return launch_pdl(copy_blocks_kernel, dim3(num_pairs, 2), dim3(256), stream, p);
+}
+
+cudaError_t launch_swap_blocks(const PoolView &pool, void *host_dev, int64_t host_blocks, const int32_t *pairs,
+                               int32_t num_pairs, int32_t direction, cudaStream_t stream) {
+    if (num_pairs == 0) return cudaSuccess;
+    unsigned int *err = device_error_word();
+    if (!err) return cudaErrorUnknown;
+    SwapParams p;
+    p.pool = reinterpret_cast<uint4 *>(const_cast<void *>(pool.base));
+    p.num_blocks = pool.num_blocks;
+    p.block_stride_v = pool.block_stride / 8;
+    p.kv_stride_v = pool.kv_stride / 8;
+    p.half_vecs = (int64_t)pool.num_kv_heads * pool.block_size * pool.head_dim / 8;
+    p.host = static_cast<uint4 *>(host_dev);
+    p.host_blocks = host_blocks;
+    p.pairs = pairs;
+    p.direction = direction;
+    p.err = err;
+    return launch_pdl(swap_blocks_kernel, dim3(num_pairs, 2), dim3(256), stream, p);
 }
 
 }  // namespace pa

@@ -45,6 +45,9 @@ cudaError_t launch_reshape_and_cache(const PoolView &pool, const void *k, const 
                                      const int64_t *slots, int64_t num_tokens, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const PoolView &pool, const int32_t *pairs, int32_t num_pairs,
                                cudaStream_t stream);
+// host_dev: the device address of the pinned host buffer
+cudaError_t launch_swap_blocks(const PoolView &pool, void *host_dev, int64_t host_blocks, const int32_t *pairs,
+                               int32_t num_pairs, int32_t direction, cudaStream_t stream);
 
 // ---- decode (pa_decode_*.cu) -----------------------------------------------
 struct DecodeArgs {

@@ -389,6 +389,45 @@ def pin_copy_blocks(orc):
     assert np.array_equal(a, c)
 
 
+# ---------------------------------------------------------------------------
+# swapping to host memory
+# ---------------------------------------------------------------------------
+
+def pin_swap_blocks(orc):
+    """Swap-out puts in host slot hb exactly the K and V rows of the tokens the
+    test placed in device block blk; swap-in into other device blocks then
+    reads back, through a table pointing at them, what the original table
+    read (library attention on the un-paged tensors)."""
+    rng = np.random.default_rng(31)
+    gen = torch.Generator().manual_seed(31)
+    NB, Hkv, Hq, b, d = 12, 2, 4, 4, 8
+    lens = [11]
+    tables = np.asarray([[7, 2, 9]], np.int32)
+    K, V = randn((1, 12, Hkv, d), gen), randn((1, 12, Hkv, d), gen)
+    pool = bits(place(K, V, lens, tables, NB, b, gen)).copy()
+    geom = oracle_pkg.dense_geom(NB, Hkv, b, d)
+    host = np.zeros((5, 2, Hkv, b, d), np.uint16)
+    out_pairs = np.asarray([[7, 3], [2, 0], [9, 4]], np.int32)
+    orc.swap_blocks(pool, geom, host, out_pairs, 0)
+    for j, (blk, hb) in enumerate(out_pairs):
+        for off in range(b):
+            t = j * b + off
+            if t < lens[0]:
+                assert np.array_equal(host[hb, 0, :, off], bits(K[0, t])), (blk, hb, off)
+                assert np.array_equal(host[hb, 1, :, off], bits(V[0, t])), (blk, hb, off)
+    assert not host[1].any() and not host[2].any()        # unused host slots untouched
+    before = pool.copy()
+    in_pairs = np.asarray([[0, 3], [5, 0], [11, 4]], np.int32)
+    orc.swap_blocks(pool, geom, host, in_pairs, 1)
+    others = [i for i in range(NB) if i not in in_pairs[:, 0]]
+    assert np.array_equal(pool[others], before[others])
+    q = randn((1, Hq, d), gen)
+    got = orc.paged_decode(bits(q), pool, geom, np.asarray([[0, 5, 11]], np.int32), np.asarray(lens, np.int32),
+                           Hq, 0.5)
+    ref = sdpa_rows(q, K[0, :lens[0]], V[0, :lens[0]], 0.5)[0].numpy()
+    assert np.abs(got[0] - ref).max() < 1e-12
+
+
 PINS: Dict[str, Callable] = {name: fn for name, fn in globals().items() if name.startswith("pin_")}
 
 

@@ -151,3 +151,125 @@ def test_unknown_sequence(pa):
     bm.free_seq(s)
     with pytest.raises(pa.PagedAttentionError):
         bm.fork(s)
+
+
+# ---------------------------------------------------------------------------
+# swapping to host slots (how-pagedattention-works, feature table, preemption
+# row; "What interviewers probe next")
+# ---------------------------------------------------------------------------
+
+def test_swap_out_and_in(pa):
+    bm = pa.BlockManager(16, 4)
+    bm.set_host_pool(8)
+    s = bm.add_seq()
+    bm.append_tokens(s, 10)                       # 3 blocks: 0, 1, 2
+    table, tokens = bm.table(s)
+    pairs = bm.swap_out(s)
+    assert pairs[:, 0].tolist() == table.tolist() and pairs[:, 1].tolist() == [0, 1, 2]
+    assert bm.is_swapped(s) and bm.num_free() == 16 and bm.num_free_host() == 5
+    for call in (lambda: bm.append_tokens(s, 1), lambda: bm.table(s), lambda: bm.fork(s), lambda: bm.swap_out(s)):
+        with pytest.raises(pa.PagedAttentionError) as e:
+            call()
+        assert e.value.status == 8                # PA_ERR_SWAPPED
+    other = bm.add_seq()
+    bm.append_tokens(other, 8)                    # reuses two of the released blocks meanwhile
+    back = bm.swap_in(s)
+    assert back[:, 1].tolist() == [0, 1, 2]       # same host slots, in table order
+    t_other, _ = bm.table(other)
+    assert set(back[:, 0].tolist()).isdisjoint(t_other.tolist()) and len(set(back[:, 0].tolist())) == 3
+    table2, tokens2 = bm.table(s)
+    assert tokens2 == tokens and table2.tolist() == back[:, 0].tolist()
+    assert not bm.is_swapped(s) and bm.num_free_host() == 8
+    with pytest.raises(pa.PagedAttentionError) as e:
+        bm.swap_in(s)
+    assert e.value.status == 8
+
+
+def test_swap_keeps_shared_blocks_for_other_tables(pa):
+    orc = oracle.load()
+    bm = pa.BlockManager(16, 4)
+    bm.set_host_pool(4)
+    parent = bm.add_seq()
+    bm.append_tokens(parent, 6)                   # blocks 0, 1 (last partly filled)
+    child = bm.fork(parent)
+    pairs = bm.swap_out(child)
+    assert pairs[:, 0].tolist() == [0, 1]
+    assert bm.refcount(0) == 1 and bm.refcount(1) == 1   # the parent still holds both
+    check_invariants(bm, [parent], orc)
+    bm.swap_in(child)
+    t_child, _ = bm.table(child)
+    assert set(t_child.tolist()).isdisjoint({0, 1})     # private copies now
+    check_invariants(bm, [parent, child], orc)
+    slots, cow = bm.append_tokens(child, 1)
+    assert cow is None                            # nothing shared left to copy
+
+
+def test_swap_capacity_and_release(pa):
+    bm = pa.BlockManager(6, 4)
+    bm.set_host_pool(2)
+    s = bm.add_seq()
+    bm.append_tokens(s, 12)                       # 3 blocks > 2 host slots
+    table, _ = bm.table(s)
+    with pytest.raises(pa.PagedAttentionError) as e:
+        bm.swap_out(s)
+    assert e.value.status == 6 and not bm.is_swapped(s) and bm.table(s)[0].tolist() == table.tolist()
+    bm.set_host_pool(4)
+    bm.swap_out(s)
+    with pytest.raises(pa.PagedAttentionError) as e:
+        bm.set_host_pool(8)                       # slots in use
+    assert e.value.status == 1
+    fillers = [bm.add_seq() for _ in range(2)]
+    for f in fillers:
+        bm.append_tokens(f, 12)                   # 6 device blocks in use: none left
+    with pytest.raises(pa.PagedAttentionError) as e:
+        bm.swap_in(s)
+    assert e.value.status == 6 and bm.is_swapped(s)
+    bm.free_seq(s)                                # a swapped-out sequence releases its host slots
+    assert bm.num_free_host() == 4
+
+
+def test_random_operations_with_swaps(pa):
+    orc = oracle.load()
+    rng = np.random.default_rng(7)
+    bm = pa.BlockManager(96, 8)
+    bm.set_host_pool(64)
+    live, swapped = [], set()
+    for step in range(500):
+        op = rng.choice(["add", "append", "fork", "free", "out", "in"], p=[0.12, 0.4, 0.1, 0.13, 0.12, 0.13])
+        on_device = [s for s in live if s not in swapped]
+        if op == "add" or not live:
+            live.append(bm.add_seq())
+        elif op == "append" and on_device:
+            s = int(rng.choice(on_device))
+            try:
+                bm.append_tokens(s, int(rng.integers(1, 30)))
+            except pa.PagedAttentionError as e:
+                assert e.status == 6
+        elif op == "fork" and on_device:
+            live.append(bm.fork(int(rng.choice(on_device))))
+        elif op == "free":
+            s = int(rng.choice(live))
+            bm.free_seq(s)
+            live.remove(s)
+            swapped.discard(s)
+        elif op == "out" and on_device:
+            s = int(rng.choice(on_device))
+            try:
+                pairs = bm.swap_out(s)
+                swapped.add(s)
+                assert len(set(pairs[:, 1].tolist())) == len(pairs)
+            except pa.PagedAttentionError as e:
+                assert e.status == 6
+        elif op == "in" and swapped:
+            s = int(rng.choice(sorted(swapped)))
+            try:
+                pairs = bm.swap_in(s)
+                swapped.discard(s)
+                assert bm.table(s)[0].tolist() == pairs[:, 0].tolist()
+            except pa.PagedAttentionError as e:
+                assert e.status == 6
+        check_invariants(bm, [s for s in live if s not in swapped], orc)
+        assert all(bm.is_swapped(s) for s in swapped)
+    for s in list(swapped):
+        bm.free_seq(s)
+    assert bm.num_free_host() == 64

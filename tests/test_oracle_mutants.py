@@ -40,6 +40,9 @@ MUTANTS = [
     ("copy_keys_only", "for (int64_t kv = 0; kv < 2; ++kv)", "for (int64_t kv = 0; kv < 1; ++kv)", 1),
     ("copy_reversed", "pool[pool_elem(p, dst, kv, h, off) + i] = pool[pool_elem(p, src, kv, h, off) + i];",
      "pool[pool_elem(p, src, kv, h, off) + i] = pool[pool_elem(p, dst, kv, h, off) + i];", 1),
+    ("swap_host_layout", "(((hb * 2 + half) * H + h) * b + off) * d", "(((hb * H + h) * 2 + half) * b + off) * d", 1),
+    ("swap_direction", "if (direction == 0)", "if (direction != 0)", 1),
+    ("swap_keys_only", "for (int64_t half = 0; half < 2; ++half)", "for (int64_t half = 0; half < 1; ++half)", 1),
 ]
 
 
