@@ -13,29 +13,32 @@
 // Design:
 //  * One CTA per 128-row M-tile of one (sequence, kv-head): row r is query
 //    j0 + r / G of head g*G + r % G, so every K/V tile staged in shared memory
-//    serves the whole query group.  Nine warps: one producer lane issues every
-//    copy and MMA; eight softmax warps in two warpgroups each own 64 of a
-//    row's 128 keys (tensor-memory lanes follow warp % 4).
-//  * TMA (cp.async.bulk.tensor, 128-byte swizzle) brings Q and the K/V tiles:
-//    a K or V tile of 128 keys is 8 blocks x 2 halves of d, one box of
-//    16 rows x 64 dims per (block, half), addressed through a 5-D tensor map of
-//    the pool's (d, slot, head, K|V, block) view.  Blocks past the sequence
-//    end, or with an out-of-range table entry, are fetched from an
-//    out-of-bounds coordinate, which TMA fills with zeros.  No multicast.
+//    serves the whole query group.  Eleven warps: eight softmax warps in two
+//    warpgroups each own 64 of a row's 128 keys (tensor-memory lanes follow
+//    warp % 4); lane 0 of the MMA warp issues every MMA; a K warp and a V warp
+//    issue the tensor copies, one lane per box.
+//  * TMA (cp.async.bulk.tensor, 128-byte swizzle) brings Q and the K/V tiles.
+//    A K tile of 128 keys is 8 blocks x 2 halves of d, one box of 16 rows x
+//    64 dims per (block, half) through a 5-D tensor map of the pool's
+//    (d, slot, head, K|V, block) view, laid out [half][128 keys][128 B] (the
+//    Q.K operand needs a uniform 8-row stride over the tile).  A V tile is one
+//    4 KiB box per block, laid out [block][half][16 keys][128 B] (each 16-key
+//    P.V step is one block).  Blocks past the sequence end, or with an
+//    out-of-range table entry, are fetched from an out-of-bounds coordinate,
+//    which TMA fills with zeros.  No multicast.
 //  * S = Q.K^T and O += P.V are tcgen05.mma kind::f16 (bf16 in, fp32 out)
 //    with M = N = 128, K = 16 per instruction, accumulators in tensor memory
-//    (two S buffers in columns 0..255, O in 256..383), tracked with
-//    tcgen05.commit on mbarriers.  The producer issues Q.K(t+1) into the
-//    other S buffer before P.V(t), so the tensor pipe works on the next tile
-//    while the softmax warps process this one.
+//    (three S buffers in columns 0..383, O in 384..511), tracked with
+//    tcgen05.commit on mbarriers.  Q.K runs two tiles ahead of P.V, so the
+//    tensor pipe works on later tiles while the softmax warps process this
+//    one.
 //  * Softmax: each thread owns half of one row.  It reads S with tcgen05.ld,
-//    applies the scale and the causal mask, agrees with the other half on the
-//    tile maximum through shared memory, keeps a reference maximum in the
-//    log2 domain that only moves when a tile's maximum exceeds it by more
-//    than 8 (so p <= 2^8 and O needs rescaling rarely; the result is exact
-//    because l and O share the reference), writes P as bf16 into one of two
-//    swizzled shared-memory buffers the next MMA reads, and sums the same
-//    rounded values into l.
+//    applies the causal mask, agrees with the other half on the tile maximum
+//    through shared memory, keeps a reference maximum in the log2 domain that
+//    only moves when a tile's maximum exceeds it by more than 8 (so p <= 2^8
+//    and O needs rescaling rarely; the result is exact because l and O share
+//    the reference), writes P as bf16 into one of two swizzled shared-memory
+//    buffers the next MMA reads, and sums the fp32 probabilities into l.
 //  * K and V rings of two stages each; a K slot is refilled once its Q.K MMA
 //    has completed, a V slot once its P.V MMA has.
 //  * Every wait is bounded; on expiry the kernel records PA_DEVERR_TIMEOUT,
@@ -67,7 +70,8 @@ constexpr uint32_t kOffP = kOffV + 2 * kTile; // 2 buffers
 constexpr uint32_t kOffX = kOffP + 2 * kTile; // [2 halves][128 rows] fp32 exchange
 constexpr uint32_t kOffBar = kOffX + 1024;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // + alignment slack
-constexpr uint32_t kTmemCols = 512;         // S0, S1, O (128 columns each)
+constexpr int kSBufs = 3;                   // S accumulators in tensor memory
+constexpr uint32_t kTmemCols = 512;         // S0, S1, S2, O (128 columns each)
 constexpr uint32_t kVBlock = 2u * kBS * 128u; // one block's V box, bytes
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 domain
@@ -212,10 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sP = base + kOffP;
     float *xch = reinterpret_cast<float *>(gbase + kOffX);
     const uint32_t barQ = base + kOffBar;
-    const uint32_t barK = barQ + 8, barV = barQ + 24, barS = barQ + 40, barSfree = barQ + 56, barP = barQ + 72,
-                   barOP = barQ + 88, barEnd = barQ + 104;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 128);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffBar + 132);
+    // barriers: Q | K[2] | V[2] | S[3] | S free[3] | P[2] | P.V done[2] | drain
+    const uint32_t barK = barQ + 8, barV = barQ + 24, barS = barQ + 40, barSfree = barQ + 64, barP = barQ + 88,
+                   barOP = barQ + 104, barEnd = barQ + 120;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 136);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffBar + 140);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
@@ -228,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        const uint32_t counts[14] = {1, 1, 1, 1, 1, 1, 1, 256, 256, 256, 256, 1, 1, 1};
-        for (int i = 0; i < 14; ++i)
+        const uint32_t counts[16] = {1, 1, 1, 1, 1, 1, 1, 1, 256, 256, 256, 256, 256, 1, 1, 1};
+        for (int i = 0; i < 16; ++i)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(barQ + 8 * i), "r"(counts[i]) : "memory");
         *abort_flag = 0;
         fence_barrier_init();
@@ -238,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + 256;
+    const uint32_t tO = tmem + kSBufs * 128;
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -280,8 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (t >= 2) {   // the slot's previous tile has been consumed by its MMA
-                const uint32_t free_bar = (is_k ? barS : barOP) + 8 * st;
-                ok = __all_sync(0xffffffffu, mbar_wait(free_bar, (uint32_t)(((t - 2) >> 1) & 1), p.err));
+                const uint32_t free_bar = is_k ? barS + 8 * ((t - 2) % kSBufs) : barOP + 8 * st;
+                const uint32_t par = is_k ? (uint32_t)(((t - 2) / kSBufs) & 1) : (uint32_t)(((t - 2) >> 1) & 1);
+                ok = __all_sync(0xffffffffu, mbar_wait(free_bar, par, p.err));
                 if (!ok) {
                     *abort_flag = 1;
                     break;
@@ -308,14 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
             auto qk = [&](int t) {
-                const int st = t & 1;
+                const int st = t & 1, sb = t % kSBufs;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    umma(tmem + st * 128, smem_desc(sQ + off, 16, 1024), smem_desc(sK + st * kTile + off, 16, 1024),
+                    umma(tmem + sb * 128, smem_desc(sQ + off, 16, 1024), smem_desc(sK + st * kTile + off, 16, 1024),
                          idesc_qk, kk > 0);
                 }
-                umma_commit(barS + 8 * st);
+                umma_commit(barS + 8 * sb);
             };
             bool ok = true;
             auto wait = [&](uint32_t bar, uint32_t parity) {
@@ -326,17 +332,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return ok;
             };
             int committed_pv = 0;
+            // Q.K runs two tiles ahead of P.V (three S buffers)
             if (wait(barQ, 0) && wait(barK, 0)) {
                 tc_fence_after();
                 qk(0);
+                if (n_tiles > 1 && wait(barK + 8, 0)) {
+                    tc_fence_after();
+                    qk(1);
+                }
             }
             for (int t = 0; t < n_tiles && ok && !*abort_flag; ++t) {
-                const int st = t & 1, st1 = (t + 1) & 1;
-                if (t + 1 < n_tiles) {
-                    if (!wait(barK + 8 * st1, (uint32_t)(((t + 1) >> 1) & 1))) break;
-                    if (t >= 1 && !wait(barSfree + 8 * st1, (uint32_t)(((t - 1) >> 1) & 1))) break;
+                const int st = t & 1;
+                if (t + 2 < n_tiles) {
+                    if (!wait(barK + 8 * st, (uint32_t)(((t + 2) >> 1) & 1))) break;
+                    if (t >= 1 && !wait(barSfree + 8 * ((t - 1) % kSBufs), (uint32_t)(((t - 1) / kSBufs) & 1)))
+                        break;
                     tc_fence_after();
-                    qk(t + 1);
+                    qk(t + 2);
                 }
                 if (!wait(barP + 8 * st, (uint32_t)((t >> 1) & 1))) break;
                 if (!wait(barV + 8 * st, (uint32_t)((t >> 1) & 1))) break;
@@ -373,19 +385,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 l2 = make_float2(0.f, 0.f);
         int done = 0;
         for (int t = 0; t < n_tiles; ++t) {
-            const int st = t & 1;
-            bool ok = mbar_wait(barS + 8 * st, (uint32_t)((t >> 1) & 1), p.err);
+            const int st = t & 1, sb = t % kSBufs;
+            bool ok = mbar_wait(barS + 8 * sb, (uint32_t)((t / kSBufs) & 1), p.err);
             uint32_t sr[2][32];
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
-                tmem_ld32(tmem + st * 128 + lane_off + hf * 64, sr[0]);
-                tmem_ld32(tmem + st * 128 + lane_off + hf * 64 + 32, sr[1]);
+                tmem_ld32(tmem + sb * 128 + lane_off + hf * 64, sr[0]);
+                tmem_ld32(tmem + sb * 128 + lane_off + hf * 64 + 32, sr[1]);
                 tmem_ld_wait();
             } else {
                 ok = false;
             }
             tc_fence_before();
-            mbar_arrive_u32(barSfree + 8 * st);
+            mbar_arrive_u32(barSfree + 8 * sb);
             const int key0 = t * kKeys + hf * 64;
             if (!__all_sync(0xffffffffu, key0 + 63 <= pos)) {   // tile crosses some row's causal edge
 #pragma unroll
