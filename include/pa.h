@@ -239,7 +239,7 @@ pa_status pa_copy_blocks(const pa_kv_pool *pool, const int32_t *pairs, int32_t n
  * 0 .. ctx_lens[s] + j.  The chunk's own K/V must already be in the pool
  * (pa_reshape_and_cache).  QK^T and PV run on the tcgen05 tensor cores with
  * fp32 accumulation in tensor memory.
- * Supported: head_dim 128, block_size 16, group size 1, 2, 4 or 8.
+ * Supported: head_dim 128, block_size 8, 16, 32 or 64, group size 1, 2, 4 or 8.
  */
 pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool,
                            const int32_t *block_tables, int32_t max_blocks_per_seq,

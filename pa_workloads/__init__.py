@@ -219,13 +219,14 @@ def beam_fork(seed: int = SEED_BASE + 4, prompts: int = 32, beams: int = 4) -> W
 
 
 def prefill_chunk(seed: int = SEED_BASE + 4, batch: int = 16, ctx=4096, chunk: int = 512,
-                  num_blocks: int = 8192, num_q_heads: int = 64, num_kv_heads: int = 8) -> Workload:
+                  num_blocks: int = 8192, num_q_heads: int = 64, num_kv_heads: int = 8,
+                  block_size: int = 16) -> Workload:
     """16 sequences, each with `ctx` cached tokens (a number, or one per
     sequence) and a `chunk`-token causal query chunk at positions
     ctx .. ctx+chunk-1 whose K/V are first written by the slot writer;
-    64/8 heads, d=128, b=16, random placement."""
+    64/8 heads, d=128, b=16 unless given, random placement."""
     rng = np.random.default_rng(seed + 1000)
-    b = 16
+    b = block_size
     ctx_lens = np.full(batch, ctx, dtype=np.int32) if np.isscalar(ctx) else np.asarray(ctx, np.int32)
     total = ctx_lens.astype(np.int64) + chunk
     counts = [_blocks_for(int(L), b) for L in total]

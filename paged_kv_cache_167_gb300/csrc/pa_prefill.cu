@@ -46,6 +46,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <type_traits>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -60,7 +62,6 @@ constexpr int kThreads = (kSoftWarps + 3) * 32;
 constexpr int kRows = 128;                  // M tile
 constexpr int kKeys = 128;                  // N tile of Q.K (keys per iteration)
 constexpr int kD = 128;                     // head_dim
-constexpr int kBS = 16;                     // block_size
 constexpr uint32_t kHalf = 128u * 128u;     // one [128 rows][64 bf16] swizzled half tile, bytes
 constexpr uint32_t kTile = 2u * kHalf;      // [2 halves][128 rows][128 B]
 constexpr uint32_t kOffQ = 0;
@@ -72,7 +73,6 @@ constexpr uint32_t kOffBar = kOffX + 1024;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // + alignment slack
 constexpr int kSBufs = 3;                   // S accumulators in tensor memory
 constexpr uint32_t kTmemCols = 512;         // S0, S1, S2, O (128 columns each)
-constexpr uint32_t kVBlock = 2u * kBS * 128u; // one block's V box, bytes
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 domain
 static_assert(kSmemBytes <= 232448, "shared memory");
@@ -205,11 +205,14 @@ __device__ __forceinline__ float max_tree64(const uint32_t (&a)[32], const uint3
 //              O rescale when the reference moved ; signal P(t)
 // Barriers: S ready (MMA commit), S free (256 arrivals), P ready (256 arrivals),
 // P.V done per P buffer (MMA commit), K / V / Q landed (TMA), drain (MMA commit).
-template <int G>
+template <int G, int BS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const Params p) {
     constexpr int QPT = kRows / G;   // queries per M-tile
+    constexpr int NBT = kKeys / BS;  // blocks per 128-key tile
+    constexpr uint32_t kVBlock = 2u * BS * 128u;   // one block's V box: [half][BS keys][128 B]
+    static_assert(BS == 8 || BS == 16 || BS == 32 || BS == 64, "block size");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     unsigned char *gbase = smem_raw + (base - smem_addr(smem_raw));
@@ -253,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctx = ctx < 0 ? 0 : p.max_ctx_len;
     }
     const int seq_end = ctx + p.chunk;                         // keys 0 .. seq_end - 1 exist
-    const int nblk_seq = (seq_end + kBS - 1) / kBS;
+    const int nblk_seq = (seq_end + BS - 1) / BS;
     const int last_q = min(j0 + QPT, p.chunk) - 1;             // last valid query of this tile
     const int n_tiles = (ctx + last_q + 1 + kKeys - 1) / kKeys;
     constexpr uint32_t idesc_qk = idesc_bf16(kRows, kKeys, false);
@@ -276,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (*abort_flag) break;
             const int st = t & 1;
             int id = (int)p.num_blocks;   // out-of-bounds coordinate: zero fill
-            if (lane < kKeys / kBS) {
-                const int bi = t * (kKeys / kBS) + lane;
+            if (lane < NBT) {
+                const int bi = t * NBT + lane;
                 if (bi < nblk_seq) {
                     const int v = __ldg(table_row + bi);
                     if (v < 0 || v >= p.num_blocks) raise_error(p.err, PA_DEVERR_BLOCK_ID);
@@ -298,10 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst = slot0 + st * kTile;
             if (is_k) {
                 const int blk = __shfl_sync(0xffffffffu, id, lane >> 1);
-                if (lane < 2 * (kKeys / kBS))
-                    tma_load_5d(dst + (lane & 1) * kHalf + (lane >> 1) * 2048, &tmap_k, (lane & 1) * 64, 0, g, 0,
+                if (lane < 2 * NBT)
+                    tma_load_5d(dst + (lane & 1) * kHalf + (lane >> 1) * (BS * 128), &tmap_k, (lane & 1) * 64, 0, g, 0,
                                 blk, bar0 + 8 * st);
-            } else if (lane < kKeys / kBS) {
+            } else if (lane < NBT) {
                 tma_load_5d(dst + lane * kVBlock, &tmap_v, 0, 0, 0, g, id, bar0 + 8 * st);
             }
             issued = t + 1;
@@ -354,10 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait(barV + 8 * st, (uint32_t)((t >> 1) & 1))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk) {   // 16 keys = one block's V box
+                for (int kk = 0; kk < kKeys / 16; ++kk) {
+                    // 16 keys of the V tile: within one block for b >= 16 (8-key groups
+                    // 1024 B apart), or two whole blocks for b = 8 (groups one block apart)
                     const uint32_t a_off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    const uint32_t v_off = (uint32_t)(kk * 16 / BS) * kVBlock + (uint32_t)((kk * 16) % BS) * 128u;
                     umma(tO, smem_desc(sP + st * kTile + a_off, 16, 1024),
-                         smem_desc(sV + st * kTile + kk * kVBlock, kVBlock / 2, 1024), idesc_pv,
+                         smem_desc(sV + st * kTile + v_off, BS * 128, BS >= 16 ? 1024 : kVBlock), idesc_pv,
                          (t > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(barOP + 8 * st);
@@ -474,14 +480,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // keys past the sequence end inside its last block: zero their V rows
             // (their p is 0, but the slots may hold non-finite junk)
             const int tile0 = t * kKeys;
-            const int tail_lo = seq_end - tile0, blk_end = ((seq_end + kBS - 1) / kBS) * kBS - tile0;
-            if (tail_lo > 0 && tail_lo < kKeys && (seq_end % kBS) != 0) {
+            const int tail_lo = seq_end - tile0, blk_end = ((seq_end + BS - 1) / BS) * BS - tile0;
+            if (tail_lo > 0 && tail_lo < kKeys && (seq_end % BS) != 0) {
                 mbar_wait(barV + 8 * st, (uint32_t)((t >> 1) & 1), p.err);
                 const int nrows = min(blk_end, kKeys) - tail_lo;
                 for (int idx = tid; idx < nrows * 2 * 8; idx += kSoftWarps * 32) {
                     const int rr = tail_lo + idx / 16, h = (idx / 8) & 1, c16 = idx & 7;
-                    const uint32_t addr = sV + st * kTile + (uint32_t)(rr / kBS) * kVBlock + h * (kVBlock / 2) +
-                                          (uint32_t)(rr % kBS) * 128u + (uint32_t)c16 * 16u;
+                    const uint32_t addr = sV + st * kTile + (uint32_t)(rr / BS) * kVBlock + h * (kVBlock / 2) +
+                                          (uint32_t)(rr % BS) * 128u + (uint32_t)c16 * 16u;
                     asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
                 }
             }
@@ -532,14 +538,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side --------------------------------------------------------------
 
-template <int G>
+template <int G, int BS>
 cudaError_t launch_group(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mkv, const CUtensorMap &mv,
                          const Params &prm, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<G, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
@@ -556,13 +562,14 @@ cudaError_t launch_group(const PrefillArgs &a, const CUtensorMap &mq, const CUte
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<G>, mq, mkv, mv, prm);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<G, BS>, mq, mkv, mv, prm);
 }
 
 }  // namespace prefill
 
 bool prefill_supported(int head_dim, int group, int block_size) {
-    return head_dim == prefill::kD && block_size == prefill::kBS &&
+    return head_dim == prefill::kD &&
+           (block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64) &&
            (group == 1 || group == 2 || group == 4 || group == 8);
 }
 
@@ -590,10 +597,11 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     }
     // pool viewed as (d, slot, kv-head, K|V, block); box 64 x 16 x 1 x 1 x 1
     {
-        cuuint64_t dims[5] = {(cuuint64_t)kD, (cuuint64_t)kBS, (cuuint64_t)Hkv, 2, (cuuint64_t)a.pool.num_blocks};
-        cuuint64_t strides[4] = {(cuuint64_t)kD * 2, (cuuint64_t)kBS * kD * 2, (cuuint64_t)a.pool.kv_stride * 2,
+        const int BS = a.pool.block_size;
+        cuuint64_t dims[5] = {(cuuint64_t)kD, (cuuint64_t)BS, (cuuint64_t)Hkv, 2, (cuuint64_t)a.pool.num_blocks};
+        cuuint64_t strides[4] = {(cuuint64_t)kD * 2, (cuuint64_t)BS * kD * 2, (cuuint64_t)a.pool.kv_stride * 2,
                                  (cuuint64_t)a.pool.block_stride * 2};
-        cuuint32_t box[5] = {64, (cuuint32_t)kBS, 1, 1, 1};
+        cuuint32_t box[5] = {64, (cuuint32_t)BS, 1, 1, 1};
         cuuint32_t estr[5] = {1, 1, 1, 1, 1};
         if (encode(&mkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(a.pool.base), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -613,11 +621,21 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     prm.num_blocks = a.pool.num_blocks;
     prm.scale_log2 = a.scale * kLog2e;
     prm.err = err;
+    auto by_block = [&](auto gtag) -> cudaError_t {
+        constexpr int GG = decltype(gtag)::value;
+        switch (a.pool.block_size) {
+            case 8: return launch_group<GG, 8>(a, mq, mkv, mv, prm, stream);
+            case 16: return launch_group<GG, 16>(a, mq, mkv, mv, prm, stream);
+            case 32: return launch_group<GG, 32>(a, mq, mkv, mv, prm, stream);
+            case 64: return launch_group<GG, 64>(a, mq, mkv, mv, prm, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    };
     switch (G) {
-        case 1: return launch_group<1>(a, mq, mkv, mv, prm, stream);
-        case 2: return launch_group<2>(a, mq, mkv, mv, prm, stream);
-        case 4: return launch_group<4>(a, mq, mkv, mv, prm, stream);
-        case 8: return launch_group<8>(a, mq, mkv, mv, prm, stream);
+        case 1: return by_block(std::integral_constant<int, 1>());
+        case 2: return by_block(std::integral_constant<int, 2>());
+        case 4: return by_block(std::integral_constant<int, 4>());
+        case 8: return by_block(std::integral_constant<int, 8>());
         default: return cudaErrorInvalidValue;
     }
 }

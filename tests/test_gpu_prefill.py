@@ -65,6 +65,22 @@ def test_prefill_small(pa, group, hkv, ctx, chunk):
     assert_close(out, oracle_prefill(c), f"G={group} ctx={ctx} C={chunk}")
 
 
+@pytest.mark.parametrize("bs", [8, 32, 64])
+@pytest.mark.parametrize("group,hkv,ctx,chunk", [
+    (8, 2, [0, 37], 45),
+    (2, 2, [300, 1], 70),
+    (1, 1, [129, 600], 130),
+])
+def test_prefill_block_sizes(pa, bs, group, hkv, ctx, chunk):
+    """Block sizes other than 16: a 128-key tile spans 16, 4 or 2 blocks."""
+    w = wl.prefill_chunk(batch=len(ctx), ctx=ctx, chunk=chunk, num_blocks=256, num_q_heads=group * hkv,
+                         num_kv_heads=hkv, seed=700 + bs + group + chunk, block_size=bs)
+    c = Case(w)
+    out = run_prefill(pa, c, junk_tail=True)
+    assert not torch.isnan(out).any()
+    assert_close(out, oracle_prefill(c), f"b={bs} G={group} ctx={ctx} C={chunk}")
+
+
 def test_prefill_junk_past_sequence_end(pa):
     w = wl.prefill_chunk(batch=2, ctx=[33, 100], chunk=21, num_blocks=64, num_q_heads=16, num_kv_heads=2, seed=77)
     c = Case(w)
