@@ -147,7 +147,7 @@ int32_t pa_decode_partition_tokens(const pa_kv_pool *pool, int32_t num_seqs, int
  * q-head h reads kv-head h / (num_q_heads / Hkv).  All query heads of a KV
  * group are served from one staged copy of each block.  Accumulation is fp32;
  * out is rounded to bf16 (round to nearest even).
- * Supported: head_dim 64 or 128; block_size 4, 8, 16 or 32; group size
+ * Supported: head_dim 64 or 128; block_size 4, 8, 16, 32 or 64; group size
  * num_q_heads / Hkv of 1, 2, 4 or 8.
  */
 pa_status pa_decode(void *out, const void *q, const pa_kv_pool *pool,

@@ -102,12 +102,12 @@ pa_status plan_decode(const PoolView &pool, int32_t num_seqs, int32_t num_q_head
 
 }  // namespace
 
-int decode_stage_tokens(int block_size) { return block_size >= 16 ? block_size : 16; }
+int decode_stage_tokens(int) { return 16; }
 
 bool decode_supported(int head_dim, int group, int block_size) {
     const bool d_ok = head_dim == 64 || head_dim == 128;
     const bool g_ok = group == 1 || group == 2 || group == 4 || group == 8;
-    const bool b_ok = block_size == 4 || block_size == 8 || block_size == 16 || block_size == 32;
+    const bool b_ok = block_size == 4 || block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64;
     return d_ok && g_ok && b_ok;
 }
 

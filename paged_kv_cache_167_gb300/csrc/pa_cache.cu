@@ -200,7 +200,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-cudaError_t encode_pool_block_map(CUtensorMap *map, const PoolView &pool, int kv) {
+cudaError_t encode_pool_block_map(CUtensorMap *map, const PoolView &pool, int kv, int box_rows) {
     auto encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const int D = pool.head_dim, BS = pool.block_size;
@@ -208,7 +208,7 @@ cudaError_t encode_pool_block_map(CUtensorMap *map, const PoolView &pool, int kv
     cuuint64_t dims[5] = {64, (cuuint64_t)BS, (cuuint64_t)(D / 64), (cuuint64_t)pool.num_kv_heads,
                           (cuuint64_t)pool.num_blocks};
     cuuint64_t strides[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)BS * D * 2, (cuuint64_t)pool.block_stride * 2};
-    cuuint32_t box[5] = {64, (cuuint32_t)BS, (cuuint32_t)(D / 64), 1, 1};
+    cuuint32_t box[5] = {64, (cuuint32_t)box_rows, (cuuint32_t)(D / 64), 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     if (encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<char *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -88,19 +88,27 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
+// A pipeline stage is 16 tokens: BPS whole blocks when b < 16, else a 16-row
+// part of one block (one copy box of ROWS slots starting at slot_of(stage)).
 template <int D, int BS>
 struct Shape {
-    static constexpr int TPS = BS >= 16 ? BS : 16;    // tokens per pipeline stage
-    static constexpr int BPS = TPS / BS;              // blocks per stage
-    static constexpr int KS = TPS / 16;               // 16-token MMA steps per stage
+    static constexpr int TPS = 16;                    // tokens per pipeline stage
+    static constexpr int ROWS = BS < 16 ? BS : 16;    // token slots per copy box
+    static constexpr int BPS = TPS / ROWS;            // copy boxes (blocks) per stage
+    static constexpr int KS = 1;                      // 16-token MMA steps per stage
     static constexpr int HALVES = D / 64;             // 128-byte halves of a token row
-    static constexpr int BOX = BS * D * 2;            // bytes of one (block, K|V, head) copy
+    static constexpr int BOX = ROWS * D * 2;          // bytes of one (K|V, head) copy box
     static constexpr int REGION = BOX < 1024 ? 1024 : BOX;   // its place in a slot (swizzle-atom aligned)
     static constexpr int SLOT = BPS * REGION;         // bytes of a stage's K (or V) slot
     static constexpr int NCH = D / 32;                // 16-byte chunks of a K row that one lane reads
     static constexpr int DK = D / 16;                 // Q.K steps over d = P.V tiles of d
     static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(BS == 4 || BS == 8 || BS == 16 || BS == 32, "block size");
+    static_assert(BS == 4 || BS == 8 || BS == 16 || BS == 32 || BS == 64, "block size");
+    // logical block of box ib of the stage starting at token tok0, and the
+    // first slot the box copies (stages start on multiples of 16 tokens when
+    // b >= 16, so a box never leaves its block)
+    static __device__ __forceinline__ int block_of(int tok0, int ib) { return tok0 / BS + (BS < 16 ? ib : 0); }
+    static __device__ __forceinline__ int slot_of(int tok0) { return BS < 16 ? 0 : tok0 % BS; }
 };
 
 // Per-warp ring of NS stage slots, K slots then V slots.  A block's box starts
@@ -203,7 +211,7 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t a) {
 template <int D, int BS>
 __device__ __forceinline__ uint32_t row_off(int j, int hh) {
     using S = Shape<D, BS>;
-    return (uint32_t)((j / BS) * S::REGION + (hh * BS + j % BS) * 128);
+    return (uint32_t)((j / S::ROWS) * S::REGION + (hh * S::ROWS + j % S::ROWS) * 128);
 }
 __device__ __forceinline__ uint32_t chunk_at(uint32_t row, int c) {
     return row + ((((uint32_t)c) ^ ((row >> 7) & 7u)) << 4);
@@ -493,7 +501,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
     __syncwarp();
 
     const int nblk_seq = (L + BS - 1) / BS;
-    const int blk0 = tok_begin / BS;
     const int nstages = (ntok + S::TPS - 1) / S::TPS;
     const int my_stages = nstages > warp ? (nstages - warp + kWarps - 1) / kWarps : 0;
     const int32_t *table_row = p.tables + (size_t)s * p.max_blocks;
@@ -504,7 +511,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
     auto load_ids = [&](int base) -> int {
         const int kb = base + lane;
         const int k = kb / S::BPS, ib = kb % S::BPS;
-        const int logical = blk0 + (warp + k * kWarps) * S::BPS + ib;
+        const int logical = S::block_of(tok_begin + (warp + k * kWarps) * S::TPS, ib);
         int id = 0;
         if (k < my_stages && logical < nblk_seq) {
             id = __ldg(table_row + logical);
@@ -525,8 +532,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
             id_cache = load_ids(kb_base);
         }
         const int slot = k % kStages;
-        const int first_blk = blk0 + (warp + k * kWarps) * S::BPS;
-        const int nvalid = min(S::BPS, nblk_seq - first_blk);
+        const int stok = tok_begin + (warp + k * kWarps) * S::TPS;   // the stage's first token
+        const int nvalid = min(S::BPS, nblk_seq - S::block_of(stok, 0));
+        const int c_slot = S::slot_of(stok);
         int ids[S::BPS];
 #pragma unroll
         for (int ib = 0; ib < S::BPS; ++ib) ids[ib] = __shfl_sync(0xffffffffu, id_cache, k * S::BPS + ib - kb_base);
@@ -536,8 +544,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
 #pragma unroll
             for (int ib = 0; ib < S::BPS; ++ib) {
                 if (ib < nvalid) {
-                    tensor_copy_5d(kslot + ib * S::REGION, &tmk, 0, 0, 0, g, ids[ib], &bar[slot]);
-                    tensor_copy_5d(vslot + ib * S::REGION, &tmv, 0, 0, 0, g, ids[ib], &bar[slot]);
+                    tensor_copy_5d(kslot + ib * S::REGION, &tmk, 0, c_slot, 0, g, ids[ib], &bar[slot]);
+                    tensor_copy_5d(vslot + ib * S::REGION, &tmv, 0, c_slot, 0, g, ids[ib], &bar[slot]);
                 }
             }
         }
@@ -624,7 +632,7 @@ __global__ void __launch_bounds__(G *D / 4) paged_decode_reduce_kernel(const Par
 // Stages of one sequence (one kv-head); lengths validated as in effective_len.
 template <int BS>
 __device__ __forceinline__ int seq_stages(const Params &p, int s, bool report) {
-    constexpr int TPS = BS >= 16 ? BS : 16;
+    constexpr int TPS = 16;
     const int L = effective_len(p, s, BS, report);
     return (L + TPS - 1) / TPS;
 }
@@ -824,7 +832,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
                 int j = 0;
                 while (j + 1 < nseg && sk->seg_lb[j + 1] <= i) ++j;
                 const int s = sk->seg_s[j];
-                const int logical = (sk->seg_kb[j] + i - sk->seg_lb[j]) * S::BPS + ib;
+                const int logical = S::block_of((sk->seg_kb[j] + i - sk->seg_lb[j]) * S::TPS, ib);
                 const int L = effective_len(p, s, BS, false);
                 if (logical < (L + BS - 1) / BS) {
                     id = __ldg(p.tables + (size_t)s * p.max_blocks + logical);
@@ -849,6 +857,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
             int j = 0;
             while (j + 1 < nseg && sk->seg_lb[j + 1] <= i) ++j;
             const int g = sk->seg_g[j];
+            const int c_slot = S::slot_of((sk->seg_kb[j] + i - sk->seg_lb[j]) * S::TPS);
             const int slot = (kq + k) % kSkStages;
             int ids[S::BPS];
 #pragma unroll
@@ -863,8 +872,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
 #pragma unroll
                 for (int ib = 0; ib < S::BPS; ++ib) {
                     if (ids[ib] >= 0) {
-                        tensor_copy_5d(kslot + ib * S::REGION, &tmk, 0, 0, 0, g, ids[ib], &bar[slot]);
-                        tensor_copy_5d(vslot + ib * S::REGION, &tmv, 0, 0, 0, g, ids[ib], &bar[slot]);
+                        tensor_copy_5d(kslot + ib * S::REGION, &tmk, 0, c_slot, 0, g, ids[ib], &bar[slot]);
+                        tensor_copy_5d(vslot + ib * S::REGION, &tmv, 0, c_slot, 0, g, ids[ib], &bar[slot]);
                     }
                 }
             }
@@ -1053,6 +1062,7 @@ cudaError_t launch_group(const CUtensorMap &tmk, const CUtensorMap &tmv, const P
         case 8: return launch_shape<D, G, 8>(tmk, tmv, prm, num_kv_heads, num_seqs, stream_k, stream);
         case 16: return launch_shape<D, G, 16>(tmk, tmv, prm, num_kv_heads, num_seqs, stream_k, stream);
         case 32: return launch_shape<D, G, 32>(tmk, tmv, prm, num_kv_heads, num_seqs, stream_k, stream);
+        case 64: return launch_shape<D, G, 64>(tmk, tmv, prm, num_kv_heads, num_seqs, stream_k, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1062,9 +1072,10 @@ cudaError_t launch_for_dim(const DecodeArgs &a, cudaStream_t stream) {
     unsigned int *err = device_error_word();
     if (!err) return cudaErrorUnknown;
     CUtensorMap tmk, tmv;
-    cudaError_t e = encode_pool_block_map(&tmk, a.pool, 0);
+    const int rows = a.pool.block_size < 16 ? a.pool.block_size : 16;   // slots per copy box
+    cudaError_t e = encode_pool_block_map(&tmk, a.pool, 0, rows);
     if (e != cudaSuccess) return e;
-    e = encode_pool_block_map(&tmv, a.pool, 1);
+    e = encode_pool_block_map(&tmv, a.pool, 1, rows);
     if (e != cudaSuccess) return e;
     Params prm;
     prm.out = static_cast<__nv_bfloat16 *>(a.out);

@@ -35,10 +35,11 @@ int device_sm_count();
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Tensor map of the K (kv = 0) or V (kv = 1) half of a pool layer as (d within
-// a 64-wide half, slot, half of d, kv-head, block): one box is a whole
-// (block, K|V, kv-head) slab, laid out [half][slot][64] with 128-byte swizzle
-// (head_dim 64 or 128).  A block coordinate of num_blocks reads as zeros.
-cudaError_t encode_pool_block_map(CUtensorMap *map, const PoolView &pool, int kv);
+// a 64-wide half, slot, half of d, kv-head, block): one box is `box_rows`
+// slots (the whole block when box_rows = block_size) of one (block, K|V,
+// kv-head) slab, laid out [half][slot][64] with 128-byte swizzle (head_dim 64
+// or 128).  A block coordinate of num_blocks reads as zeros.
+cudaError_t encode_pool_block_map(CUtensorMap *map, const PoolView &pool, int kv, int box_rows);
 
 // ---- slot writer and block copies (pa_cache.cu) ---------------------------
 cudaError_t launch_reshape_and_cache(const PoolView &pool, const void *k, const void *v,

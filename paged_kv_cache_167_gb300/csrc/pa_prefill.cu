@@ -609,7 +609,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
             return cudaErrorInvalidValue;
     }
     CUtensorMap mv;   // V: one box per block (both halves of d)
-    if (encode_pool_block_map(&mv, a.pool, 1) != cudaSuccess) return cudaErrorInvalidValue;
+    if (encode_pool_block_map(&mv, a.pool, 1, a.pool.block_size) != cudaSuccess) return cudaErrorInvalidValue;
     Params prm;
     prm.out = static_cast<__nv_bfloat16 *>(a.out);
     prm.tables = a.tables;

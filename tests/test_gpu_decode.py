@@ -78,7 +78,7 @@ SWEEP_LENS = [1, 3, 16, 17, 63, 64, 65, 200, 331]
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
-@pytest.mark.parametrize("bs", [4, 8, 16, 32])
+@pytest.mark.parametrize("bs", [4, 8, 16, 32, 64])
 def test_shape_sweep(pa, d, group, bs):
     hkv = 2
     w = wl.custom(SWEEP_LENS, hkv * group, hkv, d, bs, seed=1000 + d + group * 10 + bs)
