@@ -353,6 +353,44 @@ pa_status pa_bm_swap_in(pa_bm *bm, int32_t seq, int32_t *pairs_out, int32_t cap,
 int64_t pa_bm_num_free_host(const pa_bm *bm);
 int32_t pa_bm_is_swapped(const pa_bm *bm, int32_t seq);
 
+/* ---------------------------------------------------------------------------
+ * Capacity of a KV budget, contiguous reservation against paging.
+ * [P1] "A strong answer": the worked Llama 3.1 70B arithmetic (a contiguous
+ * allocator reserves max_seq_len tokens a request; with b-token blocks a
+ * request holds ceil(L/b) blocks, so 850 tokens take 54 blocks of 16) and the
+ * shared-system-prompt paragraph (the prefix's blocks are stored once and
+ * every table points at them).  [P3] "How many tail slots remain unused?":
+ * ceil(T/b)*b - T idle slots per sequence.  Host arithmetic, O(n_lens).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int64_t contiguous_requests;   /* floor(budget / (max_seq_len * bytes_per_token))           */
+    int64_t paged_requests;        /* requests admitted from lens[] in turn (see below)          */
+    double contiguous_waste;       /* 1 - sum(L) / (n * max_seq_len): unused share of reservations */
+    double paged_waste;            /* 1 - sum(L) / sum(ceil(L/b) * b), nothing shared            */
+    double mean_tail_slots;        /* mean of ceil(L/b) * b - L                                   */
+    double prefix_bytes_contiguous;/* n * prefix * bytes_per_token: a copy per request            */
+    double prefix_bytes_paged;     /* (floor(prefix/b) * b + n * (prefix mod b)) * bytes_per_token */
+} pa_capacity;
+
+/*
+ * lens[0..n_lens) are request lengths in tokens (each a copy of the same
+ * shared_prefix_tokens-token prompt prefix followed by its own tokens, so
+ * shared_prefix_tokens <= L <= max_seq_len; 0 = no shared prefix).  Paged
+ * admission stores the prefix's floor(prefix/b) whole blocks once (a partial
+ * last prefix block stays private: the request's first own token goes there),
+ * then takes requests from lens[] in turn, cycling, each holding
+ * ceil(L/b) - floor(prefix/b) blocks of b * bytes_per_token bytes, and stops at
+ * the first one that does not fit in floor(budget / (b * bytes_per_token))
+ * blocks.  Returns PA_ERR_INVALID_ARG for NULL pointers, n_lens <= 0,
+ * block_size, max_seq_len or bytes_per_token <= 0, a negative budget or
+ * prefix, a length outside [prefix, max_seq_len], a list whose requests hold
+ * no private block at all, or a product that overflows int64; *out is then
+ * unspecified.
+ */
+pa_status pa_capacity_estimate(const int64_t *lens, int64_t n_lens, int64_t shared_prefix_tokens,
+                               int32_t block_size, int64_t max_seq_len, int64_t bytes_per_token,
+                               int64_t budget_bytes, pa_capacity *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -103,6 +103,7 @@ class Oracle:
             "orc_reshape_and_cache": (None, [P, G, P, P, P, I64]),
             "orc_copy_blocks": (None, [P, G, P, I64]),
             "orc_swap_blocks": (None, [P, G, P, P, I64, I32]),
+            "orc_capacity": (I32, [P, I64, I64, I64, I64, I64, I64, P]),
             "orc_paged_decode_rows": (None, [P, P, P, G, P, I64, P, I64, D, P, I64]),
             "orc_paged_decode": (None, [P, P, P, G, P, I64, P, I64, I64, D]),
             "orc_prefill_rows": (None, [P, P, P, G, P, I64, P, I64, I64, D, P, I64]),
@@ -164,6 +165,24 @@ class Oracle:
         pairs = _i32(pairs).reshape(-1, 2)
         self._lib.orc_swap_blocks(_ptr(pool), ctypes.byref(geom), _ptr(host), _ptr(pairs), pairs.shape[0],
                                   int(direction))
+
+    # -- capacity ---------------------------------------------------------------
+    def capacity(self, lens, shared_prefix_tokens: int, block_size: int, max_seq_len: int,
+                 bytes_per_token: int, budget_bytes: int) -> dict:
+        """Contiguous against paged capacity of a KV budget for the length mix
+        ``lens`` (requests taken from it in turn); see ``orc_capacity``."""
+        lens = np.ascontiguousarray(lens, dtype=np.int64)
+        out = np.zeros(7, np.float64)
+        rc = self._lib.orc_capacity(_ptr(lens), len(lens), int(shared_prefix_tokens), int(block_size),
+                                    int(max_seq_len), int(bytes_per_token), int(budget_bytes), _ptr(out))
+        if rc != 0:
+            raise ValueError("invalid capacity arguments")
+        keys = ("contiguous_requests", "paged_requests", "contiguous_waste", "paged_waste", "mean_tail_slots",
+                "prefix_bytes_contiguous", "prefix_bytes_paged")
+        res = dict(zip(keys, out.tolist()))
+        res["contiguous_requests"] = int(res["contiguous_requests"])
+        res["paged_requests"] = int(res["paged_requests"])
+        return res
 
     # -- attention -------------------------------------------------------------
     def paged_decode(self, q: np.ndarray, pool: np.ndarray, geom: PoolGeom, tables, seq_lens,

@@ -312,3 +312,83 @@ void orc_prefill(double *out, const uint16_t *q, const uint16_t *pool, const orc
                            h / group, scale);
             }
 }
+
+/* Capacity of a KV budget (how-pagedattention-works, "A strong answer": the
+ * worked Llama 3.1 70B example and the shared-system-prompt paragraph;
+ * auto-20261007-1900-en, "How many tail slots remain unused?").  Every
+ * quantity is obtained by simulating the two allocators request by request
+ * and token by token, not from a closed form.
+ *   contiguous: each admitted request reserves max_len token slots up front;
+ *     requests are admitted while the next reservation still fits the budget.
+ *   paged: the shared prefix's whole blocks are allocated once; then requests
+ *     are taken from lens[] in turn, cycling, and each one's tokens past those
+ *     shared blocks are placed slot by slot, a fresh block opening whenever a
+ *     token lands at offset 0; the first request whose blocks do not all fit
+ *     is returned and admission stops.
+ * out[0] contiguous requests, out[1] paged requests, out[2] the unused share
+ * of the contiguous reservations of lens[] (one request each), out[3] the
+ * unused share of the blocks those requests hold when nothing is shared,
+ * out[4] mean unused tail slots per request, out[5] bytes the prefix takes
+ * when every request keeps its own copy, out[6] bytes it takes when its whole
+ * blocks are shared (a partial last prefix block stays per request).
+ * Returns -1 on invalid input (as the library call's argument rules). */
+int orc_capacity(const int64_t *lens, int64_t n, int64_t prefix, int64_t b, int64_t max_len,
+                 int64_t bytes_per_token, int64_t budget, double *out)
+{
+    if (n <= 0 || b <= 0 || max_len <= 0 || bytes_per_token <= 0 || budget < 0 || prefix < 0)
+        return -1;
+    int64_t private_total = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (lens[i] < prefix || lens[i] > max_len) return -1;
+        private_total += lens[i] - (prefix / b) * b;
+    }
+    if (private_total == 0) return -1;
+
+    /* contiguous allocator */
+    int64_t reserved = 0, contiguous = 0;
+    while (reserved + max_len * bytes_per_token <= budget) {
+        reserved += max_len * bytes_per_token;
+        contiguous += 1;
+    }
+
+    /* per-request slot accounting without sharing */
+    double used = 0.0, reserved_slots = 0.0, held_slots = 0.0, tail = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t slots = 0;
+        for (int64_t t = 0; t < lens[i]; ++t)
+            if (t % b == 0) slots += b;
+        used += (double)lens[i];
+        reserved_slots += (double)max_len;
+        held_slots += (double)slots;
+        tail += (double)(slots - lens[i]);
+    }
+
+    /* paged allocator with the prefix's whole blocks shared */
+    int64_t free_blocks = budget / (b * bytes_per_token);
+    int64_t shared = prefix / b, paged = 0;
+    if (free_blocks >= shared) {
+        free_blocks -= shared;
+        for (int64_t r = 0;; ++r) {
+            const int64_t len = lens[r % n];
+            int64_t opened = 0, ok = 1;
+            for (int64_t t = shared * b; t < len; ++t) {
+                if (t % b == 0) {
+                    if (free_blocks == 0) { ok = 0; break; }
+                    free_blocks -= 1;
+                    opened += 1;
+                }
+            }
+            if (!ok) { free_blocks += opened; break; }
+            paged += 1;
+        }
+    }
+
+    out[0] = (double)contiguous;
+    out[1] = (double)paged;
+    out[2] = 1.0 - used / reserved_slots;
+    out[3] = 1.0 - used / held_slots;
+    out[4] = tail / (double)n;
+    out[5] = (double)n * (double)prefix * (double)bytes_per_token;
+    out[6] = ((double)shared * (double)b + (double)n * (double)(prefix - shared * b)) * (double)bytes_per_token;
+    return 0;
+}

@@ -30,6 +30,14 @@ _P, _I64, _I32, _U32, _F, _SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
                                   ctypes.c_float, ctypes.c_size_t)
 
 
+class PaCapacity(ctypes.Structure):
+    """``pa_capacity``: contiguous against paged capacity of a KV budget."""
+    _fields_ = [("contiguous_requests", ctypes.c_int64), ("paged_requests", ctypes.c_int64),
+                ("contiguous_waste", ctypes.c_double), ("paged_waste", ctypes.c_double),
+                ("mean_tail_slots", ctypes.c_double), ("prefix_bytes_contiguous", ctypes.c_double),
+                ("prefix_bytes_paged", ctypes.c_double)]
+
+
 class PaKvPool(ctypes.Structure):
     """``pa_kv_pool``: one layer's view of the block pool (strides in elements)."""
     _fields_ = [("base", ctypes.c_void_p), ("num_blocks", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
@@ -67,6 +75,7 @@ SIGNATURES = {
     "pa_bm_swap_in": (_I32, [_P, _I32, _P, _I32, ctypes.POINTER(_I32)]),
     "pa_bm_num_free_host": (_I64, [_P]),
     "pa_bm_is_swapped": (_I32, [_P, _I32]),
+    "pa_capacity_estimate": (_I32, [_P, _I64, _I64, _I32, _I64, _I64, _I64, ctypes.POINTER(PaCapacity)]),
 }
 
 
@@ -286,3 +295,15 @@ def slot_mapping(tables: np.ndarray, seq_idx: Sequence[int], positions: Sequence
                                  tables.shape[1], seq_idx.ctypes.data_as(_P), positions.ctypes.data_as(_P),
                                  len(positions), block_size, num_blocks), "pa_slot_mapping")
     return out
+
+
+def capacity_estimate(lens: Sequence[int], shared_prefix_tokens: int, block_size: int, max_seq_len: int,
+                      bytes_per_token: int, budget_bytes: int) -> dict:
+    """Contiguous against paged capacity of a KV budget for the length mix
+    ``lens`` (``pa_capacity_estimate``), as a dict of the struct's fields."""
+    lens = np.ascontiguousarray(lens, dtype=np.int64)
+    out = PaCapacity()
+    _check(lib().pa_capacity_estimate(lens.ctypes.data_as(_P), len(lens), shared_prefix_tokens, block_size,
+                                      max_seq_len, bytes_per_token, budget_bytes, ctypes.byref(out)),
+           "pa_capacity_estimate")
+    return {name: getattr(out, name) for name, _ in PaCapacity._fields_}

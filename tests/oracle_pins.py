@@ -428,6 +428,90 @@ def pin_swap_blocks(orc):
     assert np.abs(got[0] - ref).max() < 1e-12
 
 
+# ---------------------------------------------------------------------------
+# capacity of a KV budget, contiguous against paged
+# ---------------------------------------------------------------------------
+
+def pin_capacity_worked_example(orc):
+    """The page's Llama 3.1 70B arithmetic: 328 KB a token, 8,192-token
+    reservations, an 850-token chat request, 16-token blocks, 435 GB."""
+    g = golden("capacity_worked_example.json")
+    i, pr = g["inputs"], g["printed"]
+    bpt, L, b = i["bytes_per_token"], i["request_tokens"], i["block_size"]
+    c = orc.capacity([L], 0, b, i["max_seq_len"], bpt, i["budget_bytes"])
+    assert round(i["max_seq_len"] * bpt / 1e9, 2) == pr["contiguous_reservation_gb"]
+    assert round(L * bpt / 1e9, 2) == pr["used_gb"]
+    assert round((i["max_seq_len"] - L) * bpt / 1e9, 2) == pr["waste_gb"]
+    assert c["contiguous_requests"] == pr["contiguous_requests"], c
+    assert round(c["contiguous_waste"], 2) == pr["waste_fraction"], c
+    assert (L + c["mean_tail_slots"]) / b == pr["blocks_per_request"], c
+    assert round(b * bpt / 1e6, 1) == pr["block_mb"]
+    assert abs(c["paged_requests"] - pr["paged_requests_about"]) <= pr["paged_requests_rel_tol"] * \
+        pr["paged_requests_about"], c
+    assert round(c["paged_requests"] / c["contiguous_requests"]) == pr["gain_about"], c
+
+
+def pin_capacity_shared_prefix(orc):
+    """A 2,000-token system prompt at 328 KB a token is 656 MB; 200
+    conversations hold 131 GB of it when each keeps a copy, 656 MB when its
+    blocks are shared.  Shared whole blocks also raise the paged concurrency
+    to what the private blocks alone allow."""
+    g = golden("capacity_worked_example.json")
+    sp, bpt = g["shared_prefix"], g["inputs"]["bytes_per_token"]
+    P, n, b = sp["prefix_tokens"], sp["conversations"], 16
+    lens = [P + 850] * n
+    c = orc.capacity(lens, P, b, 8192, bpt, 435 * 10**9)
+    assert round(P * bpt / 1e6) == sp["prefix_mb"]
+    assert round(c["prefix_bytes_contiguous"] / 1e9) == sp["contiguous_duplicate_gb"], c
+    assert round(c["prefix_bytes_paged"] / 1e6) == sp["paged_mb"], c
+    total = (435 * 10**9) // (b * bpt)
+    assert c["paged_requests"] == (total - P // b) // -(-(P + 850 - (P // b) * b) // b), c
+    # a prefix that ends inside a block: that block stays private to each request
+    c2 = orc.capacity([P + 10 + 850] * n, P + 10, b, 8192, bpt, 435 * 10**9)
+    assert c2["prefix_bytes_paged"] == ((P // b) * b + n * 10) * bpt, c2
+
+
+def pin_capacity_small_by_hand(orc):
+    """lens (3, 10), b = 4, 12-token reservations, 1 byte a token, 20 bytes:
+    one reservation fits; five blocks serve 3 (1 block), 10 (3 blocks), 3 (1
+    block), and the next 10 finds none.  Held slots 4 + 12 for 13 tokens."""
+    c = orc.capacity([3, 10], 0, 4, 12, 1, 20)
+    assert c["contiguous_requests"] == 1 and c["paged_requests"] == 3, c
+    assert abs(c["contiguous_waste"] - (1 - 13 / 24)) < 1e-15, c
+    assert abs(c["paged_waste"] - (1 - 13 / 16)) < 1e-15, c
+    assert c["mean_tail_slots"] == 1.5, c
+    # budgets that are exact multiples admit the last reservation / block
+    assert orc.capacity([12], 0, 4, 12, 1, 24)["contiguous_requests"] == 2
+    assert orc.capacity([12], 0, 4, 12, 1, 24)["paged_requests"] == 2
+    assert orc.capacity([12], 0, 4, 12, 1, 23)["contiguous_requests"] == 1
+    assert orc.capacity([12], 0, 4, 12, 1, 11)["paged_requests"] == 0
+    # zero-token requests hold nothing; the tail bound of the block layout holds per request
+    c = orc.capacity([0, 5], 0, 4, 12, 1, 8)
+    assert c["paged_requests"] == 3 and c["mean_tail_slots"] == 1.5, c
+    for bad in (([], 0), ([5], 6), ([13], 0), ([0], 0)):
+        try:
+            orc.capacity(bad[0], bad[1], 4, 12, 1, 20)
+        except ValueError:
+            continue
+        raise AssertionError(f"capacity accepted {bad}")
+
+
+def pin_capacity_chat_mix(orc):
+    """Chats averaging about 500 tokens under a 4,096-token maximum leave
+    80-95% of max-length reservations unused; with 16-token pages only tail
+    slots are lost, under 5%."""
+    g = golden("capacity_worked_example.json")["chat_mix"]
+    rng = np.random.default_rng(500)
+    lens = np.clip(np.rint(rng.lognormal(np.log(420), 0.6, 4000)), 1, g["max_context"]).astype(np.int64)
+    assert abs(lens.mean() - g["mean_tokens_about"]) < 50
+    c = orc.capacity(lens, 0, 16, g["max_context"], 328000, 435 * 10**9)
+    lo, hi = g["reserved_unused_range"]
+    assert lo <= c["contiguous_waste"] <= hi, c
+    assert c["paged_waste"] < g["paged_waste_below"], c
+    assert abs(c["mean_tail_slots"] - 7.5) < 0.5, c            # uniform tails average (b - 1) / 2
+    assert c["paged_requests"] > 5 * c["contiguous_requests"], c
+
+
 PINS: Dict[str, Callable] = {name: fn for name, fn in globals().items() if name.startswith("pin_")}
 
 

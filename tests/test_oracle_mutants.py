@@ -43,6 +43,14 @@ MUTANTS = [
     ("swap_host_layout", "(((hb * 2 + half) * H + h) * b + off) * d", "(((hb * H + h) * 2 + half) * b + off) * d", 1),
     ("swap_direction", "if (direction == 0)", "if (direction != 0)", 1),
     ("swap_keys_only", "for (int64_t half = 0; half < 2; ++half)", "for (int64_t half = 0; half < 1; ++half)", 1),
+    ("capacity_prefix_unshared", "int64_t shared = prefix / b, paged = 0;", "int64_t shared = 0, paged = 0;", 1),
+    ("capacity_waste_inverted", "out[2] = 1.0 - used / reserved_slots;", "out[2] = used / reserved_slots;", 1),
+    ("capacity_reserve_used", "reserved_slots += (double)max_len;", "reserved_slots += (double)lens[i];", 1),
+    ("capacity_strict_budget", "reserved + max_len * bytes_per_token <= budget",
+     "reserved + max_len * bytes_per_token < budget", 1),
+    ("capacity_tail_from_remainder", "tail += (double)(slots - lens[i]);", "tail += (double)(b - lens[i] % b);", 1),
+    ("capacity_budget_rounded_up", "int64_t free_blocks = budget / (b * bytes_per_token);",
+     "int64_t free_blocks = (budget + b * bytes_per_token - 1) / (b * bytes_per_token);", 1),
 ]
 
 
