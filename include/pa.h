@@ -353,6 +353,57 @@ pa_status pa_bm_swap_in(pa_bm *bm, int32_t seq, int32_t *pairs_out, int32_t cap,
 int64_t pa_bm_num_free_host(const pa_bm *bm);
 int32_t pa_bm_is_swapped(const pa_bm *bm, int32_t seq);
 
+/*
+ * Prefix cache ([P1] shared-system-prompt paragraph: a prefix many requests
+ * share is stored once and every table points at its blocks; [P3] "Shared
+ * prefixes need matching computation": a block's K/V depend on all the tokens
+ * before it and on the conditions of the computation, so equal tokens after a
+ * different context, or under another model, do not match).
+ * The manager keeps an index of full blocks keyed by (the entry before it, a
+ * caller-given 64-bit condition key -- model, adapter, anything else the K/V
+ * depend on --, the block's b token ids), compared exactly (the chained hash
+ * of the token ids only picks the bucket).  The index holds one reference on
+ * every cached block.  Blocks that only the index holds are evictable: an
+ * allocation that finds the free list empty, or pa_bm_prefix_evict, drops the
+ * least recently used such entry together with every entry after it in its
+ * chain, and blocks left unreferenced return to the free list.  Blocks
+ * available to appends, swap-ins and pa_bm_can_admit are the free ones plus
+ * the evictable ones; pa_bm_num_free counts free ones only.
+ *
+ * pa_bm_prefix_match: tokens (int32 ids) of the whole blocks at the head of
+ * tokens[0..n_tokens) that are cached under condition (a multiple of b).
+ * Changes nothing.
+ * pa_bm_add_seq_cached: a new sequence whose table starts with those cached
+ * blocks (reference + 1 each) and whose length is the matched token count,
+ * written to *matched_tokens_out; the caller appends and computes the rest.
+ * Pass fewer tokens than the prompt to keep some of it to compute.
+ * pa_bm_cache_seq: publishes the first floor(n_tokens/b) blocks of seq, whose
+ * token ids are tokens[0..n_tokens) (n_tokens <= its length), after their K/V
+ * were written.  Blocks whose (context, tokens) are already cached keep the
+ * existing entry; the chain continues from it.  Publishing stops at a block the
+ * index already holds under other content.  *inserted_out (may be NULL) is the
+ * number of new entries.  Matching and publishing count as uses for the
+ * least-recently-used order, deeper blocks older than the ones before them.
+ * pa_bm_prefix_evict evicts until n_blocks blocks are free or nothing is
+ * evictable; *freed_out (may be NULL) is the number freed.
+ * pa_bm_prefix_stats: cumulative matched and offered tokens of
+ * pa_bm_add_seq_cached.
+ * Errors: PA_ERR_INVALID_ARG for NULL or negative arguments or n_tokens past
+ * the sequence's length, PA_ERR_NOT_FOUND / PA_ERR_SWAPPED as for the other
+ * sequence calls.
+ */
+pa_status pa_bm_prefix_match(const pa_bm *bm, const int32_t *tokens, int64_t n_tokens, uint64_t condition,
+                             int64_t *matched_tokens_out);
+pa_status pa_bm_add_seq_cached(pa_bm *bm, const int32_t *tokens, int64_t n_tokens, uint64_t condition,
+                               int32_t *seq_out, int64_t *matched_tokens_out);
+pa_status pa_bm_cache_seq(pa_bm *bm, int32_t seq, const int32_t *tokens, int64_t n_tokens, uint64_t condition,
+                          int64_t *inserted_out);
+pa_status pa_bm_prefix_evict(pa_bm *bm, int64_t n_blocks, int64_t *freed_out);
+/* Cached entries, evictable entries (-1 for a NULL manager). */
+int64_t pa_bm_num_cached(const pa_bm *bm);
+int64_t pa_bm_num_evictable(const pa_bm *bm);
+pa_status pa_bm_prefix_stats(const pa_bm *bm, int64_t *hit_tokens_out, int64_t *query_tokens_out);
+
 /* ---------------------------------------------------------------------------
  * Capacity of a KV budget, contiguous reservation against paging.
  * [P1] "A strong answer": the worked Llama 3.1 70B arithmetic (a contiguous

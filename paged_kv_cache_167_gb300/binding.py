@@ -75,6 +75,13 @@ SIGNATURES = {
     "pa_bm_swap_in": (_I32, [_P, _I32, _P, _I32, ctypes.POINTER(_I32)]),
     "pa_bm_num_free_host": (_I64, [_P]),
     "pa_bm_is_swapped": (_I32, [_P, _I32]),
+    "pa_bm_prefix_match": (_I32, [_P, _P, _I64, ctypes.c_uint64, ctypes.POINTER(_I64)]),
+    "pa_bm_add_seq_cached": (_I32, [_P, _P, _I64, ctypes.c_uint64, ctypes.POINTER(_I32), ctypes.POINTER(_I64)]),
+    "pa_bm_cache_seq": (_I32, [_P, _I32, _P, _I64, ctypes.c_uint64, ctypes.POINTER(_I64)]),
+    "pa_bm_prefix_evict": (_I32, [_P, _I64, ctypes.POINTER(_I64)]),
+    "pa_bm_num_cached": (_I64, [_P]),
+    "pa_bm_num_evictable": (_I64, [_P]),
+    "pa_bm_prefix_stats": (_I32, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "pa_capacity_estimate": (_I32, [_P, _I64, _I64, _I32, _I64, _I64, _I64, ctypes.POINTER(PaCapacity)]),
 }
 

@@ -1,7 +1,8 @@
 """Python handle on the host block manager (``pa_bm_*`` in ``include/pa.h``).
 
-Marshalling only; the free list, reference counts, forks and copy-on-write
-planning live in ``csrc/pa_block_manager.cpp``.
+Marshalling only; the free list, reference counts, forks, copy-on-write
+planning, swapping and the prefix-cache index live in
+``csrc/pa_block_manager.cpp``.
 """
 from __future__ import annotations
 
@@ -110,6 +111,51 @@ class BlockManager:
         if r < 0:
             raise PagedAttentionError(7, "pa_bm_is_swapped")
         return r == 1
+
+    # ---- prefix cache (see pa_bm_prefix_match .. pa_bm_prefix_stats)
+
+    @staticmethod
+    def _tokens(tokens) -> np.ndarray:
+        return np.ascontiguousarray(tokens, dtype=np.int32)
+
+    def prefix_match(self, tokens, condition: int = 0) -> int:
+        """Tokens of the cached whole blocks at the head of ``tokens``."""
+        t, m = self._tokens(tokens), _I64()
+        _check(lib().pa_bm_prefix_match(self._h, t.ctypes.data_as(ctypes.c_void_p), len(t), condition,
+                                        ctypes.byref(m)), "pa_bm_prefix_match")
+        return m.value
+
+    def add_seq_cached(self, tokens, condition: int = 0) -> Tuple[int, int]:
+        """New sequence starting with the cached blocks of ``tokens``' head;
+        returns (sequence id, matched tokens)."""
+        t, sid, m = self._tokens(tokens), _I32(), _I64()
+        _check(lib().pa_bm_add_seq_cached(self._h, t.ctypes.data_as(ctypes.c_void_p), len(t), condition,
+                                          ctypes.byref(sid), ctypes.byref(m)), "pa_bm_add_seq_cached")
+        return sid.value, m.value
+
+    def cache_seq(self, seq: int, tokens, condition: int = 0) -> int:
+        """Publishes seq's whole blocks holding ``tokens``; returns new entries."""
+        t, n = self._tokens(tokens), _I64()
+        _check(lib().pa_bm_cache_seq(self._h, seq, t.ctypes.data_as(ctypes.c_void_p), len(t), condition,
+                                     ctypes.byref(n)), "pa_bm_cache_seq")
+        return n.value
+
+    def prefix_evict(self, n_blocks: int) -> int:
+        freed = _I64()
+        _check(lib().pa_bm_prefix_evict(self._h, n_blocks, ctypes.byref(freed)), "pa_bm_prefix_evict")
+        return freed.value
+
+    def num_cached(self) -> int:
+        return int(lib().pa_bm_num_cached(self._h))
+
+    def num_evictable(self) -> int:
+        return int(lib().pa_bm_num_evictable(self._h))
+
+    def prefix_stats(self) -> Tuple[int, int]:
+        """(matched tokens, offered tokens) over all add_seq_cached calls."""
+        hit, query = _I64(), _I64()
+        _check(lib().pa_bm_prefix_stats(self._h, ctypes.byref(hit), ctypes.byref(query)), "pa_bm_prefix_stats")
+        return hit.value, query.value
 
 
 __all__ = ["BlockManager", "PagedAttentionError"]

@@ -14,8 +14,14 @@ each compares it with something else --
 * invariants the pages state (output independent of physical placement; shared
   prefix blocks equal private copies; C=1 prefill equals decode).
 
-Run as ``python -m tests.oracle_pins --library PATH`` to print a JSON list of
-the pins that fail for the oracle built at PATH (exit status 1 if any fail).
+The ``pin_prefix_*`` pins hold the prefix-cache reference model
+(``oracle/prefix_cache.py``, the class in ``prefix_model``) to the pages'
+shared-prompt example, to the rule that a block matches only after an equal
+context, to brute-force longest-prefix search and to hand-worked eviction.
+
+Run as ``python -m tests.oracle_pins --library PATH [--prefix-model FILE]`` to
+print a JSON list of the pins that fail for the oracle built at PATH and the
+prefix-cache model in FILE (exit status 1 if any fail).
 """
 from __future__ import annotations
 
@@ -36,6 +42,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 import oracle as oracle_pkg  # noqa: E402
+from oracle import prefix_cache as prefix_model  # noqa: E402
 
 BF16 = torch.bfloat16
 
@@ -512,6 +519,150 @@ def pin_capacity_chat_mix(orc):
     assert c["paged_requests"] > 5 * c["contiguous_requests"], c
 
 
+# ---------------------------------------------------------------------------
+# prefix-cache reference model
+# ---------------------------------------------------------------------------
+
+def pin_prefix_shared_system_prompt(orc):
+    """how-pagedattention-works, shared-system-prompt paragraph: a 2,000-token
+    prompt shared by 200 conversations is one set of 125 blocks that every
+    table points at, each block counting 200 tables plus the cache."""
+    g = golden("capacity_worked_example.json")["shared_prefix"]
+    P, n, b = g["prefix_tokens"], g["conversations"], 16
+    m = prefix_model.PrefixCacheModel(12000, b)
+    rng = np.random.default_rng(2000)
+    prompt = rng.integers(0, 32000, P).tolist()
+    s0, hit = m.add_seq_cached(prompt)
+    assert hit == 0
+    m.append(s0, P)
+    assert m.cache_seq(s0, prompt) == P // b
+    seqs = [s0]
+    for _ in range(n - 1):
+        own = rng.integers(0, 32000, 850).tolist()
+        s, hit = m.add_seq_cached(prompt + own)
+        assert hit == P, hit
+        m.append(s, 850)
+        seqs.append(s)
+    m.append(s0, 850)
+    heads = {tuple(m.seqs[s][0][:P // b]) for s in seqs}
+    assert len(heads) == 1
+    assert all(m.ref[blk] == n + 1 for blk in next(iter(heads)))
+    assert m.num_free() == 12000 - P // b - n * (-(-850 // b))
+    assert m.hit_tokens == (n - 1) * P
+
+
+def pin_prefix_context_matters(orc):
+    """auto-20261007-1900-en, "Shared prefixes need matching computation": equal
+    tokens after another context, or under another condition, do not match."""
+    b = 4
+    m = prefix_model.PrefixCacheModel(64, b)
+    x0, x1, y0, y1 = [1, 2, 3, 4], [5, 6, 7, 8], [9, 9, 9, 9], [8, 7, 6, 5]
+    s, _ = m.add_seq_cached(x0 + x1)
+    m.append(s, 8)
+    assert m.cache_seq(s, x0 + x1) == 2
+    assert m.prefix_match(y0 + x1) == 0
+    assert m.prefix_match(x0 + y1) == b
+    assert m.prefix_match(x0 + x1, condition=1) == 0
+    assert m.prefix_match(x0 + x1 + [3, 3]) == 2 * b
+    assert m.prefix_match(x0 + x1[:b - 1]) == b          # a partial block is never matched
+    assert m.prefix_match(x0[:b - 1]) == 0
+    assert m.prefix_match([]) == 0
+    # content already cached keeps its entry; the chain continues from it
+    t = m.add_seq()
+    m.append(t, 12)
+    assert m.cache_seq(t, x0 + x1 + y0) == 1
+    assert m.prefix_match(x0 + x1 + y0) == 3 * b
+    # a block already cached under other content ends publishing
+    u = m.add_seq()
+    m.append(u, 8)
+    assert m.cache_seq(u, y1 + y1) == 2
+    assert m.cache_seq(u, y0 + y1) == 0 and m.prefix_match(y0) == 0
+
+
+def pin_prefix_brute_force(orc):
+    """Longest cached prefix in whole blocks equals a direct scan of every
+    published token list (no eviction: the pool never runs out)."""
+    rng = np.random.default_rng(77)
+    b = 2
+    m = prefix_model.PrefixCacheModel(10000, b)
+    published = []
+    for _ in range(40):
+        cond = int(rng.integers(0, 2))
+        toks = rng.integers(0, 2, int(rng.integers(0, 12))).tolist()
+        s = m.add_seq()
+        m.append(s, len(toks))
+        m.cache_seq(s, toks, cond)
+        published.append((cond, toks))
+    for _ in range(400):
+        cond = int(rng.integers(0, 2))
+        q = rng.integers(0, 2, int(rng.integers(0, 14))).tolist()
+        best = 0
+        for c, toks in published:
+            if c != cond:
+                continue
+            k = 0
+            while (k + 1) * b <= min(len(q), len(toks)) and q[:(k + 1) * b] == toks[:(k + 1) * b]:
+                k += 1
+            best = max(best, k)
+        assert m.prefix_match(q, cond) == best * b, (q, cond)
+
+
+def pin_prefix_lru_hand_worked(orc):
+    """Four 2-token blocks.  A = [1,2,3,4] and B = [5,6,7,8] are cached and
+    their sequences freed, then A is used again; a sequence needing two blocks
+    evicts B's deeper block, then B's first; A stays."""
+    m = prefix_model.PrefixCacheModel(4, 2)
+    for toks in ([1, 2, 3, 4], [5, 6, 7, 8]):
+        s, _ = m.add_seq_cached(toks)
+        m.append(s, 4)
+        m.cache_seq(s, toks)
+        m.free_seq(s)
+    assert m.num_free() == 0 and m.available() == 4
+    s, hit = m.add_seq_cached([1, 2, 3, 4])
+    assert hit == 4
+    m.free_seq(s)
+    d = m.add_seq()
+    m.append(d, 2)
+    assert m.prefix_match([5, 6, 7, 8]) == 2 and m.prefix_match([1, 2, 3, 4]) == 4
+    m.append(d, 2)
+    assert m.prefix_match([5, 6, 7, 8]) == 0 and m.prefix_match([1, 2, 3, 4]) == 4
+    # three blocks, one free: a two-block need evicts A's deeper block only
+    m = prefix_model.PrefixCacheModel(3, 2)
+    s, _ = m.add_seq_cached([1, 2, 3, 4])
+    m.append(s, 4)
+    m.cache_seq(s, [1, 2, 3, 4])
+    m.free_seq(s)
+    d = m.add_seq()
+    m.append(d, 4)
+    assert m.prefix_match([1, 2, 3, 4]) == 2
+    try:
+        m.append(d, 3)                                   # needs 2 blocks, 1 can be had
+    except prefix_model.NoBlocks:
+        pass
+    else:
+        raise AssertionError("append beyond the pool succeeded")
+    assert m.prefix_match([1, 2, 3, 4]) == 2
+
+
+def pin_prefix_evict_subtree(orc):
+    """Evicting an entry drops the entries that extend it, even one whose block
+    a live sequence holds (the sequence keeps the block)."""
+    m = prefix_model.PrefixCacheModel(8, 2)
+    a = m.add_seq()
+    m.append(a, 2)
+    assert m.cache_seq(a, [1, 2]) == 1
+    c = m.add_seq()
+    m.append(c, 4)
+    assert m.cache_seq(c, [1, 2, 3, 4]) == 1               # its block 1 hangs under A's entry
+    m.free_seq(a)
+    assert len(m.evictable()) == 1 and len(m.entries) == 2
+    assert m.evict(1) == 1
+    assert len(m.entries) == 0 and m.prefix_match([1, 2, 3, 4]) == 0
+    assert m.num_free() == 6
+    m.free_seq(c)
+    assert m.num_free() == 8
+
+
 PINS: Dict[str, Callable] = {name: fn for name, fn in globals().items() if name.startswith("pin_")}
 
 
@@ -529,7 +680,14 @@ def main(argv=None) -> int:
     import argparse
     ap = argparse.ArgumentParser()
     ap.add_argument("--library", default=oracle_pkg.LIBRARY)
+    ap.add_argument("--prefix-model", default=None)
     args = ap.parse_args(argv)
+    if args.prefix_model:
+        import importlib.util
+        spec = importlib.util.spec_from_file_location("prefix_cache_under_test", args.prefix_model)
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        globals()["prefix_model"] = mod
     bad = failing_pins(oracle_pkg.Oracle(args.library))
     print(json.dumps(bad))
     return 1 if bad else 0

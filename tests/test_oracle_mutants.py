@@ -4,6 +4,8 @@ Each mutant is ``pa_oracle.c`` with one plausible slip (a dropped term, a
 wrong sign or index, a transposed operand, an off-by-one), built with gcc into
 a temporary library and run through every pin in a child process (so that a
 mutant which reads out of bounds cannot take the test run down with it).
+The prefix-cache reference model (``oracle/prefix_cache.py``) gets the same
+treatment with its own list of slips.
 """
 import os
 import subprocess
@@ -71,3 +73,30 @@ def test_unmutated_oracle_passes_in_child(tmp_path):
     proc = subprocess.run([sys.executable, "-m", "tests.oracle_pins", "--library", lib],
                           cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert proc.returncode == 0, proc.stdout + proc.stderr
+
+
+PREFIX_MODEL = os.path.join(ROOT, "oracle", "prefix_cache.py")
+
+# (name, original text, replacement, count of occurrences expected) in oracle/prefix_cache.py
+PREFIX_MUTANTS = [
+    ("prefix_block_tokens_only", "(condition, tuple(tokens[:(i + 1) * self.b]))",
+     "(condition, tuple(tokens[i * self.b:(i + 1) * self.b]))", 2),
+    ("prefix_condition_ignored", "key = (condition, tuple(", "key = (0, tuple(", 2),
+    ("prefix_lru_newest", "victim = min(cands", "victim = max(cands", 1),
+    ("prefix_stamp_root_first", "for k in reversed(chain):", "for k in chain:", 1),
+    ("prefix_extensions_kept", "for k in [k for k in self.entries if k[0] == cond and k[1][:len(prefix)] == prefix]:",
+     "for k in [victim]:", 1),
+    ("prefix_cache_takes_no_reference", "                self.ref[blk] += 1\n                inserted += 1",
+     "                inserted += 1", 1),
+]
+
+
+@pytest.mark.parametrize("name,old,new,count", PREFIX_MUTANTS, ids=[m[0] for m in PREFIX_MUTANTS])
+def test_prefix_model_mutant_is_caught(tmp_path, name, old, new, count):
+    src = open(PREFIX_MODEL).read()
+    assert src.count(old) == count, f"mutation site for {name} not found as expected"
+    mutated = tmp_path / f"{name}.py"
+    mutated.write_text(src.replace(old, new))
+    proc = subprocess.run([sys.executable, "-m", "tests.oracle_pins", "--prefix-model", str(mutated)],
+                          cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert proc.returncode != 0, f"mutant {name} passed every pin:\n{proc.stdout}{proc.stderr}"
