@@ -110,3 +110,20 @@ def test_invalid_arguments(pa):
         with pytest.raises(pa.PagedAttentionError) as e:
             pa.capacity_estimate(*args)
         assert e.value.status == 1, args
+
+
+def test_shared_prefix_workload_mix(pa, orc):
+    """The 256-sequence shared-prompt workload's lengths (2,000-token prompt plus
+    a lognormal suffix, at most 8,192 tokens) at Llama 3.1 70B's 328 KB a token:
+    the library equals the oracle, and sharing the prompt's 125 blocks beats
+    both private paging and contiguous reservation."""
+    import pa_workloads as wl
+    w = wl.CONFIGS["shared_prefix"]()
+    lens = w.seq_lens.astype(np.int64)
+    args = dict(block_size=16, max_seq_len=8192, bytes_per_token=328000, budget_bytes=435 * 10**9)
+    shared = pa.capacity_estimate(lens, 2000, **args)
+    private = pa.capacity_estimate(lens, 0, **args)
+    same(shared, orc.capacity(lens, 2000, 16, 8192, 328000, 435 * 10**9))
+    same(private, orc.capacity(lens, 0, 16, 8192, 328000, 435 * 10**9))
+    assert shared["paged_requests"] > private["paged_requests"] > shared["contiguous_requests"]
+    assert shared["contiguous_waste"] > 0.5 and shared["paged_waste"] < 0.01
