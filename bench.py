@@ -260,8 +260,10 @@ class DecodeStep:
 
     def decode(self, layer: int = 0):
         w = self.w
+        # lengths and tables are host copies, never written by the slot writer
+        # that each decode call follows: the early-metadata launch applies
         self.pa.decode(self.out, self.qs[layer], self.pools[layer], self.tables, self.seq_lens, w.max_seq_len,
-                       w.scale, w.partition_tokens, self.ws)
+                       w.scale, w.partition_tokens, self.ws, flags=self.pa.PA_DECODE_EARLY_METADATA)
 
 
 def run_ours(args, world, rank, local):
@@ -406,7 +408,7 @@ def run_ours(args, world, rank, local):
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
                    "seq_len_min": int(w.seq_lens.min()), "seq_len_max": int(w.seq_lens.max()),
                    "seq_len_mean": float(w.seq_lens.mean()), "pool_blocks": w.num_blocks,
-                   "schedule": "balanced stream-K (persistent, 2 CTAs/SM)" if step.part == 0
+                   "schedule": "balanced stream-K (persistent, 2 CTAs/SM), early-metadata launch" if step.part == 0
                    else f"split-context, {step.part}-token partitions x {step.num_parts}",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "layers": step.layers,

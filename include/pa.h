@@ -157,6 +157,29 @@ pa_status pa_decode(void *out, const void *q, const pa_kv_pool *pool,
                     void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * pa_decode with option flags; pa_decode is pa_decode_ex with flags = 0.
+ *
+ * PA_DECODE_EARLY_METADATA: the caller promises that seq_lens and
+ * block_tables are not written by the kernel this call immediately follows
+ * in `stream` (host-to-device copies, or kernels before that one, are fine).
+ * The decode kernel is launched with programmatic stream serialisation
+ * either way; with this flag it reads the lengths and table entries and
+ * plans its schedule while that previous kernel is still running, and only
+ * q, the pool and the workspace wait for it to finish, which takes the
+ * lengths -> schedule -> table chain off the call's start.  It applies to
+ * the automatic plan (partition_tokens = 0) with at most 128 sequences and
+ * is otherwise ignored; results are identical with and without it.
+ * Unknown flag bits give PA_ERR_INVALID_ARG.
+ */
+#define PA_DECODE_EARLY_METADATA 0x1u
+pa_status pa_decode_ex(void *out, const void *q, const pa_kv_pool *pool,
+                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                       const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                       int32_t max_seq_len, float scale, int32_t partition_tokens,
+                       void *workspace, size_t workspace_bytes, uint32_t flags,
+                       cudaStream_t stream);
+
+/*
  * pa_decode without a caller workspace, for callers that cannot allocate
  * device memory: e.g. a plugin that its host framework hands only input and
  * output buffers (the framework's allocator owns all device memory), or a

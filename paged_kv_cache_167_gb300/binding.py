@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3:
                 4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE", 6: "PA_ERR_NO_BLOCKS", 7: "PA_ERR_NOT_FOUND",
                 8: "PA_ERR_SWAPPED"}
 PA_SWAP_OUT, PA_SWAP_IN = 0, 1
+PA_DECODE_EARLY_METADATA = 0x1
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 PA_DTYPE_BF16 = 0
 
@@ -53,6 +54,7 @@ SIGNATURES = {
     "pa_decode_workspace_size": (_SZ, [_POOL, _I32, _I32, _I32, _I32]),
     "pa_decode_partition_tokens": (_I32, [_POOL, _I32, _I32, _I32, _I32]),
     "pa_decode": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _P]),
+    "pa_decode_ex": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _U32, _P]),
     "pa_decode_noalloc": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P]),
     "pa_copy_blocks": (_I32, [_POOL, _P, _I32, _P]),
     "pa_swap_blocks": (_I32, [_POOL, _P, _I64, _P, _I32, _I32, _P]),
@@ -194,9 +196,11 @@ def decode_partition_tokens(pool: torch.Tensor, num_seqs: int, num_q_heads: int,
 
 def decode(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_tables: torch.Tensor,
            seq_lens: torch.Tensor, max_seq_len: int, scale: float, partition_tokens: int = 0,
-           workspace: Optional[torch.Tensor] = None, layer: Optional[int] = None, stream=None) -> None:
-    """pa_decode.  ``workspace`` is a uint8 CUDA tensor of at least
-    decode_workspace_size(...) bytes (None when that size is 0)."""
+           workspace: Optional[torch.Tensor] = None, layer: Optional[int] = None, stream=None,
+           flags: int = 0) -> None:
+    """pa_decode (pa_decode_ex when ``flags`` is non-zero).  ``workspace`` is a
+    uint8 CUDA tensor of at least decode_workspace_size(...) bytes (None when
+    that size is 0)."""
     desc = pool_desc(pool, layer)
     B, Hq, _ = q.shape
     if out.shape != q.shape:
@@ -206,11 +210,14 @@ def decode(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_tables:
     ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
     if workspace is not None:
         ws_ptr, ws_bytes = _dev(workspace, torch.uint8, "workspace"), workspace.numel()
-    _check(lib().pa_decode(_dev(out, torch.bfloat16, "out"), _dev(q, torch.bfloat16, "q"), ctypes.byref(desc),
-                           _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
-                           _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, int(max_seq_len), float(scale),
-                           int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)),
-           "pa_decode")
+    args = (_dev(out, torch.bfloat16, "out"), _dev(q, torch.bfloat16, "q"), ctypes.byref(desc),
+            _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+            _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, int(max_seq_len), float(scale), int(partition_tokens),
+            ws_ptr, ws_bytes)
+    if flags:
+        _check(lib().pa_decode_ex(*args, int(flags), _stream(stream)), "pa_decode_ex")
+    else:
+        _check(lib().pa_decode(*args, _stream(stream)), "pa_decode")
 
 
 def decode_noalloc(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_tables: torch.Tensor,

@@ -70,6 +70,7 @@ struct CacheParams {
 
 // One thread per 16-B vector of a (token, K/V, head) row.
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheParams p) {
+    asm volatile("griddepcontrol.launch_dependents;");   // the next kernel still waits for this grid to finish
     asm volatile("griddepcontrol.wait;" ::: "memory");   // inputs may come from the previous kernel
     const int64_t per_token = 2ll * p.num_kv_heads * p.row_vecs;
     const int64_t total = p.num_tokens * per_token;

@@ -54,7 +54,10 @@
 //    is bounded.
 //  * Launched with programmatic stream serialisation: set-up that reads no
 //    global memory overlaps the previous kernel's tail, and every global read
-//    waits on griddepcontrol.wait.
+//    waits on griddepcontrol.wait -- except, when the caller sets the
+//    early-metadata flag (lengths and tables not written by the previous
+//    kernel), the stream-K kernel's reads of lengths and table entries and
+//    the planning of its first listing, which then overlap that kernel too.
 #pragma once
 
 #include <cfloat>
@@ -76,6 +79,7 @@
 #define PA_DECODE_WARPS 4
 #endif
 
+
 namespace pa {
 namespace decode {
 
@@ -83,6 +87,7 @@ constexpr int kWarps = PA_DECODE_WARPS;        // warps per CTA, each owning eve
 constexpr int kStages = PA_DECODE_STAGES;      // ring depth per warp, split-context kernel
 constexpr int kSkStages = PA_DECODE_SK_STAGES; // ring depth per warp, stream-K kernel
 constexpr int kMinCtas = PA_DECODE_MIN_CTAS;   // resident CTAs per SM the register budget targets
+constexpr int kOnePassSeqs = kWarps * 32;       // stream-K: sequences listed in one pass, one per thread
 constexpr int kMaxSegs = 32;                   // stream-K: units per pass of a CTA's range
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -162,8 +167,9 @@ struct Params {
     int32_t num_parts;         // split-context: partitions; stream-K: 1
     float *ws_o;               // split-context [B][Hq][P][D]; stream-K records [2C][G][D]
     float *ws_ml;              // split-context [B][Hq][P][2]; stream-K records [2C][G][2]
-    int32_t *ws_cum;           // stream-K: [B + 1] exclusive prefix of stages per sequence (all kv-heads)
+    int32_t *ws_cum;           // stream-K, more than kOnePassSeqs sequences: [B + 1] stage prefix (all kv-heads)
     int32_t num_ctas;          // stream-K grid size
+    int32_t early_meta;        // stream-K: lengths and tables may be read before griddepcontrol.wait
     unsigned int *err;
 };
 
@@ -686,12 +692,18 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
         }
         fence_barrier_init();
     }
-    grid_dependency_wait();
+    // With early_meta (one-pass listing only) the lengths and the table are
+    // read, and the first listing made, while the previous kernel in the
+    // stream finishes; q, the pool and the workspace are touched only after
+    // griddepcontrol.wait.
+    static_assert(NT == kOnePassSeqs, "the merge kernel sums the stage prefix itself up to kOnePassSeqs");
+    const bool one_pass = B <= NT;
+    bool waited = !(p.early_meta && one_pass);
+    if (waited) grid_dependency_wait();
 
     // ---- total work W (stages over all units) and this CTA's range [gs, ge)
     // With at most NT sequences (one per thread) each thread keeps its
     // sequence's stage count and first global stage for the listing below.
-    const bool one_pass = B <= NT;
     int my_ns = 0, my_first = 0;
     int total = 0;
     for (int base = 0; base < B; base += NT) {
@@ -700,15 +712,23 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
         const int v = Hkv * ns;
         int chunk;
         const int inc = block_inclusive_scan(v, sk->scan, chunk);
-        if (c == 0 && s < B) p.ws_cum[s] = total + inc - v;
+        if (!one_pass && c == 0 && s < B) p.ws_cum[s] = total + inc - v;   // the merge kernel's prefix
         my_ns = ns;
         my_first = total + inc - v;
         total += chunk;
     }
-    if (c == 0 && tid == 0) p.ws_cum[B] = total;
+    if (!one_pass && c == 0 && tid == 0) p.ws_cum[B] = total;
+    auto wait_inputs = [&]() {   // the deferred wait (early_meta)
+        if (waited) return;
+        grid_dependency_wait();
+        waited = true;
+    };
     const int per = (total + p.num_ctas - 1) / p.num_ctas;
     const int gs = min(total, c * per), ge = min(total, gs + per);
-    if (gs >= ge) return;    // nothing issued, nothing to wait for
+    if (gs >= ge) {          // nothing issued, nothing to wait for
+        wait_inputs();       // the kernels before this one finish before the merge kernel starts
+        return;
+    }
 
     // ---- the sequence whose units contain gs (the serial listing's start)
     if (!one_pass) {
@@ -805,19 +825,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
         cur_rem = sk->found_base;
         if (nseg == 0) break;
 
-        // q of the first two segments
-        auto issue_q = [&](int j) {
-            if (j >= nseg) return;
-            const int b = (jbase + j) & 1;
-            const size_t head0 = (size_t)sk->seg_s[j] * p.num_q_heads + (size_t)sk->seg_g[j] * G;
-            mbar_arrive_expect_tx(&sk->qbar[b], (uint32_t)(G * D * 2));
-            bulk_g2s(sk->q[b], p.q + head0 * D, (uint32_t)(G * D * 2), &sk->qbar[b]);
-        };
-        if (tid == 0) {
-            issue_q(0);
-            issue_q(1);
-        }
-
         // this warp's local stages: i = warp + kWarps * k, k < my_n
         const int my_n = nlocal > warp ? (nlocal - warp + kWarps - 1) / kWarps : 0;
         // register cache of block ids for the warp's stages: lane l holds block
@@ -847,6 +854,20 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
             return id;
         };
         int id_cache = load_ids(0);
+        wait_inputs();
+
+        // q of the first two segments
+        auto issue_q = [&](int j) {
+            if (j >= nseg) return;
+            const int b = (jbase + j) & 1;
+            const size_t head0 = (size_t)sk->seg_s[j] * p.num_q_heads + (size_t)sk->seg_g[j] * G;
+            mbar_arrive_expect_tx(&sk->qbar[b], (uint32_t)(G * D * 2));
+            bulk_g2s(sk->q[b], p.q + head0 * D, (uint32_t)(G * D * 2), &sk->qbar[b]);
+        };
+        if (tid == 0) {
+            issue_q(0);
+            issue_q(1);
+        }
         auto issue = [&](int k) {   // warp-uniform k
             if (k >= my_n) return;
             if (k * S::BPS - kb_base >= 32) {
@@ -880,6 +901,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
         };
 #pragma unroll
         for (int k = 0; k < kSkStages; ++k) issue(k);
+        // the merge kernel may start now: it sums the lengths, then waits for this grid
+        grid_launch_dependents();
 
         int k = 0;   // this warp's next stage in this listing
         for (int j = 0; j < nseg; ++j) {
@@ -943,27 +966,69 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
         if (!sk->more) break;
         __syncthreads();
     }
+    wait_inputs();   // only if no segment was listed
     grid_launch_dependents();
 }
 
 // Finish the stream-K schedule for one (sequence, kv-head) unit: zero output
 // for an empty sequence; merge the partial records of a unit that two or more
 // CTAs shared; nothing for a unit one CTA completed.  grid (Hkv, B).
+// For up to kOnePassSeqs sequences the stage prefix is summed from the
+// lengths before griddepcontrol.wait: the decode kernel this one follows
+// never writes them, and every decode CTA waited for the kernels before it.
+// Every decode CTA lets this kernel launch once it has issued its first
+// copies, so the sums above run while the decode kernel streams.
 template <int D, int G, int BS>
 __global__ void __launch_bounds__(G *D / 4) paged_decode_sk_merge_kernel(const Params p) {
-    grid_dependency_wait();
-    const int g = blockIdx.x, s = blockIdx.y;
-    const int h = threadIdx.x / (D / 4);
-    const int i = (threadIdx.x % (D / 4)) * 4;
+    grid_launch_dependents();   // the next kernel waits for this grid's completion before using its data
+    constexpr int NT = G * D / 4;
+    const int g = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
+    const int h = tid / (D / 4);
+    const int i = (tid % (D / 4)) * 4;
+    const int B = p.num_seqs, Hkv = p.num_kv_heads;
     const size_t row = (size_t)s * p.num_q_heads + (size_t)g * G + h;
     const int ns = seq_stages<BS>(p, s, false);
+    int before = 0, total = 0;
+    const bool local = B <= kOnePassSeqs;
+    if (local) {
+        for (int t = tid; t < B; t += NT) {
+            const int v = Hkv * seq_stages<BS>(p, t, false);
+            total += v;
+            before += t < s ? v : 0;
+        }
+        constexpr int W = NT < 32 ? NT : 32;
+        constexpr unsigned mask = NT < 32 ? ((1u << NT) - 1u) : 0xffffffffu;
+#pragma unroll
+        for (int o = W / 2; o > 0; o >>= 1) {
+            before += __shfl_xor_sync(mask, before, o);
+            total += __shfl_xor_sync(mask, total, o);
+        }
+        if constexpr (NT > 32) {
+            __shared__ int red[2][NT / 32];
+            if ((tid & 31) == 0) {
+                red[0][tid >> 5] = before;
+                red[1][tid >> 5] = total;
+            }
+            __syncthreads();
+            before = total = 0;
+#pragma unroll
+            for (int w = 0; w < NT / 32; ++w) {
+                before += red[0][w];
+                total += red[1][w];
+            }
+        }
+    }
+    grid_dependency_wait();
     if (ns == 0) {
         *reinterpret_cast<uint2 *>(p.out + row * D + i) = make_uint2(0u, 0u);
         return;
     }
-    const int total = p.ws_cum[p.num_seqs];
+    if (!local) {
+        before = p.ws_cum[s];
+        total = p.ws_cum[B];
+    }
     const int per = (total + p.num_ctas - 1) / p.num_ctas;
-    const int start = p.ws_cum[s] + g * ns, last = start + ns - 1;
+    const int start = before + g * ns, last = start + ns - 1;
     const int ca = start / per, cb = last / per;
     if (ca == cb) return;
     float M = -INFINITY;
@@ -1095,6 +1160,7 @@ cudaError_t launch_for_dim(const DecodeArgs &a, cudaStream_t stream) {
     prm.ws_ml = a.ws_ml;
     prm.ws_cum = a.ws_cum;
     prm.num_ctas = a.num_ctas;
+    prm.early_meta = a.early_meta ? 1 : 0;
     prm.err = err;
     const int G = a.num_q_heads / a.pool.num_kv_heads;
     const int bs = a.pool.block_size, H = a.pool.num_kv_heads, B = a.num_seqs;

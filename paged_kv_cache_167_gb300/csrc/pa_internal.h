@@ -69,6 +69,7 @@ struct DecodeArgs {
     bool stream_k;             // persistent balanced schedule (automatic plan)
     int32_t *ws_cum;           // stream-K: [B + 1] stage prefix
     int32_t num_ctas;          // stream-K grid size C
+    bool early_meta = false;   // stream-K: read lengths and tables before the previous kernel completes
 };
 
 // Tokens per pipeline stage of the decode kernel for a block size (the

@@ -62,6 +62,10 @@ def test_host_validation(B):
     assert L.pa_decode(*args(good, part=24)) == 1                       # partition % b
     assert L.pa_decode(*args(good, part=16)) == 3                       # workspace missing
     assert L.pa_decode(*args(_pool(B, kvstride=100))) == 1              # overlapping halves
+    ex = lambda flags, **kw: args(good, **kw)[:-1] + (flags, P(0))
+    assert L.pa_decode_ex(*ex(0x2)) == 1                                 # unknown flag bit
+    assert L.pa_decode_ex(*ex(B.PA_DECODE_EARLY_METADATA, out=P(0))) == 1  # same checks as pa_decode
+    assert L.pa_decode_ex(*ex(B.PA_DECODE_EARLY_METADATA, part=16)) == 3
     assert L.pa_reshape_and_cache(ctypes.byref(good), P(0), P(0), P(0), 0, P(0)) == 0  # nothing to do
     assert L.pa_reshape_and_cache(ctypes.byref(good), P(0x20008), ok_ptr, ok_ptr, 4, P(0)) == 1
     assert L.pa_copy_blocks(ctypes.byref(good), P(0), -1, P(0)) == 1

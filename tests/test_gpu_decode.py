@@ -33,13 +33,13 @@ def write_new_tokens(pa, c: Case):
     c.orc.reshape_and_cache(c.pool_ref, c.geom, bits(c.cpu["new_k"]), bits(c.cpu["new_v"]), oslots)
 
 
-def run_decode(pa, c: Case, partition_tokens=None):
+def run_decode(pa, c: Case, partition_tokens=None, flags=0):
     w = c.w
     part = w.partition_tokens if partition_tokens is None else partition_tokens
     out = torch.empty_like(c.q)
     nbytes = pa.decode_workspace_size(c.pool, w.batch, w.num_q_heads, w.max_seq_len, part)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=c.dev) if nbytes else None
-    pa.decode(out, c.q, c.pool, c.tables, c.seq_lens, w.max_seq_len, w.scale, part, ws)
+    pa.decode(out, c.q, c.pool, c.tables, c.seq_lens, w.max_seq_len, w.scale, part, ws, flags=flags)
     torch.cuda.synchronize()
     assert pa.get_device_error() == 0
     return out
@@ -88,6 +88,7 @@ def test_shape_sweep(pa, d, group, bs):
     ref = oracle_decode(c)
     for part in (0, bs, 4 * bs, 64 if 64 % bs == 0 else bs):
         assert_close(run_decode(pa, c, part), ref, f"d={d} G={group} b={bs} part={part}")
+    assert_close(run_decode(pa, c, 0, pa.PA_DECODE_EARLY_METADATA), ref, f"d={d} G={group} b={bs} early")
 
 
 @pytest.mark.parametrize("name,sample", [("llama70b_decode", None), ("long_context", None),
@@ -123,7 +124,9 @@ def test_many_short_units_per_cta(pa, batch, hkv):
     w = wl.custom(list(lens), hkv, hkv, 64, 16, seed=77 + batch)
     c = Case(w)
     write_new_tokens(pa, c)
-    assert_close(run_decode(pa, c, 0), oracle_decode(c), f"B={batch} Hkv={hkv}")
+    ref = oracle_decode(c)
+    assert_close(run_decode(pa, c, 0), ref, f"B={batch} Hkv={hkv}")
+    assert_close(run_decode(pa, c, 0, pa.PA_DECODE_EARLY_METADATA), ref, f"B={batch} Hkv={hkv} early")
 
 
 def test_partitions_agree(pa):
@@ -271,3 +274,37 @@ def test_device_errors_are_reported_not_faulted(pa):
     assert pa.get_device_error() & B.DEVERR_SEQ_LEN
     # still healthy afterwards
     assert_close(run_decode(pa, c, 0), oracle_decode(c), "after errors")
+
+
+def test_early_metadata_back_to_back(pa):
+    """PA_DECODE_EARLY_METADATA in the bench's launch pattern: each call follows
+    the slot writer that wrote its layer's new tokens (a kernel that writes the
+    pool, not the lengths or the table), calls alternate between two layers'
+    pools and queries, and nothing synchronises between them; every output
+    equals the oracle's."""
+    w = wl.CONFIGS["llama70b_decode"]()
+    tensors = wl.make_tensors(w, "cpu")
+    c = Case(w, tensors=tensors)
+    gen = torch.Generator().manual_seed(99)
+    q2 = torch.randn(c.q.shape, generator=gen).to(torch.bfloat16)
+    pool2 = c.pool.clone()
+    pool2_ref = c.pool_ref.copy()
+    slots = pa.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size, w.num_blocks)
+    slots_dev = torch.as_tensor(slots, device=c.dev)
+    for pool, ref_pool in ((c.pool, c.pool_ref), (pool2, pool2_ref)):
+        c.orc.reshape_and_cache(ref_pool, c.geom, bits(tensors["new_k"]), bits(tensors["new_v"]), slots)
+    qs = [c.q, q2.to(c.dev)]
+    pools = [c.pool, pool2]
+    nbytes = pa.decode_workspace_size(c.pool, w.batch, w.num_q_heads, w.max_seq_len, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=c.dev)
+    outs = [torch.empty_like(c.q) for _ in range(6)]
+    for i in range(6):
+        pa.reshape_and_cache(pools[i % 2], c.new_k, c.new_v, slots_dev)
+        pa.decode(outs[i], qs[i % 2], pools[i % 2], c.tables, c.seq_lens, w.max_seq_len, w.scale, 0, ws,
+                  flags=pa.PA_DECODE_EARLY_METADATA)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    refs = [c.orc.paged_decode(bits(tensors["q"]), c.pool_ref, c.geom, w.tables, w.seq_lens, w.num_q_heads, w.scale),
+            c.orc.paged_decode(bits(q2), pool2_ref, c.geom, w.tables, w.seq_lens, w.num_q_heads, w.scale)]
+    for i in range(6):
+        assert_close(outs[i], refs[i % 2], f"call {i}")
