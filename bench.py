@@ -1,9 +1,12 @@
 """Benchmark of one paged decode step on GB300.
 
-A step is the whole decode hot path for one batch: the slot writer stores
-each sequence's newest token (pa_reshape_and_cache), then paged GQA decode
-attention (pa_decode: split-context partition kernel plus, when the context
-is split, the partition reduce) attends every cached token.  The default
+A step is the whole decode hot path for one batch: each sequence's newest
+token is stored in its slot and paged GQA decode attention attends every
+cached token.  With one new token per sequence at its last position (the
+default workload) both happen in one call, pa_decode_ex with new_k / new_v:
+the stream-K decode kernel stores each token just before it fetches the
+block holding it, and its merge kernel follows; otherwise the slot writer
+(pa_reshape_and_cache) runs first and pa_decode after it.  The default
 workload is the Llama-3.1-70B-shaped single layer: 64 sequences of 600-850
 tokens, 64 query / 8 KV heads, head_dim 128, bf16, 16-token blocks placed at
 random in a 16,384-block pool.
@@ -20,8 +23,8 @@ an L2 flush by a 256 MiB read -- is reported as ``per_step_flushed``; it adds
 a fixed ~5 us of event and launch latency to every step.  ``e2e`` is the
 same metric through the C ABI from pinned host buffers (per-step inputs
 copied in and the output copied back inside the timed region; the KV pool
-is device-resident state).  ``roofline`` reports the decode call against the
-measured HBM copy bandwidth.  ``prefill`` times chunked prefill (16
+is device-resident state).  ``roofline`` reports the attention call alone
+(pa_decode, no stores) against the measured HBM copy bandwidth.  ``prefill`` times chunked prefill (16
 sequences x 4,096 cached + 512 new tokens) against the measured bf16 tensor
 peak.  ``cpu_baseline`` times the CPU oracle on the host cores.
 
@@ -253,10 +256,27 @@ class DecodeStep:
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
         # part == 0: the balanced (stream-K) schedule, a persistent kernel plus its merge kernel
         self.num_parts = -(-w.max_seq_len // self.part) if self.part > 0 else 1
-        self.launches_per_step = 1 + (2 if self.part == 0 or self.num_parts > 1 else 1)
+        decode_launches = 2 if self.part == 0 or self.num_parts > 1 else 1
+        # one new token per sequence, at its last position: the decode call
+        # stores it itself (pa_decode_ex with new_k / new_v)
+        self.fused = (self.part == 0 and len(w.new_seq_idx) == w.batch
+                      and np.array_equal(w.new_seq_idx, np.arange(w.batch))
+                      and np.array_equal(w.new_positions, w.seq_lens.astype(np.int64) - 1))
+        self.launches_per_step = decode_launches + (0 if self.fused else 1)
 
     def write(self, layer: int = 0):
         self.pa.reshape_and_cache(self.pools[layer], self.new_k, self.new_v, self.slots)
+
+    def step(self, layer: int = 0):
+        """One decode step: store the new tokens' K/V, attend."""
+        if not self.fused:
+            self.write(layer)
+            self.decode(layer)
+            return
+        w = self.w
+        self.pa.decode(self.out, self.qs[layer], self.pools[layer], self.tables, self.seq_lens, w.max_seq_len,
+                       w.scale, w.partition_tokens, self.ws, flags=self.pa.PA_DECODE_EARLY_METADATA,
+                       new_k=self.new_k, new_v=self.new_v)
 
     def decode(self, layer: int = 0):
         w = self.w
@@ -289,8 +309,7 @@ def run_ours(args, world, rank, local):
             dist.barrier()
 
     for i in range(args.warmup):
-        step.write(i % step.layers)
-        step.decode(i % step.layers)
+        step.step(i % step.layers)
     torch.cuda.synchronize()
     assert pa.get_device_error() == 0, "device error during warm-up"
 
@@ -308,8 +327,9 @@ def run_ours(args, world, rank, local):
         e0.record(stream)
         for i in range(K):
             if write:
-                step.write(i % step.layers)
-            step.decode(i % step.layers)
+                step.step(i % step.layers)
+            else:
+                step.decode(i % step.layers)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -325,8 +345,9 @@ def run_ours(args, world, rank, local):
             flush_fn()
             ev[i][0].record(stream)
             if write:
-                step.write()
-            step.decode()
+                step.step()
+            else:
+                step.decode()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -348,20 +369,21 @@ def run_ours(args, world, rank, local):
     host_lens = torch.as_tensor(w.seq_lens).pin_memory()
     host_slots = torch.empty(len(step.slots_host), dtype=torch.int64).pin_memory()
     host_out = torch.empty_like(tensors["q"]).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (host_q, host_k, host_v, host_tables, host_lens, host_slots))
+    h2d = sum(t.numel() * t.element_size() for t in (host_q, host_k, host_v, host_tables, host_lens) +
+              (() if step.fused else (host_slots,)))
     d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step():
-        host_slots.numpy()[:] = pa.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size,
-                                                w.num_blocks)
         step.q.copy_(host_q, non_blocking=True)
         step.new_k.copy_(host_k, non_blocking=True)
         step.new_v.copy_(host_v, non_blocking=True)
         step.tables.copy_(host_tables, non_blocking=True)
         step.seq_lens.copy_(host_lens, non_blocking=True)
-        step.slots.copy_(host_slots, non_blocking=True)
-        step.write()
-        step.decode()
+        if not step.fused:   # the slot writer needs the slots
+            host_slots.numpy()[:] = pa.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size,
+                                                    w.num_blocks)
+            step.slots.copy_(host_slots, non_blocking=True)
+        step.step()
         host_out.copy_(step.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -410,6 +432,8 @@ def run_ours(args, world, rank, local):
                    "seq_len_mean": float(w.seq_lens.mean()), "pool_blocks": w.num_blocks,
                    "schedule": "balanced stream-K (persistent, 2 CTAs/SM), early-metadata launch" if step.part == 0
                    else f"split-context, {step.part}-token partitions x {step.num_parts}",
+                   "step": "new tokens stored by the decode call (pa_decode_ex new_k/new_v), then attention"
+                   if step.fused else "slot writer (pa_reshape_and_cache), then pa_decode",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "layers": step.layers,
                    "l2": f"inputs larger than L2: steps rotate over {step.layers} layers' pools and q, "

@@ -157,7 +157,20 @@ pa_status pa_decode(void *out, const void *q, const pa_kv_pool *pool,
                     void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * pa_decode with option flags; pa_decode is pa_decode_ex with flags = 0.
+ * pa_decode with the decode step's slot write and option flags; pa_decode is
+ * pa_decode_ex with new_k = new_v = NULL and flags = 0.
+ *
+ * new_k, new_v (device, 16-B aligned, both NULL or both set): [num_seqs][Hkv]
+ * [head_dim] bf16, the K and V of the token each sequence is decoding.  For
+ * every sequence with 0 < seq_lens[s] <= its bound, the call first stores them
+ * at position seq_lens[s] - 1 (slot block_tables[s][(L-1)/b] * b + (L-1) % b),
+ * exactly what pa_reshape_and_cache would store there, and attention then
+ * includes them.  With the automatic plan the decode kernel itself stores each
+ * token just before it fetches the block holding it, which saves the slot
+ * writer's launch; with an explicit partition_tokens a small kernel stores them
+ * first.  An out-of-range length or table entry writes nothing and raises the
+ * same error bits as decode.  ([P1] "A strong answer": each decode step adds
+ * one token's K/V to the sequence's last block.)
  *
  * PA_DECODE_EARLY_METADATA: the caller promises that seq_lens and
  * block_tables are not written by the kernel this call immediately follows
@@ -168,7 +181,9 @@ pa_status pa_decode(void *out, const void *q, const pa_kv_pool *pool,
  * q, the pool and the workspace wait for it to finish, which takes the
  * lengths -> schedule -> table chain off the call's start.  It applies to
  * the automatic plan (partition_tokens = 0) with at most 128 sequences and
- * is otherwise ignored; results are identical with and without it.
+ * is otherwise ignored; results are identical with and without it.  (The
+ * pool may be written by that previous kernel: the slot writer is the usual
+ * one.)
  * Unknown flag bits give PA_ERR_INVALID_ARG.
  */
 #define PA_DECODE_EARLY_METADATA 0x1u
@@ -176,8 +191,8 @@ pa_status pa_decode_ex(void *out, const void *q, const pa_kv_pool *pool,
                        const int32_t *block_tables, int32_t max_blocks_per_seq,
                        const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
                        int32_t max_seq_len, float scale, int32_t partition_tokens,
-                       void *workspace, size_t workspace_bytes, uint32_t flags,
-                       cudaStream_t stream);
+                       void *workspace, size_t workspace_bytes, const void *new_k,
+                       const void *new_v, uint32_t flags, cudaStream_t stream);
 
 /*
  * pa_decode without a caller workspace, for callers that cannot allocate

@@ -54,7 +54,7 @@ SIGNATURES = {
     "pa_decode_workspace_size": (_SZ, [_POOL, _I32, _I32, _I32, _I32]),
     "pa_decode_partition_tokens": (_I32, [_POOL, _I32, _I32, _I32, _I32]),
     "pa_decode": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _P]),
-    "pa_decode_ex": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _U32, _P]),
+    "pa_decode_ex": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _P, _P, _U32, _P]),
     "pa_decode_noalloc": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P]),
     "pa_copy_blocks": (_I32, [_POOL, _P, _I32, _P]),
     "pa_swap_blocks": (_I32, [_POOL, _P, _I64, _P, _I32, _I32, _P]),
@@ -197,10 +197,11 @@ def decode_partition_tokens(pool: torch.Tensor, num_seqs: int, num_q_heads: int,
 def decode(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_tables: torch.Tensor,
            seq_lens: torch.Tensor, max_seq_len: int, scale: float, partition_tokens: int = 0,
            workspace: Optional[torch.Tensor] = None, layer: Optional[int] = None, stream=None,
-           flags: int = 0) -> None:
-    """pa_decode (pa_decode_ex when ``flags`` is non-zero).  ``workspace`` is a
-    uint8 CUDA tensor of at least decode_workspace_size(...) bytes (None when
-    that size is 0)."""
+           flags: int = 0, new_k: Optional[torch.Tensor] = None, new_v: Optional[torch.Tensor] = None) -> None:
+    """pa_decode (pa_decode_ex when ``flags``, ``new_k`` or ``new_v`` is given).
+    ``workspace`` is a uint8 CUDA tensor of at least decode_workspace_size(...)
+    bytes (None when that size is 0); ``new_k`` / ``new_v`` ([B][Hkv][d] bf16)
+    are stored at each sequence's last position before attending."""
     desc = pool_desc(pool, layer)
     B, Hq, _ = q.shape
     if out.shape != q.shape:
@@ -214,8 +215,13 @@ def decode(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_tables:
             _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
             _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, int(max_seq_len), float(scale), int(partition_tokens),
             ws_ptr, ws_bytes)
-    if flags:
-        _check(lib().pa_decode_ex(*args, int(flags), _stream(stream)), "pa_decode_ex")
+    if flags or new_k is not None or new_v is not None:
+        nk = _dev(new_k, torch.bfloat16, "new_k") if new_k is not None else ctypes.c_void_p(0)
+        nv = _dev(new_v, torch.bfloat16, "new_v") if new_v is not None else ctypes.c_void_p(0)
+        for name, t in (("new_k", new_k), ("new_v", new_v)):
+            if t is not None and (t.dim() != 3 or t.shape[0] != B or t.shape[1:] != (desc.num_kv_heads, desc.head_dim)):
+                raise ValueError(f"{name} must be [num_seqs][num_kv_heads][head_dim]")
+        _check(lib().pa_decode_ex(*args, nk, nv, int(flags), _stream(stream)), "pa_decode_ex")
     else:
         _check(lib().pa_decode(*args, _stream(stream)), "pa_decode")
 

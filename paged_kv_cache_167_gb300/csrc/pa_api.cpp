@@ -177,14 +177,18 @@ pa_status pa_decode(void *out, const void *q, const pa_kv_pool *pool, const int3
                     int32_t max_seq_len, float scale, int32_t partition_tokens, void *workspace,
                     size_t workspace_bytes, cudaStream_t stream) {
     return pa_decode_ex(out, q, pool, block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_q_heads,
-                        max_seq_len, scale, partition_tokens, workspace, workspace_bytes, 0u, stream);
+                        max_seq_len, scale, partition_tokens, workspace, workspace_bytes, nullptr, nullptr, 0u,
+                        stream);
 }
 
 pa_status pa_decode_ex(void *out, const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
                        int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
                        int32_t max_seq_len, float scale, int32_t partition_tokens, void *workspace,
-                       size_t workspace_bytes, uint32_t flags, cudaStream_t stream) {
+                       size_t workspace_bytes, const void *new_k, const void *new_v, uint32_t flags,
+                       cudaStream_t stream) {
     if ((flags & ~PA_DECODE_EARLY_METADATA) != 0) return PA_ERR_INVALID_ARG;
+    if ((new_k == nullptr) != (new_v == nullptr)) return PA_ERR_INVALID_ARG;
+    if (new_k && (!aligned16(new_k) || !aligned16(new_v))) return PA_ERR_INVALID_ARG;
     PoolView view;
     pa_status st = resolve_pool(pool, &view);
     if (st != PA_OK) return st;
@@ -219,6 +223,16 @@ pa_status pa_decode_ex(void *out, const void *q, const pa_kv_pool *pool, const i
     a.stream_k = plan.stream_k;
     a.num_ctas = plan.num_ctas;
     a.early_meta = (flags & PA_DECODE_EARLY_METADATA) != 0;
+    if (new_k) {
+        if (plan.stream_k) {   // the stream-K kernel stores each last token itself
+            a.new_k = new_k;
+            a.new_v = new_v;
+        } else if (launch_append_last(view, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                                      plan.partition_tokens * plan.num_partitions, new_k, new_v,
+                                      stream) != cudaSuccess) {
+            return PA_ERR_CUDA;
+        }
+    }
     return launch_decode(a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

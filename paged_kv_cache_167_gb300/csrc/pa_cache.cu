@@ -230,6 +230,88 @@ int device_sm_count() {
     return g_sm_count[dev];
 }
 
+// Stores the K/V of each sequence's last token (position seq_lens[s] - 1) at
+// its slot through the block table: the slot writer's work for one decode
+// step, with the slots derived on the device.  One thread per 16-B vector of
+// a (sequence, K/V, head) row.
+struct AppendParams {
+    uint4 *pool;
+    int64_t num_blocks;
+    int64_t block_stride_v;
+    int64_t kv_stride_v;
+    int32_t num_kv_heads;
+    int32_t block_size;
+    int32_t row_vecs;
+    const int32_t *tables;
+    int32_t max_blocks;
+    const int32_t *seq_lens;
+    int32_t num_seqs;
+    int32_t max_len;             // lengths above this are invalid
+    const uint4 *k;              // [B][Hkv][D]
+    const uint4 *v;
+    unsigned int *err;
+};
+
+__global__ void __launch_bounds__(256) append_last_kernel(const AppendParams p) {
+    asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t per_seq = 2ll * p.num_kv_heads * p.row_vecs;
+    const int64_t total = (int64_t)p.num_seqs * per_seq;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int s = (int)(idx / per_seq);
+        int64_t r = idx - (int64_t)s * per_seq;
+        const int kv = (int)(r / ((int64_t)p.num_kv_heads * p.row_vecs));
+        r -= (int64_t)kv * p.num_kv_heads * p.row_vecs;
+        const int h = (int)(r / p.row_vecs), c = (int)(r % p.row_vecs);
+        const int L = __ldg(p.seq_lens + s);
+        if (L <= 0) continue;
+        if (L > p.max_len || L > p.max_blocks * p.block_size) {
+            if (kv == 0 && h == 0 && c == 0) raise_error(p.err, PA_DEVERR_SEQ_LEN);
+            continue;
+        }
+        const int blk = __ldg(p.tables + (size_t)s * p.max_blocks + (L - 1) / p.block_size);
+        if (blk < 0 || blk >= p.num_blocks) {
+            if (kv == 0 && h == 0 && c == 0) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+            continue;
+        }
+        const int off = (L - 1) % p.block_size;
+        const uint4 *src = (kv == 0 ? p.k : p.v) + ((size_t)s * p.num_kv_heads + h) * p.row_vecs + c;
+        p.pool[blk * p.block_stride_v + kv * p.kv_stride_v + ((int64_t)h * p.block_size + off) * p.row_vecs + c] =
+            *src;
+    }
+}
+
+cudaError_t launch_append_last(const PoolView &pool, const int32_t *tables, int32_t max_blocks,
+                               const int32_t *seq_lens, int32_t num_seqs, int32_t max_len, const void *k,
+                               const void *v, cudaStream_t stream) {
+    if (num_seqs == 0) return cudaSuccess;
+    unsigned int *err = device_error_word();
+    if (!err) return cudaErrorUnknown;
+    AppendParams p;
+    p.pool = reinterpret_cast<uint4 *>(const_cast<void *>(pool.base));
+    p.num_blocks = pool.num_blocks;
+    p.block_stride_v = pool.block_stride / 8;
+    p.kv_stride_v = pool.kv_stride / 8;
+    p.num_kv_heads = pool.num_kv_heads;
+    p.block_size = pool.block_size;
+    p.row_vecs = pool.head_dim / 8;
+    p.tables = tables;
+    p.max_blocks = max_blocks;
+    p.seq_lens = seq_lens;
+    p.num_seqs = num_seqs;
+    p.max_len = max_len;
+    p.k = static_cast<const uint4 *>(k);
+    p.v = static_cast<const uint4 *>(v);
+    p.err = err;
+    const int64_t total = (int64_t)num_seqs * 2 * pool.num_kv_heads * p.row_vecs;
+    const int threads = 256;
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    int64_t blocks = (total + threads - 1) / threads;
+    if (cap > 0 && blocks > cap) blocks = cap;
+    return launch_pdl(append_last_kernel, dim3((unsigned)blocks), dim3(threads), stream, p);
+}
+
 cudaError_t launch_reshape_and_cache(const PoolView &pool, const void *k, const void *v,
                                      const int64_t *slots, int64_t num_tokens, cudaStream_t stream) {
     if (num_tokens == 0) return cudaSuccess;

@@ -170,6 +170,13 @@ struct Params {
     int32_t *ws_cum;           // stream-K, more than kOnePassSeqs sequences: [B + 1] stage prefix (all kv-heads)
     int32_t num_ctas;          // stream-K grid size
     int32_t early_meta;        // stream-K: lengths and tables may be read before griddepcontrol.wait
+    // stream-K append: the K/V of each sequence's last token, stored at its
+    // slot before the stage holding it is fetched (nullptr: no append)
+    const __nv_bfloat16 *new_k;  // [B][Hkv][D]
+    const __nv_bfloat16 *new_v;
+    __nv_bfloat16 *pool;         // the layer's pool view (element strides below)
+    int64_t block_stride;
+    int64_t kv_stride;
     unsigned int *err;
 };
 
@@ -845,7 +852,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
                     id = __ldg(p.tables + (size_t)s * p.max_blocks + logical);
                     if (id < 0 || id >= p.num_blocks) {
                         raise_error(p.err, PA_DEVERR_BLOCK_ID);
-                        id = 0;
+                        id = -2;   // not fetched, not written
                     }
                 } else {
                     id = -1;   // past the sequence end: not fetched
@@ -878,12 +885,39 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
             int j = 0;
             while (j + 1 < nseg && sk->seg_lb[j + 1] <= i) ++j;
             const int g = sk->seg_g[j];
-            const int c_slot = S::slot_of((sk->seg_kb[j] + i - sk->seg_lb[j]) * S::TPS);
+            const int tok0 = (sk->seg_kb[j] + i - sk->seg_lb[j]) * S::TPS;
+            const int c_slot = S::slot_of(tok0);
             const int slot = (kq + k) % kSkStages;
             int ids[S::BPS];
 #pragma unroll
             for (int ib = 0; ib < S::BPS; ++ib)
                 ids[ib] = __shfl_sync(0xffffffffu, id_cache, k * S::BPS + ib - kb_base);
+            if (p.new_k != nullptr) {
+                // the stage holding the sequence's last token stores that token's
+                // K and V first; the copy below then reads them back from the pool
+                const int s = sk->seg_s[j];
+                const int L = __ldg(p.seq_lens + s), last = L - 1;   // an out-of-range length writes nothing
+                if (L <= min(p.max_blocks * BS, p.num_parts * p.part_tokens) && last >= tok0 &&
+                    last < tok0 + S::TPS) {
+                    const int ib = BS < 16 ? last / BS - tok0 / BS : 0;
+                    int blk = 0;
+#pragma unroll
+                    for (int x = 0; x < S::BPS; ++x) blk = x == ib ? ids[x] : blk;
+                    if (blk >= 0) {
+                        constexpr int CH = D / 8;   // 16-byte chunks per row
+                        const int half = lane / CH, c16 = lane % CH;
+                        if (half < 2) {
+                            const __nv_bfloat16 *src = (half == 0 ? p.new_k : p.new_v) +
+                                                       ((size_t)s * p.num_kv_heads + g) * D + c16 * 8;
+                            __nv_bfloat16 *dst = p.pool + (size_t)blk * p.block_stride + half * p.kv_stride +
+                                                 ((size_t)g * BS + last % BS) * D + c16 * 8;
+                            *reinterpret_cast<uint4 *>(dst) = __ldg(reinterpret_cast<const uint4 *>(src));
+                        }
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        __syncwarp();
+                    }
+                }
+            }
             if (lane == 0) {
                 int nvalid = 0;
 #pragma unroll
@@ -1161,6 +1195,11 @@ cudaError_t launch_for_dim(const DecodeArgs &a, cudaStream_t stream) {
     prm.ws_cum = a.ws_cum;
     prm.num_ctas = a.num_ctas;
     prm.early_meta = a.early_meta ? 1 : 0;
+    prm.new_k = static_cast<const __nv_bfloat16 *>(a.new_k);
+    prm.new_v = static_cast<const __nv_bfloat16 *>(a.new_v);
+    prm.pool = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.pool.base));
+    prm.block_stride = a.pool.block_stride;
+    prm.kv_stride = a.pool.kv_stride;
     prm.err = err;
     const int G = a.num_q_heads / a.pool.num_kv_heads;
     const int bs = a.pool.block_size, H = a.pool.num_kv_heads, B = a.num_seqs;

@@ -44,6 +44,9 @@ cudaError_t encode_pool_block_map(CUtensorMap *map, const PoolView &pool, int kv
 // ---- slot writer and block copies (pa_cache.cu) ---------------------------
 cudaError_t launch_reshape_and_cache(const PoolView &pool, const void *k, const void *v,
                                      const int64_t *slots, int64_t num_tokens, cudaStream_t stream);
+cudaError_t launch_append_last(const PoolView &pool, const int32_t *tables, int32_t max_blocks,
+                               const int32_t *seq_lens, int32_t num_seqs, int32_t max_len, const void *k,
+                               const void *v, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const PoolView &pool, const int32_t *pairs, int32_t num_pairs,
                                cudaStream_t stream);
 // host_dev: the device address of the pinned host buffer
@@ -70,6 +73,8 @@ struct DecodeArgs {
     int32_t *ws_cum;           // stream-K: [B + 1] stage prefix
     int32_t num_ctas;          // stream-K grid size C
     bool early_meta = false;   // stream-K: read lengths and tables before the previous kernel completes
+    const void *new_k = nullptr;   // stream-K: last token's K/V per sequence, stored before attending
+    const void *new_v = nullptr;
 };
 
 // Tokens per pipeline stage of the decode kernel for a block size (the

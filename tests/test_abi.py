@@ -62,7 +62,9 @@ def test_host_validation(B):
     assert L.pa_decode(*args(good, part=24)) == 1                       # partition % b
     assert L.pa_decode(*args(good, part=16)) == 3                       # workspace missing
     assert L.pa_decode(*args(_pool(B, kvstride=100))) == 1              # overlapping halves
-    ex = lambda flags, **kw: args(good, **kw)[:-1] + (flags, P(0))
+    ex = lambda flags, nk=P(0), nv=P(0), **kw: args(good, **kw)[:-1] + (nk, nv, flags, P(0))
+    assert L.pa_decode_ex(*ex(0, nk=ok_ptr)) == 1                       # new_k without new_v
+    assert L.pa_decode_ex(*ex(0, nk=ok_ptr, nv=P(0x20008))) == 1        # misaligned new_v
     assert L.pa_decode_ex(*ex(0x2)) == 1                                 # unknown flag bit
     assert L.pa_decode_ex(*ex(B.PA_DECODE_EARLY_METADATA, out=P(0))) == 1  # same checks as pa_decode
     assert L.pa_decode_ex(*ex(B.PA_DECODE_EARLY_METADATA, part=16)) == 3

@@ -308,3 +308,95 @@ def test_early_metadata_back_to_back(pa):
             c.orc.paged_decode(bits(q2), pool2_ref, c.geom, w.tables, w.seq_lens, w.num_q_heads, w.scale)]
     for i in range(6):
         assert_close(outs[i], refs[i % 2], f"call {i}")
+
+
+def append_inputs(c: Case):
+    """[B][Hkv][d] new K/V per sequence (rows of empty sequences are zero and
+    ignored) and the oracle's pool after the same stores."""
+    w = c.w
+    nk = torch.zeros((w.batch, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16)
+    nv = torch.zeros_like(nk)
+    nk[torch.as_tensor(w.new_seq_idx.astype(np.int64))] = c.cpu["new_k"]
+    nv[torch.as_tensor(w.new_seq_idx.astype(np.int64))] = c.cpu["new_v"]
+    oslots = c.orc.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size)
+    c.orc.reshape_and_cache(c.pool_ref, c.geom, bits(c.cpu["new_k"]), bits(c.cpu["new_v"]), oslots)
+    return nk.to(c.dev), nv.to(c.dev)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("bs", [4, 8, 16, 32, 64])
+def test_decode_with_append(pa, d, bs):
+    """pa_decode_ex with new_k / new_v: each sequence's last token is stored at
+    its slot (bit-exact with the oracle's slot writer) and attended, with the
+    automatic plan (stored inside the decode kernel) and with partitions (a
+    separate store kernel first)."""
+    for part in (0, 4 * bs):
+        w = wl.custom(SWEEP_LENS + [0], 8, 2, d, bs, seed=2000 + d + bs)
+        c = Case(w)
+        nk, nv = append_inputs(c)
+        out = run_decode_ex(pa, c, part, nk, nv, pa.PA_DECODE_EARLY_METADATA)
+        assert np.array_equal(bits(c.pool), c.pool_ref), f"b={bs} part={part}: pool after the append"
+        assert_close(out, oracle_decode(c), f"d={d} b={bs} part={part} append")
+
+
+def run_decode_ex(pa, c: Case, part, nk, nv, flags):
+    w = c.w
+    out = torch.empty_like(c.q)
+    nbytes = pa.decode_workspace_size(c.pool, w.batch, w.num_q_heads, w.max_seq_len, part)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=c.dev) if nbytes else None
+    pa.decode(out, c.q, c.pool, c.tables, c.seq_lens, w.max_seq_len, w.scale, part, ws, flags=flags,
+              new_k=nk, new_v=nv)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    return out
+
+
+@pytest.mark.parametrize("name,sample", [("llama70b_decode", None), ("shared_prefix", 2048), ("beam_fork", 2048)])
+def test_append_full_size(pa, name, sample):
+    """The full-size workloads through the fused append + decode call, as the
+    bench times it."""
+    w = wl.CONFIGS[name]()
+    c = Case(w)
+    if w.copy_pairs is not None and len(w.copy_pairs):
+        pa.copy_blocks(c.pool, torch.as_tensor(w.copy_pairs, device=c.dev))
+        c.orc.copy_blocks(c.pool_ref, c.geom, w.copy_pairs)
+    nk, nv = append_inputs(c)
+    out = run_decode_ex(pa, c, 0, nk, nv, pa.PA_DECODE_EARLY_METADATA)
+    assert np.array_equal(bits(c.pool), c.pool_ref), "pool after the append"
+    if sample is None:
+        assert_close(out, oracle_decode(c), name)
+    else:
+        rng = np.random.default_rng(6)
+        flat = rng.choice(w.batch * w.num_q_heads, size=sample, replace=False)
+        rows = np.stack([flat // w.num_q_heads, flat % w.num_q_heads], axis=1)
+        assert_close(out[rows[:, 0], rows[:, 1]], oracle_decode(c, rows), name)
+
+
+def test_append_errors_write_nothing(pa):
+    """An out-of-range length or table entry stores nothing for that sequence
+    (and raises its error bit); the other sequences are appended."""
+    from paged_kv_cache_167_gb300 import binding as B
+    w = wl.custom([40, 9, 17], 8, 2, 64, 16, num_blocks=16, seed=31)
+    c = Case(w)
+    nk, nv = append_inputs(c)
+    before = bits(c.pool).copy()
+    tables = c.tables.clone()
+    tables[1, 0] = w.num_blocks + 3            # sequence 1's last block is out of range
+    lens = c.seq_lens.clone()
+    lens[2] = w.max_blocks * w.block_size + 5  # sequence 2's length is out of range
+    out = torch.empty_like(c.q)
+    nbytes = pa.decode_workspace_size(c.pool, w.batch, w.num_q_heads, w.max_seq_len, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=c.dev)
+    pa.get_device_error(clear=True)
+    pa.decode(out, c.q, c.pool, tables, lens, w.max_seq_len, w.scale, 0, ws, new_k=nk, new_v=nv)
+    torch.cuda.synchronize()
+    e = pa.get_device_error()
+    assert e & B.DEVERR_BLOCK_ID and e & B.DEVERR_SEQ_LEN
+    after = bits(c.pool)
+    # only sequence 0's last slot changed
+    slot0 = c.orc.slot_mapping(w.tables, np.asarray([0], np.int32), np.asarray([39]), w.block_size)[0]
+    blk, off = divmod(int(slot0), w.block_size)
+    mask = np.ones(after.shape, bool)
+    mask[blk, :, :, off] = False
+    assert np.array_equal(after[mask], before[mask])
+    assert np.array_equal(after[blk, 0, :, off], bits(c.cpu["new_k"])[0])
