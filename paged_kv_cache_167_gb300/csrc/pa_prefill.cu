@@ -67,8 +67,7 @@ constexpr uint32_t kTile = 2u * kHalf;      // [2 halves][128 rows][128 B]
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTile;   // 2 stages, [half][128 keys][128 B]
 constexpr uint32_t kOffV = kOffK + 2 * kTile; // 2 stages, [block][half][16 keys][128 B]
-constexpr uint32_t kOffP = kOffV + 2 * kTile; // 2 buffers
-constexpr uint32_t kOffX = kOffP + 2 * kTile; // [2 halves][128 rows] fp32 exchange
+constexpr uint32_t kOffX = kOffV + 2 * kTile; // [2 halves][128 rows] fp32 exchange
 constexpr uint32_t kOffBar = kOffX + 1024;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // + alignment slack
 constexpr int kSBufs = 3;                   // S accumulators in tensor memory
@@ -146,6 +145,15 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
         : "memory");
 }
 
+// A operand from tensor memory (M rows in lanes, K along columns, two bf16 per column).
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
@@ -182,6 +190,13 @@ __device__ __forceinline__ void mbar_arrive_u32(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Tensor-memory column of keys kk*16 .. kk*16+15 of P in S buffer sb: each
+// half of a row's keys is written, two bf16 per column, by the warpgroup that
+// read it, into the first 32 of the 64 S columns it read.
+__device__ __forceinline__ uint32_t p_col(int sb, int kk) {
+    return (uint32_t)(sb * 128 + (kk >> 2) * 64 + (kk & 3) * 8);
+}
+
 __device__ __forceinline__ void pair_sync(int warp) {   // warps w and w + 4 own the same rows
     asm volatile("bar.sync %0, %1;" ::"r"(1 + (warp & 3)), "r"(64) : "memory");
 }
@@ -216,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     unsigned char *gbase = smem_raw + (base - smem_addr(smem_raw));
-    const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sP = base + kOffP;
+    const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
     float *xch = reinterpret_cast<float *>(gbase + kOffX);
     const uint32_t barQ = base + kOffBar;
     // barriers: Q | K[2] | V[2] | S[3] | S free[3] | P[2] | P.V done[2] | drain
@@ -360,11 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
                     // 16 keys of the V tile: within one block for b >= 16 (8-key groups
                     // 1024 B apart), or two whole blocks for b = 8 (groups one block apart)
-                    const uint32_t a_off = (kk >> 2) * kHalf + (kk & 3) * 32;
                     const uint32_t v_off = (uint32_t)(kk * 16 / BS) * kVBlock + (uint32_t)((kk * 16) % BS) * 128u;
-                    umma(tO, smem_desc(sP + st * kTile + a_off, 16, 1024),
-                         smem_desc(sV + st * kTile + v_off, BS * 128, BS >= 16 ? 1024 : kVBlock), idesc_pv,
-                         (t > 0 || kk > 0) ? 1u : 0u);
+                    umma_ts(tO, tmem + p_col(t % kSBufs, kk),
+                            smem_desc(sV + st * kTile + v_off, BS * 128, BS >= 16 ? 1024 : kVBlock), idesc_pv,
+                            (t > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(barOP + 8 * st);
                 committed_pv = t + 1;
@@ -435,31 +449,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 c2 = make_float2(c, c);
             const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
             const float2 nm2 = make_float2(nm, nm);
-            // P buffer st was last read by P.V(t-2)
-            if (t >= 2) mbar_wait(barOP + 8 * st, (uint32_t)(((t - 2) >> 1) & 1), p.err);
+            // P goes back into this half's S columns (read above), two bf16 per
+            // column; Q.K(t + 3) overwrites them only after P.V(t) has read them
             float2 ps2 = make_float2(0.f, 0.f);
-            const uint32_t prow = sP + st * kTile + hf * kHalf + (uint32_t)r * 128u;
+            uint32_t pw[32];
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {        // 8 keys = one 16-byte chunk
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cc][q4 * 8 + 2 * e]),
-                                                                __uint_as_float(sr[cc][q4 * 8 + 2 * e + 1])),
-                                                    c2, nm2);
-                        const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                        ps2 = __fadd2_rn(ps2, pe);
-                        w[e] = pack_bf16x2(pe.x, pe.y);
-                    }
-                    const uint32_t chunk = (uint32_t)(cc * 4 + q4);
-                    const uint32_t addr = prow + ((chunk ^ (uint32_t)(r & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                                 "r"(w[2]), "r"(w[3])
-                                 : "memory");
+                for (int e = 0; e < 16; ++e) {
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cc][2 * e]),
+                                                            __uint_as_float(sr[cc][2 * e + 1])),
+                                                c2, nm2);
+                    const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                    ps2 = __fadd2_rn(ps2, pe);
+                    pw[cc * 16 + e] = pack_bf16x2(pe.x, pe.y);
                 }
             }
+            tmem_st32(tmem + sb * 128 + lane_off + hf * 64, pw);
+            tmem_st_wait();
             l2.x = l2.x * alpha + (ps2.x + ps2.y);
             // rescale this half of O once P.V(t-1) has completed
             if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
