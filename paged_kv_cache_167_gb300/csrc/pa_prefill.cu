@@ -37,8 +37,10 @@
 //    through shared memory, keeps a reference maximum in the log2 domain that
 //    only moves when a tile's maximum exceeds it by more than 8 (so p <= 2^8
 //    and O needs rescaling rarely; the result is exact because l and O share
-//    the reference), writes P as bf16 into one of two swizzled shared-memory
-//    buffers the next MMA reads, and sums the fp32 probabilities into l.
+//    the reference), writes P as bf16 back into the first half of the S
+//    columns it read (tcgen05.st, two bf16 per column), from where P.V takes
+//    its A operand, and sums the fp32 probabilities into l.  The S buffer is
+//    written again only by Q.K(t + 3), which the MMA lane issues after P.V(t).
 //  * K and V rings of two stages each; a K slot is refilled once its Q.K MMA
 //    has completed, a V slot once its P.V MMA has.
 //  * Every wait is bounded; on expiry the kernel records PA_DEVERR_TIMEOUT,
