@@ -138,6 +138,62 @@ def measure_swap(pa, step, iters: int = 5):
     return {"blocks": n, "bytes": host.numel() * 2, **res}
 
 
+def unique_decode_bytes(w: wl.Workload) -> int:
+    """decode_bytes with every physical block's K/V counted once however many
+    tables share it (the slots read of a shared block: the most any of its
+    sequences reads)."""
+    b = w.block_size
+    fill = {}
+    for s, L in enumerate(w.seq_lens.astype(np.int64)):
+        for i in range(int(-(-L // b))):
+            blk = int(w.tables[s, i])
+            fill[blk] = max(fill.get(blk, 0), int(min(b, L - i * b)))
+    kv = sum(fill.values()) * w.num_kv_heads * w.head_dim * 2 * 2
+    return decode_bytes(w) - int(w.seq_lens.astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 4 + kv
+
+
+def measure_paging_overhead(pa, step, K: int, warmup: int):
+    """Back-to-back attention calls (as the roofline times them) on copies of
+    the layers' pools whose blocks are placed sequence after sequence in
+    table order; None when blocks are shared or the plan is split-context."""
+    w, dev = step.w, step.dev
+    nb = (-(-w.seq_lens.astype(np.int64) // w.block_size)).astype(np.int64)
+    ids = np.full_like(w.tables, -1)
+    base = 0
+    for s in range(w.batch):
+        ids[s, :nb[s]] = np.arange(base, base + nb[s])
+        base += int(nb[s])
+    old = w.tables[ids >= 0]
+    if step.part != 0 or base > w.num_blocks or len(np.unique(old)) != len(old):
+        return None
+    src = torch.as_tensor(old.astype(np.int64), device=dev)
+    dst = torch.as_tensor(ids[ids >= 0].astype(np.int64), device=dev)
+    pools = torch.zeros_like(step.pools)
+    for layer in range(step.layers):
+        pools[layer][dst] = step.pools[layer][src]
+    tables = torch.as_tensor(ids.astype(np.int32), device=dev)
+
+    def call(i):
+        pa.decode(step.out, step.qs[i % step.layers], pools[i % step.layers], tables, step.seq_lens, w.max_seq_len,
+                  w.scale, 0, step.ws, flags=pa.PA_DECODE_EARLY_METADATA)
+
+    for i in range(warmup):
+        call(i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(max(2e7, 4e5 * K)))
+    e0.record(stream)
+    for i in range(K):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0, "device error during the identity-placement calls"
+    ms = e0.elapsed_time(e1) / K
+    del pools
+    return {"identity_ms": round(ms, 5)}
+
+
 def decode_bytes(w: wl.Workload) -> int:
     """Algorithmic bytes of one decode call: every attended K and V row once,
     q and out once, the table entries used and the lengths."""
@@ -399,6 +455,7 @@ def run_ours(args, world, rank, local):
         e2e_s += time.perf_counter() - t0
     barrier()
 
+    paging = measure_paging_overhead(pa, step, K, args.warmup)
     prefill = None if args.no_prefill else measure_prefill(pa, dev, flush_read)
     swap = measure_swap(pa, step)
 
@@ -446,8 +503,11 @@ def run_ours(args, world, rank, local):
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
-                     "algorithmic_bytes": alg, "decode_ms": round(decode_avg_ms, 5)},
+                     "algorithmic_bytes": alg, "unique_bytes": unique_decode_bytes(w),
+                     "decode_ms": round(decode_avg_ms, 5)},
         "kv_read_gbs": round(achieved, 1),
+        "derived": {"full_model_80_layers_tokens_per_s": round(value / 80, 1),
+                    "note": "value / 80: one such step per layer of an 80-layer model, attention only"},
         "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches_per_step * K,
@@ -462,6 +522,11 @@ def run_ours(args, world, rank, local):
                                         "peak": bf16_peak, "peak_kind": peak_kind, "unit": "TFLOP/s",
                                         "frac": round(pflop / (pms / 1e3) / 1e12 / bf16_peak, 4),
                                         "flops": pflop}}
+    if paging is not None:
+        line["paging_overhead"] = dict(paging, random_ms=round(decode_avg_ms, 5),
+                                       ratio=round(decode_avg_ms / paging["identity_ms"], 4),
+                                       note="the attention call on the same K/V with every sequence's blocks "
+                                            "consecutive in the pool (identity placement) against random placement")
     line["swap"] = dict(swap, note="pa_swap_blocks between the decode pool and pinned host memory, one kernel "
                                    "over the CPU-GPU link")
     if not args.no_cpu_baseline:
