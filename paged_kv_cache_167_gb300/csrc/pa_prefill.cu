@@ -15,8 +15,9 @@
 //    j0 + r / G of head g*G + r % G, so every K/V tile staged in shared memory
 //    serves the whole query group.  Eleven warps: eight softmax warps in two
 //    warpgroups each own 64 of a row's 128 keys (tensor-memory lanes follow
-//    warp % 4); lane 0 of the MMA warp issues every MMA; a K warp and a V warp
-//    issue the tensor copies, one lane per box.
+//    warp % 4); lane 0 of one warp issues the Q.K MMAs and lane 0 of another
+//    the P.V MMAs, so each runs ahead as far as its own inputs allow; a K warp
+//    and a V warp issue the tensor copies, one lane per box.
 //  * TMA (cp.async.bulk.tensor, 128-byte swizzle) brings Q and the K/V tiles.
 //    A K tile of 128 keys is 8 blocks x 2 halves of d, one box of 16 rows x
 //    64 dims per (block, half) through a 5-D tensor map of the pool's
@@ -29,9 +30,9 @@
 //  * S = Q.K^T and O += P.V are tcgen05.mma kind::f16 (bf16 in, fp32 out)
 //    with M = N = 128, K = 16 per instruction, accumulators in tensor memory
 //    (three S buffers in columns 0..383, O in 384..511), tracked with
-//    tcgen05.commit on mbarriers.  Q.K runs two tiles ahead of P.V, so the
-//    tensor pipe works on later tiles while the softmax warps process this
-//    one.
+//    tcgen05.commit on mbarriers.  Q.K runs up to three tiles ahead of P.V,
+//    so the tensor pipe works on later tiles while the softmax warps process
+//    this one.
 //  * Softmax: each thread owns half of one row.  It reads S with tcgen05.ld,
 //    applies the causal mask, agrees with the other half on the tile maximum
 //    through shared memory, keeps a reference maximum in the log2 domain that
@@ -57,10 +58,11 @@ namespace pa {
 namespace prefill {
 
 constexpr int kSoftWarps = 8;               // two warpgroups, each owning 64 of a row's 128 keys
-constexpr int kMmaWarp = kSoftWarps;        // lane 0 issues every MMA
+constexpr int kMmaWarp = kSoftWarps;        // lane 0 issues the P.V MMAs
 constexpr int kKWarp = kSoftWarps + 1;      // copies Q and the K tiles
 constexpr int kVWarp = kSoftWarps + 2;      // copies the V tiles
-constexpr int kThreads = (kSoftWarps + 3) * 32;
+constexpr int kQkWarp = kSoftWarps + 3;     // lane 0 issues the Q.K MMAs
+constexpr int kThreads = (kSoftWarps + 4) * 32;
 constexpr int kRows = 128;                  // M tile
 constexpr int kKeys = 128;                  // N tile of Q.K (keys per iteration)
 constexpr int kD = 128;                     // head_dim
@@ -236,11 +238,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
     float *xch = reinterpret_cast<float *>(gbase + kOffX);
     const uint32_t barQ = base + kOffBar;
-    // barriers: Q | K[2] | V[2] | S[3] | S free[3] | P[2] | P.V done[2] | drain
+    // barriers: Q | K[2] | V[2] | S[3] | S free[3] | P[2] | P.V done[2] | drain (P.V, Q.K issuers) |
+    // P.V done per S buffer[3]
     const uint32_t barK = barQ + 8, barV = barQ + 24, barS = barQ + 40, barSfree = barQ + 64, barP = barQ + 88,
-                   barOP = barQ + 104, barEnd = barQ + 120;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 136);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffBar + 140);
+                   barOP = barQ + 104, barEnd = barQ + 120, barEndQk = barQ + 128, barSdone = barQ + 136;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 160);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffBar + 164);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
@@ -253,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        const uint32_t counts[16] = {1, 1, 1, 1, 1, 1, 1, 1, 256, 256, 256, 256, 256, 1, 1, 1};
-        for (int i = 0; i < 16; ++i)
+        const uint32_t counts[20] = {1, 1, 1, 1, 1, 1, 1, 1, 256, 256, 256, 256, 256, 1, 1, 1, 1, 1, 1, 1};
+        for (int i = 0; i < 20; ++i)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(barQ + 8 * i), "r"(counts[i]) : "memory");
         *abort_flag = 0;
         fence_barrier_init();
@@ -331,18 +334,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = max(0, issued - 2); t < issued; ++t) mbar_wait(bar0 + 8 * (t & 1), (uint32_t)((t >> 1) & 1), p.err);
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp || warp == kQkWarp) {
+        // Two issuing lanes in two warps keep the tensor pipe's queue fed: one
+        // issues Q.K(t) as soon as K(t) has landed and S buffer t % 3 is free
+        // (P.V(t - 3), which read P(t - 3) from it, has completed; a barrier per
+        // S buffer tracks that), the other
+        // P.V(t) as soon as P(t) and V(t) are in place.  Each commits and drains
+        // only its own MMAs.
         if (lane == 0) {
-            auto qk = [&](int t) {
-                const int st = t & 1, sb = t % kSBufs;
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    umma(tmem + sb * 128, smem_desc(sQ + off, 16, 1024), smem_desc(sK + st * kTile + off, 16, 1024),
-                         idesc_qk, kk > 0);
-                }
-                umma_commit(barS + 8 * sb);
-            };
+            const bool is_qk = warp == kQkWarp;
             bool ok = true;
             auto wait = [&](uint32_t bar, uint32_t parity) {
                 if (ok && !mbar_wait(bar, parity, p.err)) {
@@ -351,48 +351,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return ok;
             };
-            int committed_pv = 0;
-            // Q.K runs two tiles ahead of P.V (three S buffers)
-            if (wait(barQ, 0) && wait(barK, 0)) {
-                tc_fence_after();
-                qk(0);
-                if (n_tiles > 1 && wait(barK + 8, 0)) {
-                    tc_fence_after();
-                    qk(1);
-                }
-            }
-            for (int t = 0; t < n_tiles && ok && !*abort_flag; ++t) {
-                const int st = t & 1;
-                if (t + 2 < n_tiles) {
-                    if (!wait(barK + 8 * st, (uint32_t)(((t + 2) >> 1) & 1))) break;
-                    if (t >= 1 && !wait(barSfree + 8 * ((t - 1) % kSBufs), (uint32_t)(((t - 1) / kSBufs) & 1)))
-                        break;
-                    tc_fence_after();
-                    qk(t + 2);
-                }
-                if (!wait(barP + 8 * st, (uint32_t)((t >> 1) & 1))) break;
-                if (!wait(barV + 8 * st, (uint32_t)((t >> 1) & 1))) break;
-                tc_fence_after();
+            int done = 0;
+            if (is_qk) {
+                if (wait(barQ, 0)) {
+                    for (int t = 0; t < n_tiles && ok && !*abort_flag; ++t) {
+                        const int st = t & 1, sb = t % kSBufs;
+                        if (!wait(barK + 8 * st, (uint32_t)((t >> 1) & 1))) break;
+                        // S buffer sb held P(t - 3): its P.V must have completed (P.V(t)
+                        // cannot complete before this Q.K, so the phase cannot be lapped)
+                        if (t >= kSBufs && !wait(barSdone + 8 * sb, (uint32_t)(((t - kSBufs) / kSBufs) & 1))) break;
+                        tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    // 16 keys of the V tile: within one block for b >= 16 (8-key groups
-                    // 1024 B apart), or two whole blocks for b = 8 (groups one block apart)
-                    const uint32_t v_off = (uint32_t)(kk * 16 / BS) * kVBlock + (uint32_t)((kk * 16) % BS) * 128u;
-                    umma_ts(tO, tmem + p_col(t % kSBufs, kk),
-                            smem_desc(sV + st * kTile + v_off, BS * 128, BS >= 16 ? 1024 : kVBlock), idesc_pv,
-                            (t > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kD / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                            umma(tmem + sb * 128, smem_desc(sQ + off, 16, 1024),
+                                 smem_desc(sK + st * kTile + off, 16, 1024), idesc_qk, kk > 0);
+                        }
+                        umma_commit(barS + 8 * sb);
+                        done = t + 1;
+                    }
                 }
-                umma_commit(barOP + 8 * st);
-                committed_pv = t + 1;
+            } else {
+                for (int t = 0; t < n_tiles && ok && !*abort_flag; ++t) {
+                    const int st = t & 1;
+                    if (!wait(barP + 8 * st, (uint32_t)((t >> 1) & 1))) break;
+                    if (!wait(barV + 8 * st, (uint32_t)((t >> 1) & 1))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kKeys / 16; ++kk) {
+                        // 16 keys of the V tile: within one block for b >= 16 (8-key groups
+                        // 1024 B apart), or two whole blocks for b = 8 (groups one block apart)
+                        const uint32_t v_off = (uint32_t)(kk * 16 / BS) * kVBlock + (uint32_t)((kk * 16) % BS) * 128u;
+                        umma_ts(tO, tmem + p_col(t % kSBufs, kk),
+                                smem_desc(sV + st * kTile + v_off, BS * 128, BS >= 16 ? 1024 : kVBlock), idesc_pv,
+                                (t > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(barOP + 8 * st);
+                    umma_commit(barSdone + 8 * (t % kSBufs));
+                    done = t + 1;
+                }
             }
             if (!ok || *abort_flag) {
-                // give up: one more commit tracks every MMA issued so far
+                // give up: one more commit tracks every MMA this lane issued
                 *abort_flag = 1;
-                umma_commit(barEnd);
-                mbar_wait(barEnd, 0, p.err);
-            } else if (committed_pv > 0) {
-                const int t = committed_pv - 1;   // all MMAs done before the memory is released
-                mbar_wait(barOP + 8 * (t & 1), (uint32_t)((t >> 1) & 1), p.err);
+                const uint32_t end = is_qk ? barEndQk : barEnd;
+                umma_commit(end);
+                mbar_wait(end, 0, p.err);
+            } else if (done > 0) {
+                const int t = done - 1;   // this lane's MMAs done before the memory is released
+                if (is_qk)
+                    mbar_wait(barS + 8 * (t % kSBufs), (uint32_t)((t / kSBufs) & 1), p.err);
+                else
+                    mbar_wait(barOP + 8 * (t & 1), (uint32_t)((t >> 1) & 1), p.err);
             }
         }
         __syncwarp();
