@@ -342,6 +342,25 @@ class DecodeStep:
                        w.scale, w.partition_tokens, self.ws, flags=self.pa.PA_DECODE_EARLY_METADATA)
 
 
+def rank_workload(name: str, rank: int) -> wl.Workload:
+    """The batch one rank decodes: every rank its own Llama-shaped batch (same
+    shapes, its own lengths, placement and values: weak scaling); the other
+    workloads are the same on every rank."""
+    if name == "llama70b_decode":
+        return wl.CONFIGS[name](seed=wl.SEED_BASE + 1 + 1000 * rank)
+    return wl.CONFIGS[name]()
+
+
+def reduce_max(values, world: int, device) -> list:
+    """Element-wise maximum of each rank's timings over all ranks (the job's
+    time is its slowest rank's); a plain list on one rank."""
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def run_ours(args, world, rank, local):
     import paged_kv_cache_167_gb300 as pa
 
@@ -350,8 +369,7 @@ def run_ours(args, world, rank, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    w = wl.CONFIGS[args.config](seed=wl.SEED_BASE + 1 + 1000 * rank) if args.config == "llama70b_decode" \
-        else wl.CONFIGS[args.config]()
+    w = rank_workload(args.config, rank)
     tensors = wl.make_tensors(w, "cpu")
     step = DecodeStep(pa, w, dev, tensors, layers=args.layers)
     stream = torch.cuda.current_stream()
@@ -459,12 +477,9 @@ def run_ours(args, world, rank, local):
     prefill = None if args.no_prefill else measure_prefill(pa, dev, flush_read)
     swap = measure_swap(pa, step)
 
-    elapsed = torch.tensor([total_ms, e2e_s * 1e3, decode_total_ms / K, sum(wstep_ms), sum(flushed_ms),
-                            float(np.mean(flushed_decode_ms))], dtype=torch.float64, device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms, decode_avg_ms, wtotal_ms, ftotal_ms, fdecode_ms = elapsed.tolist()
+    total_ms, e2e_ms, decode_avg_ms, wtotal_ms, ftotal_ms, fdecode_ms = reduce_max(
+        [total_ms, e2e_s * 1e3, decode_total_ms / K, sum(wstep_ms), sum(flushed_ms), float(np.mean(flushed_decode_ms))],
+        world, dev)
 
     if rank != 0:
         if world > 1:
