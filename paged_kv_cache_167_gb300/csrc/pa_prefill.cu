@@ -42,8 +42,9 @@
 //    columns it read (tcgen05.st, two bf16 per column), from where P.V takes
 //    its A operand, and sums the fp32 probabilities into l.  The S buffer is
 //    written again only by Q.K(t + 3), which the MMA lane issues after P.V(t).
-//  * K and V rings of two stages each; a K slot is refilled once its Q.K MMA
-//    has completed, a V slot once its P.V MMA has.
+//  * K and V rings of three stages each (Q and six 32 KiB tiles fill 224 KiB
+//    of shared memory); a K slot is refilled once its Q.K MMA has completed,
+//    a V slot once its P.V MMA has.
 //  * Every wait is bounded; on expiry the kernel records PA_DEVERR_TIMEOUT,
 //    waits (bounded) for its outstanding work and frees its tensor memory.
 #include <cuda.h>
@@ -69,9 +70,13 @@ constexpr int kD = 128;                     // head_dim
 constexpr uint32_t kHalf = 128u * 128u;     // one [128 rows][64 bf16] swizzled half tile, bytes
 constexpr uint32_t kTile = 2u * kHalf;      // [2 halves][128 rows][128 B]
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTile;   // 2 stages, [half][128 keys][128 B]
-constexpr uint32_t kOffV = kOffK + 2 * kTile; // 2 stages, [block][half][16 keys][128 B]
-constexpr uint32_t kOffX = kOffV + 2 * kTile; // [2 halves][128 rows] fp32 exchange
+#ifndef PA_PREFILL_KV_STAGES
+#define PA_PREFILL_KV_STAGES 3
+#endif
+constexpr int kKV = PA_PREFILL_KV_STAGES;    // K and V ring depth
+constexpr uint32_t kOffK = kOffQ + kTile;   // kKV stages, [half][128 keys][128 B]
+constexpr uint32_t kOffV = kOffK + kKV * kTile; // kKV stages, [block][half][16 keys][128 B]
+constexpr uint32_t kOffX = kOffV + kKV * kTile; // [2 halves][128 rows] fp32 exchange
 constexpr uint32_t kOffBar = kOffX + 1024;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // + alignment slack
 constexpr int kSBufs = 3;                   // S accumulators in tensor memory
@@ -238,12 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
     float *xch = reinterpret_cast<float *>(gbase + kOffX);
     const uint32_t barQ = base + kOffBar;
-    // barriers: Q | K[2] | V[2] | S[3] | S free[3] | P[2] | P.V done[2] | drain (P.V, Q.K issuers) |
+    // barriers: Q | K[kKV] | V[kKV] | S[3] | S free[3] | P[2] | P.V done[2] | drain (P.V, Q.K issuers) |
     // P.V done per S buffer[3]
-    const uint32_t barK = barQ + 8, barV = barQ + 24, barS = barQ + 40, barSfree = barQ + 64, barP = barQ + 88,
-                   barOP = barQ + 104, barEnd = barQ + 120, barEndQk = barQ + 128, barSdone = barQ + 136;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 160);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffBar + 164);
+    const uint32_t barK = barQ + 8, barV = barK + 8 * kKV, barS = barV + 8 * kKV, barSfree = barS + 24,
+                   barP = barSfree + 24, barOP = barP + 16, barEnd = barOP + 16, barEndQk = barEnd + 8,
+                   barSdone = barEndQk + 8;
+    constexpr int kNumBars = 1 + 2 * kKV + 3 + 3 + 2 + 2 + 2 + 3;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 8 * kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffBar + 8 * kNumBars + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
@@ -256,9 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        const uint32_t counts[20] = {1, 1, 1, 1, 1, 1, 1, 1, 256, 256, 256, 256, 256, 1, 1, 1, 1, 1, 1, 1};
-        for (int i = 0; i < 20; ++i)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(barQ + 8 * i), "r"(counts[i]) : "memory");
+        for (int i = 0; i < kNumBars; ++i) {
+            const uint32_t b = barQ + 8 * i;
+            const bool softmax_arrivals = (b >= barSfree && b < barOP);   // S free[3] and P[2]: 256 threads
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(softmax_arrivals ? 256u : 1u)
+                         : "memory");
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -297,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int t = 0; t < n_tiles; ++t) {
             if (*abort_flag) break;
-            const int st = t & 1;
+            const int st = t % kKV;
             int id = (int)p.num_blocks;   // out-of-bounds coordinate: zero fill
             if (lane < NBT) {
                 const int bi = t * NBT + lane;
@@ -307,10 +317,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else id = v;
                 }
             }
-            if (t >= 2) {   // the slot's previous tile has been consumed by its MMA
-                const uint32_t free_bar = is_k ? barS + 8 * ((t - 2) % kSBufs) : barOP + 8 * st;
-                const uint32_t par = is_k ? (uint32_t)(((t - 2) / kSBufs) & 1) : (uint32_t)(((t - 2) >> 1) & 1);
-                ok = __all_sync(0xffffffffu, mbar_wait(free_bar, par, p.err));
+            if (t >= kKV) {   // the slot's previous tile has been consumed by its MMAs
+                // (Q.K for a K slot, P.V for a V slot; the next completion of either
+                // barrier needs the copy issued below, so its phase cannot be lapped)
+                const int tp = t - kKV;
+                const uint32_t free_bar = (is_k ? barS : barSdone) + 8 * (tp % kSBufs);
+                ok = __all_sync(0xffffffffu, mbar_wait(free_bar, (uint32_t)((tp / kSBufs) & 1), p.err));
                 if (!ok) {
                     *abort_flag = 1;
                     break;
@@ -330,8 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             issued = t + 1;
         }
         if (!ok || *abort_flag) {
-            // wait (bounded) for this warp's last two copies before the memory is released
-            for (int t = max(0, issued - 2); t < issued; ++t) mbar_wait(bar0 + 8 * (t & 1), (uint32_t)((t >> 1) & 1), p.err);
+            // wait (bounded) for this warp's copies still in flight before the memory is released
+            for (int t = max(0, issued - kKV); t < issued; ++t)
+                mbar_wait(bar0 + 8 * (t % kKV), (uint32_t)((t / kKV) & 1), p.err);
         }
         __syncwarp();
     } else if (warp == kMmaWarp || warp == kQkWarp) {
@@ -355,8 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (is_qk) {
                 if (wait(barQ, 0)) {
                     for (int t = 0; t < n_tiles && ok && !*abort_flag; ++t) {
-                        const int st = t & 1, sb = t % kSBufs;
-                        if (!wait(barK + 8 * st, (uint32_t)((t >> 1) & 1))) break;
+                        const int st = t % kKV, sb = t % kSBufs;
+                        if (!wait(barK + 8 * st, (uint32_t)((t / kKV) & 1))) break;
                         // S buffer sb held P(t - 3): its P.V must have completed (P.V(t)
                         // cannot complete before this Q.K, so the phase cannot be lapped)
                         if (t >= kSBufs && !wait(barSdone + 8 * sb, (uint32_t)(((t - kSBufs) / kSBufs) & 1))) break;
@@ -373,9 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 for (int t = 0; t < n_tiles && ok && !*abort_flag; ++t) {
-                    const int st = t & 1;
-                    if (!wait(barP + 8 * st, (uint32_t)((t >> 1) & 1))) break;
-                    if (!wait(barV + 8 * st, (uint32_t)((t >> 1) & 1))) break;
+                    const int st = t % kKV;
+                    if (!wait(barP + 8 * (t & 1), (uint32_t)((t >> 1) & 1))) break;
+                    if (!wait(barV + 8 * st, (uint32_t)((t / kKV) & 1))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kKeys / 16; ++kk) {
@@ -386,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 smem_desc(sV + st * kTile + v_off, BS * 128, BS >= 16 ? 1024 : kVBlock), idesc_pv,
                                 (t > 0 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(barOP + 8 * st);
+                    umma_commit(barOP + 8 * (t & 1));
                     umma_commit(barSdone + 8 * (t % kSBufs));
                     done = t + 1;
                 }
@@ -417,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 l2 = make_float2(0.f, 0.f);
         int done = 0;
         for (int t = 0; t < n_tiles; ++t) {
-            const int st = t & 1, sb = t % kSBufs;
+            const int st = t & 1, sb = t % kSBufs;   // st: P barrier of this tile
             bool ok = mbar_wait(barS + 8 * sb, (uint32_t)((t / kSBufs) & 1), p.err);
             uint32_t sr[2][32];
             if (__all_sync(0xffffffffu, ok)) {
@@ -501,11 +514,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tile0 = t * kKeys;
             const int tail_lo = seq_end - tile0, blk_end = ((seq_end + BS - 1) / BS) * BS - tile0;
             if (tail_lo > 0 && tail_lo < kKeys && (seq_end % BS) != 0) {
-                mbar_wait(barV + 8 * st, (uint32_t)((t >> 1) & 1), p.err);
+                const int sv = t % kKV;   // V ring slot of this tile
+                mbar_wait(barV + 8 * sv, (uint32_t)((t / kKV) & 1), p.err);
                 const int nrows = min(blk_end, kKeys) - tail_lo;
                 for (int idx = tid; idx < nrows * 2 * 8; idx += kSoftWarps * 32) {
                     const int rr = tail_lo + idx / 16, h = (idx / 8) & 1, c16 = idx & 7;
-                    const uint32_t addr = sV + st * kTile + (uint32_t)(rr / BS) * kVBlock + h * (kVBlock / 2) +
+                    const uint32_t addr = sV + sv * kTile + (uint32_t)(rr / BS) * kVBlock + h * (kVBlock / 2) +
                                           (uint32_t)(rr % BS) * 128u + (uint32_t)c16 * 16u;
                     asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
                 }
