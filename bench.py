@@ -194,6 +194,70 @@ def measure_paging_overhead(pa, step, K: int, warmup: int):
     return {"identity_ms": round(ms, 5)}
 
 
+def cascade_group_size(w: wl.Workload):
+    """Sequences per group that share a prefix, for the workloads built that
+    way (one prompt shared by the whole batch; the beams of a prompt)."""
+    if w.name == "shared_prefix":
+        return w.batch
+    if w.name == "beam_fork":
+        return int(w.notes["beams"])
+    return None
+
+
+def measure_cascade(pa, step, K: int, warmup: int):
+    """The same decode step as a cascade: pa_prefix_attention over each
+    group's shared prefix (read once for the group), then pa_decode_cascade
+    over the private suffixes with the new tokens stored by the call.  Back to
+    back over the layers, as the step is timed.  None for workloads without
+    shared prefixes or off the balanced schedule."""
+    w, dev = step.w, step.dev
+    gsz = cascade_group_size(w)
+    if gsz is None or not step.fused:
+        return None
+    plan = pa.cascade_plan(w.tables, w.seq_lens, gsz, w.block_size)
+    pt = torch.as_tensor(plan["prefix_tables"], device=dev)
+    pl = torch.as_tensor(plan["prefix_lens"], device=dev)
+    st = torch.as_tensor(plan["suffix_tables"], device=dev)
+    sl = torch.as_tensor(plan["suffix_lens"], device=dev)
+    max_p, max_s = int(plan["prefix_lens"].max()), max(1, int(plan["suffix_lens"].max()))
+    o_part = torch.empty(step.q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty((w.batch, w.num_q_heads), dtype=torch.float32, device=dev)
+    nbytes = pa.decode_workspace_size(step.pool, w.batch, w.num_q_heads, max_s, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
+
+    def prefix(i):
+        pa.prefix_attention(o_part, lse, step.qs[i % step.layers], step.pools[i % step.layers], pt, pl, gsz, max_p,
+                            w.scale)
+
+    def suffix(i):
+        pa.decode_cascade(step.out, step.qs[i % step.layers], step.pools[i % step.layers], st, sl, max_s, w.scale,
+                          o_part, lse, 0, ws, flags=pa.PA_DECODE_EARLY_METADATA, new_k=step.new_k, new_v=step.new_v)
+
+    def timed(calls):
+        for i in range(warmup):
+            for c in calls:
+                c(i)
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(max(2e7, 4e5 * K)))
+        e0.record(stream)
+        for i in range(K):
+            for c in calls:
+                c(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    step_ms = timed([prefix, suffix])
+    prefix_ms = timed([prefix])
+    suffix_ms = timed([suffix])
+    assert pa.get_device_error() == 0, "device error during the cascade calls"
+    return {"group_size": gsz, "groups": int(len(plan["prefix_lens"])),
+            "prefix_tokens_mean": float(plan["prefix_lens"].mean()),
+            "step_ms": round(step_ms, 5), "prefix_ms": round(prefix_ms, 5), "suffix_ms": round(suffix_ms, 5)}
+
+
 def decode_bytes(w: wl.Workload) -> int:
     """Algorithmic bytes of one decode call: every attended K and V row once,
     q and out once, the table entries used and the lengths."""
@@ -474,6 +538,7 @@ def run_ours(args, world, rank, local):
     barrier()
 
     paging = measure_paging_overhead(pa, step, K, args.warmup)
+    casc = measure_cascade(pa, step, K, args.warmup)
     prefill = None if args.no_prefill else measure_prefill(pa, dev, flush_read)
     swap = measure_swap(pa, step)
 
@@ -542,6 +607,15 @@ def run_ours(args, world, rank, local):
                                        ratio=round(decode_avg_ms / paging["identity_ms"], 4),
                                        note="the attention call on the same K/V with every sequence's blocks "
                                             "consecutive in the pool (identity placement) against random placement")
+    if casc is not None:
+        ub = unique_decode_bytes(w)
+        line["cascade"] = dict(casc, tokens_per_s=round(w.batch / (casc["step_ms"] / 1e3), 1),
+                               speedup_vs_step=round((total_ms / K) / casc["step_ms"], 3),
+                               unique_gbs=round(ub / (casc["step_ms"] / 1e3) / 1e9, 1),
+                               unique_frac=round(ub / (casc["step_ms"] / 1e3) / 1e9 / peak, 4),
+                               note="pa_prefix_attention over each group's shared prefix (tensor cores, read once "
+                                    "per group), then pa_decode_cascade over the private suffixes with the new "
+                                    "tokens stored by the call; unique bytes over the whole step")
     line["swap"] = dict(swap, note="pa_swap_blocks between the decode pool and pinned host memory, one kernel "
                                    "over the CPU-GPU link")
     if not args.no_cpu_baseline:

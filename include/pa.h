@@ -277,13 +277,91 @@ pa_status pa_copy_blocks(const pa_kv_pool *pool, const int32_t *pairs, int32_t n
  * 0 .. ctx_lens[s] + j.  The chunk's own K/V must already be in the pool
  * (pa_reshape_and_cache).  QK^T and PV run on the tcgen05 tensor cores with
  * fp32 accumulation in tensor memory.
- * Supported: head_dim 128, block_size 8, 16, 32 or 64, group size 1, 2, 4 or 8.
+ * Supported: head_dim 128, block_size 8, 16, 32 or 64, group size 1, 2, 4 or 8;
+ * at most 65,535 sequences.
  */
 pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool,
                            const int32_t *block_tables, int32_t max_blocks_per_seq,
                            const int32_t *ctx_lens, int32_t num_seqs, int32_t chunk_len,
                            int32_t num_q_heads, int32_t max_ctx_len, float scale,
                            cudaStream_t stream);
+
+/*
+ * Cascade decode, pass 1: attention of every decode query of a group of
+ * sequences over the prefix the group shares, reading the prefix's K/V once
+ * for the whole group.  [P1] shared-system-prompt paragraph: the shared
+ * prompt's blocks are held once and every sharer's table points at them;
+ * [P3] "Shared prefixes need matching computation".  The pages share the
+ * memory; reading it once is this library's design: attention over keys
+ * A u B is the log-sum-exp merge of attention over A and over B.
+ *   o_part        device, [num_groups][group_size][num_q_heads][d] fp32, 16-B
+ *                 aligned: each row's softmax-weighted V over the prefix
+ *   lse           device, [num_groups][group_size][num_q_heads] fp32: the row's
+ *                 log(sum_t exp(scale * q.K_t)) over the prefix (natural log;
+ *                 -inf and o_part 0 when the prefix is empty)
+ *   q             device, [num_groups][group_size][num_q_heads][d] bf16: the
+ *                 decode batch's q, its sequences ordered group by group
+ *   prefix_tables device, [num_groups][max_prefix_blocks] int32: the group's
+ *                 shared blocks
+ *   prefix_lens   device, [num_groups] int32, each in [0, max_prefix_len]
+ *   max_prefix_len host bound, <= max_prefix_blocks * block_size
+ *   scale         as pa_prefill_chunk
+ * Every query of group i attends all prefix_lens[i] keys (no causal mask: the
+ * prefix precedes every query).  Runs the pa_prefill_chunk kernel (tcgen05,
+ * fp32 accumulation) without its mask; same supported shapes.  At most 65,535
+ * groups.  An out-of-range length or table entry raises the device error bits
+ * as prefill does.
+ */
+pa_status pa_prefix_attention(float *o_part, float *lse, const void *q, const pa_kv_pool *pool,
+                              const int32_t *prefix_tables, int32_t max_prefix_blocks,
+                              const int32_t *prefix_lens, int32_t num_groups, int32_t group_size,
+                              int32_t num_q_heads, int32_t max_prefix_len, float scale,
+                              cudaStream_t stream);
+
+/*
+ * Host planning of a cascade decode over groups of group_size consecutive
+ * sequences (all arrays host memory).  For each group the prefix is the
+ * longest run of leading table entries that every member holds in common,
+ * in whole blocks, and at most floor((min length - 1) / block_size) blocks so
+ * that every member keeps at least one token of its own (the token being
+ * decoded is then always in the suffix).
+ *   tables         [num_seqs][max_blocks] int32; seq_lens [num_seqs]
+ *   prefix_tables  out [num_seqs / group_size][max_blocks]: the shared ids, then -1
+ *   prefix_lens    out [num_seqs / group_size]: shared blocks * block_size
+ *   suffix_tables  out [num_seqs][max_blocks]: each row's ids after the prefix, then -1
+ *   suffix_lens    out [num_seqs]: seq_lens[s] - the group's prefix length
+ * PA_ERR_INVALID_ARG when num_seqs is not a multiple of group_size, a size is
+ * not positive, or a length is negative or above max_blocks * block_size.
+ */
+pa_status pa_cascade_plan(const int32_t *tables, int32_t max_blocks, const int32_t *seq_lens,
+                          int32_t num_seqs, int32_t group_size, int32_t block_size,
+                          int32_t *prefix_tables, int32_t *prefix_lens, int32_t *suffix_tables,
+                          int32_t *suffix_lens);
+
+/*
+ * Cascade decode, pass 2: pa_decode_ex over each sequence's private suffix,
+ * with pass 1's (prefix_o, prefix_lse) folded into every output row as one
+ * more partial (weight exp(lse - M) against the suffix's own sum).  The
+ * result is attention over prefix and suffix together.
+ *   suffix_tables  device, [num_seqs][max_blocks_per_seq] int32: the blocks
+ *                  after the shared prefix (the prefix must be whole blocks,
+ *                  so suffix position 0 is offset 0 of suffix_tables[s][0])
+ *   suffix_lens    device, [num_seqs] int32: tokens after the prefix (0: the
+ *                  output is the prefix term alone)
+ *   max_suffix_len host bound on every suffix_lens[s]
+ *   prefix_o, prefix_lse  device, [num_seqs][num_q_heads]([d]) fp32 as written
+ *                  by pa_prefix_attention (prefix_o 16-B aligned); both required
+ *   new_k, new_v, flags   as pa_decode_ex, positions counted in the suffix
+ * All other arguments, the workspace and the errors as pa_decode_ex.  The same
+ * scale must be passed to both passes.
+ */
+pa_status pa_decode_cascade(void *out, const void *q, const pa_kv_pool *pool,
+                            const int32_t *suffix_tables, int32_t max_blocks_per_seq,
+                            const int32_t *suffix_lens, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t max_suffix_len, float scale, int32_t partition_tokens,
+                            void *workspace, size_t workspace_bytes, const float *prefix_o,
+                            const float *prefix_lse, const void *new_k, const void *new_v,
+                            uint32_t flags, cudaStream_t stream);
 
 /*
  * Reads (and, if clear != 0, resets) the current device's error word after

@@ -106,6 +106,7 @@ class Oracle:
             "orc_capacity": (I32, [P, I64, I64, I64, I64, I64, I64, P]),
             "orc_paged_decode_rows": (None, [P, P, P, G, P, I64, P, I64, D, P, I64]),
             "orc_paged_decode": (None, [P, P, P, G, P, I64, P, I64, I64, D]),
+            "orc_paged_decode_lse": (None, [P, P, P, P, G, P, I64, P, I64, I64, D]),
             "orc_prefill_rows": (None, [P, P, P, G, P, I64, P, I64, I64, D, P, I64]),
             "orc_prefill": (None, [P, P, P, G, P, I64, P, I64, I64, I64, D]),
         }
@@ -204,6 +205,19 @@ class Oracle:
                                         _ptr(tables), tables.shape[1], _ptr(seq_lens),
                                         num_q_heads, float(scale), _ptr(rows), rows.shape[0])
         return out
+
+    def paged_decode_lse(self, q: np.ndarray, pool: np.ndarray, geom: PoolGeom, tables, seq_lens,
+                         num_q_heads: int, scale: float):
+        """Decode attention with each row's log-sum-exp log(sum_t exp(scale q.K_t)):
+        returns (out fp64 [B][Hq][d], lse fp64 [B][Hq]; -inf with no keys)."""
+        q, pool, tables, seq_lens = _u16(q), _u16(pool), _i32(tables), _i32(seq_lens)
+        B = seq_lens.shape[0]
+        out = np.empty((B, num_q_heads, geom.head_dim), dtype=np.float64)
+        lse = np.empty((B, num_q_heads), dtype=np.float64)
+        self._lib.orc_paged_decode_lse(_ptr(out), _ptr(lse), _ptr(q), _ptr(pool), ctypes.byref(geom),
+                                       _ptr(tables), tables.shape[1], _ptr(seq_lens), B, num_q_heads,
+                                       float(scale))
+        return out, lse
 
     def prefill(self, q: np.ndarray, pool: np.ndarray, geom: PoolGeom, tables, ctx_lens,
                 num_q_heads: int, scale: float, rows: Optional[np.ndarray] = None) -> np.ndarray:

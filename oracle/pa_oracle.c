@@ -186,13 +186,18 @@ void orc_swap_blocks(uint16_t *pool, const orc_pool *p, uint16_t *host, const in
 /* Attention of one query row over the first n_keys positions of one
  * sequence, kv-head kvh.  Step 1 gathers K and V position by position
  * through the table (the conceptual lookup code); step 2 is standard scaled
- * dot-product attention on the gathered rows.  out is [d]. */
-static void attend_row(double *out, const uint16_t *q_row, const uint16_t *pool, const orc_pool *p,
-                       const int32_t *table_row, int64_t n_keys, int64_t kvh, double scale)
+ * dot-product attention on the gathered rows.  out is [d].  When lse is not
+ * NULL it receives log(sum_t exp(x_t)), the log of the softmax denominator
+ * (-inf over zero keys). */
+static void attend_row(double *out, double *lse, const uint16_t *q_row, const uint16_t *pool,
+                       const orc_pool *p, const int32_t *table_row, int64_t n_keys, int64_t kvh,
+                       double scale)
 {
     const int64_t d = p->head_dim, b = p->block_size;
     for (int64_t i = 0; i < d; ++i)
         out[i] = 0.0;
+    if (lse)
+        *lse = -INFINITY;
     if (n_keys <= 0)
         return;
 
@@ -231,6 +236,9 @@ static void attend_row(double *out, const uint16_t *q_row, const uint16_t *pool,
         l += x[t];
     }
 
+    if (lse)
+        *lse = m + log(l);
+
     /* out = sum_t w_t V_t */
     for (int64_t t = 0; t < n_keys; ++t)
         for (int64_t i = 0; i < d; ++i)
@@ -256,7 +264,7 @@ void orc_paged_decode_rows(double *out, const uint16_t *q, const uint16_t *pool,
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t r = 0; r < n_rows; ++r) {
         int64_t s = rows[2 * r], h = rows[2 * r + 1];
-        attend_row(out + r * d, q + (s * num_q_heads + h) * d, pool, p, tables + s * max_blocks,
+        attend_row(out + r * d, NULL, q + (s * num_q_heads + h) * d, pool, p, tables + s * max_blocks,
                    seq_lens[s], h / group, scale);
     }
 }
@@ -271,8 +279,26 @@ void orc_paged_decode(double *out, const uint16_t *q, const uint16_t *pool, cons
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
     for (int64_t s = 0; s < num_seqs; ++s)
         for (int64_t h = 0; h < num_q_heads; ++h)
-            attend_row(out + (s * num_q_heads + h) * d, q + (s * num_q_heads + h) * d, pool, p,
+            attend_row(out + (s * num_q_heads + h) * d, NULL, q + (s * num_q_heads + h) * d, pool, p,
                        tables + s * max_blocks, seq_lens[s], h / group, scale);
+}
+
+/* Decode attention of all rows with each row's log-sum-exp: out [B][Hq][d],
+ * lse [B][Hq].  Attention over keys A followed by keys B equals the
+ * weighted mean of the attention over A and over B with weights
+ * exp(lse_A) and exp(lse_B); a cascade over a shared prefix rests on it. */
+void orc_paged_decode_lse(double *out, double *lse, const uint16_t *q, const uint16_t *pool,
+                          const orc_pool *p, const int32_t *tables, int64_t max_blocks,
+                          const int32_t *seq_lens, int64_t num_seqs, int64_t num_q_heads, double scale)
+{
+    const int64_t d = p->head_dim;
+    const int64_t group = num_q_heads / p->num_kv_heads;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t s = 0; s < num_seqs; ++s)
+        for (int64_t h = 0; h < num_q_heads; ++h)
+            attend_row(out + (s * num_q_heads + h) * d, lse + s * num_q_heads + h,
+                       q + (s * num_q_heads + h) * d, pool, p, tables + s * max_blocks, seq_lens[s],
+                       h / group, scale);
 }
 
 /* Chunked prefill against paged context, for selected (s, j, h) rows.
@@ -290,7 +316,7 @@ void orc_prefill_rows(double *out, const uint16_t *q, const uint16_t *pool, cons
     for (int64_t r = 0; r < n_rows; ++r) {
         int64_t s = rows[3 * r], j = rows[3 * r + 1], h = rows[3 * r + 2];
         int64_t visible = (int64_t)ctx_lens[s] + j + 1;
-        attend_row(out + r * d, q + ((s * chunk + j) * num_q_heads + h) * d, pool, p,
+        attend_row(out + r * d, NULL, q + ((s * chunk + j) * num_q_heads + h) * d, pool, p,
                    tables + s * max_blocks, visible, h / group, scale);
     }
 }
@@ -308,7 +334,7 @@ void orc_prefill(double *out, const uint16_t *q, const uint16_t *pool, const orc
             for (int64_t h = 0; h < num_q_heads; ++h) {
                 int64_t visible = (int64_t)ctx_lens[s] + j + 1;
                 int64_t row = (s * chunk + j) * num_q_heads + h;
-                attend_row(out + row * d, q + row * d, pool, p, tables + s * max_blocks, visible,
+                attend_row(out + row * d, NULL, q + row * d, pool, p, tables + s * max_blocks, visible,
                            h / group, scale);
             }
 }

@@ -256,6 +256,41 @@ def custom(lens, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size:
                     new_positions=seq[has].astype(np.int64) - 1, partition_tokens=partition_tokens)
 
 
+def shared_groups(prefix_lens, suffix_lens, group_size: int, num_q_heads: int, num_kv_heads: int,
+                  head_dim: int = 128, block_size: int = 16, seed: int = SEED_BASE + 200,
+                  name: str = "shared_groups") -> Workload:
+    """Decode batch of len(prefix_lens) groups of ``group_size`` consecutive
+    sequences.  The tables of group i start with the same prefix_lens[i] // b
+    physical blocks (prefix_lens are whole blocks); sequence k of the group
+    then holds suffix_lens[i * group_size + k] tokens in private blocks.
+    Random placement, a pool with spare blocks, scale 1/sqrt(head_dim)."""
+    rng = np.random.default_rng(seed)
+    b = block_size
+    prefix_lens = [int(x) for x in prefix_lens]
+    suffix_lens = [int(x) for x in suffix_lens]
+    assert all(p % b == 0 for p in prefix_lens) and len(suffix_lens) == len(prefix_lens) * group_size
+    B = len(suffix_lens)
+    lens = np.asarray([prefix_lens[s // group_size] + suffix_lens[s] for s in range(B)], dtype=np.int32)
+    need = sum(p // b for p in prefix_lens) + sum(_blocks_for(x, b) for x in suffix_lens)
+    nb = max(8, 2 * need + 3)
+    ids = iter(rng.permutation(nb).astype(np.int32).tolist())
+    width = max(1, max(_blocks_for(int(L), b) for L in lens))
+    tables = np.full((B, width), -1, dtype=np.int32)
+    for gi, plen in enumerate(prefix_lens):
+        shared = [next(ids) for _ in range(plen // b)]
+        for k in range(group_size):
+            s = gi * group_size + k
+            own = [next(ids) for _ in range(_blocks_for(suffix_lens[s], b))]
+            row = shared + own
+            tables[s, :len(row)] = row
+    has = lens > 0
+    return Workload(name, "decode", num_q_heads, num_kv_heads, head_dim, b, nb, 1.0 / math.sqrt(head_dim),
+                    lens, tables, _referenced(tables), seed,
+                    new_seq_idx=np.nonzero(has)[0].astype(np.int32),
+                    new_positions=lens[has].astype(np.int64) - 1,
+                    notes={"prefix_lens": np.asarray(prefix_lens, np.int32), "group_size": group_size})
+
+
 CONFIGS = {
     "tiny": tiny,
     "tiny_page_example": tiny_page_example,

@@ -59,6 +59,10 @@ SIGNATURES = {
     "pa_copy_blocks": (_I32, [_POOL, _P, _I32, _P]),
     "pa_swap_blocks": (_I32, [_POOL, _P, _I64, _P, _I32, _I32, _P]),
     "pa_prefill_chunk": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _I32, _F, _P]),
+    "pa_prefix_attention": (_I32, [_P, _P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _I32, _F, _P]),
+    "pa_decode_cascade": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _P, _P, _P, _P,
+                                 _U32, _P]),
+    "pa_cascade_plan": (_I32, [_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P, _P]),
     "pa_get_device_error": (_I32, [ctypes.POINTER(_U32), _I32, _P]),
     "pa_block_layout": (_I32, [_I64, _I32, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "pa_slot_mapping": (_I32, [_P, _P, _I32, _I32, _P, _P, _I64, _I32, _I64]),
@@ -282,6 +286,80 @@ def prefill_chunk(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_
                                   ctypes.byref(desc), _dev(block_tables, torch.int32, "block_tables"),
                                   block_tables.shape[1], _dev(ctx_lens, torch.int32, "ctx_lens"), B, C, Hq,
                                   int(max_ctx_len), float(scale), _stream(stream)), "pa_prefill_chunk")
+
+
+def prefix_attention(o_part: torch.Tensor, lse: torch.Tensor, q: torch.Tensor, pool: torch.Tensor,
+                     prefix_tables: torch.Tensor, prefix_lens: torch.Tensor, group_size: int, max_prefix_len: int,
+                     scale: float, layer: Optional[int] = None, stream=None) -> None:
+    """pa_prefix_attention: q [num_groups * group_size][Hq][d] bf16 (sequences
+    group by group); o_part fp32 of q's shape, lse fp32 [B][Hq]."""
+    desc = pool_desc(pool, layer)
+    B, Hq, _ = q.shape
+    if group_size <= 0 or B % group_size != 0:
+        raise ValueError("the batch must be whole groups")
+    G = B // group_size
+    if o_part.shape != q.shape or tuple(lse.shape) != (B, Hq):
+        raise ValueError("o_part must have q's shape and lse [B][Hq]")
+    if prefix_tables.dim() != 2 or prefix_tables.shape[0] != G or prefix_lens.numel() != G:
+        raise ValueError("prefix_tables / prefix_lens do not match the groups")
+    _check(lib().pa_prefix_attention(_dev(o_part, torch.float32, "o_part"), _dev(lse, torch.float32, "lse"),
+                                     _dev(q, torch.bfloat16, "q"), ctypes.byref(desc),
+                                     _dev(prefix_tables, torch.int32, "prefix_tables"), prefix_tables.shape[1],
+                                     _dev(prefix_lens, torch.int32, "prefix_lens"), G, int(group_size), Hq,
+                                     int(max_prefix_len), float(scale), _stream(stream)), "pa_prefix_attention")
+
+
+def decode_cascade(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, suffix_tables: torch.Tensor,
+                   suffix_lens: torch.Tensor, max_suffix_len: int, scale: float, prefix_o: torch.Tensor,
+                   prefix_lse: torch.Tensor, partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                   layer: Optional[int] = None, stream=None, flags: int = 0, new_k: Optional[torch.Tensor] = None,
+                   new_v: Optional[torch.Tensor] = None) -> None:
+    """pa_decode_cascade: decode over each sequence's suffix with the prefix
+    partial (prefix_attention's o_part and lse) folded into every row."""
+    desc = pool_desc(pool, layer)
+    B, Hq, _ = q.shape
+    if out.shape != q.shape or prefix_o.shape != q.shape or tuple(prefix_lse.shape) != (B, Hq):
+        raise ValueError("out and prefix_o must have q's shape, prefix_lse [B][Hq]")
+    if suffix_tables.dim() != 2 or suffix_tables.shape[0] != B or suffix_lens.numel() != B:
+        raise ValueError("suffix_tables / suffix_lens do not match the batch")
+    for name, t in (("new_k", new_k), ("new_v", new_v)):
+        if t is not None and (t.dim() != 3 or t.shape[0] != B or t.shape[1:] != (desc.num_kv_heads, desc.head_dim)):
+            raise ValueError(f"{name} must be [num_seqs][num_kv_heads][head_dim]")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, torch.uint8, "workspace"), workspace.numel()
+    nk = _dev(new_k, torch.bfloat16, "new_k") if new_k is not None else ctypes.c_void_p(0)
+    nv = _dev(new_v, torch.bfloat16, "new_v") if new_v is not None else ctypes.c_void_p(0)
+    _check(lib().pa_decode_cascade(_dev(out, torch.bfloat16, "out"), _dev(q, torch.bfloat16, "q"),
+                                   ctypes.byref(desc), _dev(suffix_tables, torch.int32, "suffix_tables"),
+                                   suffix_tables.shape[1], _dev(suffix_lens, torch.int32, "suffix_lens"), B, Hq,
+                                   int(max_suffix_len), float(scale), int(partition_tokens), ws_ptr, ws_bytes,
+                                   _dev(prefix_o, torch.float32, "prefix_o"),
+                                   _dev(prefix_lse, torch.float32, "prefix_lse"), nk, nv, int(flags),
+                                   _stream(stream)), "pa_decode_cascade")
+
+
+def cascade_plan(tables, seq_lens, group_size: int, block_size: int) -> dict:
+    """pa_cascade_plan on host arrays: the prefix each group of ``group_size``
+    consecutive sequences shares (whole blocks, leaving every member at least
+    one token) and the suffixes.  Returns numpy int32 arrays prefix_tables
+    [G][W], prefix_lens [G], suffix_tables [B][W], suffix_lens [B]."""
+    t = np.ascontiguousarray(np.asarray(tables, dtype=np.int32))
+    L = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32).reshape(-1))
+    if t.ndim != 2 or t.shape[0] != L.shape[0]:
+        raise ValueError("tables must be [B][W] with one length per row")
+    B, W = t.shape
+    if group_size <= 0 or B % group_size != 0:
+        raise ValueError("the batch must be whole groups")
+    G = B // group_size
+    pt = np.empty((G, W), np.int32)
+    pl = np.empty(G, np.int32)
+    st = np.empty((B, W), np.int32)
+    sl = np.empty(B, np.int32)
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    _check(lib().pa_cascade_plan(ptr(t), W, ptr(L), B, int(group_size), int(block_size), ptr(pt), ptr(pl), ptr(st),
+                                 ptr(sl)), "pa_cascade_plan")
+    return {"prefix_tables": pt, "prefix_lens": pl, "suffix_tables": st, "suffix_lens": sl}
 
 
 def get_device_error(clear: bool = True, stream=None) -> int:

@@ -181,11 +181,13 @@ pa_status pa_decode(void *out, const void *q, const pa_kv_pool *pool, const int3
                         stream);
 }
 
-pa_status pa_decode_ex(void *out, const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
-                       int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
-                       int32_t max_seq_len, float scale, int32_t partition_tokens, void *workspace,
-                       size_t workspace_bytes, const void *new_k, const void *new_v, uint32_t flags,
-                       cudaStream_t stream) {
+namespace {
+
+pa_status decode_impl(void *out, const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                      int32_t max_seq_len, float scale, int32_t partition_tokens, void *workspace,
+                      size_t workspace_bytes, const float *prefix_o, const float *prefix_lse, const void *new_k,
+                      const void *new_v, uint32_t flags, cudaStream_t stream) {
     if ((flags & ~PA_DECODE_EARLY_METADATA) != 0) return PA_ERR_INVALID_ARG;
     if ((new_k == nullptr) != (new_v == nullptr)) return PA_ERR_INVALID_ARG;
     if (new_k && (!aligned16(new_k) || !aligned16(new_v))) return PA_ERR_INVALID_ARG;
@@ -223,6 +225,8 @@ pa_status pa_decode_ex(void *out, const void *q, const pa_kv_pool *pool, const i
     a.stream_k = plan.stream_k;
     a.num_ctas = plan.num_ctas;
     a.early_meta = (flags & PA_DECODE_EARLY_METADATA) != 0;
+    a.pre_o = prefix_o;
+    a.pre_lse = prefix_lse;
     if (new_k) {
         if (plan.stream_k) {   // the stream-K kernel stores each last token itself
             a.new_k = new_k;
@@ -234,6 +238,32 @@ pa_status pa_decode_ex(void *out, const void *q, const pa_kv_pool *pool, const i
         }
     }
     return launch_decode(a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+pa_status pa_decode_ex(void *out, const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
+                       int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                       int32_t max_seq_len, float scale, int32_t partition_tokens, void *workspace,
+                       size_t workspace_bytes, const void *new_k, const void *new_v, uint32_t flags,
+                       cudaStream_t stream) {
+    return decode_impl(out, q, pool, block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_q_heads,
+                       max_seq_len, scale, partition_tokens, workspace, workspace_bytes, nullptr, nullptr, new_k,
+                       new_v, flags, stream);
+}
+
+pa_status pa_decode_cascade(void *out, const void *q, const pa_kv_pool *pool, const int32_t *suffix_tables,
+                            int32_t max_blocks_per_seq, const int32_t *suffix_lens, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t max_suffix_len, float scale, int32_t partition_tokens,
+                            void *workspace, size_t workspace_bytes, const float *prefix_o,
+                            const float *prefix_lse, const void *new_k, const void *new_v, uint32_t flags,
+                            cudaStream_t stream) {
+    if (num_seqs > 0 && (!prefix_o || !prefix_lse || !aligned16(prefix_o) ||
+                         (reinterpret_cast<uintptr_t>(prefix_lse) % 4) != 0))
+        return PA_ERR_INVALID_ARG;
+    return decode_impl(out, q, pool, suffix_tables, max_blocks_per_seq, suffix_lens, num_seqs, num_q_heads,
+                       max_suffix_len, scale, partition_tokens, workspace, workspace_bytes, prefix_o, prefix_lse,
+                       new_k, new_v, flags, stream);
 }
 
 pa_status pa_copy_blocks(const pa_kv_pool *pool, const int32_t *pairs, int32_t num_pairs, cudaStream_t stream) {
@@ -279,6 +309,7 @@ pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool, con
     if (!prefill_supported(view.head_dim, num_q_heads / view.num_kv_heads, view.block_size))
         return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0 || chunk_len == 0) return PA_OK;
+    if (num_seqs > 65535 || (int64_t)num_seqs * chunk_len > (int64_t)INT32_MAX) return PA_ERR_INVALID_ARG;
     if (!out || !q || !block_tables || !ctx_lens || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
     if ((int64_t)max_ctx_len + chunk_len > (int64_t)max_blocks_per_seq * view.block_size) return PA_ERR_INVALID_ARG;
@@ -294,6 +325,42 @@ pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool, con
     a.num_q_heads = num_q_heads;
     a.max_ctx_len = max_ctx_len;
     a.scale = scale;
+    return launch_prefill(a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_prefix_attention(float *o_part, float *lse, const void *q, const pa_kv_pool *pool,
+                              const int32_t *prefix_tables, int32_t max_prefix_blocks, const int32_t *prefix_lens,
+                              int32_t num_groups, int32_t group_size, int32_t num_q_heads, int32_t max_prefix_len,
+                              float scale, cudaStream_t stream) {
+    PoolView view;
+    pa_status st = resolve_pool(pool, &view);
+    if (st != PA_OK) return st;
+    if (num_groups < 0 || group_size < 0 || num_q_heads <= 0 || max_prefix_len < 0) return PA_ERR_INVALID_ARG;
+    if (num_q_heads % view.num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (!prefill_supported(view.head_dim, num_q_heads / view.num_kv_heads, view.block_size))
+        return PA_ERR_UNSUPPORTED;
+    if (num_groups == 0 || group_size == 0) return PA_OK;
+    if (!o_part || !lse || !q || !prefix_tables || !prefix_lens || max_prefix_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (!aligned16(o_part) || (reinterpret_cast<uintptr_t>(lse) % 4) != 0 || !aligned16(q)) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
+    if ((int64_t)max_prefix_len > (int64_t)max_prefix_blocks * view.block_size) return PA_ERR_INVALID_ARG;
+    // grid z is the group; the row coordinate group * group_size + j is an int32
+    if (num_groups > 65535 || (int64_t)num_groups * group_size > (int64_t)INT32_MAX) return PA_ERR_INVALID_ARG;
+    PrefillArgs a;
+    a.out = nullptr;
+    a.q = q;
+    a.pool = view;
+    a.tables = prefix_tables;
+    a.max_blocks = max_prefix_blocks;
+    a.ctx_lens = prefix_lens;
+    a.num_seqs = num_groups;
+    a.chunk_len = group_size;
+    a.num_q_heads = num_q_heads;
+    a.max_ctx_len = max_prefix_len;
+    a.scale = scale;
+    a.causal = false;
+    a.o_part = o_part;
+    a.lse = lse;
     return launch_prefill(a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -178,7 +178,61 @@ struct Params {
     int64_t block_stride;
     int64_t kv_stride;
     unsigned int *err;
+    // cascade: attention of each row over a shared prefix, computed apart
+    // (o normalised by its l, lse its natural-log sum of exp), folded into
+    // every final output row (nullptr: none)
+    const float *pre_o;          // [B][Hq][D]
+    const float *pre_lse;        // [B][Hq]
 };
+
+// The prefix term of one output row: its log-sum-exp and N dims of its
+// normalised output (lse = -inf: no term).  Loaded ahead of use, so that the
+// load latency hides behind other work.
+template <int N>
+struct PrefixTerm {
+    float lse;
+    float o[N];
+};
+
+template <int N>
+__device__ __forceinline__ PrefixTerm<N> load_prefix(const Params &p, size_t row, int D, int i, bool want = true) {
+    static_assert(N == 2 || N == 4, "two or four dims");
+    PrefixTerm<N> t;
+    t.lse = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < N; ++k) t.o[k] = 0.f;
+    if (want && p.pre_lse != nullptr) {
+        t.lse = __ldg(p.pre_lse + row);
+        if constexpr (N == 2) {
+            const float2 v = __ldg(reinterpret_cast<const float2 *>(p.pre_o + row * D + i));
+            t.o[0] = v.x;
+            t.o[1] = v.y;
+        } else {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(p.pre_o + row * D + i));
+            t.o[0] = v.x;
+            t.o[1] = v.y;
+            t.o[2] = v.z;
+            t.o[3] = v.w;
+        }
+    }
+    return t;
+}
+
+// Fold a prefix term into a merge in progress: acc[] holds sum_w weight_w *
+// o_w over N dims, wsum the sum of the weights, M their reference maximum
+// (log2 domain).  The prefix enters as one more record with l = 1 and
+// m = lse * log2(e).  Without a term nothing changes.
+template <int N>
+__device__ __forceinline__ void fold_prefix(const PrefixTerm<N> &t, float M, float &wsum, float (&acc)[N]) {
+    if (t.lse == -INFINITY) return;
+    const float mp = t.lse * 1.4426950408889634f;
+    const float Mn = fmaxf(M, mp);
+    const float fd = M == -INFINITY ? 0.f : fast_exp2(M - Mn);
+    const float fp = fast_exp2(mp - Mn);
+    wsum = wsum * fd + fp;
+#pragma unroll
+    for (int k = 0; k < N; ++k) acc[k] = acc[k] * fd + fp * t.o[k];
+}
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
@@ -436,14 +490,34 @@ __device__ __forceinline__ void warp_publish(WarpState<D> &st, bool has_work, in
     }
 }
 
-// Combine the kWarps warps' (m, l, o) for G heads; write bf16 rows to
-// `out_rows` (final) or fp32 partials: o normalised by l at o_base + h*o_hs,
-// (m, l) at ml_base + h*ml_hs.
+// The prefix terms of the (head, dim pair) items a thread finishes in
+// cta_combine_store: item idx = threadIdx.x + it * kWarps * 32.
 template <int D, int G>
-__device__ __forceinline__ void cta_combine_store(const float *cm, const float *cl, const float *co, bool final,
-                                                  __nv_bfloat16 *out_rows, float *o_base, size_t o_hs, float *ml_base,
-                                                  size_t ml_hs) {
-    for (int idx = threadIdx.x; idx < G * D / 2; idx += blockDim.x) {
+struct CombinePrefix {
+    static constexpr int kItems = G * D / 2;
+    static constexpr int kIt = (kItems + kWarps * 32 - 1) / (kWarps * 32);
+    PrefixTerm<2> t[kIt];
+    __device__ __forceinline__ void load(const Params &p, size_t row0, bool want) {
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int idx = threadIdx.x + it * kWarps * 32;
+            t[it] = load_prefix<2>(p, row0 + idx / (D / 2), D, (idx % (D / 2)) * 2, want && idx < kItems);
+        }
+    }
+};
+
+// Combine the kWarps warps' (m, l, o) for G heads (blockDim.x = kWarps * 32);
+// write bf16 rows to `out_rows` (final, with the prefix terms folded in) or
+// fp32 partials: o normalised by l at o_base + h*o_hs, (m, l) at ml_base + h*ml_hs.
+template <int D, int G>
+__device__ __forceinline__ void cta_combine_store(const CombinePrefix<D, G> &pre, const float *cm, const float *cl,
+                                                  const float *co, bool final, __nv_bfloat16 *out_rows, float *o_base,
+                                                  size_t o_hs, float *ml_base, size_t ml_hs) {
+    using CP = CombinePrefix<D, G>;
+#pragma unroll
+    for (int it = 0; it < CP::kIt; ++it) {
+        const int idx = threadIdx.x + it * kWarps * 32;
+        if (idx >= CP::kItems) break;
         const int h = idx / (D / 2);
         const int i = (idx % (D / 2)) * 2;
         float M = -INFINITY;
@@ -460,10 +534,13 @@ __device__ __forceinline__ void cta_combine_store(const float *cm, const float *
                 oy += ov.y * f;
             }
         }
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
         if (final) {
-            reinterpret_cast<uint32_t *>(out_rows + h * D + i)[0] = pack_bf16x2(ox * inv, oy * inv);
+            float acc[2] = {ox, oy};
+            fold_prefix<2>(pre.t[it], M, lsum, acc);
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            reinterpret_cast<uint32_t *>(out_rows + h * D + i)[0] = pack_bf16x2(acc[0] * inv, acc[1] * inv);
         } else {
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
             *reinterpret_cast<float2 *>(o_base + h * o_hs + i) = make_float2(ox * inv, oy * inv);
             if (i == 0) *reinterpret_cast<float2 *>(ml_base + h * ml_hs) = make_float2(M, lsum);
         }
@@ -504,14 +581,20 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
         // past the sequence end; with a single partition (L == 0) the output
         // is zero by the library's reading of attention over no keys.
         if (p.num_parts == 1)
-            for (int i = threadIdx.x; i < G * D / 2; i += blockDim.x)
-                reinterpret_cast<uint32_t *>(p.out + head0 * D)[i] = 0u;
+            for (int i = threadIdx.x; i < G * D / 2; i += blockDim.x) {
+                float acc[2] = {0.f, 0.f}, wsum = 0.f;
+                fold_prefix<2>(load_prefix<2>(p, head0 + i / (D / 2), D, (i % (D / 2)) * 2), -INFINITY, wsum, acc);
+                const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+                reinterpret_cast<uint32_t *>(p.out + head0 * D)[i] = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            }
         return;
     }
 
     uint32_t qf[D / 8];
     load_qf<D, G, false>(qf, p.q + head0 * D, lane);
     __syncwarp();
+    CombinePrefix<D, G> pre;   // loaded now, used after the last stage
+    pre.load(p, head0, p.num_parts == 1);
 
     const int nblk_seq = (L + BS - 1) / BS;
     const int nstages = (ntok + S::TPS - 1) / S::TPS;
@@ -603,7 +686,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
     __syncthreads();
     grid_launch_dependents();
     const size_t rowp = head0 * p.num_parts + part;
-    cta_combine_store<D, G>(cm, cl, co, p.num_parts == 1, p.out + head0 * D, p.ws_o + rowp * D,
+    cta_combine_store<D, G>(pre, cm, cl, co, p.num_parts == 1, p.out + head0 * D, p.ws_o + rowp * D,
                             (size_t)p.num_parts * D, p.ws_ml + rowp * 2, (size_t)p.num_parts * 2);
 }
 
@@ -619,6 +702,7 @@ __global__ void __launch_bounds__(G *D / 4) paged_decode_reduce_kernel(const Par
     const int np = (L + p.part_tokens - 1) / p.part_tokens;
     const size_t row = (size_t)s * p.num_q_heads + (size_t)g * G + h;
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + row * p.num_parts;
+    const PrefixTerm<4> pre = load_prefix<4>(p, row, D, i);
     float M = -INFINITY;
     for (int q = 0; q < np; ++q) M = fmaxf(M, ml[q].x);
     float wsum = 0.f;
@@ -635,8 +719,10 @@ __global__ void __launch_bounds__(G *D / 4) paged_decode_reduce_kernel(const Par
             acc.w += w * ov.w;
         }
     }
+    float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+    fold_prefix<4>(pre, M, wsum, a4);
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    uint2 packed = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    uint2 packed = make_uint2(pack_bf16x2(a4[0] * inv, a4[1] * inv), pack_bf16x2(a4[2] * inv, a4[3] * inv));
     *reinterpret_cast<uint2 *>(p.out + row * D + i) = packed;
 }
 
@@ -943,6 +1029,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
             const int s = sk->seg_s[j], g = sk->seg_g[j];
             const int L = effective_len(p, s, BS, false);
             const int ns = (L + S::TPS - 1) / S::TPS;
+            const bool complete = sk->seg_kb[j] == 0 && sk->seg_ke[j] == ns;
+            const size_t head0 = (size_t)s * p.num_q_heads + (size_t)g * G;
+            CombinePrefix<D, G> pre;   // loaded now, used at the segment's end
+            pre.load(p, head0, complete);
             const int jg = jbase + j;
             const bool qok = mbar_wait_bounded(&sk->qbar[jg & 1], (uint32_t)((jg >> 1) & 1), p.err);
             if (!__syncthreads_and(qok)) {
@@ -977,11 +1067,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
                 ok = false;
                 break;
             }
-            const bool complete = sk->seg_kb[j] == 0 && sk->seg_ke[j] == ns;
             const bool is_first = first_seg && j == 0;
             const int rec = 2 * c + (is_first ? 0 : 1);
-            const size_t head0 = (size_t)s * p.num_q_heads + (size_t)g * G;
-            cta_combine_store<D, G>(sk->cm, sk->cl, sk->co, complete, p.out + head0 * D,
+            cta_combine_store<D, G>(pre, sk->cm, sk->cl, sk->co, complete, p.out + head0 * D,
                                     p.ws_o + (size_t)rec * G * D, D, p.ws_ml + (size_t)rec * G * 2, 2);
             __syncthreads();   // scratch and this q buffer are free again
             if (tid == 0) issue_q(j + 2);
@@ -1053,8 +1141,13 @@ __global__ void __launch_bounds__(G *D / 4) paged_decode_sk_merge_kernel(const P
         }
     }
     grid_dependency_wait();
-    if (ns == 0) {
-        *reinterpret_cast<uint2 *>(p.out + row * D + i) = make_uint2(0u, 0u);
+    const PrefixTerm<4> pre = load_prefix<4>(p, row, D, i);
+    if (ns == 0) {   // no keys of its own: zero, or the prefix term alone
+        float a4[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
+        fold_prefix<4>(pre, -INFINITY, wsum, a4);
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        *reinterpret_cast<uint2 *>(p.out + row * D + i) =
+            make_uint2(pack_bf16x2(a4[0] * inv, a4[1] * inv), pack_bf16x2(a4[2] * inv, a4[3] * inv));
         return;
     }
     if (!local) {
@@ -1085,9 +1178,11 @@ __global__ void __launch_bounds__(G *D / 4) paged_decode_sk_merge_kernel(const P
             acc.w += w * ov.w;
         }
     }
+    float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+    fold_prefix<4>(pre, M, wsum, a4);
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     *reinterpret_cast<uint2 *>(p.out + row * D + i) =
-        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+        make_uint2(pack_bf16x2(a4[0] * inv, a4[1] * inv), pack_bf16x2(a4[2] * inv, a4[3] * inv));
 }
 
 // ---- launchers -----------------------------------------------------------------
@@ -1196,6 +1291,8 @@ cudaError_t launch_for_dim(const DecodeArgs &a, cudaStream_t stream) {
     prm.num_ctas = a.num_ctas;
     prm.early_meta = a.early_meta ? 1 : 0;
     prm.new_k = static_cast<const __nv_bfloat16 *>(a.new_k);
+    prm.pre_o = a.pre_o;
+    prm.pre_lse = a.pre_lse;
     prm.new_v = static_cast<const __nv_bfloat16 *>(a.new_v);
     prm.pool = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.pool.base));
     prm.block_stride = a.pool.block_stride;

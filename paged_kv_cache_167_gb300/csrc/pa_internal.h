@@ -75,6 +75,8 @@ struct DecodeArgs {
     bool early_meta = false;   // stream-K: read lengths and tables before the previous kernel completes
     const void *new_k = nullptr;   // stream-K: last token's K/V per sequence, stored before attending
     const void *new_v = nullptr;
+    const float *pre_o = nullptr;      // cascade: prefix partial [B][Hq][d] fp32 (normalised)
+    const float *pre_lse = nullptr;    // and its log-sum-exp [B][Hq]
 };
 
 // Tokens per pipeline stage of the decode kernel for a block size (the
@@ -96,6 +98,9 @@ struct PrefillArgs {
     int32_t num_q_heads;
     int32_t max_ctx_len;
     float scale;
+    bool causal = true;        // false: every query sees keys 0 .. ctx_lens[s] - 1
+    float *o_part = nullptr;   // non-null: fp32 normalised output + lse instead of out
+    float *lse = nullptr;
 };
 bool prefill_supported(int head_dim, int group, int block_size);
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);

@@ -10,6 +10,13 @@
 // sees); attn-paged-attention-mcq-hard (zenaique.com), conceptual block-lookup
 // listing (the gather belongs inside the kernel's tiling loop).
 //
+// The same kernel, without the causal mask, runs the shared-prefix pass of a
+// cascade decode: sequence s stands for a group of C sequences that share
+// their first ctx_lens[s] tokens (whole blocks, one table), its "chunk" holds
+// the C sequences' decode queries, and every query sees all ctx_lens[s] keys.
+// That pass writes fp32 output normalised by l together with each row's
+// log-sum-exp, which the decode of the private suffixes folds in.
+//
 // Design:
 //  * One CTA per 128-row M-tile of one (sequence, kv-head): row r is query
 //    j0 + r / G of head g*G + r % G, so every K/V tile staged in shared memory
@@ -82,6 +89,7 @@ constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // + alignment slack
 constexpr int kSBufs = 3;                   // S accumulators in tensor memory
 constexpr uint32_t kTmemCols = 512;         // S0, S1, S2, O (128 columns each)
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 domain
 static_assert(kSmemBytes <= 232448, "shared memory");
 
@@ -96,6 +104,9 @@ struct Params {
     int64_t num_blocks;
     float scale_log2;
     unsigned int *err;
+    int32_t causal;              // 0: every query of sequence s sees keys 0 .. ctx_lens[s] - 1
+    float *o_part;               // non-null: fp32 output normalised by l, [B][C][Hq][D], instead of out
+    float *lse;                  // with o_part: [B][C][Hq] natural-log sum of exp(scale * q.k)
 };
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -285,10 +296,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0 && mt == 0 && g == 0) raise_error(p.err, PA_DEVERR_SEQ_LEN);
         ctx = ctx < 0 ? 0 : p.max_ctx_len;
     }
-    const int seq_end = ctx + p.chunk;                         // keys 0 .. seq_end - 1 exist
+    // causal: keys 0 .. ctx + C - 1 exist and query j sees 0 .. ctx + j;
+    // otherwise keys 0 .. ctx - 1 exist and every query sees all of them
+    const int seq_end = p.causal ? ctx + p.chunk : ctx;
     const int nblk_seq = (seq_end + BS - 1) / BS;
     const int last_q = min(j0 + QPT, p.chunk) - 1;             // last valid query of this tile
-    const int n_tiles = (ctx + last_q + 1 + kKeys - 1) / kKeys;
+    const int n_tiles = ((p.causal ? ctx + last_q + 1 : ctx) + kKeys - 1) / kKeys;   // 0 only without causal
     constexpr uint32_t idesc_qk = idesc_bf16(kRows, kKeys, false);
     constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, true);
 
@@ -424,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = (warp & 3) * 32 + lane, hf = warp >> 2;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const int jr = j0 + r / G;
-        const int pos = min(ctx + jr, seq_end - 1);   // last key this row may attend
+        const int pos = p.causal ? min(ctx + jr, seq_end - 1) : seq_end - 1;   // last key this row may attend
         const float c = p.scale_log2;
         float m_ref = -INFINITY;                       // reference maximum, log2 domain
         float2 l2 = make_float2(0.f, 0.f);
@@ -529,10 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_u32(barP + 8 * st);
             done = t + 1;
         }
-        // ---- epilogue: O / l to bf16, this thread's row and key half
+        // ---- epilogue: O / l, this thread's row and key half: bf16, or fp32
+        // with the row's log-sum-exp
         const float l = l2.x;
-        const bool fin = done == n_tiles && !*abort_flag &&
-                         mbar_wait(barOP + 8 * ((n_tiles - 1) & 1), (uint32_t)(((n_tiles - 1) >> 1) & 1), p.err);
+        const bool empty = n_tiles == 0;   // no keys: O = 0, lse = -inf, tensor memory never written
+        const bool fin = empty || (done == n_tiles && !*abort_flag &&
+                                   mbar_wait(barOP + 8 * ((n_tiles - 1) & 1), (uint32_t)(((n_tiles - 1) >> 1) & 1),
+                                             p.err));
         xch[hf * 128 + r] = l;
         pair_sync(warp);
         const float lt = l + xch[(1 - hf) * 128 + r];
@@ -540,14 +556,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__all_sync(0xffffffffu, fin)) {
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
             const bool row_ok = jr < p.chunk;
-            __nv_bfloat16 *dst =
-                p.out + (((size_t)s * p.chunk + jr) * p.num_q_heads + (size_t)g * G + (r % G)) * kD + hf * 64;
+            const size_t row = ((size_t)s * p.chunk + jr) * p.num_q_heads + (size_t)g * G + (r % G);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(tO + lane_off + hf * 64 + cc * 32, o);
-                tmem_ld_wait();
-                if (row_ok) {
+                if (!empty) {
+                    tmem_ld32(tO + lane_off + hf * 64 + cc * 32, o);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                if (row_ok && p.o_part != nullptr) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + row * kD + hf * 64 + cc * 32);
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        dst[q4] = make_float4(__uint_as_float(o[q4 * 4 + 0]) * inv, __uint_as_float(o[q4 * 4 + 1]) * inv,
+                                              __uint_as_float(o[q4 * 4 + 2]) * inv, __uint_as_float(o[q4 * 4 + 3]) * inv);
+                } else if (row_ok) {
+                    __nv_bfloat16 *dst = p.out + row * kD + hf * 64;
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint4 v;
@@ -559,6 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            // sum of exp2(s * scale * log2 e) over the row's keys is lt * 2^m_ref
+            if (row_ok && p.o_part != nullptr && hf == 0)
+                p.lse[row] = lt > 0.f ? (m_ref + log2f(lt)) * kLn2 : -INFINITY;
         }
     }
     tc_fence_before();
@@ -654,6 +684,9 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     prm.num_blocks = a.pool.num_blocks;
     prm.scale_log2 = a.scale * kLog2e;
     prm.err = err;
+    prm.causal = a.causal ? 1 : 0;
+    prm.o_part = a.o_part;
+    prm.lse = a.lse;
     auto by_block = [&](auto gtag) -> cudaError_t {
         constexpr int GG = decltype(gtag)::value;
         switch (a.pool.block_size) {

@@ -308,6 +308,62 @@ def pin_decode_shared_prefix(orc):
     assert np.array_equal(a, c)
 
 
+def pin_decode_lse(orc):
+    """The log-sum-exp log(sum_t exp(scale q.K_t)) that a cascade merges by:
+    log(n) for a zero query; scale q.k + log(n) when every key is k; a naive
+    pure-Python sum on tiny inputs; and the merge identity -- attention over
+    a prefix and a suffix, weighted by exp(lse), is attention over both."""
+    Hq, Hkv, d, b, NB = 4, 2, 8, 4, 32
+    gen = torch.Generator().manual_seed(11)
+    rng = np.random.default_rng(11)
+    geom = oracle_pkg.dense_geom(NB, Hkv, b, d)
+    lens = [3, 9, 16, 1]
+    B = len(lens)
+    K, V = randn((B, 16, Hkv, d), gen), randn((B, 16, Hkv, d), gen)
+    tables = random_tables(rng, lens, NB, b)
+    pool = place(K, V, lens, tables, NB, b, gen)
+    L = np.asarray(lens, np.int32)
+    out0, lse0 = orc.paged_decode_lse(np.zeros((B, Hq, d), np.uint16), bits(pool), geom, tables, L, Hq, 0.3)
+    assert np.abs(lse0 - np.log(L)[:, None]).max() < 1e-13
+    q = randn((B, Hq, d), gen)
+    out, lse = orc.paged_decode_lse(bits(q), bits(pool), geom, tables, L, Hq, 0.3)
+    assert np.array_equal(out, orc.paged_decode(bits(q), bits(pool), geom, tables, L, Hq, 0.3))
+    qf, Kf = q.double().tolist(), K.double().tolist()
+    for s in range(B):
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            z = math.fsum(math.exp(0.3 * math.fsum(qf[s][h][i] * Kf[s][t][g][i] for i in range(d)))
+                          for t in range(lens[s]))
+            assert abs(lse[s, h] - math.log(z)) < 1e-12, (s, h)
+    # every key equal to k: each score is scale q.k
+    k = randn((Hkv, d), gen)
+    Ke = k.unsqueeze(0).unsqueeze(0).expand(B, 16, Hkv, d).contiguous()
+    pool_e = place(Ke, V, lens, tables, NB, b, gen)
+    _, lse_e = orc.paged_decode_lse(bits(q), bits(pool_e), geom, tables, L, Hq, 0.3)
+    for s in range(B):
+        for h in range(Hq):
+            dot = math.fsum(qf[s][h][i] * float(k[h // 2, i]) for i in range(d))
+            assert abs(lse_e[s, h] - (0.3 * dot + math.log(lens[s]))) < 1e-12, (s, h)
+    # merge identity: the first two blocks as a prefix, the rest as a suffix
+    full = [16, 12, 9]
+    Bf = len(full)
+    tab = random_tables(rng, full, NB, b)
+    Kf2, Vf2 = randn((Bf, 16, Hkv, d), gen), randn((Bf, 16, Hkv, d), gen)
+    pool_f = place(Kf2, Vf2, full, tab, NB, b, gen)
+    qm = randn((Bf, Hq, d), gen)
+    o_all, l_all = orc.paged_decode_lse(bits(qm), bits(pool_f), geom, tab, np.asarray(full, np.int32), Hq, 0.3)
+    o_a, l_a = orc.paged_decode_lse(bits(qm), bits(pool_f), geom, tab[:, :2], np.full(Bf, 2 * b, np.int32), Hq, 0.3)
+    o_b, l_b = orc.paged_decode_lse(bits(qm), bits(pool_f), geom, np.ascontiguousarray(tab[:, 2:]),
+                                    np.asarray(full, np.int32) - 2 * b, Hq, 0.3)
+    M = np.maximum(l_a, l_b)
+    wa, wb = np.exp(l_a - M)[..., None], np.exp(l_b - M)[..., None]
+    assert np.abs((wa * o_a + wb * o_b) / (wa + wb) - o_all).max() < 1e-13
+    assert np.abs(np.logaddexp(l_a, l_b) - l_all).max() < 1e-12
+    # no keys: -inf and zeros
+    o_z, l_z = orc.paged_decode_lse(bits(qm), bits(pool_f), geom, tab, np.zeros(Bf, np.int32), Hq, 0.3)
+    assert np.all(np.isneginf(l_z)) and not o_z.any()
+
+
 def pin_decode_layered_pool(orc):
     """The pages' pool shape [NB][2][layers][Hkv][b][d]: a layer's view through
     strides equals a dense pool holding only that layer."""

@@ -1,0 +1,203 @@
+"""GPU parity of the cascade decode (pa_cascade_plan, pa_prefix_attention,
+pa_decode_cascade) against the oracle, through the C ABI.
+
+The cascade attends a prefix shared by a group of sequences once for the
+whole group and each sequence's own blocks apart, then merges the two by
+log-sum-exp; the result must be attention over the whole sequence, so the
+reference is the oracle's plain decode over the full tables.  The prefix pass
+alone is checked against the oracle's decode over the prefix tables (output)
+and its log-sum-exp.  Log-sum-exp tolerance: the kernel sums fp32
+probabilities of fp32 scores (accumulated from bf16 operands in fp32), so its
+error is a few fp32 ulps of the running sum; 1e-3 absolute leaves a wide
+margin while a dropped key (log(n) against log(n - 1), at least 1/n) or a
+wrong scale fails it at these sizes."""
+import numpy as np
+import pytest
+import torch
+
+import pa_workloads as wl
+from tests.parity import Case, assert_close
+
+pytestmark = pytest.mark.gpu
+
+bits = wl.bf16_bits
+LSE_ATOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_167_gb300 as pa
+    assert torch.cuda.is_available(), "a CUDA device is required"
+    pa.get_device_error(clear=True)
+    return pa
+
+
+def write_new_tokens(pa, c: Case):
+    """Store each sequence's last token through the slot writer (GPU) and the
+    oracle's writer (host copy), as a decode step does before attending."""
+    w = c.w
+    slots = pa.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size, w.num_blocks)
+    pa.reshape_and_cache(c.pool, c.new_k, c.new_v, torch.as_tensor(slots, device=c.dev))
+    c.orc.reshape_and_cache(c.pool_ref, c.geom, bits(c.cpu["new_k"]), bits(c.cpu["new_v"]),
+                            c.orc.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size))
+
+
+def prefix_pass(pa, c: Case, plan, group_size):
+    w, dev = c.w, c.dev
+    o_part = torch.empty(c.q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty((w.batch, w.num_q_heads), dtype=torch.float32, device=dev)
+    pa.prefix_attention(o_part, lse, c.q, c.pool, torch.as_tensor(plan["prefix_tables"], device=dev),
+                        torch.as_tensor(plan["prefix_lens"], device=dev), group_size,
+                        int(plan["prefix_lens"].max()), w.scale)
+    return o_part, lse
+
+
+def cascade(pa, c: Case, plan, group_size, partition_tokens=0, flags=0, new_kv=None):
+    w, dev = c.w, c.dev
+    o_part, lse = prefix_pass(pa, c, plan, group_size)
+    max_s = max(1, int(plan["suffix_lens"].max()))
+    out = torch.empty_like(c.q)
+    nbytes = pa.decode_workspace_size(c.pool, w.batch, w.num_q_heads, max_s, partition_tokens)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
+    nk, nv = new_kv if new_kv is not None else (None, None)
+    pa.decode_cascade(out, c.q, c.pool, torch.as_tensor(plan["suffix_tables"], device=dev),
+                      torch.as_tensor(plan["suffix_lens"], device=dev), max_s, w.scale, o_part, lse,
+                      partition_tokens, ws, flags=flags, new_k=nk, new_v=nv)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    return out, o_part, lse
+
+
+def oracle_full(c: Case, rows=None):
+    return c.orc.paged_decode(bits(c.cpu["q"]), c.pool_ref, c.geom, c.w.tables, c.w.seq_lens,
+                              c.w.num_q_heads, c.w.scale, rows=rows)
+
+
+def oracle_prefix(c: Case, plan, group_size):
+    per_seq = np.repeat(plan["prefix_tables"], group_size, axis=0)
+    lens = np.repeat(plan["prefix_lens"], group_size).astype(np.int32)
+    return c.orc.paged_decode_lse(bits(c.cpu["q"]), c.pool_ref, c.geom, per_seq, lens, c.w.num_q_heads,
+                                  c.w.scale)
+
+
+def check_lse(got: torch.Tensor, ref: np.ndarray, what: str):
+    g = got.cpu().numpy().astype(np.float64)
+    empty = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(g), empty), f"{what}: -inf pattern differs"
+    err = np.abs(g[~empty] - ref[~empty])
+    assert err.size == 0 or err.max() <= LSE_ATOL, f"{what}: lse max err {err.max()}"
+
+
+def designed_plan(w, group_size):
+    """The split the workload was built with (its groups' prefix lengths),
+    written out without the planner."""
+    b = w.block_size
+    plens = np.asarray(w.notes["prefix_lens"], np.int32)
+    W = w.tables.shape[1]
+    pt = np.full((len(plens), W), -1, np.int32)
+    st = np.full((w.batch, W), -1, np.int32)
+    for gi, plen in enumerate(plens):
+        pt[gi, :plen // b] = w.tables[gi * group_size, :plen // b]
+    for s in range(w.batch):
+        row = w.tables[s, plens[s // group_size] // b:]
+        st[s, :len(row)] = row
+    return {"prefix_tables": pt, "prefix_lens": plens, "suffix_tables": st,
+            "suffix_lens": np.asarray(w.seq_lens, np.int32) - np.repeat(plens, group_size)}
+
+
+def grouped_case(group, group_size, prefix_lens, seed, bs=16):
+    rng = np.random.default_rng(seed)
+    suffix = rng.integers(1, 300, size=len(prefix_lens) * group_size).tolist()
+    w = wl.shared_groups(prefix_lens, suffix, group_size, 2 * group, 2, 128, bs, seed=seed)
+    return Case(w)
+
+
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("group", [1, 4, 8])
+@pytest.mark.parametrize("group_size", [1, 3, 16, 37])
+def test_prefix_pass_matches_oracle(pa, group, group_size):
+    """Output and log-sum-exp of every query over its group's prefix: several
+    128-key tiles, a ragged last tile, an empty prefix, groups that fill a
+    fraction of an M-tile or several M-tiles."""
+    c = grouped_case(group, group_size, [0, 16, 400, 1024, 144], seed=group * 100 + group_size)
+    plan = designed_plan(c.w, group_size)
+    if group_size > 1:   # the planner finds the same split (alone, a sequence shares all its full blocks)
+        got = pa.cascade_plan(c.w.tables, c.w.seq_lens, group_size, c.w.block_size)
+        for k in plan:
+            assert np.array_equal(got[k], plan[k]), k
+    o_part, lse = prefix_pass(pa, c, plan, group_size)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    ref_o, ref_lse = oracle_prefix(c, plan, group_size)
+    assert_close(o_part, ref_o, f"prefix o G={group} n={group_size}")
+    check_lse(lse, ref_lse, f"prefix lse G={group} n={group_size}")
+
+
+@pytest.mark.parametrize("group", [2, 8])
+@pytest.mark.parametrize("group_size", [1, 4, 9])
+@pytest.mark.parametrize("part", [0, 64, 512])
+def test_cascade_matches_full_decode(pa, group, group_size, part):
+    """Prefix pass + suffix decode with the fold equals attention over the
+    whole sequence, on the balanced schedule (part 0) and on split-context
+    partitions (single and several partitions)."""
+    c = grouped_case(group, group_size, [0, 32, 496, 1536], seed=7 + group * 10 + group_size)
+    plan = pa.cascade_plan(c.w.tables, c.w.seq_lens, group_size, c.w.block_size)
+    out, _, _ = cascade(pa, c, plan, group_size, part)
+    assert_close(out, oracle_full(c), f"cascade G={group} n={group_size} part={part}")
+
+
+@pytest.mark.parametrize("part", [0, 32, 256])
+def test_empty_suffix_is_prefix_alone(pa, part):
+    """Sequences with no tokens after the prefix (suffix length 0) get the
+    prefix term alone; a group with no prefix gets plain decode; a sequence
+    with neither gets zeros."""
+    w = wl.shared_groups([64, 0, 208], [0, 5, 0, 130, 0, 0], 2, 8, 2, 128, 16, seed=31)
+    c = Case(w)
+    plan = designed_plan(w, 2)
+    assert list(plan["suffix_lens"]) == [0, 5, 0, 130, 0, 0]
+    out, _, _ = cascade(pa, c, plan, 2, part)
+    ref = oracle_full(c)
+    assert_close(out, ref, f"empty suffix part={part}")
+    assert not out[2].float().abs().sum().item() and not ref[2].any()   # no prefix, no suffix
+
+
+@pytest.mark.parametrize("part", [0, 128])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_cascade_with_append(pa, part, flags):
+    """The suffix decode stores each sequence's new token (positions counted in
+    the suffix) before attending, as pa_decode_ex does."""
+    c = grouped_case(8, 4, [256, 64, 0], seed=55)
+    w = c.w
+    plan = pa.cascade_plan(w.tables, w.seq_lens, 4, w.block_size)
+    out, _, _ = cascade(pa, c, plan, 4, part, flags=flags, new_kv=(c.new_k, c.new_v))
+    c.orc.reshape_and_cache(c.pool_ref, c.geom, bits(c.cpu["new_k"]), bits(c.cpu["new_v"]),
+                            c.orc.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size))
+    assert np.array_equal(bits(c.pool), c.pool_ref), "the appended K/V differ from the slot writer's"
+    assert_close(out, oracle_full(c), f"cascade append part={part} flags={flags}")
+
+
+@pytest.mark.parametrize("name,group_size", [("shared_prefix", 256), ("beam_fork", 4)])
+def test_full_size_cascade(pa, name, group_size):
+    """The shared-prompt batch (one group of 256 over a 2,000-token prompt) and
+    the beam batch (32 groups of 4 beams after copy-on-write), as the bench
+    runs them, on sampled rows."""
+    w = wl.CONFIGS[name]()
+    c = Case(w)
+    if w.copy_pairs is not None and len(w.copy_pairs):
+        pa.copy_blocks(c.pool, torch.as_tensor(w.copy_pairs, device=c.dev))
+        c.orc.copy_blocks(c.pool_ref, c.geom, w.copy_pairs)
+    write_new_tokens(pa, c)
+    plan = pa.cascade_plan(w.tables, w.seq_lens, group_size, w.block_size)
+    if name == "shared_prefix":
+        assert list(plan["prefix_lens"]) == [2000]
+    else:
+        plen = w.notes["prompt_lens"]
+        assert np.array_equal(plan["prefix_lens"], (plen // 16) * 16)
+    out, _, _ = cascade(pa, c, plan, group_size, 0, flags=1)
+    rng = np.random.default_rng(9)
+    flat = rng.choice(w.batch * w.num_q_heads, size=2048, replace=False)
+    rows = np.stack([flat // w.num_q_heads, flat % w.num_q_heads], axis=1)
+    assert_close(out[rows[:, 0], rows[:, 1]], oracle_full(c, rows), name)

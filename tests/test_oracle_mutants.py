@@ -26,11 +26,13 @@ MUTANTS = [
      "int64_t logical = (pos + 1) / block_size;", 1),
     ("slot_transposed", "return phys * block_size + off;", "return off * block_size + phys;", 1),
     ("dropped_scale", "x[t] = scale * dot;", "x[t] = dot;", 1),
+    ("lse_drops_max", "*lse = m + log(l);", "*lse = log(l);", 1),
+    ("lse_of_weights_mean", "*lse = m + log(l);", "*lse = m + log(l / (double)n_keys);", 1),
     ("exp_sign", "x[t] = exp(x[t] - m);", "x[t] = exp(m - x[t]);", 1),
     ("unnormalised", "out[i] += (x[t] / l) * values[t * d + i];", "out[i] += x[t] * values[t * d + i];", 1),
     ("values_from_keys", "const uint16_t *vrow = pool + pool_elem(p, phys, 1, kvh, off);",
      "const uint16_t *vrow = pool + pool_elem(p, phys, 0, kvh, off);", 1),
-    ("gqa_interleaved", "h / group", "h % p->num_kv_heads", 4),
+    ("gqa_interleaved", "h / group", "h % p->num_kv_heads", 5),
     ("slab_transposed", "(h * p->block_size + off) * p->head_dim",
      "(off * p->num_kv_heads + h) * p->head_dim", 1),
     ("kv_stride_single_layer", "kv * p->kv_stride",
