@@ -77,6 +77,22 @@ def test_host_validation(B):
     for bad_scale in (0.0, -0.1, float("nan")):                          # scale must be finite and > 0
         assert L.pa_prefill_chunk(ok_ptr, ok_ptr, ctypes.byref(good), ok_ptr, 8, ok_ptr, 1, 4, 64, 10,
                                   bad_scale, P(0)) == 1
+    # cascade entry points: prefix terms are required, aligned; the prefix pass validates like prefill
+    cas = lambda po, pl, **kw: args(good, **kw)[:-1] + (po, pl, P(0), P(0), 0, P(0))
+    assert L.pa_decode_cascade(*cas(P(0), ok_ptr)) == 1                 # no prefix output
+    assert L.pa_decode_cascade(*cas(ok_ptr, P(0))) == 1                 # no prefix lse
+    assert L.pa_decode_cascade(*cas(P(0x20008), ok_ptr)) == 1           # misaligned prefix output
+    assert L.pa_decode_cascade(*cas(ok_ptr, ok_ptr, part=16)) == 3      # workspace missing, as pa_decode
+    pfx = lambda o, lse, scale=0.1, groups=1, gsz=4, maxlen=64: (o, lse, ok_ptr, ctypes.byref(good), ok_ptr, 8,
+                                                                 ok_ptr, groups, gsz, 64, maxlen, scale, P(0))
+    assert L.pa_prefix_attention(*pfx(ok_ptr, ok_ptr, groups=0)) == 0   # nothing to do
+    assert L.pa_prefix_attention(*pfx(P(0x20008), ok_ptr)) == 1          # misaligned output
+    assert L.pa_prefix_attention(*pfx(ok_ptr, P(0))) == 1                # no lse
+    assert L.pa_prefix_attention(*pfx(ok_ptr, ok_ptr, scale=0.0)) == 1
+    assert L.pa_prefix_attention(*pfx(ok_ptr, ok_ptr, maxlen=8 * 16 + 1)) == 1   # longer than the table
+    assert L.pa_prefix_attention(*pfx(ok_ptr, ok_ptr, groups=70000)) == 1        # grid limit
+    assert L.pa_prefix_attention(ok_ptr, ok_ptr, ok_ptr, ctypes.byref(_pool(B, d=64)), ok_ptr, 8, ok_ptr, 1, 4, 64,
+                                 10, 0.1, P(0)) == 2
     err = ctypes.c_uint32()
     assert L.pa_get_device_error(None, 0, P(0)) == 1
 
