@@ -222,6 +222,37 @@ pa_status pa_decode_noalloc(void *out, const void *q, const pa_kv_pool *pool,
                             cudaStream_t stream);
 
 /*
+ * One decode step from host buffers: copies q, the tables, the lengths and
+ * (optionally) the new tokens' K/V from host memory into `staging`, runs
+ * pa_decode_ex on them, and copies the output back to `out_host`, all queued
+ * on `stream` (one asynchronous copy per input).  The pool stays on the device.
+ * The caller synchronises the stream before reading out_host; host buffers
+ * should be page-locked (pinned) for the copies to run asynchronously.
+ *   out_host, q_host     host, [num_seqs][num_q_heads][d] bf16
+ *   tables_host          host, [num_seqs][max_blocks_per_seq] int32
+ *   seq_lens_host        host, [num_seqs] int32
+ *   new_k_host, new_v_host  host, [num_seqs][Hkv][d] bf16, both NULL or both set
+ *                        (stored at each sequence's last position, as pa_decode_ex)
+ *   staging              device, 256-byte aligned, at least
+ *                        pa_decode_host_staging_size(...) bytes (else PA_ERR_WORKSPACE);
+ *                        owned by the caller, not read by the step until the
+ *                        copies into it have landed
+ *   workspace            as pa_decode
+ * flags as pa_decode_ex, except that PA_DECODE_EARLY_METADATA is ignored: the
+ * tables and lengths are written by the copies just before the decode.  The
+ * pages have no counterpart to this call.
+ */
+size_t pa_decode_host_staging_size(const pa_kv_pool *pool, int32_t num_seqs, int32_t num_q_heads,
+                                   int32_t max_blocks_per_seq);
+pa_status pa_decode_host(void *out_host, const void *q_host, const pa_kv_pool *pool,
+                         const int32_t *tables_host, int32_t max_blocks_per_seq,
+                         const int32_t *seq_lens_host, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t max_seq_len, float scale, int32_t partition_tokens,
+                         const void *new_k_host, const void *new_v_host, uint32_t flags, void *staging,
+                         size_t staging_bytes, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
  * Copy-on-write block copies.  [P1] feature table, beam-search row: forks
  * share blocks and only the block that diverges is copied; [P2] interviewer
  * follow-up on beam search: a fresh block receives the diverging block's

@@ -55,6 +55,9 @@ SIGNATURES = {
     "pa_decode_partition_tokens": (_I32, [_POOL, _I32, _I32, _I32, _I32]),
     "pa_decode": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _P]),
     "pa_decode_ex": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _P, _P, _U32, _P]),
+    "pa_decode_host_staging_size": (_SZ, [_POOL, _I32, _I32, _I32]),
+    "pa_decode_host": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _P, _U32, _P, _SZ, _P, _SZ,
+                              _P]),
     "pa_decode_noalloc": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P]),
     "pa_copy_blocks": (_I32, [_POOL, _P, _I32, _P]),
     "pa_swap_blocks": (_I32, [_POOL, _P, _I64, _P, _I32, _I32, _P]),
@@ -131,6 +134,16 @@ def _stream(stream) -> ctypes.c_void_p:
 def _dev(t: torch.Tensor, dtype, name: str) -> ctypes.c_void_p:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host(t: torch.Tensor, dtype, name: str) -> ctypes.c_void_p:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise TypeError(f"{name} must be a CPU tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -228,6 +241,39 @@ def decode(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_tables:
         _check(lib().pa_decode_ex(*args, nk, nv, int(flags), _stream(stream)), "pa_decode_ex")
     else:
         _check(lib().pa_decode(*args, _stream(stream)), "pa_decode")
+
+
+def decode_host_staging_size(pool: torch.Tensor, num_seqs: int, num_q_heads: int, max_blocks_per_seq: int,
+                             layer: Optional[int] = None) -> int:
+    desc = pool_desc(pool, layer)
+    return int(lib().pa_decode_host_staging_size(ctypes.byref(desc), num_seqs, num_q_heads, max_blocks_per_seq))
+
+
+def decode_host(out_host: torch.Tensor, q_host: torch.Tensor, pool: torch.Tensor, tables_host: torch.Tensor,
+                seq_lens_host: torch.Tensor, max_seq_len: int, scale: float, staging: torch.Tensor,
+                partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None, layer: Optional[int] = None,
+                stream=None, flags: int = 0, new_k_host: Optional[torch.Tensor] = None,
+                new_v_host: Optional[torch.Tensor] = None) -> None:
+    """pa_decode_host: one decode step from host (ideally pinned) tensors; the
+    output lands in ``out_host`` once ``stream`` has been synchronised.
+    ``staging`` is a uint8 CUDA tensor of decode_host_staging_size(...) bytes."""
+    desc = pool_desc(pool, layer)
+    B, Hq, _ = q_host.shape
+    if out_host.shape != q_host.shape:
+        raise ValueError("out_host must have q_host's shape")
+    if tables_host.dim() != 2 or tables_host.shape[0] != B or seq_lens_host.numel() != B:
+        raise ValueError("tables_host / seq_lens_host do not match the batch")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, torch.uint8, "workspace"), workspace.numel()
+    nk = _host(new_k_host, torch.bfloat16, "new_k_host") if new_k_host is not None else ctypes.c_void_p(0)
+    nv = _host(new_v_host, torch.bfloat16, "new_v_host") if new_v_host is not None else ctypes.c_void_p(0)
+    _check(lib().pa_decode_host(_host(out_host, torch.bfloat16, "out_host"), _host(q_host, torch.bfloat16, "q_host"),
+                                ctypes.byref(desc), _host(tables_host, torch.int32, "tables_host"),
+                                tables_host.shape[1], _host(seq_lens_host, torch.int32, "seq_lens_host"), B, Hq,
+                                int(max_seq_len), float(scale), int(partition_tokens), nk, nv, int(flags),
+                                _dev(staging, torch.uint8, "staging"), staging.numel(), ws_ptr, ws_bytes,
+                                _stream(stream)), "pa_decode_host")
 
 
 def decode_noalloc(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_tables: torch.Tensor,

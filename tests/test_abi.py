@@ -93,6 +93,17 @@ def test_host_validation(B):
     assert L.pa_prefix_attention(*pfx(ok_ptr, ok_ptr, groups=70000)) == 1        # grid limit
     assert L.pa_prefix_attention(ok_ptr, ok_ptr, ok_ptr, ctypes.byref(_pool(B, d=64)), ok_ptr, 8, ok_ptr, 1, 4, 64,
                                  10, 0.1, P(0)) == 2
+    # one step from host buffers: staging size and layout, host-side validation
+    hs = L.pa_decode_host_staging_size(ctypes.byref(good), 4, 64, 8)
+    assert hs == 2 * (4 * 64 * 128 * 2) + 2 * (4 * 8 * 128 * 2) + 256 + 256   # q, out, new K, new V, tables, lengths
+    assert L.pa_decode_host_staging_size(ctypes.byref(good), 4, 64, 0) == 0
+    host = lambda st=P(0x40000), stb=hs, nk=P(0), nv=P(0), q=ok_ptr: (
+        ok_ptr, q, ctypes.byref(good), ok_ptr, 8, ok_ptr, 4, 64, 100, 0.1, 0, nk, nv, 0, st, stb, P(0), 0, P(0))
+    assert L.pa_decode_host(*host(st=P(0))) == 3                       # no staging
+    assert L.pa_decode_host(*host(stb=hs - 1)) == 3                    # staging too small
+    assert L.pa_decode_host(*host(st=P(0x40010))) == 3                 # staging not 256-byte aligned
+    assert L.pa_decode_host(*host(q=P(0))) == 1                        # no q
+    assert L.pa_decode_host(*host(nk=ok_ptr)) == 1                     # new K without new V
     err = ctypes.c_uint32()
     assert L.pa_get_device_error(None, 0, P(0)) == 1
 

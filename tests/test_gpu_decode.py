@@ -400,3 +400,28 @@ def test_append_errors_write_nothing(pa):
     mask[blk, :, :, off] = False
     assert np.array_equal(after[mask], before[mask])
     assert np.array_equal(after[blk, 0, :, off], bits(c.cpu["new_k"])[0])
+
+
+@pytest.mark.parametrize("part", [0, 64])
+def test_decode_from_host_buffers(pa, part):
+    """pa_decode_host: q, tables, lengths and the new tokens from pinned host
+    memory, the output back to host memory, one call; the pool bit-exact with
+    the oracle's slot writer and the output within tolerance."""
+    w = wl.custom([1, 17, 300, 64, 129, 850], 16, 2, 128, 16, seed=77)
+    c = Case(w)
+    q_h, k_h, v_h = (c.cpu[k].pin_memory() for k in ("q", "new_k", "new_v"))
+    tables_h = torch.as_tensor(w.tables).pin_memory()
+    lens_h = torch.as_tensor(w.seq_lens).pin_memory()
+    out_h = torch.full_like(q_h, float("nan")).pin_memory()
+    nb = pa.decode_host_staging_size(c.pool, w.batch, w.num_q_heads, w.tables.shape[1])
+    staging = torch.empty(nb, dtype=torch.uint8, device=c.dev)
+    wsb = pa.decode_workspace_size(c.pool, w.batch, w.num_q_heads, w.max_seq_len, part)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=c.dev) if wsb else None
+    pa.decode_host(out_h, q_h, c.pool, tables_h, lens_h, w.max_seq_len, w.scale, staging, part, ws,
+                   flags=pa.PA_DECODE_EARLY_METADATA, new_k_host=k_h, new_v_host=v_h)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    c.orc.reshape_and_cache(c.pool_ref, c.geom, bits(c.cpu["new_k"]), bits(c.cpu["new_v"]),
+                            c.orc.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size))
+    assert np.array_equal(bits(c.pool), c.pool_ref), "stored K/V differ from the slot writer's"
+    assert_close(out_h, oracle_decode(c), f"host buffers part={part}")
