@@ -96,6 +96,7 @@ class Oracle:
         G = ctypes.POINTER(PoolGeom)
         sig = {
             "orc_num_threads": (I32, []),
+            "orc_set_num_threads": (I32, [I32]),
             "orc_block_layout": (I32, [I64, I64, ctypes.POINTER(I64), ctypes.POINTER(I64)]),
             "orc_address": (None, [P, I64, I64, ctypes.POINTER(I64), ctypes.POINTER(I64)]),
             "orc_slot": (I64, [P, I64, I64]),
@@ -119,6 +120,10 @@ class Oracle:
     # -- capacity arithmetic and address map ---------------------------------
     def num_threads(self) -> int:
         return int(self._lib.orc_num_threads())
+
+    def set_num_threads(self, n: int) -> int:
+        """Threads the oracle's OpenMP loops use from now on; returns the count in force."""
+        return int(self._lib.orc_set_num_threads(int(n)))
 
     def block_layout(self, tokens: int, block_size: int):
         blocks, unused = ctypes.c_int64(), ctypes.c_int64()

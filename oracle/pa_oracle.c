@@ -69,6 +69,19 @@ int orc_num_threads(void)
 #endif
 }
 
+/* Threads the OpenMP loops use from now on (n > 0); returns the count in force. */
+int orc_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
 /* bf16 bit pattern -> exact double */
 static double bf16_to_double(uint16_t h)
 {
