@@ -217,6 +217,7 @@ def measure_cascade(pa, step, K: int, warmup: int):
     plan = pa.cascade_plan(w.tables, w.seq_lens, gsz, w.block_size)
     pt = torch.as_tensor(plan["prefix_tables"], device=dev)
     pl = torch.as_tensor(plan["prefix_lens"], device=dev)
+    order = torch.as_tensor(plan["group_order"], device=dev)   # longest prefix first
     st = torch.as_tensor(plan["suffix_tables"], device=dev)
     sl = torch.as_tensor(plan["suffix_lens"], device=dev)
     max_p, max_s = int(plan["prefix_lens"].max()), max(1, int(plan["suffix_lens"].max()))
@@ -227,7 +228,7 @@ def measure_cascade(pa, step, K: int, warmup: int):
 
     def prefix(i):
         pa.prefix_attention(o_part, lse, step.qs[i % step.layers], step.pools[i % step.layers], pt, pl, gsz, max_p,
-                            w.scale)
+                            w.scale, group_order=order)
 
     def suffix(i):
         pa.decode_cascade(step.out, step.qs[i % step.layers], step.pools[i % step.layers], st, sl, max_s, w.scale,

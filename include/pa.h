@@ -53,6 +53,7 @@ typedef enum {
 #define PA_DEVERR_SLOT     0x2u /* a slot >= num_blocks * block_size                       */
 #define PA_DEVERR_SEQ_LEN  0x4u /* a length < 0, beyond the table width or the host bound  */
 #define PA_DEVERR_TIMEOUT  0x8u /* a bounded wait on a shared-memory barrier gave up       */
+#define PA_DEVERR_ORDER   0x10u /* a group order entry outside [0, num_groups)              */
 
 typedef enum { PA_DTYPE_BF16 = 0 } pa_dtype;
 
@@ -335,6 +336,13 @@ pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool,
  *   prefix_tables device, [num_groups][max_prefix_blocks] int32: the group's
  *                 shared blocks
  *   prefix_lens   device, [num_groups] int32, each in [0, max_prefix_len]
+ *   group_order   device, [num_groups] int32, a permutation of the groups, or
+ *                 NULL: the order in which the groups' CTAs start (longest
+ *                 prefix first balances the GPU's waves; pa_cascade_plan
+ *                 writes that order).  It changes no result.  An entry outside
+ *                 [0, num_groups) raises PA_DEVERR_ORDER and that CTA works on
+ *                 its own index instead (some group is then done twice and
+ *                 another not at all).
  *   max_prefix_len host bound, <= max_prefix_blocks * block_size
  *   scale         as pa_prefill_chunk
  * Every query of group i attends all prefix_lens[i] keys (no causal mask: the
@@ -345,7 +353,8 @@ pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool,
  */
 pa_status pa_prefix_attention(float *o_part, float *lse, const void *q, const pa_kv_pool *pool,
                               const int32_t *prefix_tables, int32_t max_prefix_blocks,
-                              const int32_t *prefix_lens, int32_t num_groups, int32_t group_size,
+                              const int32_t *prefix_lens, const int32_t *group_order,
+                              int32_t num_groups, int32_t group_size,
                               int32_t num_q_heads, int32_t max_prefix_len, float scale,
                               cudaStream_t stream);
 
@@ -359,6 +368,9 @@ pa_status pa_prefix_attention(float *o_part, float *lse, const void *q, const pa
  *   tables         [num_seqs][max_blocks] int32; seq_lens [num_seqs]
  *   prefix_tables  out [num_seqs / group_size][max_blocks]: the shared ids, then -1
  *   prefix_lens    out [num_seqs / group_size]: shared blocks * block_size
+ *   group_order    out [num_seqs / group_size] or NULL: the groups by prefix
+ *                  length, longest first (ties in index order), for
+ *                  pa_prefix_attention
  *   suffix_tables  out [num_seqs][max_blocks]: each row's ids after the prefix, then -1
  *   suffix_lens    out [num_seqs]: seq_lens[s] - the group's prefix length
  * PA_ERR_INVALID_ARG when num_seqs is not a multiple of group_size, a size is
@@ -366,8 +378,8 @@ pa_status pa_prefix_attention(float *o_part, float *lse, const void *q, const pa
  */
 pa_status pa_cascade_plan(const int32_t *tables, int32_t max_blocks, const int32_t *seq_lens,
                           int32_t num_seqs, int32_t group_size, int32_t block_size,
-                          int32_t *prefix_tables, int32_t *prefix_lens, int32_t *suffix_tables,
-                          int32_t *suffix_lens);
+                          int32_t *prefix_tables, int32_t *prefix_lens, int32_t *group_order,
+                          int32_t *suffix_tables, int32_t *suffix_lens);
 
 /*
  * Cascade decode, pass 2: pa_decode_ex over each sequence's private suffix,

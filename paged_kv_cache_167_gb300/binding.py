@@ -62,10 +62,10 @@ SIGNATURES = {
     "pa_copy_blocks": (_I32, [_POOL, _P, _I32, _P]),
     "pa_swap_blocks": (_I32, [_POOL, _P, _I64, _P, _I32, _I32, _P]),
     "pa_prefill_chunk": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _I32, _F, _P]),
-    "pa_prefix_attention": (_I32, [_P, _P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _I32, _F, _P]),
+    "pa_prefix_attention": (_I32, [_P, _P, _P, _POOL, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _F, _P]),
     "pa_decode_cascade": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _P, _P, _P, _P,
                                  _U32, _P]),
-    "pa_cascade_plan": (_I32, [_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P, _P]),
+    "pa_cascade_plan": (_I32, [_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "pa_get_device_error": (_I32, [ctypes.POINTER(_U32), _I32, _P]),
     "pa_block_layout": (_I32, [_I64, _I32, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "pa_slot_mapping": (_I32, [_P, _P, _I32, _I32, _P, _P, _I64, _I32, _I64]),
@@ -336,9 +336,11 @@ def prefill_chunk(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, block_
 
 def prefix_attention(o_part: torch.Tensor, lse: torch.Tensor, q: torch.Tensor, pool: torch.Tensor,
                      prefix_tables: torch.Tensor, prefix_lens: torch.Tensor, group_size: int, max_prefix_len: int,
-                     scale: float, layer: Optional[int] = None, stream=None) -> None:
+                     scale: float, group_order: Optional[torch.Tensor] = None, layer: Optional[int] = None,
+                     stream=None) -> None:
     """pa_prefix_attention: q [num_groups * group_size][Hq][d] bf16 (sequences
-    group by group); o_part fp32 of q's shape, lse fp32 [B][Hq]."""
+    group by group); o_part fp32 of q's shape, lse fp32 [B][Hq]; group_order
+    an int32 CUDA permutation of the groups (the order their CTAs start) or None."""
     desc = pool_desc(pool, layer)
     B, Hq, _ = q.shape
     if group_size <= 0 or B % group_size != 0:
@@ -348,10 +350,13 @@ def prefix_attention(o_part: torch.Tensor, lse: torch.Tensor, q: torch.Tensor, p
         raise ValueError("o_part must have q's shape and lse [B][Hq]")
     if prefix_tables.dim() != 2 or prefix_tables.shape[0] != G or prefix_lens.numel() != G:
         raise ValueError("prefix_tables / prefix_lens do not match the groups")
+    if group_order is not None and group_order.numel() != G:
+        raise ValueError("group_order must hold one entry per group")
+    order = _dev(group_order, torch.int32, "group_order") if group_order is not None else ctypes.c_void_p(0)
     _check(lib().pa_prefix_attention(_dev(o_part, torch.float32, "o_part"), _dev(lse, torch.float32, "lse"),
                                      _dev(q, torch.bfloat16, "q"), ctypes.byref(desc),
                                      _dev(prefix_tables, torch.int32, "prefix_tables"), prefix_tables.shape[1],
-                                     _dev(prefix_lens, torch.int32, "prefix_lens"), G, int(group_size), Hq,
+                                     _dev(prefix_lens, torch.int32, "prefix_lens"), order, G, int(group_size), Hq,
                                      int(max_prefix_len), float(scale), _stream(stream)), "pa_prefix_attention")
 
 
@@ -389,7 +394,8 @@ def cascade_plan(tables, seq_lens, group_size: int, block_size: int) -> dict:
     """pa_cascade_plan on host arrays: the prefix each group of ``group_size``
     consecutive sequences shares (whole blocks, leaving every member at least
     one token) and the suffixes.  Returns numpy int32 arrays prefix_tables
-    [G][W], prefix_lens [G], suffix_tables [B][W], suffix_lens [B]."""
+    [G][W], prefix_lens [G], group_order [G] (longest prefix first),
+    suffix_tables [B][W], suffix_lens [B]."""
     t = np.ascontiguousarray(np.asarray(tables, dtype=np.int32))
     L = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32).reshape(-1))
     if t.ndim != 2 or t.shape[0] != L.shape[0]:
@@ -400,12 +406,13 @@ def cascade_plan(tables, seq_lens, group_size: int, block_size: int) -> dict:
     G = B // group_size
     pt = np.empty((G, W), np.int32)
     pl = np.empty(G, np.int32)
+    go = np.empty(G, np.int32)
     st = np.empty((B, W), np.int32)
     sl = np.empty(B, np.int32)
     ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
-    _check(lib().pa_cascade_plan(ptr(t), W, ptr(L), B, int(group_size), int(block_size), ptr(pt), ptr(pl), ptr(st),
-                                 ptr(sl)), "pa_cascade_plan")
-    return {"prefix_tables": pt, "prefix_lens": pl, "suffix_tables": st, "suffix_lens": sl}
+    _check(lib().pa_cascade_plan(ptr(t), W, ptr(L), B, int(group_size), int(block_size), ptr(pt), ptr(pl), ptr(go),
+                                 ptr(st), ptr(sl)), "pa_cascade_plan")
+    return {"prefix_tables": pt, "prefix_lens": pl, "group_order": go, "suffix_tables": st, "suffix_lens": sl}
 
 
 def get_device_error(clear: bool = True, stream=None) -> int:

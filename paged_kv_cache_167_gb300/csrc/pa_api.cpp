@@ -330,7 +330,8 @@ pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool, con
 
 pa_status pa_prefix_attention(float *o_part, float *lse, const void *q, const pa_kv_pool *pool,
                               const int32_t *prefix_tables, int32_t max_prefix_blocks, const int32_t *prefix_lens,
-                              int32_t num_groups, int32_t group_size, int32_t num_q_heads, int32_t max_prefix_len,
+                              const int32_t *group_order, int32_t num_groups, int32_t group_size,
+                              int32_t num_q_heads, int32_t max_prefix_len,
                               float scale, cudaStream_t stream) {
     PoolView view;
     pa_status st = resolve_pool(pool, &view);
@@ -361,6 +362,7 @@ pa_status pa_prefix_attention(float *o_part, float *lse, const void *q, const pa
     a.causal = false;
     a.o_part = o_part;
     a.lse = lse;
+    a.order = group_order;
     return launch_prefill(a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -7,13 +7,16 @@
 // at the end of the run its group shares, so that the prefix can be attended
 // once for the whole group (pa_prefix_attention) and each sequence's own
 // blocks on their own (pa_decode_cascade).
+#include <algorithm>
 #include <cstdint>
+#include <numeric>
+#include <vector>
 
 #include "pa.h"
 
 pa_status pa_cascade_plan(const int32_t *tables, int32_t max_blocks, const int32_t *seq_lens, int32_t num_seqs,
                           int32_t group_size, int32_t block_size, int32_t *prefix_tables, int32_t *prefix_lens,
-                          int32_t *suffix_tables, int32_t *suffix_lens) {
+                          int32_t *group_order, int32_t *suffix_tables, int32_t *suffix_lens) {
     if (num_seqs < 0 || group_size <= 0 || block_size <= 0 || max_blocks <= 0) return PA_ERR_INVALID_ARG;
     if (num_seqs % group_size != 0) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
@@ -49,6 +52,13 @@ pa_status pa_cascade_plan(const int32_t *tables, int32_t max_blocks, const int32
             for (int32_t i = 0; i < max_blocks; ++i) srow[i] = i + shared < max_blocks ? row[i + shared] : -1;
             suffix_lens[s] = seq_lens[s] - shared * block_size;
         }
+    }
+    if (group_order) {   // longest prefix first, ties in index order
+        std::vector<int32_t> order(num_groups);
+        std::iota(order.begin(), order.end(), 0);
+        std::stable_sort(order.begin(), order.end(),
+                         [&](int32_t a, int32_t b) { return prefix_lens[a] > prefix_lens[b]; });
+        std::copy(order.begin(), order.end(), group_order);
     }
     return PA_OK;
 }

@@ -101,6 +101,7 @@ struct PrefillArgs {
     bool causal = true;        // false: every query sees keys 0 .. ctx_lens[s] - 1
     float *o_part = nullptr;   // non-null: fp32 normalised output + lse instead of out
     float *lse = nullptr;
+    const int32_t *order = nullptr;   // non-null: sequences in this order (a permutation)
 };
 bool prefill_supported(int head_dim, int group, int block_size);
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);

@@ -107,6 +107,7 @@ struct Params {
     int32_t causal;              // 0: every query of sequence s sees keys 0 .. ctx_lens[s] - 1
     float *o_part;               // non-null: fp32 output normalised by l, [B][C][Hq][D], instead of out
     float *lse;                  // with o_part: [B][C][Hq] natural-log sum of exp(scale * q.k)
+    const int32_t *order;        // non-null: CTA z processes sequence order[z] (a permutation of 0 .. B-1)
 };
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -264,7 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffBar + 8 * kNumBars + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int mt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+    const int mt = blockIdx.x, g = blockIdx.y;
+    int s = blockIdx.z;   // replaced by order[z] once the inputs may be read
     const int j0 = mt * QPT;
 
     if (warp == kMmaWarp) {
@@ -291,6 +293,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
+    if (p.order != nullptr) {   // the caller's order: CTAs start in it, so the longest work can go first
+        const int o = __ldg(p.order + blockIdx.z);
+        if (o >= 0 && o < (int)gridDim.z)
+            s = o;
+        else if (tid == 0 && mt == 0 && g == 0)
+            raise_error(p.err, PA_DEVERR_ORDER);
+    }
     int ctx = __ldg(p.ctx_lens + s);
     if (ctx < 0 || ctx > p.max_ctx_len) {
         if (tid == 0 && mt == 0 && g == 0) raise_error(p.err, PA_DEVERR_SEQ_LEN);
@@ -687,6 +696,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     prm.causal = a.causal ? 1 : 0;
     prm.o_part = a.o_part;
     prm.lse = a.lse;
+    prm.order = a.order;
     auto by_block = [&](auto gtag) -> cudaError_t {
         constexpr int GG = decltype(gtag)::value;
         switch (a.pool.block_size) {

@@ -84,15 +84,15 @@ def test_host_validation(B):
     assert L.pa_decode_cascade(*cas(P(0x20008), ok_ptr)) == 1           # misaligned prefix output
     assert L.pa_decode_cascade(*cas(ok_ptr, ok_ptr, part=16)) == 3      # workspace missing, as pa_decode
     pfx = lambda o, lse, scale=0.1, groups=1, gsz=4, maxlen=64: (o, lse, ok_ptr, ctypes.byref(good), ok_ptr, 8,
-                                                                 ok_ptr, groups, gsz, 64, maxlen, scale, P(0))
+                                                                 ok_ptr, P(0), groups, gsz, 64, maxlen, scale, P(0))
     assert L.pa_prefix_attention(*pfx(ok_ptr, ok_ptr, groups=0)) == 0   # nothing to do
     assert L.pa_prefix_attention(*pfx(P(0x20008), ok_ptr)) == 1          # misaligned output
     assert L.pa_prefix_attention(*pfx(ok_ptr, P(0))) == 1                # no lse
     assert L.pa_prefix_attention(*pfx(ok_ptr, ok_ptr, scale=0.0)) == 1
     assert L.pa_prefix_attention(*pfx(ok_ptr, ok_ptr, maxlen=8 * 16 + 1)) == 1   # longer than the table
     assert L.pa_prefix_attention(*pfx(ok_ptr, ok_ptr, groups=70000)) == 1        # grid limit
-    assert L.pa_prefix_attention(ok_ptr, ok_ptr, ok_ptr, ctypes.byref(_pool(B, d=64)), ok_ptr, 8, ok_ptr, 1, 4, 64,
-                                 10, 0.1, P(0)) == 2
+    assert L.pa_prefix_attention(ok_ptr, ok_ptr, ok_ptr, ctypes.byref(_pool(B, d=64)), ok_ptr, 8, ok_ptr, P(0), 1, 4,
+                                 64, 10, 0.1, P(0)) == 2
     # one step from host buffers: staging size and layout, host-side validation
     hs = L.pa_decode_host_staging_size(ctypes.byref(good), 4, 64, 8)
     assert hs == 2 * (4 * 64 * 128 * 2) + 2 * (4 * 8 * 128 * 2) + 256 + 256   # q, out, new K, new V, tables, lengths

@@ -39,6 +39,7 @@ def test_hand_example(pa):
     assert p["prefix_tables"].tolist() == [[5, 6, -1, -1], [-1, -1, -1, -1]]
     assert p["suffix_tables"].tolist() == [[7, 8, -1, -1], [9, -1, -1, -1], [5, 6, 7, 10], [1, 2, 3, 4]]
     assert p["suffix_lens"].tolist() == [32, 8, 61, 13]
+    assert p["group_order"].tolist() == [0, 1]
 
 
 def test_whole_sequence_shared_keeps_last_token(pa):
@@ -80,6 +81,8 @@ def test_random_against_scan(pa, seed):
     assert np.array_equal(p["prefix_lens"], plens)
     assert np.array_equal(p["suffix_tables"], suffix)
     assert np.array_equal(p["suffix_lens"], lens - np.repeat(plens, gsz))
+    # groups by prefix length, longest first, ties in index order
+    assert p["group_order"].tolist() == sorted(range(groups), key=lambda g: (-int(plens[g]), g))
     for gi in range(groups):
         n = plens[gi] // b
         assert np.array_equal(p["prefix_tables"][gi, :n], tables[gi * gsz, :n])

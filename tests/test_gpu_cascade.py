@@ -44,13 +44,16 @@ def write_new_tokens(pa, c: Case):
                             c.orc.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size))
 
 
-def prefix_pass(pa, c: Case, plan, group_size):
+def prefix_pass(pa, c: Case, plan, group_size, order="plan"):
     w, dev = c.w, c.dev
     o_part = torch.empty(c.q.shape, dtype=torch.float32, device=dev)
     lse = torch.empty((w.batch, w.num_q_heads), dtype=torch.float32, device=dev)
+    if isinstance(order, str):
+        order = plan.get("group_order")
     pa.prefix_attention(o_part, lse, c.q, c.pool, torch.as_tensor(plan["prefix_tables"], device=dev),
                         torch.as_tensor(plan["prefix_lens"], device=dev), group_size,
-                        int(plan["prefix_lens"].max()), w.scale)
+                        int(plan["prefix_lens"].max()), w.scale,
+                        group_order=None if order is None else torch.as_tensor(order, device=dev))
     return o_part, lse
 
 
@@ -134,6 +137,26 @@ def test_prefix_pass_matches_oracle(pa, group, group_size):
     ref_o, ref_lse = oracle_prefix(c, plan, group_size)
     assert_close(o_part, ref_o, f"prefix o G={group} n={group_size}")
     check_lse(lse, ref_lse, f"prefix lse G={group} n={group_size}")
+
+
+def test_group_order_changes_nothing(pa):
+    """The order the groups' CTAs start in is scheduling only: natural order,
+    longest first and a random permutation give bit-identical results; an
+    entry out of range raises PA_DEVERR_ORDER and nothing faults."""
+    c = grouped_case(8, 3, [1024, 16, 400, 0, 144, 2048], seed=21)
+    plan = pa.cascade_plan(c.w.tables, c.w.seq_lens, 3, c.w.block_size)
+    assert plan["group_order"].tolist() == [5, 0, 2, 4, 1, 3]
+    runs = []
+    for order in (None, plan["group_order"], np.random.default_rng(1).permutation(6).astype(np.int32)):
+        o, l = prefix_pass(pa, c, plan, 3, order)
+        torch.cuda.synchronize()
+        assert pa.get_device_error() == 0
+        runs.append((o.cpu(), l.cpu()))
+    for o, l in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(l, runs[0][1])
+    prefix_pass(pa, c, plan, 3, np.asarray([0, 1, 2, 3, 4, 6], np.int32))
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0x10
 
 
 @pytest.mark.parametrize("group", [2, 8])
