@@ -18,8 +18,10 @@
 //      - split-context partitions (explicit partition size): grid
 //        (partition, kv-head, sequence), partials merged by a reduce kernel;
 //      - stream-K (the automatic plan): a persistent grid of two CTAs per SM,
-//        each owning an equal contiguous range of all stages in (sequence,
-//        kv-head, stage) order.  A unit lying wholly inside one CTA's range is
+//        each owning an equal contiguous range of the work in (sequence,
+//        kv-head, stage) order, where each unit's stages are followed by
+//        kUnitCost stages of no work standing for its fixed cost (q, barrier,
+//        combine, store).  A unit lying wholly inside one CTA's range is
 //        written directly; a unit cut by a range boundary leaves partials in
 //        the (at most two) CTAs that share it, merged by a second kernel.  This
 //        removes the partly filled last wave and the per-CTA start-up of a
@@ -49,6 +51,9 @@
 //    are rescaled only when some head's maximum moved.
 //  * The warps' (m, l, o) are merged in shared memory; bf16 output or fp32
 //    partials (o normalised by l, m in the log2 domain, l) are written.
+//  * Cascade (a prefix term given): every writer of a final output row folds
+//    in the row's attention over a shared prefix, computed apart, as one more
+//    record (its normalised output with l = 1 and m = its log-sum-exp).
 //  * Every table entry and length is bounds-checked; an out-of-range value is
 //    reported in the error word and never dereferenced.  Every barrier wait
 //    is bounded.
