@@ -407,6 +407,15 @@ pa_status pa_decode_cascade(void *out, const void *q, const pa_kv_pool *pool,
                             uint32_t flags, cudaStream_t stream);
 
 /*
+ * Check of the bounded waits: launches one CTA whose wait on a shared-memory
+ * barrier that nothing arrives at gives up after limit_ns (1 us .. 1 s, else
+ * PA_ERR_INVALID_ARG) through the same wait every kernel uses, records
+ * PA_DEVERR_TIMEOUT and returns; read the word with pa_get_device_error.
+ * Nothing faults and the context stays usable.
+ */
+pa_status pa_check_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
+/*
  * Reads (and, if clear != 0, resets) the current device's error word after
  * synchronising `stream`.  Returns PA_ERR_DEVICE when the word is non-zero.
  */

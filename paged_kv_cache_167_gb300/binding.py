@@ -67,6 +67,7 @@ SIGNATURES = {
                                  _U32, _P]),
     "pa_cascade_plan": (_I32, [_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "pa_get_device_error": (_I32, [ctypes.POINTER(_U32), _I32, _P]),
+    "pa_check_wait_timeout": (_I32, [ctypes.c_uint64, _P]),
     "pa_block_layout": (_I32, [_I64, _I32, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "pa_slot_mapping": (_I32, [_P, _P, _I32, _I32, _P, _P, _I64, _I32, _I64]),
     "pa_bm_create": (_I32, [ctypes.POINTER(_P), _I64, _I32]),
@@ -413,6 +414,12 @@ def cascade_plan(tables, seq_lens, group_size: int, block_size: int) -> dict:
     _check(lib().pa_cascade_plan(ptr(t), W, ptr(L), B, int(group_size), int(block_size), ptr(pt), ptr(pl), ptr(go),
                                  ptr(st), ptr(sl)), "pa_cascade_plan")
     return {"prefix_tables": pt, "prefix_lens": pl, "group_order": go, "suffix_tables": st, "suffix_lens": sl}
+
+
+def check_wait_timeout(limit_ns: int, stream=None) -> None:
+    """pa_check_wait_timeout: a wait that nothing completes gives up after
+    ``limit_ns`` and records PA_DEVERR_TIMEOUT in the error word."""
+    _check(lib().pa_check_wait_timeout(int(limit_ns), _stream(stream)), "pa_check_wait_timeout")
 
 
 def get_device_error(clear: bool = True, stream=None) -> int:

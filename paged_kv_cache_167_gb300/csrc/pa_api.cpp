@@ -366,6 +366,11 @@ pa_status pa_prefix_attention(float *o_part, float *lse, const void *q, const pa
     return launch_prefill(a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status pa_check_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+    if (limit_ns < 1000u || limit_ns > 1000000000u) return PA_ERR_INVALID_ARG;
+    return launch_wait_timeout(limit_ns, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 pa_status pa_get_device_error(uint32_t *err_out, int32_t clear, cudaStream_t stream) {
     if (!err_out) return PA_ERR_INVALID_ARG;
     unsigned int *word = device_error_word();

@@ -312,6 +312,27 @@ cudaError_t launch_append_last(const PoolView &pool, const int32_t *tables, int3
     return launch_pdl(append_last_kernel, dim3((unsigned)blocks), dim3(threads), stream, p);
 }
 
+// One CTA waits on a shared-memory barrier that no thread ever arrives at,
+// through the same bounded wait every kernel uses, and gives up after
+// limit_ns: the path a kernel takes when a copy or an MMA it waits for never
+// completes, taken here without any fault.
+__global__ void __launch_bounds__(32) wait_timeout_kernel(unsigned int *err, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, err, limit_ns);   // nothing arrives: records the timeout
+}
+
+cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+    unsigned int *err = device_error_word();
+    if (!err) return cudaErrorUnknown;
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_reshape_and_cache(const PoolView &pool, const void *k, const void *v,
                                      const int64_t *slots, int64_t num_tokens, cudaStream_t stream) {
     if (num_tokens == 0) return cudaSuccess;

@@ -80,13 +80,14 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t pa
 }
 
 // Waits for the barrier phase with the given parity to complete.  Returns
-// false (after recording PA_DEVERR_TIMEOUT) if it has not after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, unsigned int *err) {
+// false (after recording PA_DEVERR_TIMEOUT) if it has not after limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, unsigned int *err,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             raise_error(err, PA_DEVERR_TIMEOUT);
             return false;
         }

@@ -26,6 +26,7 @@ struct PoolView {
 // Device address of the current device's error word (set up once per device);
 // nullptr if the CUDA runtime failed.
 unsigned int *device_error_word();
+cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device); 0 on failure.
 int device_sm_count();

@@ -104,6 +104,8 @@ def test_host_validation(B):
     assert L.pa_decode_host(*host(st=P(0x40010))) == 3                 # staging not 256-byte aligned
     assert L.pa_decode_host(*host(q=P(0))) == 1                        # no q
     assert L.pa_decode_host(*host(nk=ok_ptr)) == 1                     # new K without new V
+    assert L.pa_check_wait_timeout(999, P(0)) == 1                    # limit below 1 us
+    assert L.pa_check_wait_timeout(10**9 + 1, P(0)) == 1              # above 1 s
     err = ctypes.c_uint32()
     assert L.pa_get_device_error(None, 0, P(0)) == 1
 
