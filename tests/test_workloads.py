@@ -55,3 +55,23 @@ def test_tensors_shapes():
     unused = np.setdiff1d(np.arange(32), w.referenced)
     assert not t["pool"][unused].any()
     assert np.array_equal(wl.bf16_bits(wl.make_tensors(w)["q"]), wl.bf16_bits(t["q"]))
+
+
+def test_shared_groups():
+    """Each group's tables start with the same prefix blocks; every other block
+    is used by one table only; lengths are prefix + suffix."""
+    prefix, suffix, gsz = [32, 0, 64], [1, 17, 5, 0, 40, 16], 2
+    w = wl.shared_groups(prefix, suffix, gsz, 8, 2, 128, 16, seed=3)
+    _check_tables(w)
+    assert w.seq_lens.tolist() == [33, 49, 5, 0, 104, 80]
+    seen = {}
+    for s in range(w.batch):
+        n_pre = prefix[s // gsz] // 16
+        head = w.tables[s, :n_pre].tolist()
+        first = w.tables[(s // gsz) * gsz, :n_pre].tolist()
+        assert head == first
+        for blk in w.tables[s, n_pre:][w.tables[s, n_pre:] >= 0].tolist():
+            assert blk not in seen, blk
+            seen[blk] = s
+    shared = {b for g, p in enumerate(prefix) for b in w.tables[g * gsz, :p // 16].tolist()}
+    assert not shared & set(seen)
