@@ -556,6 +556,9 @@ def run_ours(args, world, rank, local):
     total_ms, e2e_ms, decode_avg_ms, wtotal_ms, ftotal_ms, fdecode_ms = reduce_max(
         [total_ms, e2e_s * 1e3, decode_total_ms / K, sum(wstep_ms), sum(flushed_ms), float(np.mean(flushed_decode_ms))],
         world, dev)
+    if casc is not None:   # every rank runs the same kind of workload: all or none measure a cascade
+        keys = ("step_ms", "prefix_ms", "suffix_ms")
+        casc.update(zip(keys, (round(v, 5) for v in reduce_max([casc[k] for k in keys], world, dev))))
 
     if rank != 0:
         if world > 1:
@@ -622,7 +625,7 @@ def run_ours(args, world, rank, local):
                                             "consecutive in the pool (identity placement) against random placement")
     if casc is not None:
         ub = unique_decode_bytes(w)
-        line["cascade"] = dict(casc, tokens_per_s=round(w.batch / (casc["step_ms"] / 1e3), 1),
+        line["cascade"] = dict(casc, tokens_per_s=round(world * w.batch / (casc["step_ms"] / 1e3), 1),
                                speedup_vs_step=round((total_ms / K) / casc["step_ms"], 3),
                                unique_gbs=round(ub / (casc["step_ms"] / 1e3) / 1e9, 1),
                                unique_frac=round(ub / (casc["step_ms"] / 1e3) / 1e9 / peak, 4),
