@@ -342,7 +342,8 @@ pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool,
  *                 writes that order).  It changes no result.  An entry outside
  *                 [0, num_groups) raises PA_DEVERR_ORDER and that CTA works on
  *                 its own index instead (some group is then done twice and
- *                 another not at all).
+ *                 another not at all); a repeated entry is not detected and
+ *                 leaves the rows of a missing group unwritten.
  *   max_prefix_len host bound, <= max_prefix_blocks * block_size
  *   scale         as pa_prefill_chunk
  * Every query of group i attends all prefix_lens[i] keys (no causal mask: the
