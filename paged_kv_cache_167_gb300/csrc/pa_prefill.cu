@@ -233,14 +233,18 @@ __device__ __forceinline__ float max_tree64(const uint32_t (&a)[32], const uint3
     return m[0];
 }
 
-// Timeline of tile t (the MMA lane runs one tile ahead on Q.K):
-//   K warp   : K(t) -> K slot t % 2 once Q.K(t-2) has completed
-//   V warp   : V(t) -> V slot t % 2 once P.V(t-2) has completed
-//   MMA lane : Q.K(t+1) -> S[(t+1)%2] ; P.V(t) once P(t) is ready
-//   softmax  : S[t%2] -> registers (frees S) ; row max over both halves ; P(t) ;
+// Timeline of tile t (kKV = kSBufs = 3):
+//   K warp   : K(t) -> K slot t % 3 once Q.K(t-3) has completed
+//   V warp   : V(t) -> V slot t % 3 once P.V(t-3) has completed
+//   Q.K lane : Q.K(t) -> S[t%3] once K(t) has landed and P.V(t-3) has completed
+//   P.V lane : P.V(t) once P(t) and V(t) are in place
+//   softmax  : S[t%3] -> registers ; row max over both halves ; P(t) into S[t%3] ;
 //              O rescale when the reference moved ; signal P(t)
 // Barriers: S ready (MMA commit), S free (256 arrivals), P ready (256 arrivals),
-// P.V done per P buffer (MMA commit), K / V / Q landed (TMA), drain (MMA commit).
+// P.V done per P buffer and per S buffer (MMA commit), K / V / Q landed (TMA),
+// one drain per MMA lane (MMA commit, used once).
+// A parity wait is exact only while the barrier's previous phase is known to
+// have completed; each wait below names the completion that guarantees it.
 template <int G, int BS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -386,7 +390,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return ok;
             };
-            int done = 0;
             if (is_qk) {
                 if (wait(barQ, 0)) {
                     for (int t = 0; t < n_tiles && ok && !*abort_flag; ++t) {
@@ -403,7 +406,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  smem_desc(sK + st * kTile + off, 16, 1024), idesc_qk, kk > 0);
                         }
                         umma_commit(barS + 8 * sb);
-                        done = t + 1;
                     }
                 }
             } else {
@@ -423,22 +425,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     umma_commit(barOP + 8 * (t & 1));
                     umma_commit(barSdone + 8 * (t % kSBufs));
-                    done = t + 1;
                 }
             }
-            if (!ok || *abort_flag) {
-                // give up: one more commit tracks every MMA this lane issued
-                *abort_flag = 1;
-                const uint32_t end = is_qk ? barEndQk : barEnd;
-                umma_commit(end);
-                mbar_wait(end, 0, p.err);
-            } else if (done > 0) {
-                const int t = done - 1;   // this lane's MMAs done before the memory is released
-                if (is_qk)
-                    mbar_wait(barS + 8 * (t % kSBufs), (uint32_t)((t / kSBufs) & 1), p.err);
-                else
-                    mbar_wait(barOP + 8 * (t & 1), (uint32_t)((t >> 1) & 1), p.err);
-            }
+            // One more commit, on a barrier used once, tracks every MMA this lane
+            // issued; its phase-0 wait is exact.  (Waiting on the last P.V's own
+            // barrier is not: the two P.V barriers alternate, and when P.V(t - 2)
+            // has not completed either, a parity wait for P.V(t) cannot tell the
+            // two apart and returns early.)  The softmax epilogue waits on the
+            // P.V lane's drain barrier before it reads O.
+            if (!ok || *abort_flag) *abort_flag = 1;   // give up: drain what was issued
+            const uint32_t end = is_qk ? barEndQk : barEnd;
+            umma_commit(end);
+            mbar_wait(end, 0, p.err);
         }
         __syncwarp();
     } else {
@@ -515,7 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tmem + sb * 128 + lane_off + hf * 64, pw);
             tmem_st_wait();
             l2.x = l2.x * alpha + (ps2.x + ps2.y);
-            // rescale this half of O once P.V(t-1) has completed
+            // rescale this half of O once P.V(t-1) has completed (the barrier's
+            // previous phase, P.V(t-3), completed before Q.K(t) was issued)
             if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 const int tp = t - 1;
                 mbar_wait(barOP + 8 * (tp & 1), (uint32_t)((tp >> 1) & 1), p.err);
@@ -555,9 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // with the row's log-sum-exp
         const float l = l2.x;
         const bool empty = n_tiles == 0;   // no keys: O = 0, lse = -inf, tensor memory never written
-        const bool fin = empty || (done == n_tiles && !*abort_flag &&
-                                   mbar_wait(barOP + 8 * ((n_tiles - 1) & 1), (uint32_t)(((n_tiles - 1) >> 1) & 1),
-                                             p.err));
+        // every P.V has completed once the P.V lane's drain commit has arrived
+        const bool fin = empty || (done == n_tiles && !*abort_flag && mbar_wait(barEnd, 0, p.err));
         xch[hf * 128 + r] = l;
         pair_sync(warp);
         const float lt = l + xch[(1 - hf) * 128 + r];
