@@ -19,6 +19,10 @@
  *    undefined.  Read the word with pa_get_device_error.
  *  - Tensors are bf16, row-major, densely packed unless a stride is given,
  *    and 16-byte aligned.
+ *  - Devices 0 .. 63 are supported: the library caches per-device state (the
+ *    error word's and the allocation-free scratch array's addresses, the SM
+ *    count) for those indices, and every device call made while a device
+ *    with a higher index is current returns PA_ERR_CUDA.
  *
  * Sources (page, section) for the operations:
  *  [P1] how-pagedattention-works (aiinfrainterviews.com)
@@ -215,6 +219,8 @@ pa_status pa_decode_ex(void *out, const void *q, const pa_kv_pool *pool,
  *  - All calls on a device share the array and it keeps the last call's
  *    contents (nothing in it needs to start at zero).  Calls whose kernels
  *    overlap on the GPU, e.g. on two streams, race on it: serialise them.
+ *  - Called while a device with index 64 or more is current, it returns
+ *    PA_ERR_CUDA and launches nothing.
  */
 pa_status pa_decode_noalloc(void *out, const void *q, const pa_kv_pool *pool,
                             const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -415,6 +421,22 @@ pa_status pa_decode_cascade(void *out, const void *q, const pa_kv_pool *pool,
  * Nothing faults and the context stays usable.
  */
 pa_status pa_check_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
+/*
+ * Testing hook: the number of CTAs of the balanced (partition_tokens = 0)
+ * decode grid.  ctas > 0 fixes it for every later call in the process that
+ * plans that schedule (pa_decode, pa_decode_ex, pa_decode_noalloc,
+ * pa_decode_host, pa_decode_cascade, pa_decode_workspace_size), still capped
+ * at the batch's number of 16-token stages as the default is; 0 restores the
+ * default of two CTAs per SM of the current device.  Which units a range
+ * boundary cuts, and so which partial records the merge kernel combines,
+ * follows from this number: sweeping it exercises every cut on one GPU,
+ * whatever its SM count.  Not for production use: the setting is
+ * process-wide, and a workspace sized under one setting is too small under a
+ * larger one.  Negative values give PA_ERR_INVALID_ARG.  The pages have no
+ * counterpart to this call.
+ */
+pa_status pa_set_stream_k_ctas(int32_t ctas);
 
 /*
  * Reads (and, if clear != 0, resets) the current device's error word after

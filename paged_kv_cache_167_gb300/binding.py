@@ -68,6 +68,7 @@ SIGNATURES = {
     "pa_cascade_plan": (_I32, [_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "pa_get_device_error": (_I32, [ctypes.POINTER(_U32), _I32, _P]),
     "pa_check_wait_timeout": (_I32, [ctypes.c_uint64, _P]),
+    "pa_set_stream_k_ctas": (_I32, [_I32]),
     "pa_block_layout": (_I32, [_I64, _I32, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "pa_slot_mapping": (_I32, [_P, _P, _I32, _I32, _P, _P, _I64, _I32, _I64]),
     "pa_bm_create": (_I32, [ctypes.POINTER(_P), _I64, _I32]),
@@ -420,6 +421,12 @@ def check_wait_timeout(limit_ns: int, stream=None) -> None:
     """pa_check_wait_timeout: a wait that nothing completes gives up after
     ``limit_ns`` and records PA_DEVERR_TIMEOUT in the error word."""
     _check(lib().pa_check_wait_timeout(int(limit_ns), _stream(stream)), "pa_check_wait_timeout")
+
+
+def set_stream_k_ctas(ctas: int) -> None:
+    """pa_set_stream_k_ctas (testing hook): fix the balanced decode grid at
+    ``ctas`` CTAs for later calls in this process; 0 restores the default."""
+    _check(lib().pa_set_stream_k_ctas(int(ctas)), "pa_set_stream_k_ctas")
 
 
 def get_device_error(clear: bool = True, stream=None) -> int:

@@ -1,6 +1,7 @@
 // pa_api.cpp -- the C ABI (include/pa.h): argument validation, partition
 // planning and dispatch to the kernels.  Host code only; it allocates no
 // device memory and launches nothing when validation fails.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime_api.h>
@@ -23,6 +24,9 @@ constexpr int kDecodeWarps = PA_DECODE_WARPS;  // warps per decode CTA (must mat
 #endif
 constexpr int kStreamKCtasPerSm = PA_DECODE_SK_CTAS_PER_SM;     // resident decode CTAs per SM (persistent stream-K grid)
 constexpr size_t kWsAlign = 256;
+
+// pa_set_stream_k_ctas: a fixed balanced-schedule grid size (0: two per SM).
+std::atomic<int32_t> g_stream_k_ctas{0};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -73,9 +77,12 @@ pa_status plan_decode(const PoolView &pool, int32_t num_seqs, int32_t num_q_head
         // stage) work equally; at most two partial records per CTA.
         const int64_t stage = decode_stage_tokens(pool.block_size);
         const int64_t max_stages = (int64_t)num_seqs * pool.num_kv_heads * ceil_div(max_seq_len, stage);
-        int sms = device_sm_count();
-        if (sms <= 0) sms = 148;
-        int64_t ctas = (int64_t)sms * kStreamKCtasPerSm;
+        int64_t ctas = g_stream_k_ctas.load(std::memory_order_relaxed);
+        if (ctas <= 0) {
+            int sms = device_sm_count();
+            if (sms <= 0) sms = 148;
+            ctas = (int64_t)sms * kStreamKCtasPerSm;
+        }
         if (ctas > max_stages) ctas = max_stages;
         if (ctas < 1) ctas = 1;
         plan->stream_k = true;
@@ -369,6 +376,12 @@ pa_status pa_prefix_attention(float *o_part, float *lse, const void *q, const pa
 pa_status pa_check_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
     if (limit_ns < 1000u || limit_ns > 1000000000u) return PA_ERR_INVALID_ARG;
     return launch_wait_timeout(limit_ns, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_set_stream_k_ctas(int32_t ctas) {
+    if (ctas < 0) return PA_ERR_INVALID_ARG;
+    g_stream_k_ctas.store(ctas, std::memory_order_relaxed);
+    return PA_OK;
 }
 
 pa_status pa_get_device_error(uint32_t *err_out, int32_t clear, cudaStream_t stream) {

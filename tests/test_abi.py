@@ -172,3 +172,26 @@ def test_product_does_not_touch_the_oracle():
             text = open(os.path.join(ROOT, "oracle", f)).read()
             assert not re.search(r"^\s*(import|from)\s+paged_kv_cache_167_gb300", text, re.M), f
             assert "libpa.so" not in text and "pa_decode" not in text, f
+
+
+def test_stream_k_grid_override_sizes_the_workspace(B):
+    """pa_set_stream_k_ctas fixes the balanced grid: the workspace is then
+    (B + 1) ints plus two fp32 records of G x (d + 2) per CTA, each part
+    rounded up to 256 bytes, with the grid capped at the batch's 16-token
+    stages; 0 restores the default and a negative count is refused."""
+    L = B.lib()
+    pool = _pool(B, nb=64, hkv=8, b=16, d=128)
+    r256 = lambda x: (x + 255) // 256 * 256
+    try:
+        for ctas in (1, 7, 152, 304, 1000):
+            assert L.pa_set_stream_k_ctas(ctas) == 0
+            nseq, hq, maxlen = 33, 64, 500
+            eff = min(ctas, nseq * 8 * ((maxlen + 15) // 16))
+            want = r256((nseq + 1) * 4) + r256(2 * eff * 8 * 128 * 4) + r256(2 * eff * 8 * 2 * 4)
+            assert L.pa_decode_workspace_size(ctypes.byref(pool), nseq, hq, maxlen, 0) == want
+        assert L.pa_set_stream_k_ctas(1000) == 0   # capped: 2 sequences x 8 heads x 1 stage
+        assert L.pa_decode_workspace_size(ctypes.byref(pool), 2, 64, 16, 0) == \
+            r256(3 * 4) + r256(2 * 16 * 8 * 128 * 4) + r256(2 * 16 * 8 * 2 * 4)
+        assert L.pa_set_stream_k_ctas(-1) == 1
+    finally:
+        assert L.pa_set_stream_k_ctas(0) == 0

@@ -129,6 +129,44 @@ def test_many_short_units_per_cta(pa, batch, hkv):
     assert_close(run_decode(pa, c, 0, pa.PA_DECODE_EARLY_METADATA), ref, f"B={batch} Hkv={hkv} early")
 
 
+# Balanced-schedule grid sizes: tiny grids (one CTA holds everything), sizes
+# around one and two CTAs per SM of 148- and 152-SM parts, and grids larger
+# than the number of resident CTAs.
+GRID_SWEEP = [1, 2, 3, 5, 7, 13, 31, 64, 100, 147, 148, 151, 152, 153, 255, 296, 303, 304, 305, 607, 1000]
+
+
+def _grid_workload(name):
+    rng = np.random.default_rng(404)
+    if name == "ragged":        # units of 1 .. 44 stages, many cut by range boundaries
+        lens = list(rng.integers(1, 700, size=40))
+        return wl.custom(lens, 64, 8, 128, 16, seed=405)
+    if name == "one_stage":     # 128 sequences of one stage each (the beams' suffixes)
+        return wl.custom(list(rng.integers(1, 17, size=128)), 64, 8, 128, 16, seed=406)
+    # more sequences than one listing pass holds (stage prefix in the workspace), b = 4
+    lens = list(rng.integers(0, 150, size=200))
+    return wl.custom(lens, 4, 2, 64, 4, seed=407)
+
+
+@pytest.mark.parametrize("name", ["ragged", "one_stage", "many_seqs_b4"])
+def test_stream_k_grid_sweep(pa, name):
+    """The balanced schedule at many grid sizes against the oracle.  The grid
+    size moves every CTA range boundary, and with it which units are cut,
+    which partial record each CTA writes and which records the merge kernel
+    combines; the default grid follows the device's SM count, so these sizes
+    cover what other SM counts would run."""
+    w = _grid_workload(name)
+    c = Case(w)
+    write_new_tokens(pa, c)
+    ref = oracle_decode(c)
+    try:
+        for ctas in GRID_SWEEP:
+            pa.set_stream_k_ctas(ctas)
+            assert_close(run_decode(pa, c, 0), ref, f"{name} ctas={ctas}")
+            assert_close(run_decode(pa, c, 0, pa.PA_DECODE_EARLY_METADATA), ref, f"{name} ctas={ctas} early")
+    finally:
+        pa.set_stream_k_ctas(0)
+
+
 def test_partitions_agree(pa):
     """P = 1 and many partitions both match the oracle on the same inputs."""
     w = wl.llama70b_decode(batch=16)

@@ -224,3 +224,56 @@ def test_full_size_cascade(pa, name, group_size):
     flat = rng.choice(w.batch * w.num_q_heads, size=2048, replace=False)
     rows = np.stack([flat // w.num_q_heads, flat % w.num_q_heads], axis=1)
     assert_close(out[rows[:, 0], rows[:, 1]], oracle_full(c, rows), name)
+
+
+def _beam_case(pa):
+    w = wl.beam_fork()
+    c = Case(w)
+    pa.copy_blocks(c.pool, torch.as_tensor(w.copy_pairs, device=c.dev))
+    c.orc.copy_blocks(c.pool_ref, c.geom, w.copy_pairs)
+    write_new_tokens(pa, c)
+    return w, c, pa.cascade_plan(w.tables, w.seq_lens, 4, w.block_size)
+
+
+def test_beam_cascade_repeatable_under_contention(pa):
+    """The full-size beam cascade sixteen times, every other time while a
+    second stream copies gigabytes (HBM contention makes K/V tiles land late
+    and in other orders): every run is bit-identical to the first, and the
+    first matches the oracle on every row.  The prefix pass is HBM-bound on
+    this batch; a completion wait that passes early there leaves the last key
+    tiles of one (group, kv-head) tile out of its output."""
+    w, c, plan = _beam_case(pa)
+    ref = oracle_full(c)
+    ref_o, ref_lse = oracle_prefix(c, plan, 4)
+    side = torch.cuda.Stream()
+    src = torch.empty(1 << 30, dtype=torch.uint8, device=c.dev)
+    dst = torch.empty_like(src)
+    first = None
+    for rep in range(16):
+        if rep % 2:
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    dst.copy_(src)
+        out, o_part, lse = cascade(pa, c, plan, 4, 0, flags=1)
+        torch.cuda.synchronize()
+        if first is None:
+            assert_close(o_part, ref_o, "beam prefix pass")
+            check_lse(lse, ref_lse, "beam prefix lse")
+            assert_close(out, ref, "beam cascade")
+            first = (out.clone(), o_part.clone(), lse.clone())
+        else:
+            assert torch.equal(o_part, first[1]) and torch.equal(lse, first[2]), f"prefix pass differs at run {rep}"
+            assert torch.equal(out, first[0]), f"cascade output differs at run {rep}"
+
+
+@pytest.mark.parametrize("ctas", [1, 7, 64, 151, 152, 300, 304, 1000])
+def test_beam_cascade_grid_sweep(pa, ctas):
+    """The beam batch's suffix decode (one-stage units) with the prefix folded
+    in, at several balanced-schedule grid sizes, against the oracle."""
+    w, c, plan = _beam_case(pa)
+    try:
+        pa.set_stream_k_ctas(ctas)
+        out, _, _ = cascade(pa, c, plan, 4, 0, flags=1)
+    finally:
+        pa.set_stream_k_ctas(0)
+    assert_close(out, oracle_full(c), f"beam cascade ctas={ctas}")
