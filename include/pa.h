@@ -112,8 +112,8 @@ pa_status pa_reshape_and_cache(const pa_kv_pool *pool, const void *k, const void
  * Bytes of device workspace pa_decode needs for these shapes.  With an
  * explicit partition_tokens it is 0 when one partition covers max_seq_len;
  * with partition_tokens = 0 (the balanced schedule) it is a few MB at most:
- * (num_seqs + 1) ints plus two partial records per CTA of a grid sized from
- * the current device's SM count.
+ * two fp32 partial records of (num_q_heads / Hkv) x (head_dim + 2) per CTA of
+ * a grid sized from the current device's SM count.
  */
 size_t pa_decode_workspace_size(const pa_kv_pool *pool, int32_t num_seqs, int32_t num_q_heads,
                                 int32_t max_seq_len, int32_t partition_tokens);
@@ -184,11 +184,12 @@ pa_status pa_decode(void *out, const void *q, const pa_kv_pool *pool,
  * either way; with this flag it reads the lengths and table entries and
  * plans its schedule while that previous kernel is still running, and only
  * q, the pool and the workspace wait for it to finish, which takes the
- * lengths -> schedule -> table chain off the call's start.  It applies to
- * the automatic plan (partition_tokens = 0) with at most 128 sequences and
- * is otherwise ignored; results are identical with and without it.  (The
- * pool may be written by that previous kernel: the slot writer is the usual
- * one.)
+ * lengths -> schedule -> table chain off the call's start; it also brings
+ * the first blocks each CTA will read into L2 (a prefetch hint, which reads
+ * whatever that kernel writes there correctly).  It applies to the automatic
+ * plan (partition_tokens = 0) and is otherwise ignored; results are
+ * identical with and without it.  (The pool may be written by that previous
+ * kernel: the slot writer is the usual one.)
  * Unknown flag bits give PA_ERR_INVALID_ARG.
  */
 #define PA_DECODE_EARLY_METADATA 0x1u

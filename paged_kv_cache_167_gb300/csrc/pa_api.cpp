@@ -59,10 +59,9 @@ struct DecodePlan {
     int32_t partition_tokens; // split-context plan
     int32_t num_partitions;
     int32_t num_ctas;         // stream-K grid
-    size_t ws_cum_bytes;
     size_t ws_o_bytes;
     size_t ws_ml_bytes;
-    size_t total_bytes() const { return ws_cum_bytes + ws_o_bytes + ws_ml_bytes; }
+    size_t total_bytes() const { return ws_o_bytes + ws_ml_bytes; }
 };
 
 pa_status plan_decode(const PoolView &pool, int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
@@ -89,7 +88,6 @@ pa_status plan_decode(const PoolView &pool, int32_t num_seqs, int32_t num_q_head
         plan->partition_tokens = max_seq_len > 0 ? max_seq_len : 1;   // length bound used by the kernel
         plan->num_partitions = 1;
         plan->num_ctas = (int32_t)ctas;
-        plan->ws_cum_bytes = round_up(((size_t)num_seqs + 1) * sizeof(int32_t), kWsAlign);
         plan->ws_o_bytes = round_up((size_t)2 * ctas * group * pool.head_dim * sizeof(float), kWsAlign);
         plan->ws_ml_bytes = round_up((size_t)2 * ctas * group * 2 * sizeof(float), kWsAlign);
         return PA_OK;
@@ -226,9 +224,8 @@ pa_status decode_impl(void *out, const void *q, const pa_kv_pool *pool, const in
     a.partition_tokens = plan.partition_tokens;
     a.num_partitions = plan.num_partitions;
     char *ws = static_cast<char *>(workspace);
-    a.ws_cum = plan.ws_cum_bytes ? reinterpret_cast<int32_t *>(ws) : nullptr;
-    a.ws_o = plan.ws_o_bytes ? reinterpret_cast<float *>(ws + plan.ws_cum_bytes) : nullptr;
-    a.ws_ml = plan.ws_ml_bytes ? reinterpret_cast<float *>(ws + plan.ws_cum_bytes + plan.ws_o_bytes) : nullptr;
+    a.ws_o = plan.ws_o_bytes ? reinterpret_cast<float *>(ws) : nullptr;
+    a.ws_ml = plan.ws_ml_bytes ? reinterpret_cast<float *>(ws + plan.ws_o_bytes) : nullptr;
     a.stream_k = plan.stream_k;
     a.num_ctas = plan.num_ctas;
     a.early_meta = (flags & PA_DECODE_EARLY_METADATA) != 0;

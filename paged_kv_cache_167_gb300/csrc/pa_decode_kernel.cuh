@@ -61,8 +61,12 @@
 //    global memory overlaps the previous kernel's tail, and every global read
 //    waits on griddepcontrol.wait -- except, when the caller sets the
 //    early-metadata flag (lengths and tables not written by the previous
-//    kernel), the stream-K kernel's reads of lengths and table entries and
-//    the planning of its first listing, which then overlap that kernel too.
+//    kernel), the stream-K kernel's reads of lengths and table entries, the
+//    planning of its first listing and L2 prefetches of its first stages'
+//    blocks, which then overlap that kernel too.
+//  * The stream-K merge kernel runs one block per decode CTA, so its blocks
+//    wait resident beside the decode CTAs instead of holding SMs that the
+//    next call's decode CTAs need.
 #pragma once
 
 #include <cfloat>
@@ -94,6 +98,12 @@ constexpr int kSkStages = PA_DECODE_SK_STAGES; // ring depth per warp, stream-K 
 constexpr int kMinCtas = PA_DECODE_MIN_CTAS;   // resident CTAs per SM the register budget targets
 constexpr int kOnePassSeqs = kWarps * 32;       // stream-K: sequences listed in one pass, one per thread
 constexpr int kMaxSegs = 32;                   // stream-K: units per pass of a CTA's range
+#ifndef PA_SK_PREFETCH_STAGES
+#define PA_SK_PREFETCH_STAGES 2
+#endif
+// Stream-K with early metadata: stages per warp whose K/V boxes are prefetched
+// into L2 before griddepcontrol.wait, while the previous kernel finishes.
+constexpr int kSkPrefetch = PA_SK_PREFETCH_STAGES;
 #ifndef PA_SK_UNIT_COST
 #define PA_SK_UNIT_COST 12
 #endif
@@ -182,7 +192,6 @@ struct Params {
     int32_t num_parts;         // split-context: partitions; stream-K: 1
     float *ws_o;               // split-context [B][Hq][P][D]; stream-K records [2C][G][D]
     float *ws_ml;              // split-context [B][Hq][P][2]; stream-K records [2C][G][2]
-    int32_t *ws_cum;           // stream-K, more than kOnePassSeqs sequences: [B + 1] stage prefix (all kv-heads)
     int32_t num_ctas;          // stream-K grid size
     int32_t early_meta;        // stream-K: lengths and tables may be read before griddepcontrol.wait
     // stream-K append: the K/V of each sequence's last token, stored at its
@@ -808,9 +817,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
     // read, and the first listing made, while the previous kernel in the
     // stream finishes; q, the pool and the workspace are touched only after
     // griddepcontrol.wait.
-    static_assert(NT == kOnePassSeqs, "the merge kernel sums the stage prefix itself up to kOnePassSeqs");
     const bool one_pass = B <= NT;
-    bool waited = !(p.early_meta && one_pass);
+    bool waited = !p.early_meta;
     if (waited) grid_dependency_wait();
 
     // ---- total work W (unit spans over all units) and this CTA's range [gs, ge)
@@ -824,12 +832,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
         const int v = Hkv * unit_span(ns);
         int chunk;
         const int inc = block_inclusive_scan(v, sk->scan, chunk);
-        if (!one_pass && c == 0 && s < B) p.ws_cum[s] = total + inc - v;   // the merge kernel's prefix
         my_ns = ns;
         my_first = total + inc - v;
         total += chunk;
     }
-    if (!one_pass && c == 0 && tid == 0) p.ws_cum[B] = total;
     auto wait_inputs = [&]() {   // the deferred wait (early_meta)
         if (waited) return;
         grid_dependency_wait();
@@ -991,6 +997,34 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
             return id;
         };
         int id_cache = load_ids(0);
+        if (!waited) {
+            // The previous kernel may still be writing the pool (the slot
+            // writer does) or q: the first segments' q rows and the first
+            // stages' boxes go to L2 now, as a hint, and their copies after the
+            // wait find them there.
+            if (tid < 2 && tid < nseg) {
+                const size_t head0 = (size_t)sk->seg_s[tid] * p.num_q_heads + (size_t)sk->seg_g[tid] * G;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.q + head0 * D),
+                             "r"((uint32_t)(G * D * 2))
+                             : "memory");
+            }
+#pragma unroll 1
+            for (int k = 0; k < kSkPrefetch && k < my_n && (k + 1) * S::BPS <= 32; ++k) {
+                const int i = warp + k * kWarps;
+                int j = 0;
+                while (j + 1 < nseg && sk->seg_lb[j + 1] <= i) ++j;
+                const int g = sk->seg_g[j];
+                const int c_slot = S::slot_of((sk->seg_kb[j] + i - sk->seg_lb[j]) * S::TPS);
+#pragma unroll
+                for (int ib = 0; ib < S::BPS; ++ib) {
+                    const int id = __shfl_sync(0xffffffffu, id_cache, k * S::BPS + ib);
+                    if (lane == 0 && id >= 0) {
+                        tensor_prefetch_l2_5d(&tmk, 0, c_slot, 0, g, id);
+                        tensor_prefetch_l2_5d(&tmv, 0, c_slot, 0, g, id);
+                    }
+                }
+            }
+        }
         wait_inputs();
 
         // q of the first two segments
@@ -1136,100 +1170,169 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas)
     grid_launch_dependents();
 }
 
-// Finish the stream-K schedule for one (sequence, kv-head) unit: zero output
-// for an empty sequence; merge the partial records of a unit that two or more
-// CTAs shared; nothing for a unit one CTA completed.  grid (Hkv, B).
-// For up to kOnePassSeqs sequences the stage prefix is summed from the
-// lengths before griddepcontrol.wait: the decode kernel this one follows
-// never writes them, and every decode CTA waited for the kernels before it.
-// Every decode CTA lets this kernel launch once it has issued its first
-// copies, so the sums above run while the decode kernel streams.
+// Finish the stream-K schedule.  grid (num_ctas), kWarps * 32 threads: block c
+// merges the unit that the start of decode CTA c's range cuts, when that is
+// the unit's first cut (a unit cut several times is merged by the block of its
+// first cut, from the records of every CTA it spans), and writes the rows of
+// the sequences with no keys among s = c, c + num_ctas, ...: zeros, or the
+// prefix term alone.  A unit that one CTA completed needs nothing here.
+// The unit is located from the lengths, before griddepcontrol.wait: each
+// thread sums the unit spans of a slice of the sequences and a block scan
+// gives the slices' starts.  The decode kernel this one follows never writes
+// the lengths, and every decode CTA waited for the kernels before it.
+// With one block per decode CTA (at most two per SM) the whole grid fits
+// beside the running decode CTAs, so its blocks wait resident and release no
+// SM late; the next kernel's CTAs take the SMs the decode CTAs leave.
+#ifndef PA_MERGE_THREADS
+#define PA_MERGE_THREADS 128
+#endif
+#ifndef PA_MERGE_MIN_BLOCKS
+#define PA_MERGE_MIN_BLOCKS 10
+#endif
+constexpr int kMergeThreads = PA_MERGE_THREADS;
+// Registers: two stream-K CTAs leave 65536 - 2 * 128 * 200 = 14336 per SM,
+// room for two merge blocks of 128 threads at 56 registers.  The bound of 10
+// blocks a SM caps them at 48 (one spilled word), which leaves slack for an
+// uneven placement of warps: at 56, some SMs kept the next call's decode CTAs
+// waiting for merge blocks to exit (34.93 against 34.43 us a call on the
+// Llama-shaped batch).
 template <int D, int G, int BS>
-__global__ void __launch_bounds__(G *D / 4) paged_decode_sk_merge_kernel(const Params p) {
+__global__ void __launch_bounds__(kMergeThreads, PA_MERGE_MIN_BLOCKS) paged_decode_sk_merge_kernel(const Params p) {
     grid_launch_dependents();   // the next kernel waits for this grid's completion before using its data
-    constexpr int NT = G * D / 4;
-    const int g = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
-    const int h = tid / (D / 4);
-    const int i = (tid % (D / 4)) * 4;
-    const int B = p.num_seqs, Hkv = p.num_kv_heads;
-    const size_t row = (size_t)s * p.num_q_heads + (size_t)g * G + h;
-    const int ns = seq_stages<BS>(p, s, false);
-    int before = 0, total = 0;
-    const bool local = B <= kOnePassSeqs;
-    if (local) {
-        for (int t = tid; t < B; t += NT) {
-            const int v = Hkv * unit_span(seq_stages<BS>(p, t, false));
-            total += v;
-            before += t < s ? v : 0;
-        }
-        constexpr int W = NT < 32 ? NT : 32;
-        constexpr unsigned mask = NT < 32 ? ((1u << NT) - 1u) : 0xffffffffu;
+    constexpr int NT = kMergeThreads, NW = NT / 32;
+    __shared__ int scan[NW];
+    __shared__ int found[3];    // sequence, kv-head and work position of the unit to merge (sequence -1: none)
+    const int c = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = p.num_seqs, Hkv = p.num_kv_heads, C = p.num_ctas;
+    const int per_thread = (B + NT - 1) / NT;
+    const int s0 = min(B, tid * per_thread), s1 = min(B, s0 + per_thread);
+    int mine = 0;
+    for (int s = s0; s < s1; ++s) mine += Hkv * unit_span(seq_stages<BS>(p, s, false));
+    int inc = mine;   // block scan of the slices' spans
 #pragma unroll
-        for (int o = W / 2; o > 0; o >>= 1) {
-            before += __shfl_xor_sync(mask, before, o);
-            total += __shfl_xor_sync(mask, total, o);
-        }
-        if constexpr (NT > 32) {
-            __shared__ int red[2][NT / 32];
-            if ((tid & 31) == 0) {
-                red[0][tid >> 5] = before;
-                red[1][tid >> 5] = total;
-            }
-            __syncthreads();
-            before = total = 0;
+    for (int d = 1; d < 32; d <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += u;
+    }
+    if (lane == 31) scan[warp] = inc;
+    if (tid == 0) found[0] = -1;
+    __syncthreads();
+    int total = 0, excl = inc - mine;
 #pragma unroll
-            for (int w = 0; w < NT / 32; ++w) {
-                before += red[0][w];
-                total += red[1][w];
+    for (int w = 0; w < NW; ++w) {
+        total += scan[w];
+        excl += w < warp ? scan[w] : 0;
+    }
+    const int per = (total + C - 1) / C;
+    const int P = c * per;   // the start of decode CTA c's range
+    if (c > 0 && P < total && excl <= P && P < excl + mine) {
+        int run = excl;
+        for (int s = s0; s < s1; ++s) {
+            const int ns = seq_stages<BS>(p, s, false);
+            const int span = unit_span(ns), v = Hkv * span;
+            if (P < run + v) {
+                const int g = (P - run) / span, kb = (P - run) % span, u0 = run + g * span;
+                // P falls after the unit's first stage and on one of its stages,
+                // and the unit starts in CTA c - 1's range: its first cut
+                if (kb >= 1 && kb < ns && u0 >= (c - 1) * per) {
+                    found[0] = s;
+                    found[1] = g;
+                    found[2] = u0;
+                }
+                break;
             }
+            run += v;
         }
     }
+    __syncthreads();
     grid_dependency_wait();
-    const PrefixTerm<4> pre = load_prefix<4>(p, row, D, i);
-    if (ns == 0) {   // no keys of its own: zero, or the prefix term alone
-        float a4[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
-        fold_prefix<4>(pre, -INFINITY, wsum, a4);
-        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-        *reinterpret_cast<uint2 *>(p.out + row * D + i) =
-            make_uint2(pack_bf16x2(a4[0] * inv, a4[1] * inv), pack_bf16x2(a4[2] * inv, a4[3] * inv));
-        return;
-    }
-    if (!local) {
-        before = p.ws_cum[s];
-        total = p.ws_cum[B];
-    }
-    const int per = (total + p.num_ctas - 1) / p.num_ctas;
-    const int start = before + g * unit_span(ns), last = start + ns - 1;
-    const int ca = start / per, cb = last / per;
-    if (ca == cb) return;
-    // the unit is CTA ca's first segment unless a stage of the unit before it
-    // (which ends kUnitCost positions before `start`) lies in that CTA's range
-    const int first_rec = (start - ca * per > kUnitCost) ? 1 : 0;
-    float M = -INFINITY;
-    for (int cc = ca; cc <= cb; ++cc) {
-        const int rec = 2 * cc + (cc == ca ? first_rec : 0);
-        M = fmaxf(M, p.ws_ml[((size_t)rec * G + h) * 2]);
-    }
-    float wsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-        for (int cc = ca; cc <= cb; ++cc) {
-            const int rec = 2 * cc + (cc == ca ? first_rec : 0);
-            const float2 mlq = *reinterpret_cast<const float2 *>(p.ws_ml + ((size_t)rec * G + h) * 2);
-            const float w = mlq.y * fast_exp2(mlq.x - M);
-            const float4 ov = *reinterpret_cast<const float4 *>(p.ws_o + ((size_t)rec * G + h) * D + i);
-            wsum += w;
-            acc.x += w * ov.x;
-            acc.y += w * ov.y;
-            acc.z += w * ov.z;
-            acc.w += w * ov.w;
+    if (found[0] >= 0) {
+        const int s = found[0], g = found[1], u0 = found[2];
+        const int ns = seq_stages<BS>(p, s, false);
+        const int ca = u0 / per, cb = (u0 + ns - 1) / per;
+        // the unit is CTA ca's first segment unless a stage of the unit before
+        // it (which ends kUnitCost positions before u0) lies in that CTA's range
+        const int first_rec = (u0 - ca * per > kUnitCost) ? 1 : 0;
+        const size_t row0 = (size_t)s * p.num_q_heads + (size_t)g * G;
+        // A thread's items (head, four dims) and up to kR records per pass are
+        // loaded before any is combined, so a pass costs one memory round trip;
+        // passes merge online (running maximum, rescaled sums).
+        constexpr int kItems = G * D / 4, kAll = (kItems + NT - 1) / NT, kIt = kAll < 2 ? kAll : 2, kR = 2;
+#pragma unroll 1
+        for (int t0 = 0; t0 < kAll; t0 += kIt) {
+        float M[kIt], wsum[kIt], acc[kIt][4];
+#pragma unroll
+        for (int t = 0; t < kIt; ++t) {
+            M[t] = -INFINITY;
+            wsum[t] = 0.f;
+            acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+        }
+        for (int c0 = ca; c0 <= cb; c0 += kR) {
+            float2 ml[kIt][kR];
+            float4 ov[kIt][kR];
+#pragma unroll
+            for (int t = 0; t < kIt; ++t) {
+                const int it = tid + (t0 + t) * NT, h = it / (D / 4), i = (it % (D / 4)) * 4;
+#pragma unroll
+                for (int r = 0; r < kR; ++r) {
+                    const int cc = c0 + r;
+                    ml[t][r] = make_float2(-INFINITY, 0.f);
+                    ov[t][r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (it < kItems && cc <= cb) {
+                        const size_t rec = 2 * (size_t)cc + (cc == ca ? first_rec : 0);
+                        ml[t][r] = *reinterpret_cast<const float2 *>(p.ws_ml + (rec * G + h) * 2);
+                        ov[t][r] = *reinterpret_cast<const float4 *>(p.ws_o + (rec * G + h) * D + i);
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kIt; ++t) {
+                float Mn = M[t];
+#pragma unroll
+                for (int r = 0; r < kR; ++r) Mn = fmaxf(Mn, ml[t][r].x);
+                if (Mn == -INFINITY) continue;
+                const float f = M[t] == -INFINITY ? 0.f : fast_exp2(M[t] - Mn);
+                wsum[t] *= f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[t][k] *= f;
+#pragma unroll
+                for (int r = 0; r < kR; ++r) {
+                    const float w = ml[t][r].x == -INFINITY ? 0.f : ml[t][r].y * fast_exp2(ml[t][r].x - Mn);
+                    wsum[t] += w;
+                    acc[t][0] += w * ov[t][r].x;
+                    acc[t][1] += w * ov[t][r].y;
+                    acc[t][2] += w * ov[t][r].z;
+                    acc[t][3] += w * ov[t][r].w;
+                }
+                M[t] = Mn;
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kIt; ++t) {
+            const int it = tid + (t0 + t) * NT;
+            if (it >= kItems) continue;
+            const int h = it / (D / 4), i = (it % (D / 4)) * 4;
+            const size_t row = row0 + h;
+            fold_prefix<4>(load_prefix<4>(p, row, D, i), M[t], wsum[t], acc[t]);
+            const float inv = wsum[t] > 0.f ? 1.f / wsum[t] : 0.f;
+            *reinterpret_cast<uint2 *>(p.out + row * D + i) =
+                make_uint2(pack_bf16x2(acc[t][0] * inv, acc[t][1] * inv), pack_bf16x2(acc[t][2] * inv, acc[t][3] * inv));
+        }
         }
     }
-    float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-    fold_prefix<4>(pre, M, wsum, a4);
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    *reinterpret_cast<uint2 *>(p.out + row * D + i) =
-        make_uint2(pack_bf16x2(a4[0] * inv, a4[1] * inv), pack_bf16x2(a4[2] * inv, a4[3] * inv));
+    // sequences with no keys of their own: zero rows, or the prefix term alone
+    for (int s = c; s < B; s += C) {
+        if (seq_stages<BS>(p, s, false) != 0) continue;
+        for (int it = tid; it < p.num_q_heads * (D / 4); it += NT) {
+            const size_t row = (size_t)s * p.num_q_heads + it / (D / 4);
+            const int i = (it % (D / 4)) * 4;
+            float a4[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
+            fold_prefix<4>(load_prefix<4>(p, row, D, i), -INFINITY, wsum, a4);
+            const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+            *reinterpret_cast<uint2 *>(p.out + row * D + i) =
+                make_uint2(pack_bf16x2(a4[0] * inv, a4[1] * inv), pack_bf16x2(a4[2] * inv, a4[3] * inv));
+        }
+    }
 }
 
 // ---- launchers -----------------------------------------------------------------
@@ -1279,8 +1382,8 @@ cudaError_t launch_shape(const CUtensorMap &tmk, const CUtensorMap &tmv, const P
         e = launch_pdl(paged_decode_sk_kernel<D, G, BS>, dim3(prm.num_ctas), dim3(kWarps * 32), smem, stream, tmk,
                        tmv, prm);
         if (e != cudaSuccess) return e;
-        return launch_pdl(paged_decode_sk_merge_kernel<D, G, BS>, dim3(num_kv_heads, num_seqs), dim3(G * D / 4), 0,
-                          stream, prm);
+        return launch_pdl(paged_decode_sk_merge_kernel<D, G, BS>, dim3(prm.num_ctas), dim3(kMergeThreads), 0, stream,
+                          prm);
     }
     using SP = SmemPlan<D, BS, kStages>;
     constexpr size_t smem = SP::bytes(0);
@@ -1334,7 +1437,6 @@ cudaError_t launch_for_dim(const DecodeArgs &a, cudaStream_t stream) {
     prm.num_parts = a.num_partitions;
     prm.ws_o = a.ws_o;
     prm.ws_ml = a.ws_ml;
-    prm.ws_cum = a.ws_cum;
     prm.num_ctas = a.num_ctas;
     prm.early_meta = a.early_meta ? 1 : 0;
     prm.new_k = static_cast<const __nv_bfloat16 *>(a.new_k);

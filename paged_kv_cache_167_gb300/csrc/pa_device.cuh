@@ -109,6 +109,17 @@ __device__ __forceinline__ void tensor_copy_5d(uint32_t dst, const CUtensorMap *
         : "memory");
 }
 
+// Hint: bring one box of a 5-D tensor map at (c0 .. c4) into L2.  It changes
+// no memory contents and orders nothing, so it may run before the data's
+// writer has finished: L2 is the point of coherence, and a later copy still
+// reads what that writer stored.
+__device__ __forceinline__ void tensor_prefetch_l2_5d(const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                                      int c4) {
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(map),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+                 : "memory");
+}
+
 // ---- bulk copies (TMA, non-tensor) ----------------------------------------
 
 // Global -> shared copy of `bytes` (multiple of 16, both addresses 16-B

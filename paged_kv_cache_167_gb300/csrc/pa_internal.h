@@ -71,7 +71,6 @@ struct DecodeArgs {
     float *ws_o;               // split: [B][Hq][P][d] when num_partitions > 1; stream-K: [2C][G][d]
     float *ws_ml;              // split: [B][Hq][P][2]; stream-K: [2C][G][2]
     bool stream_k;             // persistent balanced schedule (automatic plan)
-    int32_t *ws_cum;           // stream-K: [B + 1] stage prefix
     int32_t num_ctas;          // stream-K grid size C
     bool early_meta = false;   // stream-K: read lengths and tables before the previous kernel completes
     const void *new_k = nullptr;   // stream-K: last token's K/V per sequence, stored before attending

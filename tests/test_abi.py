@@ -118,13 +118,13 @@ def test_workspace_size(B):
     assert n == 64 * 64 * 2 * 128 * 4 + 64 * 64 * 2 * 2 * 4
     assert L.pa_decode_workspace_size(ctypes.byref(pool), 64, 64, 512, 512) == 0
     assert L.pa_decode_partition_tokens(ctypes.byref(pool), 64, 64, 851, 512) == 512
-    # partition_tokens = 0 selects the balanced (stream-K) schedule: a stage
-    # prefix of B + 1 ints and two partial records of G heads per CTA
+    # partition_tokens = 0 selects the balanced (stream-K) schedule: two
+    # partial records of G heads per CTA
     assert L.pa_decode_partition_tokens(ctypes.byref(pool), 64, 64, 851, 0) == 0
     ws = L.pa_decode_workspace_size(ctypes.byref(pool), 64, 64, 851, 0)
     rup = lambda x: -(-x // 256) * 256
     ctas = ws and next(c for c in range(1, 4097)
-                       if rup(65 * 4) + rup(2 * c * 8 * 128 * 4) + rup(2 * c * 8 * 2 * 4) == ws)
+                       if rup(2 * c * 8 * 128 * 4) + rup(2 * c * 8 * 2 * 4) == ws)
     assert ctas and ctas % 2 == 0
 
 
@@ -176,9 +176,9 @@ def test_product_does_not_touch_the_oracle():
 
 def test_stream_k_grid_override_sizes_the_workspace(B):
     """pa_set_stream_k_ctas fixes the balanced grid: the workspace is then
-    (B + 1) ints plus two fp32 records of G x (d + 2) per CTA, each part
-    rounded up to 256 bytes, with the grid capped at the batch's 16-token
-    stages; 0 restores the default and a negative count is refused."""
+    two fp32 records of G x (d + 2) per CTA, the outputs and the (m, l)
+    pairs each rounded up to 256 bytes, with the grid capped at the batch's
+    16-token stages; 0 restores the default and a negative count is refused."""
     L = B.lib()
     pool = _pool(B, nb=64, hkv=8, b=16, d=128)
     r256 = lambda x: (x + 255) // 256 * 256
@@ -187,11 +187,11 @@ def test_stream_k_grid_override_sizes_the_workspace(B):
             assert L.pa_set_stream_k_ctas(ctas) == 0
             nseq, hq, maxlen = 33, 64, 500
             eff = min(ctas, nseq * 8 * ((maxlen + 15) // 16))
-            want = r256((nseq + 1) * 4) + r256(2 * eff * 8 * 128 * 4) + r256(2 * eff * 8 * 2 * 4)
+            want = r256(2 * eff * 8 * 128 * 4) + r256(2 * eff * 8 * 2 * 4)
             assert L.pa_decode_workspace_size(ctypes.byref(pool), nseq, hq, maxlen, 0) == want
         assert L.pa_set_stream_k_ctas(1000) == 0   # capped: 2 sequences x 8 heads x 1 stage
         assert L.pa_decode_workspace_size(ctypes.byref(pool), 2, 64, 16, 0) == \
-            r256(3 * 4) + r256(2 * 16 * 8 * 128 * 4) + r256(2 * 16 * 8 * 2 * 4)
+            r256(2 * 16 * 8 * 128 * 4) + r256(2 * 16 * 8 * 2 * 4)
         assert L.pa_set_stream_k_ctas(-1) == 1
     finally:
         assert L.pa_set_stream_k_ctas(0) == 0
