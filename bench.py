@@ -16,17 +16,25 @@ per step, over device time with inputs resident in HBM).  A model runs one
 such step per layer, each on its own slice of the KV cache, so the timed
 loop runs K steps back to back over 8 layers' pools (and q), layer i % 8 at
 step i: a layer's K/V are touched again only after the other seven layers'
-(over 1.5 GB for the default workload, far beyond the 129 MB L2) have passed
+(over 1.3 GB for the default workload, far beyond the 129 MB L2) have passed
 through, so every step reads its K/V from HBM; no flush kernel sits between
-steps.  The older per-step measurement -- one step between CUDA events after
-an L2 flush by a 256 MiB read -- is reported as ``per_step_flushed``; it adds
-a fixed ~5 us of event and launch latency to every step.  ``e2e`` is the
-same metric through the C ABI from pinned host buffers (per-step inputs
-copied in and the output copied back inside the timed region; the KV pool
-is device-resident state).  ``roofline`` reports the attention call alone
-(pa_decode, no stores) against the measured HBM copy bandwidth.  ``prefill`` times chunked prefill (16
-sequences x 4,096 cached + 512 new tokens) against the measured bf16 tensor
-peak.  ``cpu_baseline`` times the CPU oracle on the host cores.
+steps.  The K steps are captured as CUDA graphs of 256 steps and replayed
+(the launches keep their programmatic overlap inside a graph), bracketed by
+one pair of CUDA events, so they run at device speed whatever the rate at
+which Python issues calls; the default K keeps the timed region near three
+seconds, long enough for the clock sampler.  ``per_step_flushed`` is one
+step between CUDA events after an L2 flush by a 256 MiB read; it adds a
+fixed few microseconds of event and launch latency to every step.  ``e2e``
+is the same metric through the C ABI from pinned host buffers (per-step
+inputs copied in and the output copied back inside the timed region; the KV
+pool is device-resident state).  ``roofline`` reports the attention call
+alone (pa_decode, no stores) against the measured HBM copy bandwidth.
+``configs`` reports the other decode workloads the same way (the long-context
+batch in its 512-token-partition launch, beside the automatic plan; the
+shared-prompt and beam batches plain and as a cascade; the beams'
+copy-on-write copies).  ``prefill`` times chunked prefill (16 sequences x
+4,096 cached + 512 new tokens) against the measured bf16 tensor peak.
+``cpu_baseline`` times the CPU oracle on the host cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -88,56 +96,6 @@ def prefill_flops(w: wl.Workload) -> int:
     return 4 * w.head_dim * int(visible.sum()) * w.num_q_heads
 
 
-def measure_prefill(pa, dev, flush_fn, iters: int = 10):
-    """Median device time of pa_prefill_chunk on the 16 x (4096 + 512) chunk."""
-    w = wl.prefill_chunk()
-    t = wl.make_tensors(w, dev)
-    tables = torch.as_tensor(w.tables, device=dev)
-    ctx = torch.as_tensor(w.ctx_lens, device=dev)
-    out = torch.empty_like(t["q"])
-    run = lambda: pa.prefill_chunk(out, t["q"], t["pool"], tables, ctx, int(w.ctx_lens.max()), w.scale)
-    for _ in range(3):
-        run()
-    ts = []
-    stream = torch.cuda.current_stream()
-    for _ in range(iters):
-        flush_fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        run()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ts.append(e0.elapsed_time(e1))
-    assert pa.get_device_error() == 0, "device error during prefill"
-    ms = float(np.median(ts))
-    return w, ms, prefill_flops(w)
-
-
-def measure_swap(pa, step, iters: int = 5):
-    """Median device time of pa_swap_blocks moving 1,024 blocks of the decode
-    pool (64 MiB) to pinned host memory and back."""
-    n = min(1024, step.w.num_blocks)
-    w = step.w
-    host = torch.empty((n, 2, w.num_kv_heads, w.block_size, w.head_dim), dtype=torch.bfloat16, pin_memory=True)
-    pairs = torch.stack([torch.arange(n, dtype=torch.int32), torch.arange(n, dtype=torch.int32)], 1).to(step.dev)
-    stream = torch.cuda.current_stream()
-    res = {}
-    for name, direction in (("out", pa.PA_SWAP_OUT), ("in", pa.PA_SWAP_IN)):
-        pa.swap_blocks(step.pool, host, pairs, direction)
-        ts = []
-        for _ in range(iters):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            pa.swap_blocks(step.pool, host, pairs, direction)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        ms = float(np.median(ts))
-        res[name] = {"ms": round(ms, 4), "gbs": round(host.numel() * 2 / (ms / 1e3) / 1e9, 1)}
-    assert pa.get_device_error() == 0, "device error during swap"
-    return {"blocks": n, "bytes": host.numel() * 2, **res}
-
-
 def unique_decode_bytes(w: wl.Workload) -> int:
     """decode_bytes with every physical block's K/V counted once however many
     tables share it (the slots read of a shared block: the most any of its
@@ -152,48 +110,6 @@ def unique_decode_bytes(w: wl.Workload) -> int:
     return decode_bytes(w) - int(w.seq_lens.astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 4 + kv
 
 
-def measure_paging_overhead(pa, step, K: int, warmup: int):
-    """Back-to-back attention calls (as the roofline times them) on copies of
-    the layers' pools whose blocks are placed sequence after sequence in
-    table order; None when blocks are shared or the plan is split-context."""
-    w, dev = step.w, step.dev
-    nb = (-(-w.seq_lens.astype(np.int64) // w.block_size)).astype(np.int64)
-    ids = np.full_like(w.tables, -1)
-    base = 0
-    for s in range(w.batch):
-        ids[s, :nb[s]] = np.arange(base, base + nb[s])
-        base += int(nb[s])
-    old = w.tables[ids >= 0]
-    if step.part != 0 or base > w.num_blocks or len(np.unique(old)) != len(old):
-        return None
-    src = torch.as_tensor(old.astype(np.int64), device=dev)
-    dst = torch.as_tensor(ids[ids >= 0].astype(np.int64), device=dev)
-    pools = torch.zeros_like(step.pools)
-    for layer in range(step.layers):
-        pools[layer][dst] = step.pools[layer][src]
-    tables = torch.as_tensor(ids.astype(np.int32), device=dev)
-
-    def call(i):
-        pa.decode(step.out, step.qs[i % step.layers], pools[i % step.layers], tables, step.seq_lens, w.max_seq_len,
-                  w.scale, 0, step.ws, flags=pa.PA_DECODE_EARLY_METADATA)
-
-    for i in range(warmup):
-        call(i)
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda._sleep(int(max(2e7, 4e5 * K)))
-    e0.record(stream)
-    for i in range(K):
-        call(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    assert pa.get_device_error() == 0, "device error during the identity-placement calls"
-    ms = e0.elapsed_time(e1) / K
-    del pools
-    return {"identity_ms": round(ms, 5)}
-
-
 def cascade_group_size(w: wl.Workload):
     """Sequences per group that share a prefix, for the workloads built that
     way (one prompt shared by the whole batch; the beams of a prompt)."""
@@ -202,61 +118,6 @@ def cascade_group_size(w: wl.Workload):
     if w.name == "beam_fork":
         return int(w.notes["beams"])
     return None
-
-
-def measure_cascade(pa, step, K: int, warmup: int):
-    """The same decode step as a cascade: pa_prefix_attention over each
-    group's shared prefix (read once for the group), then pa_decode_cascade
-    over the private suffixes with the new tokens stored by the call.  Back to
-    back over the layers, as the step is timed.  None for workloads without
-    shared prefixes or off the balanced schedule."""
-    w, dev = step.w, step.dev
-    gsz = cascade_group_size(w)
-    if gsz is None or not step.fused:
-        return None
-    plan = pa.cascade_plan(w.tables, w.seq_lens, gsz, w.block_size)
-    pt = torch.as_tensor(plan["prefix_tables"], device=dev)
-    pl = torch.as_tensor(plan["prefix_lens"], device=dev)
-    order = torch.as_tensor(plan["group_order"], device=dev)   # longest prefix first
-    st = torch.as_tensor(plan["suffix_tables"], device=dev)
-    sl = torch.as_tensor(plan["suffix_lens"], device=dev)
-    max_p, max_s = int(plan["prefix_lens"].max()), max(1, int(plan["suffix_lens"].max()))
-    o_part = torch.empty(step.q.shape, dtype=torch.float32, device=dev)
-    lse = torch.empty((w.batch, w.num_q_heads), dtype=torch.float32, device=dev)
-    nbytes = pa.decode_workspace_size(step.pool, w.batch, w.num_q_heads, max_s, 0)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
-
-    def prefix(i):
-        pa.prefix_attention(o_part, lse, step.qs[i % step.layers], step.pools[i % step.layers], pt, pl, gsz, max_p,
-                            w.scale, group_order=order)
-
-    def suffix(i):
-        pa.decode_cascade(step.out, step.qs[i % step.layers], step.pools[i % step.layers], st, sl, max_s, w.scale,
-                          o_part, lse, 0, ws, flags=pa.PA_DECODE_EARLY_METADATA, new_k=step.new_k, new_v=step.new_v)
-
-    def timed(calls):
-        for i in range(warmup):
-            for c in calls:
-                c(i)
-        torch.cuda.synchronize()
-        stream = torch.cuda.current_stream()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda._sleep(int(max(2e7, 4e5 * K)))
-        e0.record(stream)
-        for i in range(K):
-            for c in calls:
-                c(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / K
-
-    step_ms = timed([prefix, suffix])
-    prefix_ms = timed([prefix])
-    suffix_ms = timed([suffix])
-    assert pa.get_device_error() == 0, "device error during the cascade calls"
-    return {"group_size": gsz, "groups": int(len(plan["prefix_lens"])),
-            "prefix_tokens_mean": float(plan["prefix_lens"].mean()),
-            "step_ms": round(step_ms, 5), "prefix_ms": round(prefix_ms, 5), "suffix_ms": round(suffix_ms, 5)}
 
 
 def decode_bytes(w: wl.Workload) -> int:
@@ -269,9 +130,11 @@ def decode_bytes(w: wl.Workload) -> int:
     return kv + qo + tables + 4 * w.batch
 
 
-def traffic_record():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current decode kernel source."""
+def traffic_record(workload: str):
+    """DRAM bytes per decode launch for a workload from the committed ncu
+    summary, if it was taken on the current decode kernel source; else None.
+    Keys are workload names, with '@auto' for a batch on the automatic plan
+    that is specified with partitions."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(path):
         return None
@@ -279,7 +142,8 @@ def traffic_record():
         rec = json.load(f)
     if rec.get("kernel_source_sha256") != kernel_source_sha():
         return None
-    return rec
+    r = rec.get("records", {}).get(workload)
+    return r["dram_bytes_per_launch"] if r else None
 
 
 def kernel_source_sha() -> str:
@@ -342,6 +206,201 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class GraphLoop:
+    """fn(i) for i = 0 .. K-1, back to back on the device: captured as CUDA
+    graphs of up to `chunk` calls (programmatic launches keep their
+    overlap inside a graph) and replayed, so the steps run at device speed
+    whatever the rate at which Python issues calls.  fn must have run
+    eagerly before (the library does its one-time set-up outside capture)."""
+
+    def __init__(self, fn, K: int, chunk: int = 256):
+        self.K = K
+        self.n = max(1, min(K, chunk))
+        self.full, self.rem = divmod(K, self.n)
+        self.g_full = self._capture(fn, 0, self.n) if self.full else None
+        self.g_rem = self._capture(fn, self.full * self.n, self.rem) if self.rem else None
+
+    @staticmethod
+    def _capture(fn, start: int, count: int):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for i in range(start, start + count):
+                    fn(i)
+        torch.cuda.current_stream().wait_stream(side)
+        return g
+
+    def run(self):
+        for _ in range(self.full):
+            self.g_full.replay()
+        if self.g_rem is not None:
+            self.g_rem.replay()
+
+
+def timed_graph(fn, K: int, warmup: int, barrier=lambda: None) -> float:
+    """Milliseconds of K calls fn(0 .. K-1) replayed from CUDA graphs,
+    bracketed by one pair of CUDA events on the launching stream after
+    `warmup` eager calls and one untimed replay."""
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    loop = GraphLoop(fn, K)
+    loop.run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    loop.run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    del loop
+    return e0.elapsed_time(e1)
+
+
+def measure_prefill(pa, dev, flush_fn, iters: int = 10):
+    """Median device time of pa_prefill_chunk on the 16 x (4096 + 512) chunk,
+    one launch between CUDA events after an L2 flush."""
+    w = wl.prefill_chunk()
+    t = wl.make_tensors(w, dev)
+    tables = torch.as_tensor(w.tables, device=dev)
+    ctx = torch.as_tensor(w.ctx_lens, device=dev)
+    out = torch.empty_like(t["q"])
+    run = lambda: pa.prefill_chunk(out, t["q"], t["pool"], tables, ctx, int(w.ctx_lens.max()), w.scale)
+    for _ in range(3):
+        run()
+    ts = []
+    stream = torch.cuda.current_stream()
+    for _ in range(iters):
+        flush_fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    assert pa.get_device_error() == 0, "device error during prefill"
+    ms = float(np.median(ts))
+    return w, ms, prefill_flops(w)
+
+
+def measure_swap(pa, step, iters: int = 5):
+    """Median device time of pa_swap_blocks moving 1,024 blocks of the decode
+    pool (64 MiB) to pinned host memory and back."""
+    n = min(1024, step.w.num_blocks)
+    w = step.w
+    host = torch.empty((n, 2, w.num_kv_heads, w.block_size, w.head_dim), dtype=torch.bfloat16, pin_memory=True)
+    pairs = torch.stack([torch.arange(n, dtype=torch.int32), torch.arange(n, dtype=torch.int32)], 1).to(step.dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name, direction in (("out", pa.PA_SWAP_OUT), ("in", pa.PA_SWAP_IN)):
+        pa.swap_blocks(step.pool, host, pairs, direction)
+        ts = []
+        for _ in range(iters):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            pa.swap_blocks(step.pool, host, pairs, direction)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = float(np.median(ts))
+        res[name] = {"ms": round(ms, 4), "gbs": round(host.numel() * 2 / (ms / 1e3) / 1e9, 1)}
+    assert pa.get_device_error() == 0, "device error during swap"
+    return {"blocks": n, "bytes": host.numel() * 2, **res}
+
+
+def measure_paging_overhead(pa, step, K: int, warmup: int):
+    """The attention call (as the roofline times it) on copies of the layers'
+    pools whose blocks are placed sequence after sequence in table order;
+    None when blocks are shared or the plan is split-context."""
+    w, dev = step.w, step.dev
+    nb = (-(-w.seq_lens.astype(np.int64) // w.block_size)).astype(np.int64)
+    ids = np.full_like(w.tables, -1)
+    base = 0
+    for s in range(w.batch):
+        ids[s, :nb[s]] = np.arange(base, base + nb[s])
+        base += int(nb[s])
+    old = w.tables[ids >= 0]
+    if step.part != 0 or base > w.num_blocks or len(np.unique(old)) != len(old):
+        return None
+    src = torch.as_tensor(old.astype(np.int64), device=dev)
+    dst = torch.as_tensor(ids[ids >= 0].astype(np.int64), device=dev)
+    pools = torch.zeros_like(step.pools)
+    for layer in range(step.layers):
+        pools[layer][dst] = step.pools[layer][src]
+    tables = torch.as_tensor(ids.astype(np.int32), device=dev)
+
+    def call(i):
+        pa.decode(step.out, step.qs[i % step.layers], pools[i % step.layers], tables, step.seq_lens, w.max_seq_len,
+                  w.scale, 0, step.ws, flags=pa.PA_DECODE_EARLY_METADATA)
+
+    ms = timed_graph(call, K, warmup) / K
+    assert pa.get_device_error() == 0, "device error during the identity-placement calls"
+    del pools
+    return {"identity_ms": round(ms, 5)}
+
+
+def measure_cascade(pa, step, K: int, warmup: int):
+    """The same decode step as a cascade: pa_prefix_attention over each
+    group's shared prefix (read once for the group), then pa_decode_cascade
+    over the private suffixes with the new tokens stored by the call.  Replayed
+    over the layers, as the step is timed.  None for workloads without shared
+    prefixes or off the balanced schedule."""
+    w, dev = step.w, step.dev
+    gsz = cascade_group_size(w)
+    if gsz is None or not step.fused:
+        return None
+    plan = pa.cascade_plan(w.tables, w.seq_lens, gsz, w.block_size)
+    pt = torch.as_tensor(plan["prefix_tables"], device=dev)
+    pl = torch.as_tensor(plan["prefix_lens"], device=dev)
+    order = torch.as_tensor(plan["group_order"], device=dev)   # longest prefix first
+    st = torch.as_tensor(plan["suffix_tables"], device=dev)
+    sl = torch.as_tensor(plan["suffix_lens"], device=dev)
+    max_p, max_s = int(plan["prefix_lens"].max()), max(1, int(plan["suffix_lens"].max()))
+    o_part = torch.empty(step.q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty((w.batch, w.num_q_heads), dtype=torch.float32, device=dev)
+    nbytes = pa.decode_workspace_size(step.pool, w.batch, w.num_q_heads, max_s, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
+
+    def prefix(i):
+        pa.prefix_attention(o_part, lse, step.qs[i % step.layers], step.pools[i % step.layers], pt, pl, gsz, max_p,
+                            w.scale, group_order=order)
+
+    def suffix(i):
+        pa.decode_cascade(step.out, step.qs[i % step.layers], step.pools[i % step.layers], st, sl, max_s, w.scale,
+                          o_part, lse, 0, ws, flags=pa.PA_DECODE_EARLY_METADATA, new_k=step.new_k, new_v=step.new_v)
+
+    def both(i):
+        prefix(i)
+        suffix(i)
+
+    step_ms = timed_graph(both, K, warmup) / K
+    prefix_ms = timed_graph(prefix, K, warmup) / K
+    suffix_ms = timed_graph(suffix, K, warmup) / K
+    assert pa.get_device_error() == 0, "device error during the cascade calls"
+    return {"group_size": gsz, "groups": int(len(plan["prefix_lens"])),
+            "prefix_tokens_mean": float(plan["prefix_lens"].mean()),
+            "step_ms": step_ms, "prefix_ms": prefix_ms, "suffix_ms": suffix_ms}
+
+
+def measure_copy_blocks(pa, step, K: int, warmup: int):
+    """pa_copy_blocks on the workload's copy-on-write pairs (each copies a
+    whole block, K and V of every kv-head), alternating between two layers'
+    pools; None without pairs."""
+    w = step.w
+    if w.copy_pairs is None or not len(w.copy_pairs):
+        return None
+    pairs = torch.as_tensor(w.copy_pairs, device=step.dev)
+    ms = timed_graph(lambda i: pa.copy_blocks(step.pools[i % step.layers], pairs), K, warmup) / K
+    assert pa.get_device_error() == 0, "device error during copy_blocks"
+    nbytes = 2 * len(w.copy_pairs) * 2 * w.num_kv_heads * w.block_size * w.head_dim * 2   # read + write
+    return {"pairs": int(len(w.copy_pairs)), "ms": ms, "bytes": nbytes}
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -383,6 +442,7 @@ class DecodeStep:
         self.fused = (self.part == 0 and len(w.new_seq_idx) == w.batch
                       and np.array_equal(w.new_seq_idx, np.arange(w.batch))
                       and np.array_equal(w.new_positions, w.seq_lens.astype(np.int64) - 1))
+        self.decode_launches = decode_launches
         self.launches_per_step = decode_launches + (0 if self.fused else 1)
 
     def write(self, layer: int = 0):
@@ -399,12 +459,13 @@ class DecodeStep:
                        w.scale, w.partition_tokens, self.ws, flags=self.pa.PA_DECODE_EARLY_METADATA,
                        new_k=self.new_k, new_v=self.new_v)
 
-    def decode(self, layer: int = 0):
+    def decode(self, layer: int = 0, partition_tokens=None, ws=None):
         w = self.w
+        part = w.partition_tokens if partition_tokens is None else partition_tokens
         # lengths and tables are host copies, never written by the slot writer
         # that each decode call follows: the early-metadata launch applies
         self.pa.decode(self.out, self.qs[layer], self.pools[layer], self.tables, self.seq_lens, w.max_seq_len,
-                       w.scale, w.partition_tokens, self.ws, flags=self.pa.PA_DECODE_EARLY_METADATA)
+                       w.scale, part, self.ws if ws is None else ws, flags=self.pa.PA_DECODE_EARLY_METADATA)
 
 
 def rank_workload(name: str, rank: int) -> wl.Workload:
@@ -424,6 +485,111 @@ def reduce_max(values, world: int, device) -> list:
         import torch.distributed as dist
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return t.tolist()
+
+
+def roofline_hbm(alg: int, ms: float, peak: float, peak_kind: str, kernel: str, traffic=None, unique=None) -> dict:
+    achieved = alg / (ms / 1e3) / 1e9
+    r = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
+         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic, "algorithmic_bytes": alg,
+         "decode_ms": round(ms, 5)}
+    if unique is not None:
+        r["unique_bytes"] = unique
+        r["unique_frac"] = round(unique / (ms / 1e3) / 1e9 / peak, 4)
+    return r
+
+
+# Decode workloads reported besides the headline one, in the launch
+# configuration each is specified with (the long-context batch with its
+# 512-token partitions and the reduce kernel).
+CONFIG_NAMES = ("tiny", "long_context", "shared_prefix", "beam_fork")
+CONFIG_STEPS = 2048
+
+
+def measure_config(pa, name: str, dev, K: int, warmup: int):
+    """Timings of one decode workload: the step (new tokens stored, then
+    attention), the attention call alone, and for the long-context batch the
+    automatic plan beside its partitions; the cascade and the copy-on-write
+    copies where the workload has them.  Raw milliseconds (reduced over ranks
+    by the caller)."""
+    w = wl.CONFIGS[name]()
+    tensors = wl.make_tensors(w, dev)
+    step = DecodeStep(pa, w, dev, tensors)
+    del tensors
+    res = {}
+    copies = measure_copy_blocks(pa, step, K, warmup)
+    if copies is not None:   # the forks' copies first, as the workload's recipe
+        pairs = torch.as_tensor(w.copy_pairs, device=dev)
+        for layer in range(step.layers):
+            pa.copy_blocks(step.pools[layer], pairs)
+        res["copy_ms"] = copies["ms"]
+    res["step_ms"] = timed_graph(lambda i: step.step(i % step.layers), K, warmup) / K
+    res["decode_ms"] = timed_graph(lambda i: step.decode(i % step.layers), K, warmup) / K
+    if step.part != 0:   # the same batch on the automatic plan
+        nb = pa.decode_workspace_size(step.pool, w.batch, w.num_q_heads, w.max_seq_len, 0)
+        ws0 = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+        res["auto_decode_ms"] = timed_graph(lambda i: step.decode(i % step.layers, 0, ws0), K, warmup) / K
+    casc = measure_cascade(pa, step, K, warmup)
+    if casc is not None:
+        for k in ("step_ms", "prefix_ms", "suffix_ms"):
+            res["cascade_" + k] = casc[k]
+    assert pa.get_device_error() == 0, f"device error during {name}"
+    meta = {"w": w, "part": step.part, "num_parts": step.num_parts, "fused": step.fused,
+            "launches": step.launches_per_step, "cascade": casc, "copies": copies}
+    del step
+    torch.cuda.empty_cache()
+    return res, meta
+
+
+def config_line(name, res, meta, peak, peak_kind, world):
+    """The JSON object of one decode workload."""
+    w = meta["w"]
+    alg, uniq = decode_bytes(w), unique_decode_bytes(w)
+    part = meta["part"]
+    kernel = ("paged_decode_kernel + paged_decode_reduce_kernel" if part and meta["num_parts"] > 1
+              else "paged_decode_kernel" if part else "paged_decode_sk_kernel + paged_decode_sk_merge_kernel")
+    out = {"workload": w.name, "global_batch": world * w.batch, "num_q_heads": w.num_q_heads,
+           "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+           "seq_len_min": int(w.seq_lens.min()), "seq_len_max": int(w.seq_lens.max()),
+           "seq_len_mean": round(float(w.seq_lens.mean()), 1), "pool_blocks": w.num_blocks,
+           "schedule": f"split-context, {part}-token partitions x {meta['num_parts']}" + (" + reduce" if meta["num_parts"] > 1 else "")
+           if part else "balanced stream-K (persistent, 2 CTAs/SM), early-metadata launch",
+           "step": "new tokens stored by the decode call, then attention" if meta["fused"]
+           else "slot writer (pa_reshape_and_cache), then pa_decode",
+           "steps_timed": CONFIG_STEPS,
+           "step_ms": round(res["step_ms"], 5),
+           "tokens_per_s": round(world * w.batch / (res["step_ms"] / 1e3), 1),
+           "roofline": roofline_hbm(alg, res["decode_ms"], peak, peak_kind, kernel, traffic_record(w.name),
+                                    uniq if uniq != alg else None)}
+    if "auto_decode_ms" in res:
+        out["auto_plan"] = {"schedule": "balanced stream-K (the automatic plan) on the same batch",
+                            "roofline": roofline_hbm(alg, res["auto_decode_ms"], peak, peak_kind,
+                                                     "paged_decode_sk_kernel + paged_decode_sk_merge_kernel",
+                                                     traffic_record(w.name + "@auto"))}
+    casc = meta["cascade"]
+    if casc is not None:
+        ms = res["cascade_step_ms"]
+        out["cascade"] = {"group_size": casc["group_size"], "groups": casc["groups"],
+                          "prefix_tokens_mean": round(casc["prefix_tokens_mean"], 1),
+                          "step_ms": round(ms, 5), "prefix_ms": round(res["cascade_prefix_ms"], 5),
+                          "suffix_ms": round(res["cascade_suffix_ms"], 5),
+                          "tokens_per_s": round(world * w.batch / (ms / 1e3), 1),
+                          "speedup_vs_step": round(res["step_ms"] / ms, 3),
+                          "roofline": {"bound": "hbm", "achieved": round(uniq / (ms / 1e3) / 1e9, 1), "peak": peak,
+                                       "peak_kind": peak_kind, "unit": "GB/s",
+                                       "frac": round(uniq / (ms / 1e3) / 1e9 / peak, 4), "traffic": None,
+                                       "algorithmic_bytes": uniq,
+                                       "note": "unique bytes (each shared block once) over the whole cascade step"},
+                          "note": "pa_prefix_attention over each group's shared prefix (tensor cores, read once per "
+                                  "group), then pa_decode_cascade over the private suffixes with the new tokens "
+                                  "stored by the call"}
+    if meta["copies"] is not None:
+        cp = meta["copies"]
+        out["copy_blocks"] = {"pairs": cp["pairs"], "ms": round(res["copy_ms"], 5),
+                              "roofline": {"bound": "hbm", "achieved": round(cp["bytes"] / (res["copy_ms"] / 1e3) / 1e9, 1),
+                                           "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                                           "frac": round(cp["bytes"] / (res["copy_ms"] / 1e3) / 1e9 / peak, 4),
+                                           "algorithmic_bytes": cp["bytes"]}}
+    return out
 
 
 def run_ours(args, world, rank, local):
@@ -453,34 +619,33 @@ def run_ours(args, world, rank, local):
     assert pa.get_device_error() == 0, "device error during warm-up"
 
     K = args.steps
-
-    def timed_layers(write=True):
-        # K steps back to back, layer i % L at step i (see the module docstring)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        torch.cuda.synchronize()
-        # The GPU idles (untimed) while the host queues all K steps, so the
-        # timed steps run back to back at device speed rather than at the
-        # rate Python issues calls (that rate is what e2e measures).
-        torch.cuda._sleep(int(max(2e7, 4e5 * K)))
+    # ---- the headline: K steps back to back over the layers, replayed from CUDA graphs
+    loop = GraphLoop(lambda i: step.step(i % step.layers), K)
+    loop.run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
         e0.record(stream)
-        for i in range(K):
-            if write:
-                step.step(i % step.layers)
-            else:
-                step.decode(i % step.layers)
+        loop.run()
         e1.record(stream)
         torch.cuda.synchronize()
-        barrier()
-        return e0.elapsed_time(e1)
+    total_ms = e0.elapsed_time(e1)
+    barrier()
+    del loop
+    K_dec = min(K, 8192)   # the attention call alone, for the roofline
+    decode_total_ms = timed_graph(lambda i: step.decode(i % step.layers), K_dec, args.warmup, barrier)
+
+    K_flush = min(K, 50)
 
     def timed_flushed(flush_fn, write=True):
         # one step between events after an L2 flush; no event between the two
         # calls: it would serialise the decode kernel's programmatic launch
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K_flush)]
         barrier()
         torch.cuda.synchronize()
-        for i in range(K):
+        for i in range(K_flush):
             flush_fn()
             ev[i][0].record(stream)
             if write:
@@ -490,11 +655,8 @@ def run_ours(args, world, rank, local):
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         barrier()
-        return [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+        return [ev[i][0].elapsed_time(ev[i][1]) for i in range(K_flush)]
 
-    with ClockSampler(local) as clocks:
-        total_ms = timed_layers()
-    decode_total_ms = timed_layers(write=False)   # the decode call alone, for the roofline
     flushed_ms = timed_flushed(flush_read)
     flushed_decode_ms = timed_flushed(flush_read, write=False)
     wstep_ms = timed_flushed(flush_write)
@@ -536,11 +698,12 @@ def run_ours(args, world, rank, local):
         host_out.copy_(step.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
+    K_e2e = min(K, 400)
     for _ in range(args.warmup):
         e2e_step()
     barrier()
     e2e_s = 0.0
-    for _ in range(K):
+    for _ in range(K_e2e):
         flush_read()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
@@ -548,17 +711,44 @@ def run_ours(args, world, rank, local):
         e2e_s += time.perf_counter() - t0
     barrier()
 
-    paging = measure_paging_overhead(pa, step, K, args.warmup)
-    casc = measure_cascade(pa, step, K, args.warmup)
+    K_side = min(K, CONFIG_STEPS)
+    paging = measure_paging_overhead(pa, step, K_side, args.warmup)
+    casc = measure_cascade(pa, step, K_side, args.warmup)
     prefill = None if args.no_prefill else measure_prefill(pa, dev, flush_read)
     swap = measure_swap(pa, step)
+    head_launches = step.launches_per_step
+    head_fused, head_part, head_parts = step.fused, step.part, step.num_parts
+    del step
+    torch.cuda.empty_cache()
 
-    total_ms, e2e_ms, decode_avg_ms, wtotal_ms, ftotal_ms, fdecode_ms = reduce_max(
-        [total_ms, e2e_s * 1e3, decode_total_ms / K, sum(wstep_ms), sum(flushed_ms), float(np.mean(flushed_decode_ms))],
-        world, dev)
-    if casc is not None:   # every rank runs the same kind of workload: all or none measure a cascade
-        keys = ("step_ms", "prefix_ms", "suffix_ms")
-        casc.update(zip(keys, (round(v, 5) for v in reduce_max([casc[k] for k in keys], world, dev))))
+    configs = []
+    if not args.no_configs:
+        for name in CONFIG_NAMES:
+            if name != args.config:
+                configs.append((name,) + measure_config(pa, name, dev, min(K, CONFIG_STEPS), args.warmup))
+
+    flat = [total_ms, e2e_s * 1e3, decode_total_ms / K_dec, sum(wstep_ms), sum(flushed_ms),
+            float(np.mean(flushed_decode_ms))]
+    keys = []
+    for name, res, _ in configs:
+        for k in sorted(res):
+            keys.append((name, k))
+            flat.append(res[k])
+    if casc is not None:
+        for k in ("step_ms", "prefix_ms", "suffix_ms"):
+            flat.append(casc[k])
+    red = reduce_max(flat, world, dev)
+    total_ms, e2e_ms, decode_avg_ms, wtotal_ms, ftotal_ms, fdecode_ms = red[:6]
+    off = 6
+    for (name, k) in keys:
+        for cname, res, _ in configs:
+            if cname == name:
+                res[k] = red[off]
+        off += 1
+    if casc is not None:
+        for k in ("step_ms", "prefix_ms", "suffix_ms"):
+            casc[k] = red[off]
+            off += 1
 
     if rank != 0:
         if world > 1:
@@ -569,8 +759,6 @@ def run_ours(args, world, rank, local):
     value = tokens / (total_ms / 1e3)
     alg = decode_bytes(w)
     peak, bf16_peak, peak_kind = measured_peaks()
-    achieved = alg / (decode_avg_ms / 1e3) / 1e9
-    traffic = traffic_record()
     clk = clocks.summary()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
@@ -581,40 +769,41 @@ def run_ours(args, world, rank, local):
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
                    "seq_len_min": int(w.seq_lens.min()), "seq_len_max": int(w.seq_lens.max()),
                    "seq_len_mean": float(w.seq_lens.mean()), "pool_blocks": w.num_blocks,
-                   "schedule": "balanced stream-K (persistent, 2 CTAs/SM), early-metadata launch" if step.part == 0
-                   else f"split-context, {step.part}-token partitions x {step.num_parts}",
+                   "schedule": "balanced stream-K (persistent, 2 CTAs/SM), early-metadata launch" if head_part == 0
+                   else f"split-context, {head_part}-token partitions x {head_parts}",
                    "step": "new tokens stored by the decode call (pa_decode_ex new_k/new_v), then attention"
-                   if step.fused else "slot writer (pa_reshape_and_cache), then pa_decode",
+                   if head_fused else "slot writer (pa_reshape_and_cache), then pa_decode",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "layers": step.layers,
-                   "l2": f"inputs larger than L2: steps rotate over {step.layers} layers' pools and q, "
-                         f"{(step.layers - 1) * alg / 1e9:.2f} GB of other layers' K/V between reuses of a layer; no flush"},
-        "per_step_flushed": {"ms_per_step": round(ftotal_ms / K, 5), "tokens_per_s": round(tokens / (ftotal_ms / 1e3), 1),
+                   "layers": args.layers,
+                   "timing": "K steps replayed from CUDA graphs of 256 steps, one CUDA event pair around all K",
+                   "l2": f"inputs larger than L2: steps rotate over {args.layers} layers' pools and q, "
+                         f"{(args.layers - 1) * alg / 1e9:.2f} GB of other layers' K/V between reuses of a layer; no flush"},
+        "per_step_flushed": {"steps": K_flush, "ms_per_step": round(ftotal_ms / K_flush, 5),
+                             "tokens_per_s": round(world * w.batch * K_flush / (ftotal_ms / 1e3), 1),
                              "decode_ms": round(fdecode_ms, 5),
-                             "tokens_per_s_after_write_flush": round(tokens / (wtotal_ms / 1e3), 1),
+                             "decode_frac": round(alg / (fdecode_ms / 1e3) / 1e9 / peak, 4),
+                             "tokens_per_s_after_write_flush": round(world * w.batch * K_flush / (wtotal_ms / 1e3), 1),
                              "l2": "flushed before each step by reading a 256 MiB buffer; one event pair per step"},
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode kernel + merge kernel)",
-                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4),
-                     "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
-                     "algorithmic_bytes": alg, "unique_bytes": unique_decode_bytes(w),
-                     "decode_ms": round(decode_avg_ms, 5)},
-        "kv_read_gbs": round(achieved, 1),
+        "roofline": roofline_hbm(alg, decode_avg_ms, peak, peak_kind, "pa_decode (decode kernel + merge kernel)",
+                                 traffic_record(w.name), unique_decode_bytes(w)),
+        "kv_read_gbs": round(alg / (decode_avg_ms / 1e3) / 1e9, 1),
         "derived": {"full_model_80_layers_tokens_per_s": round(value / 80, 1),
                     "note": "value / 80: one such step per layer of an 80-layer model, attention only"},
-        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
+        "e2e": {"value": round(world * w.batch * K_e2e / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K_e2e,
                 "call": "pa_decode_host (pinned host q, new K/V, tables, lengths in; output back; one call)"
                 if staging is not None else "host-to-device copies, pa_reshape_and_cache, pa_decode, copy back"},
-        "gpu_launches": step.launches_per_step * K,
-        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+        "gpu_launches": head_launches * K,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                   "samples_under_load": clk["samples"], "window_s": round(total_ms / 1e3, 3)},
     }
     if prefill is not None:
         pw, pms, pflop = prefill
         line["prefill"] = {"workload": f"{pw.batch} seqs x ({int(pw.ctx_lens[0])} cached + {pw.chunk} chunk) tokens, "
                                        f"{pw.num_q_heads}/{pw.num_kv_heads} heads, d={pw.head_dim}",
                            "ms": round(pms, 4), "tflops": round(pflop / (pms / 1e3) / 1e12, 1),
-                           "roofline": {"bound": "tensor", "achieved": round(pflop / (pms / 1e3) / 1e12, 1),
+                           "roofline": {"bound": "tensor", "kernel": "prefill_kernel (tcgen05)",
+                                        "achieved": round(pflop / (pms / 1e3) / 1e12, 1),
                                         "peak": bf16_peak, "peak_kind": peak_kind, "unit": "TFLOP/s",
                                         "frac": round(pflop / (pms / 1e3) / 1e12 / bf16_peak, 4),
                                         "flops": pflop}}
@@ -628,12 +817,11 @@ def run_ours(args, world, rank, local):
         line["cascade"] = dict(casc, tokens_per_s=round(world * w.batch / (casc["step_ms"] / 1e3), 1),
                                speedup_vs_step=round((total_ms / K) / casc["step_ms"], 3),
                                unique_gbs=round(ub / (casc["step_ms"] / 1e3) / 1e9, 1),
-                               unique_frac=round(ub / (casc["step_ms"] / 1e3) / 1e9 / peak, 4),
-                               note="pa_prefix_attention over each group's shared prefix (tensor cores, read once "
-                                    "per group), then pa_decode_cascade over the private suffixes with the new "
-                                    "tokens stored by the call; unique bytes over the whole step")
+                               unique_frac=round(ub / (casc["step_ms"] / 1e3) / 1e9 / peak, 4))
     line["swap"] = dict(swap, note="pa_swap_blocks between the decode pool and pinned host memory, one kernel "
                                    "over the CPU-GPU link")
+    if configs:
+        line["configs"] = {name: config_line(name, res, meta, peak, peak_kind, world) for name, res, meta in configs}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, tensors, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -649,13 +837,19 @@ def run_ours(args, world, rank, local):
 def oracle_pass(orc, w, tensors_bits, seqs):
     """The oracle's decode step for sequences `seqs`: write their new tokens,
     then attend every query head."""
+    rows = np.stack(np.meshgrid(seqs, np.arange(w.num_q_heads), indexing="ij"), axis=-1).reshape(-1, 2)
+    oracle_rows(orc, w, tensors_bits, rows)
+
+
+def oracle_rows(orc, w, tensors_bits, rows):
+    """The oracle's decode step for query rows (sequence, head): write those
+    sequences' new tokens, then attend the rows."""
     import oracle
     pool, q, k, v = tensors_bits
     geom = oracle.dense_geom(w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
-    sel = np.isin(w.new_seq_idx, seqs)
+    sel = np.isin(w.new_seq_idx, rows[:, 0])
     slots = orc.slot_mapping(w.tables, w.new_seq_idx[sel], w.new_positions[sel], w.block_size)
     orc.reshape_and_cache(pool, geom, k[sel], v[sel], slots)
-    rows = np.stack(np.meshgrid(seqs, np.arange(w.num_q_heads), indexing="ij"), axis=-1).reshape(-1, 2)
     orc.paged_decode(q, pool, geom, w.tables, w.seq_lens, w.num_q_heads, w.scale, rows=rows)
 
 
@@ -694,6 +888,9 @@ def cpu_baseline(w, tensors, budget_s: float = 10.0):
 
 
 def run_reference(args, world, rank, local):
+    """The oracle as it stands on the host cores, on this arm's workload: each
+    step a random sample of the batch's query rows (a decoded token is one
+    sequence's num_q_heads rows), sized so the run takes about a minute."""
     if rank != 0:
         return
     import oracle
@@ -702,30 +899,33 @@ def run_reference(args, world, rank, local):
     tensors = wl.make_tensors(w, "cpu")
     tb = (wl.bf16_bits(tensors["pool"]).copy(), wl.bf16_bits(tensors["q"]), wl.bf16_bits(tensors["new_k"]),
           wl.bf16_bits(tensors["new_v"]))
-    # size a step so that warm-up plus timed steps stay near a minute
-    t0 = time.perf_counter()
-    oracle_pass(orc, w, tb, np.arange(1))
-    per_seq = max(time.perf_counter() - t0, 1e-4)
-    per_step = int(max(1, min(w.batch, 60.0 / (args.steps + args.warmup) / per_seq)))
+    all_rows = np.stack(np.meshgrid(np.arange(w.batch), np.arange(w.num_q_heads), indexing="ij"),
+                        axis=-1).reshape(-1, 2).astype(np.int32)
     rng = np.random.default_rng(0)
+    probe = all_rows[rng.choice(len(all_rows), min(len(all_rows), 64), replace=False)]
+    t0 = time.perf_counter()
+    oracle_rows(orc, w, tb, probe)
+    per_row = max((time.perf_counter() - t0) / len(probe), 1e-6)
+    per_step = int(max(1, min(len(all_rows), 60.0 / (args.steps + args.warmup) / per_row)))
     for _ in range(args.warmup):
-        oracle_pass(orc, w, tb, rng.choice(w.batch, per_step, replace=False))
+        oracle_rows(orc, w, tb, all_rows[rng.choice(len(all_rows), per_step, replace=False)])
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_pass(orc, w, tb, rng.choice(w.batch, per_step, replace=False))
+        oracle_rows(orc, w, tb, all_rows[rng.choice(len(all_rows), per_step, replace=False)])
     elapsed = time.perf_counter() - t0
-    value = per_step * args.steps / elapsed
+    value = per_step * args.steps / w.num_q_heads / elapsed
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps * 1e3, 3),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic: seeded bf16 N(0,1) K/V/q, random physical block placement",
         "config": {"workload": w.name, "global_batch": w.batch, "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-                   "sequences_per_step": per_step},
+                   "query_rows_per_step": per_step},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": orc.num_threads(),
                          "kind": "oracle",
-                         "sample": f"{per_step} random sequences of the batch per step, all query heads"},
+                         "sample": f"{per_step} random query rows (sequence, head) of the batch per step; "
+                                   f"a token is {w.num_q_heads} rows"},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -735,13 +935,14 @@ def run_reference(args, world, rank, local):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=81920)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="llama70b_decode",
                     choices=["tiny", "llama70b_decode", "long_context", "shared_prefix", "beam_fork"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other decode workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=DecodeStep.LAYERS,
                     help="layers' pools the timed steps rotate over (1 keeps one pool, e.g. for profiling)")
