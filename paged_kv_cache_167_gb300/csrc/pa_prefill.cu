@@ -65,7 +65,10 @@
 namespace pa {
 namespace prefill {
 
-constexpr int kSoftWarps = 8;               // two warpgroups, each owning 64 of a row's 128 keys
+constexpr int kSoftWarps = 8;               // softmax warps: two per TMEM lane quadrant
+constexpr int kParts = kSoftWarps / 4;      // warps sharing a row: each owns kPK of its 128 keys
+constexpr int kPK = 128 / kParts;           // keys of a row per softmax thread (64)
+constexpr int kPC = kPK / 32;               // 32-column TMEM accesses per thread and tile
 constexpr int kMmaWarp = kSoftWarps;        // lane 0 issues the P.V MMAs
 constexpr int kKWarp = kSoftWarps + 1;      // copies Q and the K tiles
 constexpr int kVWarp = kSoftWarps + 2;      // copies the V tiles
@@ -78,16 +81,15 @@ constexpr uint32_t kHalf = 128u * 128u;     // one [128 rows][64 bf16] swizzled 
 constexpr uint32_t kTile = 2u * kHalf;      // [2 halves][128 rows][128 B]
 constexpr uint32_t kOffQ = 0;
 #ifndef PA_PREFILL_KV_STAGES
-#define PA_PREFILL_KV_STAGES 3
+#define PA_PREFILL_KV_STAGES 2
 #endif
-constexpr int kKV = PA_PREFILL_KV_STAGES;    // K and V ring depth
+constexpr int kKV = PA_PREFILL_KV_STAGES;    // K and V ring depth (2 and 3 measured alike)
 constexpr uint32_t kOffK = kOffQ + kTile;   // kKV stages, [half][128 keys][128 B]
 constexpr uint32_t kOffV = kOffK + kKV * kTile; // kKV stages, [block][half][16 keys][128 B]
-constexpr uint32_t kOffX = kOffV + kKV * kTile; // [2 halves][128 rows] fp32 exchange
-constexpr uint32_t kOffBar = kOffX + 1024;
+constexpr uint32_t kOffBar = kOffV + kKV * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // + alignment slack
-constexpr int kSBufs = 3;                   // S accumulators in tensor memory
-constexpr uint32_t kTmemCols = 512;         // S0, S1, S2, O (128 columns each)
+constexpr int kSBufs = 2;                   // S accumulators in tensor memory
+constexpr uint32_t kTmemCols = 512;         // S0, S1, O0, O1 (128 columns each)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 domain
@@ -202,6 +204,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[32]) {   // r[0..15]
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr),
+        PA_W8(0), PA_W8(8)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -212,14 +222,26 @@ __device__ __forceinline__ void mbar_arrive_u32(uint32_t bar) {
 }
 
 // Tensor-memory column of keys kk*16 .. kk*16+15 of P in S buffer sb: each
-// half of a row's keys is written, two bf16 per column, by the warpgroup that
-// read it, into the first 32 of the 64 S columns it read.
+// part of a row's keys is written, two bf16 per column, by the warp that read
+// it, into the first half of the S columns it read.
 __device__ __forceinline__ uint32_t p_col(int sb, int kk) {
-    return (uint32_t)(sb * 128 + (kk >> 2) * 64 + (kk & 3) * 8);
+    constexpr int kSteps = kPK / 16;   // 16-key P.V steps per softmax thread
+    return (uint32_t)(sb * 128 + (kk / kSteps) * kPK + (kk % kSteps) * 8);
 }
 
-__device__ __forceinline__ void pair_sync(int warp) {   // warps w and w + 4 own the same rows
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + (warp & 3)), "r"(64) : "memory");
+__device__ __forceinline__ void part_sync(int warp) {   // warps w, w + 4, ... own the same rows
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + (warp & 3)), "r"(kParts * 32) : "memory");
+}
+
+__device__ __forceinline__ float max_tree32(const uint32_t (&a)[32]) {
+    float m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m[i] = fmaxf(__uint_as_float(a[i]), __uint_as_float(a[i + 16]));
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    return m[0];
 }
 
 __device__ __forceinline__ float max_tree64(const uint32_t (&a)[32], const uint32_t (&b)[32]) {
@@ -257,14 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     unsigned char *gbase = smem_raw + (base - smem_addr(smem_raw));
     const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
-    float *xch = reinterpret_cast<float *>(gbase + kOffX);
     const uint32_t barQ = base + kOffBar;
     // barriers: Q | K[kKV] | V[kKV] | S[3] | S free[3] | P[2] | P.V done[2] | drain (P.V, Q.K issuers) |
-    // P.V done per S buffer[3]
+    // P.V done per S buffer[3] | K slot free[kKV] | V slot free[kKV]
     const uint32_t barK = barQ + 8, barV = barK + 8 * kKV, barS = barV + 8 * kKV, barSfree = barS + 24,
                    barP = barSfree + 24, barOP = barP + 16, barEnd = barOP + 16, barEndQk = barEnd + 8,
-                   barSdone = barEndQk + 8;
-    constexpr int kNumBars = 1 + 2 * kKV + 3 + 3 + 2 + 2 + 2 + 3;
+                   barSdone = barEndQk + 8, barKfree = barSdone + 24, barVfree = barKfree + 8 * kKV;
+    constexpr int kNumBars = 1 + 2 * kKV + 3 + 3 + 2 + 2 + 2 + 3 + 2 * kKV;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 8 * kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffBar + 8 * kNumBars + 4);
 
@@ -282,8 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             const uint32_t b = barQ + 8 * i;
-            const bool softmax_arrivals = (b >= barSfree && b < barOP);   // S free[3] and P[2]: 256 threads
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(softmax_arrivals ? 256u : 1u)
+            const bool softmax_arrivals = (b >= barSfree && b < barOP);   // S free[3] and P[2]: the softmax threads
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b),
+                         "r"(softmax_arrivals ? (uint32_t)(kSoftWarps * 32) : 1u)
                          : "memory");
         }
         *abort_flag = 0;
@@ -319,7 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, true);
 
     if (warp == kKWarp || warp == kVWarp) {
-        // ---- copy warps: a lane per box, block ids fetched a tile at a time
+        // ---- copy warps: a lane per box.  Block ids sit in registers: one
+        // load of the 32 lanes holds blocks c * 32 + lane, i.e. tiles c * TPC ..
+        // c * TPC + TPC - 1, and the next load is issued a whole load ahead,
+        // so no copy waits on a table read (a dependent read per tile held the
+        // copies ~1,800 cycles apart, slower than the MMAs consume tiles).
+        constexpr int TPC = 32 / NBT;
         const bool is_k = warp == kKWarp;
         const int32_t *table_row = p.tables + (size_t)s * p.max_blocks;
         const uint32_t bar0 = is_k ? barK : barV;
@@ -329,26 +356,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane < 2) tma_load_4d(sQ + lane * kHalf, &tmap_q, lane * 64, 0, g, s * p.chunk + j0, barQ);
         }
+        auto load_ids = [&](int c) -> int {
+            const int bi = c * 32 + lane;
+            int id = (int)p.num_blocks;   // out-of-bounds coordinate: zero fill
+            if (bi < nblk_seq && bi < n_tiles * NBT) {
+                const int v = __ldg(table_row + bi);
+                if (v < 0 || v >= p.num_blocks) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                else id = v;
+            }
+            return id;
+        };
+        int ids_cur = load_ids(0), ids_next = load_ids(1);
         int issued = 0;
         bool ok = true;
         for (int t = 0; t < n_tiles; ++t) {
             if (*abort_flag) break;
             const int st = t % kKV;
-            int id = (int)p.num_blocks;   // out-of-bounds coordinate: zero fill
-            if (lane < NBT) {
-                const int bi = t * NBT + lane;
-                if (bi < nblk_seq) {
-                    const int v = __ldg(table_row + bi);
-                    if (v < 0 || v >= p.num_blocks) raise_error(p.err, PA_DEVERR_BLOCK_ID);
-                    else id = v;
-                }
+            if (t > 0 && t % TPC == 0) {
+                ids_cur = ids_next;
+                ids_next = load_ids(t / TPC + 1);
             }
+            const int tb = (t % TPC) * NBT;   // the tile's first block in the loaded ids
+            const int id = __shfl_sync(0xffffffffu, ids_cur, (tb + lane) & 31);
             if (t >= kKV) {   // the slot's previous tile has been consumed by its MMAs
-                // (Q.K for a K slot, P.V for a V slot; the next completion of either
-                // barrier needs the copy issued below, so its phase cannot be lapped)
+                // (Q.K for a K slot, P.V for a V slot, each committing to the slot's
+                // own barrier; its next completion needs the copy issued below, so
+                // its phase cannot be lapped)
                 const int tp = t - kKV;
-                const uint32_t free_bar = (is_k ? barS : barSdone) + 8 * (tp % kSBufs);
-                ok = __all_sync(0xffffffffu, mbar_wait(free_bar, (uint32_t)((tp / kSBufs) & 1), p.err));
+                const uint32_t free_bar = (is_k ? barKfree : barVfree) + 8 * (tp % kKV);
+                ok = __all_sync(0xffffffffu, mbar_wait(free_bar, (uint32_t)((tp / kKV) & 1), p.err));
                 if (!ok) {
                     *abort_flag = 1;
                     break;
@@ -358,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             const uint32_t dst = slot0 + st * kTile;
             if (is_k) {
-                const int blk = __shfl_sync(0xffffffffu, id, lane >> 1);
+                const int blk = __shfl_sync(0xffffffffu, ids_cur, (tb + (lane >> 1)) & 31);
                 if (lane < 2 * NBT)
                     tma_load_5d(dst + (lane & 1) * kHalf + (lane >> 1) * (BS * 128), &tmap_k, (lane & 1) * 64, 0, g, 0,
                                 blk, bar0 + 8 * st);
@@ -406,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  smem_desc(sK + st * kTile + off, 16, 1024), idesc_qk, kk > 0);
                         }
                         umma_commit(barS + 8 * sb);
+                        umma_commit(barKfree + 8 * st);   // K slot st is free again
                     }
                 }
             } else {
@@ -419,12 +456,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // 16 keys of the V tile: within one block for b >= 16 (8-key groups
                         // 1024 B apart), or two whole blocks for b = 8 (groups one block apart)
                         const uint32_t v_off = (uint32_t)(kk * 16 / BS) * kVBlock + (uint32_t)((kk * 16) % BS) * 128u;
-                        umma_ts(tO, tmem + p_col(t % kSBufs, kk),
+                        // keys of the first half accumulate into O0, of the second into O1
+                        umma_ts(tO + (uint32_t)(kk / (kKeys / 32)) * 128u, tmem + p_col(t % kSBufs, kk),
                                 smem_desc(sV + st * kTile + v_off, BS * 128, BS >= 16 ? 1024 : kVBlock), idesc_pv,
-                                (t > 0 || kk > 0) ? 1u : 0u);
+                                (t > 0 || kk % (kKeys / 32) > 0) ? 1u : 0u);
                     }
                     umma_commit(barOP + 8 * (t & 1));
                     umma_commit(barSdone + 8 * (t % kSBufs));
+                    umma_commit(barVfree + 8 * st);   // V slot st is free again
                 }
             }
             // One more commit, on a barrier used once, tracks every MMA this lane
@@ -440,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---- softmax warps: row r, key half hf (scale_log2 > 0: maxima of raw scores)
-        const int r = (warp & 3) * 32 + lane, hf = warp >> 2;
+        // ---- softmax warps: row r, key part pt (scale_log2 > 0: maxima of raw scores)
+        const int r = (warp & 3) * 32 + lane, pt = warp >> 2;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const int jr = j0 + r / G;
         const int pos = p.causal ? min(ctx + jr, seq_end - 1) : seq_end - 1;   // last key this row may attend
@@ -452,40 +491,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < n_tiles; ++t) {
             const int st = t & 1, sb = t % kSBufs;   // st: P barrier of this tile
             bool ok = mbar_wait(barS + 8 * sb, (uint32_t)((t / kSBufs) & 1), p.err);
-            uint32_t sr[2][32];
+            uint32_t sr[kPC][32];
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
-                tmem_ld32(tmem + sb * 128 + lane_off + hf * 64, sr[0]);
-                tmem_ld32(tmem + sb * 128 + lane_off + hf * 64 + 32, sr[1]);
+#pragma unroll
+                for (int cc = 0; cc < kPC; ++cc) tmem_ld32(tmem + sb * 128 + lane_off + pt * kPK + cc * 32, sr[cc]);
                 tmem_ld_wait();
             } else {
                 ok = false;
             }
             tc_fence_before();
             mbar_arrive_u32(barSfree + 8 * sb);
-            const int key0 = t * kKeys + hf * 64;
-            if (!__all_sync(0xffffffffu, key0 + 63 <= pos)) {   // tile crosses some row's causal edge
+            const int key0 = t * kKeys + pt * kPK;
+            if (!__all_sync(0xffffffffu, key0 + kPK - 1 <= pos)) {   // tile crosses some row's causal edge
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc)
+                for (int cc = 0; cc < kPC; ++cc)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (key0 + cc * 32 + i > pos) sr[cc][i] = __float_as_uint(-INFINITY);
             }
-            const float mh = max_tree64(sr[0], sr[1]);
-            // both halves of the row agree on the tile maximum and on giving up
-            xch[hf * 128 + r] = (ok && !*abort_flag) ? mh : __int_as_float(0x7fc00001);
-            pair_sync(warp);
-            const float other = xch[(1 - hf) * 128 + r];
-            const float mine = xch[hf * 128 + r];
-            pair_sync(warp);
-            const bool stop = __any_sync(0xffffffffu, __float_as_int(other) == 0x7fc00001 ||
-                                                          __float_as_int(mine) == 0x7fc00001);
-            if (stop) {
+            float mh;
+            if constexpr (kPC == 2) mh = max_tree64(sr[0], sr[1]);
+            else mh = max_tree32(sr[0]);
+            if (__any_sync(0xffffffffu, !ok || *abort_flag)) {   // give up
                 *abort_flag = 1;
                 mbar_arrive_u32(barP + 8 * st);   // keep the arrival count balanced
                 break;
             }
-            const float mt_ = fmaxf(mh, other) * c;
+            // this half's own reference: it moves only when the tile maximum
+            // exceeds it by more than kRescaleThreshold; the halves' sums meet in
+            // the epilogue, so the halves never wait for each other here
+            const float mrow = mh;
+            const float mt_ = mrow * c;
             float alpha = 1.f;
             if (mt_ > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt_ != -INFINITY)) {
                 alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - mt_);
@@ -494,12 +531,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 c2 = make_float2(c, c);
             const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
             const float2 nm2 = make_float2(nm, nm);
-            // P goes back into this half's S columns (read above), two bf16 per
+            // P goes back into this part's S columns (read above), two bf16 per
             // column; Q.K(t + 3) overwrites them only after P.V(t) has read them
             float2 ps2 = make_float2(0.f, 0.f);
             uint32_t pw[32];
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < kPC; ++cc) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cc][2 * e]),
@@ -510,23 +547,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pw[cc * 16 + e] = pack_bf16x2(pe.x, pe.y);
                 }
             }
-            tmem_st32(tmem + sb * 128 + lane_off + hf * 64, pw);
+            if constexpr (kPC == 2) tmem_st32(tmem + sb * 128 + lane_off + pt * kPK, pw);
+            else tmem_st16(tmem + sb * 128 + lane_off + pt * kPK, pw);
             tmem_st_wait();
             l2.x = l2.x * alpha + (ps2.x + ps2.y);
-            // rescale this half of O once P.V(t-1) has completed (the barrier's
-            // previous phase, P.V(t-3), completed before Q.K(t) was issued)
+            // rescale this half's accumulator (all of d) once P.V(t-1) has completed
+            // (the barrier's previous phase, P.V(t-3), completed before Q.K(t - 1)
+            // was issued, which S(t - 1), read before this tile, needed)
             if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 const int tp = t - 1;
                 mbar_wait(barOP + 8 * (tp & 1), (uint32_t)((tp >> 1) & 1), p.err);
                 tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
+                for (int cc = 0; cc < kD / 32; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(tO + lane_off + hf * 64 + cc * 32, o);
+                    tmem_ld32(tO + pt * 128 + lane_off + cc * 32, o);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(tO + lane_off + hf * 64 + cc * 32, o);
+                    tmem_st32(tO + pt * 128 + lane_off + cc * 32, o);
                 }
                 tmem_st_wait();
             }
@@ -534,7 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (their p is 0, but the slots may hold non-finite junk)
             const int tile0 = t * kKeys;
             const int tail_lo = seq_end - tile0, blk_end = ((seq_end + BS - 1) / BS) * BS - tile0;
-            if (tail_lo > 0 && tail_lo < kKeys && (seq_end % BS) != 0) {
+            const bool zero_tail = tail_lo > 0 && tail_lo < kKeys && (seq_end % BS) != 0;
+            if (zero_tail) {
                 const int sv = t % kKV;   // V ring slot of this tile
                 mbar_wait(barV + 8 * sv, (uint32_t)((t / kKV) & 1), p.err);
                 const int nrows = min(blk_end, kKeys) - tail_lo;
@@ -545,57 +585,91 @@ __global__ void __launch_bounds__(kThreads, 1)
                     asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
                 }
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // the zeroed V rows (generic proxy) before the P.V that reads them (async proxy)
+            if (zero_tail) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
             mbar_arrive_u32(barP + 8 * st);
             done = t + 1;
         }
-        // ---- epilogue: O / l, this thread's row and key half: bf16, or fp32
-        // with the row's log-sum-exp
+        // ---- epilogue: the row's two halves merged by their references (O0 f0 +
+        // O1 f1) / (l0 f0 + l1 f1), f_h = 2^(m_h - max(m0, m1)); this thread
+        // writes half of d: bf16, or fp32 with the row's log-sum-exp.  The
+        // halves' (m, l) meet in the Q tile, free once every Q.K has completed
+        // (each did before its S was read).
         const float l = l2.x;
         const bool empty = n_tiles == 0;   // no keys: O = 0, lse = -inf, tensor memory never written
         // every P.V has completed once the P.V lane's drain commit has arrived
         const bool fin = empty || (done == n_tiles && !*abort_flag && mbar_wait(barEnd, 0, p.err));
-        xch[hf * 128 + r] = l;
-        pair_sync(warp);
-        const float lt = l + xch[(1 - hf) * 128 + r];
+        float mh2[kParts], lh2[kParts];
+#pragma unroll
+        for (int q = 0; q < kParts; ++q) {
+            mh2[q] = -INFINITY;
+            lh2[q] = 0.f;
+        }
+        if (!empty) {   // (with no keys the Q copy may still be landing; O and l are zero anyway)
+            float *mx = reinterpret_cast<float *>(gbase + kOffQ);
+            float *lx = mx + kParts * 128;
+            mx[pt * 128 + r] = m_ref;
+            lx[pt * 128 + r] = l;
+            part_sync(warp);
+#pragma unroll
+            for (int q = 0; q < kParts; ++q) {
+                mh2[q] = mx[q * 128 + r];
+                lh2[q] = lx[q * 128 + r];
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kParts; ++q) M = fmaxf(M, mh2[q]);
+        float f[kParts], lt = 0.f;
+#pragma unroll
+        for (int q = 0; q < kParts; ++q) {
+            f[q] = mh2[q] == -INFINITY ? 0.f : fast_exp2(mh2[q] - M);
+            lt += lh2[q] * f[q];
+        }
         tc_fence_after();
         if (__all_sync(0xffffffffu, fin)) {
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
             const bool row_ok = jr < p.chunk;
             const size_t row = ((size_t)s * p.chunk + jr) * p.num_q_heads + (size_t)g * G + (r % G);
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t o[32];
-                if (!empty) {
-                    tmem_ld32(tO + lane_off + hf * 64 + cc * 32, o);
-                    tmem_ld_wait();
-                } else {
+            for (int cc = 0; cc < kD / kParts / 32; ++cc) {
+                const int d0 = pt * (kD / kParts) + cc * 32;   // this chunk's first dim
+                float o[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                if (!empty) {
+#pragma unroll
+                    for (int q = 0; q < kParts; ++q) {
+                        uint32_t oq[32];
+                        tmem_ld32(tO + q * 128 + lane_off + d0, oq);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] += __uint_as_float(oq[i]) * f[q];
+                    }
                 }
                 if (row_ok && p.o_part != nullptr) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + row * kD + hf * 64 + cc * 32);
+                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + row * kD + d0);
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4)
-                        dst[q4] = make_float4(__uint_as_float(o[q4 * 4 + 0]) * inv, __uint_as_float(o[q4 * 4 + 1]) * inv,
-                                              __uint_as_float(o[q4 * 4 + 2]) * inv, __uint_as_float(o[q4 * 4 + 3]) * inv);
+                        dst[q4] = make_float4(o[q4 * 4 + 0] * inv, o[q4 * 4 + 1] * inv, o[q4 * 4 + 2] * inv,
+                                              o[q4 * 4 + 3] * inv);
                 } else if (row_ok) {
-                    __nv_bfloat16 *dst = p.out + row * kD + hf * 64;
+                    __nv_bfloat16 *dst = p.out + row * kD + d0;
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
-                        v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
-                        v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
-                        v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(dst + cc * 32 + q4 * 8) = v;
+                        v.x = pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+                        v.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+                        v.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+                        v.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
+                        *reinterpret_cast<uint4 *>(dst + q4 * 8) = v;
                     }
                 }
             }
-            // sum of exp2(s * scale * log2 e) over the row's keys is lt * 2^m_ref
-            if (row_ok && p.o_part != nullptr && hf == 0)
-                p.lse[row] = lt > 0.f ? (m_ref + log2f(lt)) * kLn2 : -INFINITY;
+            // sum of exp2(s * scale * log2 e) over the row's keys is lt * 2^M
+            if (row_ok && p.o_part != nullptr && pt == 0)
+                p.lse[row] = lt > 0.f ? (M + log2f(lt)) * kLn2 : -INFINITY;
         }
     }
     tc_fence_before();
