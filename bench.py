@@ -378,13 +378,24 @@ def measure_cascade(pa, step, K: int, warmup: int):
         prefix(i)
         suffix(i)
 
+    def grouped(i):
+        pa.decode_grouped(step.out, step.qs[i % step.layers], step.pools[i % step.layers], pt, pl, st, sl, gsz, max_p,
+                          max_s, w.scale, group_order=order, new_k=step.new_k, new_v=step.new_v)
+
     step_ms = timed_graph(both, K, warmup) / K
     prefix_ms = timed_graph(prefix, K, warmup) / K
     suffix_ms = timed_graph(suffix, K, warmup) / K
+    try:   # the one-call form, where every member's suffix fits the suffix tile
+        grouped(0)
+        grouped_ms = timed_graph(grouped, K, warmup) / K
+    except pa.PagedAttentionError as e:
+        if e.status != 2:
+            raise
+        grouped_ms = None
     assert pa.get_device_error() == 0, "device error during the cascade calls"
     return {"group_size": gsz, "groups": int(len(plan["prefix_lens"])),
             "prefix_tokens_mean": float(plan["prefix_lens"].mean()),
-            "step_ms": step_ms, "prefix_ms": prefix_ms, "suffix_ms": suffix_ms}
+            "step_ms": step_ms, "prefix_ms": prefix_ms, "suffix_ms": suffix_ms, "grouped_ms": grouped_ms}
 
 
 def measure_copy_blocks(pa, step, K: int, warmup: int):
@@ -530,8 +541,9 @@ def measure_config(pa, name: str, dev, K: int, warmup: int):
         res["auto_decode_ms"] = timed_graph(lambda i: step.decode(i % step.layers, 0, ws0), K, warmup) / K
     casc = measure_cascade(pa, step, K, warmup)
     if casc is not None:
-        for k in ("step_ms", "prefix_ms", "suffix_ms"):
-            res["cascade_" + k] = casc[k]
+        for k in ("step_ms", "prefix_ms", "suffix_ms", "grouped_ms"):
+            if casc[k] is not None:
+                res["cascade_" + k] = casc[k]
     assert pa.get_device_error() == 0, f"device error during {name}"
     meta = {"w": w, "part": step.part, "num_parts": step.num_parts, "fused": step.fused,
             "launches": step.launches_per_step, "cascade": casc, "copies": copies}
@@ -582,6 +594,17 @@ def config_line(name, res, meta, peak, peak_kind, world):
                           "note": "pa_prefix_attention over each group's shared prefix (tensor cores, read once per "
                                   "group), then pa_decode_cascade over the private suffixes with the new tokens "
                                   "stored by the call"}
+        if "cascade_grouped_ms" in res:
+            gms = res["cascade_grouped_ms"]
+            out["cascade"]["grouped"] = {
+                "step_ms": round(gms, 5), "tokens_per_s": round(world * w.batch / (gms / 1e3), 1),
+                "speedup_vs_step": round(res["step_ms"] / gms, 3),
+                "roofline": {"bound": "hbm", "kernel": "prefill_kernel, grouped (prefix tiles + one suffix tile)",
+                             "achieved": round(uniq / (gms / 1e3) / 1e9, 1), "peak": peak, "peak_kind": peak_kind,
+                             "unit": "GB/s", "frac": round(uniq / (gms / 1e3) / 1e9 / peak, 4), "traffic": None,
+                             "algorithmic_bytes": uniq, "note": "unique bytes over the one-call step"},
+                "note": "pa_decode_grouped: each group's queries over its shared prefix and then one tile of every "
+                        "member's suffix blocks, the new tokens stored by the call; one launch"}
     if meta["copies"] is not None:
         cp = meta["copies"]
         out["copy_blocks"] = {"pairs": cp["pairs"], "ms": round(res["copy_ms"], 5),
@@ -737,6 +760,7 @@ def run_ours(args, world, rank, local):
     if casc is not None:
         for k in ("step_ms", "prefix_ms", "suffix_ms"):
             flat.append(casc[k])
+        casc.pop("grouped_ms", None)
     red = reduce_max(flat, world, dev)
     total_ms, e2e_ms, decode_avg_ms, wtotal_ms, ftotal_ms, fdecode_ms = red[:6]
     off = 6

@@ -415,6 +415,43 @@ pa_status pa_decode_cascade(void *out, const void *q, const pa_kv_pool *pool,
                             uint32_t flags, cudaStream_t stream);
 
 /*
+ * Grouped decode: the cascade's two passes as one call, for groups whose
+ * members' private suffixes are short (the beams of a prompt after their
+ * copy-on-write fork).  [P1] feature table (beam-search row) and [P2]
+ * beam/copy-on-write follow-up: beams share their prompt's blocks and each
+ * owns its diverged last block; [P3] "Shared prefixes need matching
+ * computation".  Each group's queries attend its shared prefix (the
+ * pa_prefix_attention layout and tiling: K/V tiles read once for the whole
+ * group, on the tensor cores), then one more 128-key tile that holds every
+ * member's own suffix blocks, each query seeing its member's keys only; the
+ * output is attention over prefix and suffix together, written as bf16, with
+ * no partial results, second launch or workspace.
+ *   out, q         device, [num_groups * group_size][num_q_heads][d] bf16,
+ *                  sequences group by group (out written)
+ *   prefix_tables, max_prefix_blocks, prefix_lens, group_order, max_prefix_len
+ *                  as pa_prefix_attention (prefixes whole blocks)
+ *   suffix_tables  device, [num_groups * group_size][max_suffix_blocks] int32:
+ *                  each member's blocks after the prefix (pa_cascade_plan's)
+ *   suffix_lens    device, [num_groups * group_size] int32, tokens after the
+ *                  prefix, each <= max_suffix_len (else PA_DEVERR_SEQ_LEN)
+ *   max_suffix_len host bound on every suffix length
+ *   new_k, new_v   device, [num_groups * group_size][Hkv][d] bf16 or both NULL:
+ *                  each member's new token, stored at its last suffix position
+ *                  (as pa_decode_ex stores it) before it is attended
+ * Supported when the members of one M-tile (min(group_size, 128 / (num_q_heads
+ * / Hkv))) times ceil(max_suffix_len / block_size) blocks fit one 128-key
+ * tile; otherwise PA_ERR_UNSUPPORTED (use pa_prefix_attention and
+ * pa_decode_cascade).  head_dim 128 as pa_prefill_chunk.  The pages have no
+ * counterpart to the fused form; it computes what the cascade does.
+ */
+pa_status pa_decode_grouped(void *out, const void *q, const pa_kv_pool *pool, const int32_t *prefix_tables,
+                            int32_t max_prefix_blocks, const int32_t *prefix_lens, const int32_t *group_order,
+                            const int32_t *suffix_tables, int32_t max_suffix_blocks, const int32_t *suffix_lens,
+                            int32_t num_groups, int32_t group_size, int32_t num_q_heads, int32_t max_prefix_len,
+                            int32_t max_suffix_len, float scale, const void *new_k, const void *new_v,
+                            cudaStream_t stream);
+
+/*
  * Check of the bounded waits: launches one CTA whose wait on a shared-memory
  * barrier that nothing arrives at gives up after limit_ns (1 us .. 1 s, else
  * PA_ERR_INVALID_ARG) through the same wait every kernel uses, records

@@ -66,6 +66,8 @@ SIGNATURES = {
     "pa_decode_cascade": (_I32, [_P, _P, _POOL, _P, _I32, _P, _I32, _I32, _I32, _F, _I32, _P, _SZ, _P, _P, _P, _P,
                                  _U32, _P]),
     "pa_cascade_plan": (_I32, [_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
+    "pa_decode_grouped": (_I32, [_P, _P, _POOL, _P, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _F,
+                                 _P, _P, _P]),
     "pa_get_device_error": (_I32, [ctypes.POINTER(_U32), _I32, _P]),
     "pa_check_wait_timeout": (_I32, [ctypes.c_uint64, _P]),
     "pa_set_stream_k_ctas": (_I32, [_I32]),
@@ -390,6 +392,41 @@ def decode_cascade(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, suffi
                                    _dev(prefix_o, torch.float32, "prefix_o"),
                                    _dev(prefix_lse, torch.float32, "prefix_lse"), nk, nv, int(flags),
                                    _stream(stream)), "pa_decode_cascade")
+
+
+def decode_grouped(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, prefix_tables: torch.Tensor,
+                   prefix_lens: torch.Tensor, suffix_tables: torch.Tensor, suffix_lens: torch.Tensor, group_size: int,
+                   max_prefix_len: int, max_suffix_len: int, scale: float,
+                   group_order: Optional[torch.Tensor] = None, new_k: Optional[torch.Tensor] = None,
+                   new_v: Optional[torch.Tensor] = None, layer: Optional[int] = None, stream=None) -> None:
+    """pa_decode_grouped: each group's queries over its shared prefix and each
+    member's own suffix in one call (the cascade fused, for short suffixes)."""
+    desc = pool_desc(pool, layer)
+    B, Hq, _ = q.shape
+    if group_size <= 0 or B % group_size != 0:
+        raise ValueError("the batch must be whole groups")
+    G = B // group_size
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if prefix_tables.dim() != 2 or prefix_tables.shape[0] != G or prefix_lens.numel() != G:
+        raise ValueError("prefix_tables / prefix_lens do not match the groups")
+    if suffix_tables.dim() != 2 or suffix_tables.shape[0] != B or suffix_lens.numel() != B:
+        raise ValueError("suffix_tables / suffix_lens do not match the batch")
+    if group_order is not None and group_order.numel() != G:
+        raise ValueError("group_order must hold one entry per group")
+    for name, t in (("new_k", new_k), ("new_v", new_v)):
+        if t is not None and (t.dim() != 3 or t.shape[0] != B or t.shape[1:] != (desc.num_kv_heads, desc.head_dim)):
+            raise ValueError(f"{name} must be [num_seqs][num_kv_heads][head_dim]")
+    order = _dev(group_order, torch.int32, "group_order") if group_order is not None else ctypes.c_void_p(0)
+    nk = _dev(new_k, torch.bfloat16, "new_k") if new_k is not None else ctypes.c_void_p(0)
+    nv = _dev(new_v, torch.bfloat16, "new_v") if new_v is not None else ctypes.c_void_p(0)
+    _check(lib().pa_decode_grouped(_dev(out, torch.bfloat16, "out"), _dev(q, torch.bfloat16, "q"),
+                                   ctypes.byref(desc), _dev(prefix_tables, torch.int32, "prefix_tables"),
+                                   prefix_tables.shape[1], _dev(prefix_lens, torch.int32, "prefix_lens"), order,
+                                   _dev(suffix_tables, torch.int32, "suffix_tables"), suffix_tables.shape[1],
+                                   _dev(suffix_lens, torch.int32, "suffix_lens"), G, int(group_size), Hq,
+                                   int(max_prefix_len), int(max_suffix_len), float(scale), nk, nv, _stream(stream)),
+           "pa_decode_grouped")
 
 
 def cascade_plan(tables, seq_lens, group_size: int, block_size: int) -> dict:

@@ -1,6 +1,7 @@
 // pa_api.cpp -- the C ABI (include/pa.h): argument validation, partition
 // planning and dispatch to the kernels.  Host code only; it allocates no
 // device memory and launches nothing when validation fails.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -367,6 +368,58 @@ pa_status pa_prefix_attention(float *o_part, float *lse, const void *q, const pa
     a.o_part = o_part;
     a.lse = lse;
     a.order = group_order;
+    return launch_prefill(a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_decode_grouped(void *out, const void *q, const pa_kv_pool *pool, const int32_t *prefix_tables,
+                            int32_t max_prefix_blocks, const int32_t *prefix_lens, const int32_t *group_order,
+                            const int32_t *suffix_tables, int32_t max_suffix_blocks, const int32_t *suffix_lens,
+                            int32_t num_groups, int32_t group_size, int32_t num_q_heads, int32_t max_prefix_len,
+                            int32_t max_suffix_len, float scale, const void *new_k, const void *new_v,
+                            cudaStream_t stream) {
+    PoolView view;
+    pa_status st = resolve_pool(pool, &view);
+    if (st != PA_OK) return st;
+    if (num_groups < 0 || group_size < 0 || num_q_heads <= 0 || max_prefix_len < 0 || max_suffix_len < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % view.num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    const int group = num_q_heads / view.num_kv_heads;
+    if (!prefill_supported(view.head_dim, group, view.block_size)) return PA_ERR_UNSUPPORTED;
+    // one 128-key tile holds the suffix blocks of every member of an M-tile
+    const int64_t members = std::min<int64_t>(group_size, 128 / group);
+    const int64_t nb = ceil_div(max_suffix_len, view.block_size);
+    if (members * nb * view.block_size > 128) return PA_ERR_UNSUPPORTED;
+    if (num_groups == 0 || group_size == 0) return PA_OK;
+    if (!out || !q || !prefix_tables || !prefix_lens || max_prefix_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (!suffix_tables || !suffix_lens || max_suffix_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q)) return PA_ERR_INVALID_ARG;
+    if ((new_k == nullptr) != (new_v == nullptr)) return PA_ERR_INVALID_ARG;
+    if (new_k && (!aligned16(new_k) || !aligned16(new_v))) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
+    if ((int64_t)max_prefix_len > (int64_t)max_prefix_blocks * view.block_size) return PA_ERR_INVALID_ARG;
+    if ((int64_t)max_suffix_len > (int64_t)max_suffix_blocks * view.block_size) return PA_ERR_INVALID_ARG;
+    if (num_groups > 65535 || (int64_t)num_groups * group_size > (int64_t)INT32_MAX) return PA_ERR_INVALID_ARG;
+    PrefillArgs a;
+    a.out = out;
+    a.q = q;
+    a.pool = view;
+    a.tables = prefix_tables;
+    a.max_blocks = max_prefix_blocks;
+    a.ctx_lens = prefix_lens;
+    a.num_seqs = num_groups;
+    a.chunk_len = group_size;
+    a.num_q_heads = num_q_heads;
+    a.max_ctx_len = max_prefix_len;
+    a.scale = scale;
+    a.causal = false;
+    a.order = group_order;
+    a.sfx_tables = suffix_tables;
+    a.sfx_max_blocks = max_suffix_blocks;
+    a.sfx_lens = suffix_lens;
+    a.sfx_nb = (int32_t)nb;
+    a.max_sfx_len = max_suffix_len;
+    a.new_k = new_k;
+    a.new_v = new_v;
     return launch_prefill(a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -102,6 +102,14 @@ struct PrefillArgs {
     float *o_part = nullptr;   // non-null: fp32 normalised output + lse instead of out
     float *lse = nullptr;
     const int32_t *order = nullptr;   // non-null: sequences in this order (a permutation)
+    // grouped decode: members' suffix tables and lengths (nullptr: none)
+    const int32_t *sfx_tables = nullptr;
+    int32_t sfx_max_blocks = 0;
+    const int32_t *sfx_lens = nullptr;
+    int32_t sfx_nb = 0;        // suffix-tile blocks per member
+    int32_t max_sfx_len = 0;
+    const void *new_k = nullptr;
+    const void *new_v = nullptr;
 };
 bool prefill_supported(int head_dim, int group, int block_size);
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);

@@ -93,6 +93,10 @@ constexpr uint32_t kTmemCols = 512;         // S0, S1, O0, O1 (128 columns each)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 domain
+#ifndef PA_PREFILL_PRECISE_KEYS
+#define PA_PREFILL_PRECISE_KEYS 512
+#endif
+constexpr int kPreciseKeys = PA_PREFILL_PRECISE_KEYS;   // fewer visible keys: probabilities as two bf16 terms
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct Params {
@@ -110,7 +114,37 @@ struct Params {
     float *o_part;               // non-null: fp32 output normalised by l, [B][C][Hq][D], instead of out
     float *lse;                  // with o_part: [B][C][Hq] natural-log sum of exp(scale * q.k)
     const int32_t *order;        // non-null: CTA z processes sequence order[z] (a permutation of 0 .. B-1)
+    // Grouped decode (sfx_tables non-null): sequence s stands for a group of
+    // `chunk` members that share its ctx_lens[s] prefix tokens; after the
+    // prefix tiles one more tile holds every member's own suffix blocks (member
+    // m of the M-tile in blocks m * sfx_nb .. m * sfx_nb + sfx_nb - 1), and each
+    // row attends the prefix plus its member's suffix keys only.
+    const int32_t *sfx_tables;   // [groups * chunk][sfx_max_blocks]
+    int32_t sfx_max_blocks;
+    const int32_t *sfx_lens;     // [groups * chunk]
+    int32_t sfx_nb;              // tail-tile blocks per member
+    int32_t max_sfx_len;
+    // with sfx_tables: each member's new token, stored at its last suffix
+    // position before that tile is read (nullptr: none)
+    const __nv_bfloat16 *new_k;  // [groups * chunk][Hkv][D]
+    const __nv_bfloat16 *new_v;
+    __nv_bfloat16 *pool;         // the layer's pool view (element strides below)
+    int64_t block_stride;
+    int64_t kv_stride;
 };
+
+// Suffix length of member sequence `seq`, clipped to [0, its bound] (an
+// out-of-range length is reported and clipped).
+template <int BS>
+__device__ __forceinline__ int suffix_len(const Params &p, int seq, bool report) {
+    int L = __ldg(p.sfx_lens + seq);
+    const int cap = min(p.max_sfx_len, min(p.sfx_max_blocks, p.sfx_nb) * BS);
+    if (L < 0 || L > cap) {
+        if (report) raise_error(p.err, PA_DEVERR_SEQ_LEN);
+        L = L < 0 ? 0 : cap;
+    }
+    return L;
+}
 
 // ---- PTX wrappers -----------------------------------------------------------
 
@@ -267,7 +301,7 @@ __device__ __forceinline__ float max_tree64(const uint32_t (&a)[32], const uint3
 // one drain per MMA lane (MMA commit, used once).
 // A parity wait is exact only while the barrier's previous phase is known to
 // have completed; each wait below names the completion that guarantees it.
-template <int G, int BS>
+template <int G, int BS, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const Params p) {
@@ -336,7 +370,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seq_end = p.causal ? ctx + p.chunk : ctx;
     const int nblk_seq = (seq_end + BS - 1) / BS;
     const int last_q = min(j0 + QPT, p.chunk) - 1;             // last valid query of this tile
-    const int n_tiles = ((p.causal ? ctx + last_q + 1 : ctx) + kKeys - 1) / kKeys;   // 0 only without causal
+    const int n_pre = ((p.causal ? ctx + last_q + 1 : ctx) + kKeys - 1) / kKeys;   // 0 only without causal
+    // grouped decode is a separate instantiation: its code in the plain
+    // kernel, even when idle, cost the causal prefill 20% (1.18 against 0.98 ms)
+    const bool grouped = kGrouped && p.sfx_tables != nullptr && p.sfx_nb > 0;
+    const int n_tiles = n_pre + (grouped ? 1 : 0);   // grouped: the members' suffix tile last
+    // members of this M-tile (grouped): queries j0 .. j0 + members - 1
+    const int members = max(0, min(QPT, p.chunk - j0));
+    // Grouped rows that may see fewer than kPreciseKeys keys carry each
+    // probability as two bf16 terms, hi = bf16(p) and lo = bf16(p - hi), and
+    // P.V runs once for each: with few keys a single rounding of p (relative
+    // error 2^-9) does not average down (one output of an eight-key beam row
+    // moved by 1.0% of its value); with many it does, and one term is kept.
+    // The plain kernel has no second term at all: even idle, it cost the
+    // causal prefill 13% (1.09 against 0.96 ms).
+    const bool precise = kGrouped && ctx + p.max_sfx_len < kPreciseKeys;
     constexpr uint32_t idesc_qk = idesc_bf16(kRows, kKeys, false);
     constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, true);
 
@@ -356,10 +404,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane < 2) tma_load_4d(sQ + lane * kHalf, &tmap_q, lane * 64, 0, g, s * p.chunk + j0, barQ);
         }
+        int tail_id = (int)p.num_blocks;   // grouped: this lane's block of the suffix tile (out of bounds: zeros)
+        if (grouped) {
+            // each member's new token first (K warp: K rows, V warp: V rows), 16
+            // bytes a lane, then a proxy fence: this warp's tensor copy of the
+            // suffix tile is issued after it in program order
+            if (p.new_k != nullptr) {
+                for (int m = 0; m < members; ++m) {
+                    const int seq = s * p.chunk + j0 + m;
+                    const int L = suffix_len<BS>(p, seq, is_k && lane == 0 && g == 0);
+                    if (L <= 0 || lane >= kD / 8) continue;
+                    const int blk = __ldg(p.sfx_tables + (size_t)seq * p.sfx_max_blocks + (L - 1) / BS);
+                    if (blk < 0 || blk >= p.num_blocks) continue;   // reported with the tile's ids below
+                    const __nv_bfloat16 *src = (is_k ? p.new_k : p.new_v) + ((size_t)seq * gridDim.y + g) * kD + lane * 8;
+                    __nv_bfloat16 *dst = p.pool + (size_t)blk * p.block_stride + (is_k ? 0 : p.kv_stride) +
+                                         ((size_t)g * BS + (L - 1) % BS) * kD + lane * 8;
+                    *reinterpret_cast<uint4 *>(dst) = __ldg(reinterpret_cast<const uint4 *>(src));
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __syncwarp();
+            }
+            if (lane < NBT) {
+                const int m = lane / p.sfx_nb, b = lane % p.sfx_nb;
+                if (m < members) {
+                    const int seq = s * p.chunk + j0 + m;
+                    if (b * BS < suffix_len<BS>(p, seq, false)) {
+                        const int v = __ldg(p.sfx_tables + (size_t)seq * p.sfx_max_blocks + b);
+                        if (v < 0 || v >= p.num_blocks) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                        else tail_id = v;
+                    }
+                }
+            }
+        }
         auto load_ids = [&](int c) -> int {
             const int bi = c * 32 + lane;
             int id = (int)p.num_blocks;   // out-of-bounds coordinate: zero fill
-            if (bi < nblk_seq && bi < n_tiles * NBT) {
+            if (bi < nblk_seq && bi < n_pre * NBT) {
                 const int v = __ldg(table_row + bi);
                 if (v < 0 || v >= p.num_blocks) raise_error(p.err, PA_DEVERR_BLOCK_ID);
                 else id = v;
@@ -377,7 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ids_next = load_ids(t / TPC + 1);
             }
             const int tb = (t % TPC) * NBT;   // the tile's first block in the loaded ids
-            const int id = __shfl_sync(0xffffffffu, ids_cur, (tb + lane) & 31);
+            const bool tail = grouped && t == n_pre;   // the members' suffix tile
+            const int id = tail ? tail_id : __shfl_sync(0xffffffffu, ids_cur, (tb + lane) & 31);
             if (t >= kKV) {   // the slot's previous tile has been consumed by its MMAs
                 // (Q.K for a K slot, P.V for a V slot, each committing to the slot's
                 // own barrier; its next completion needs the copy issued below, so
@@ -394,7 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             const uint32_t dst = slot0 + st * kTile;
             if (is_k) {
-                const int blk = __shfl_sync(0xffffffffu, ids_cur, (tb + (lane >> 1)) & 31);
+                const int blk = tail ? __shfl_sync(0xffffffffu, tail_id, lane >> 1)
+                                     : __shfl_sync(0xffffffffu, ids_cur, (tb + (lane >> 1)) & 31);
                 if (lane < 2 * NBT)
                     tma_load_5d(dst + (lane & 1) * kHalf + (lane >> 1) * (BS * 128), &tmap_k, (lane & 1) * 64, 0, g, 0,
                                 blk, bar0 + 8 * st);
@@ -452,14 +534,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait(barV + 8 * st, (uint32_t)((t / kKV) & 1))) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < kKeys / 16; ++kk) {
-                        // 16 keys of the V tile: within one block for b >= 16 (8-key groups
-                        // 1024 B apart), or two whole blocks for b = 8 (groups one block apart)
-                        const uint32_t v_off = (uint32_t)(kk * 16 / BS) * kVBlock + (uint32_t)((kk * 16) % BS) * 128u;
-                        // keys of the first half accumulate into O0, of the second into O1
-                        umma_ts(tO + (uint32_t)(kk / (kKeys / 32)) * 128u, tmem + p_col(t % kSBufs, kk),
-                                smem_desc(sV + st * kTile + v_off, BS * 128, BS >= 16 ? 1024 : kVBlock), idesc_pv,
-                                (t > 0 || kk % (kKeys / 32) > 0) ? 1u : 0u);
+                    for (int term = 0; term < (precise ? 2 : 1); ++term) {   // hi, then lo (precise rows)
+#pragma unroll
+                        for (int kk = 0; kk < kKeys / 16; ++kk) {
+                            // 16 keys of the V tile: within one block for b >= 16 (8-key groups
+                            // 1024 B apart), or two whole blocks for b = 8 (groups one block apart)
+                            const uint32_t v_off =
+                                (uint32_t)(kk * 16 / BS) * kVBlock + (uint32_t)((kk * 16) % BS) * 128u;
+                            // keys of the first half accumulate into O0, of the second into O1
+                            umma_ts(tO + (uint32_t)(kk / (kKeys / 32)) * 128u,
+                                    tmem + p_col(t % kSBufs, kk) + (uint32_t)(term * (kPK / 2)),
+                                    smem_desc(sV + st * kTile + v_off, BS * 128, BS >= 16 ? 1024 : kVBlock),
+                                    idesc_pv, (t > 0 || term > 0 || kk % (kKeys / 32) > 0) ? 1u : 0u);
+                        }
                     }
                     umma_commit(barOP + 8 * (t & 1));
                     umma_commit(barSdone + 8 * (t % kSBufs));
@@ -484,6 +571,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const int jr = j0 + r / G;
         const int pos = p.causal ? min(ctx + jr, seq_end - 1) : seq_end - 1;   // last key this row may attend
+        // grouped: this row's keys in the suffix tile, [sfx_lo, sfx_hi)
+        const int sfx_lo = (r / G) * p.sfx_nb * BS;
+        const int sfx_hi = grouped && jr < p.chunk ? sfx_lo + suffix_len<BS>(p, s * p.chunk + jr, false) : sfx_lo;
         const float c = p.scale_log2;
         float m_ref = -INFINITY;                       // reference maximum, log2 domain
         float2 l2 = make_float2(0.f, 0.f);
@@ -503,7 +593,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive_u32(barSfree + 8 * sb);
             const int key0 = t * kKeys + pt * kPK;
-            if (!__all_sync(0xffffffffu, key0 + kPK - 1 <= pos)) {   // tile crosses some row's causal edge
+            if (grouped && t == n_pre) {   // suffix tile: the row's own member's keys only
+#pragma unroll
+                for (int cc = 0; cc < kPC; ++cc)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int k = pt * kPK + cc * 32 + i;
+                        if (k < sfx_lo || k >= sfx_hi) sr[cc][i] = __float_as_uint(-INFINITY);
+                    }
+            } else if (!__all_sync(0xffffffffu, key0 + kPK - 1 <= pos)) {   // tile crosses some row's causal edge
 #pragma unroll
                 for (int cc = 0; cc < kPC; ++cc)
 #pragma unroll
@@ -535,20 +633,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             // column; Q.K(t + 3) overwrites them only after P.V(t) has read them
             float2 ps2 = make_float2(0.f, 0.f);
             uint32_t pw[32];
+            // term 0: hi = bf16(p) into the first half of this part's S columns;
+            // term 1 (precise rows): lo = bf16(p - hi) into the second half
+#pragma unroll 1
+            for (int term = 0; term < (precise ? 2 : 1); ++term) {
 #pragma unroll
-            for (int cc = 0; cc < kPC; ++cc) {
+                for (int cc = 0; cc < kPC; ++cc) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cc][2 * e]),
-                                                            __uint_as_float(sr[cc][2 * e + 1])),
-                                                c2, nm2);
-                    const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                    ps2 = __fadd2_rn(ps2, pe);
-                    pw[cc * 16 + e] = pack_bf16x2(pe.x, pe.y);
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cc][2 * e]),
+                                                                __uint_as_float(sr[cc][2 * e + 1])),
+                                                    c2, nm2);
+                        const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        if (term == 0) {
+                            ps2 = __fadd2_rn(ps2, pe);
+                            pw[cc * 16 + e] = pack_bf16x2(pe.x, pe.y);
+                        } else {
+                            const float2 hi = bf16x2_to_float2(pack_bf16x2(pe.x, pe.y));
+                            pw[cc * 16 + e] = pack_bf16x2(pe.x - hi.x, pe.y - hi.y);
+                        }
+                    }
                 }
+                if constexpr (kPC == 2) tmem_st32(tmem + sb * 128 + lane_off + pt * kPK + term * (kPK / 2), pw);
+                else tmem_st16(tmem + sb * 128 + lane_off + pt * kPK + term * (kPK / 2), pw);
             }
-            if constexpr (kPC == 2) tmem_st32(tmem + sb * 128 + lane_off + pt * kPK, pw);
-            else tmem_st16(tmem + sb * 128 + lane_off + pt * kPK, pw);
             tmem_st_wait();
             l2.x = l2.x * alpha + (ps2.x + ps2.y);
             // rescale this half's accumulator (all of d) once P.V(t-1) has completed
@@ -585,8 +693,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
                 }
             }
+            const bool zero_sfx = grouped && t == n_pre;   // suffix tile: each member's slots past its length
+            if (zero_sfx) {
+                const int sv = t % kKV;
+                mbar_wait(barV + 8 * sv, (uint32_t)((t / kKV) & 1), p.err);
+                for (int m = 0; m < members; ++m) {
+                    const int r0 = m * p.sfx_nb * BS + suffix_len<BS>(p, s * p.chunk + j0 + m, false);
+                    const int r1 = (m + 1) * p.sfx_nb * BS;
+                    for (int idx = tid; idx < (r1 - r0) * 2 * 8; idx += kSoftWarps * 32) {
+                        const int rr = r0 + idx / 16, h = (idx / 8) & 1, c16 = idx & 7;
+                        const uint32_t addr = sV + sv * kTile + (uint32_t)(rr / BS) * kVBlock + h * (kVBlock / 2) +
+                                              (uint32_t)(rr % BS) * 128u + (uint32_t)c16 * 16u;
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                    }
+                }
+            }
             // the zeroed V rows (generic proxy) before the P.V that reads them (async proxy)
-            if (zero_tail) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (zero_tail || zero_sfx) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
             mbar_arrive_u32(barP + 8 * st);
             done = t + 1;
@@ -682,14 +805,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side --------------------------------------------------------------
 
-template <int G, int BS>
-cudaError_t launch_group(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mkv, const CUtensorMap &mv,
+template <int G, int BS, bool kGrouped>
+cudaError_t launch_kernel(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mkv, const CUtensorMap &mv,
                          const Params &prm, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<G, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<G, BS, kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
@@ -706,7 +829,14 @@ cudaError_t launch_group(const PrefillArgs &a, const CUtensorMap &mq, const CUte
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<G, BS>, mq, mkv, mv, prm);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<G, BS, kGrouped>, mq, mkv, mv, prm);
+}
+
+template <int G, int BS>
+cudaError_t launch_group(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mkv, const CUtensorMap &mv,
+                         const Params &prm, cudaStream_t stream) {
+    return a.sfx_tables != nullptr ? launch_kernel<G, BS, true>(a, mq, mkv, mv, prm, stream)
+                                   : launch_kernel<G, BS, false>(a, mq, mkv, mv, prm, stream);
 }
 
 }  // namespace prefill
@@ -769,6 +899,16 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     prm.o_part = a.o_part;
     prm.lse = a.lse;
     prm.order = a.order;
+    prm.sfx_tables = a.sfx_tables;
+    prm.sfx_max_blocks = a.sfx_max_blocks;
+    prm.sfx_lens = a.sfx_lens;
+    prm.sfx_nb = a.sfx_nb;
+    prm.max_sfx_len = a.max_sfx_len;
+    prm.new_k = static_cast<const __nv_bfloat16 *>(a.new_k);
+    prm.new_v = static_cast<const __nv_bfloat16 *>(a.new_v);
+    prm.pool = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.pool.base));
+    prm.block_stride = a.pool.block_stride;
+    prm.kv_stride = a.pool.kv_stride;
     auto by_block = [&](auto gtag) -> cudaError_t {
         constexpr int GG = decltype(gtag)::value;
         switch (a.pool.block_size) {

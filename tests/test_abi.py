@@ -195,3 +195,27 @@ def test_stream_k_grid_override_sizes_the_workspace(B):
         assert L.pa_set_stream_k_ctas(-1) == 1
     finally:
         assert L.pa_set_stream_k_ctas(0) == 0
+
+
+def test_grouped_decode_validation(B):
+    """pa_decode_grouped checks shapes on the host and launches nothing on a
+    refusal: the members of an M-tile must fit one 128-key suffix tile."""
+    L = B.lib()
+    P = ctypes.c_void_p
+    good = _pool(B, nb=64, hkv=8, b=16, d=128)
+    ok_ptr = P(0x20000)
+
+    def call(out=ok_ptr, pool=good, gsz=4, groups=2, hq=64, max_pre=64, max_sfx=32, scale=0.1, nk=P(0), nv=P(0)):
+        return L.pa_decode_grouped(out, ok_ptr, ctypes.byref(pool), ok_ptr, 8, ok_ptr, P(0), ok_ptr, 4, ok_ptr,
+                                   groups, gsz, hq, max_pre, max_sfx, scale, nk, nv, P(0))
+
+    assert call(groups=0) == 0                         # nothing to do
+    assert call(max_sfx=33) == 2                       # 4 members x 3 blocks > 128 keys
+    assert call(gsz=16, max_sfx=16) == 2               # 16 members (of G = 8) x 1 block > 128 keys
+    assert call(pool=_pool(B, d=64)) == 2              # head_dim 64 not built for the tensor-core path
+    assert call(out=P(0)) == 1
+    assert call(out=P(0x20008)) == 1                   # misaligned
+    assert call(nk=ok_ptr) == 1                        # new K without new V
+    assert call(scale=0.0) == 1
+    assert call(max_pre=8 * 16 + 1) == 1               # longer than the prefix table
+    assert call(gsz=1, max_sfx=5 * 16) == 1           # fits the tile, but longer than the 4-block suffix table

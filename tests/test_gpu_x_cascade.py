@@ -277,3 +277,96 @@ def test_beam_cascade_grid_sweep(pa, ctas):
     finally:
         pa.set_stream_k_ctas(0)
     assert_close(out, oracle_full(c), f"beam cascade ctas={ctas}")
+
+
+def grouped_call(pa, c: Case, plan, group_size, max_suffix=None, new_kv=None, order="plan"):
+    w, dev = c.w, c.dev
+    out = torch.full_like(c.q, float("nan"))
+    if isinstance(order, str):
+        order = plan.get("group_order")
+    ms = int(plan["suffix_lens"].max()) if max_suffix is None else max_suffix
+    nk, nv = new_kv if new_kv is not None else (None, None)
+    pa.decode_grouped(out, c.q, c.pool, torch.as_tensor(plan["prefix_tables"], device=dev),
+                      torch.as_tensor(plan["prefix_lens"], device=dev),
+                      torch.as_tensor(plan["suffix_tables"], device=dev),
+                      torch.as_tensor(plan["suffix_lens"], device=dev), group_size,
+                      int(plan["prefix_lens"].max()), ms, w.scale,
+                      group_order=None if order is None else torch.as_tensor(order, device=dev), new_k=nk, new_v=nv)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    return out
+
+
+@pytest.mark.parametrize("group,group_size,bs,max_sfx", [(8, 4, 16, 32), (8, 8, 16, 16), (4, 3, 16, 32),
+                                                         (1, 2, 16, 64), (2, 1, 16, 128), (8, 24, 8, 8)])
+@pytest.mark.parametrize("append", [False, True])
+def test_grouped_decode_matches_oracle(pa, group, group_size, bs, max_sfx, append):
+    """pa_decode_grouped (prefix tiles, then one tile of every member's suffix
+    blocks under a per-row block-diagonal mask) equals the oracle's attention
+    over the whole tables: group sizes filling a fraction of an M-tile, one
+    and several M-tiles per group (24 members of 8 heads), empty suffixes and
+    empty prefixes; with `append`, each member's new token is stored by the
+    call first, the pool bit-exact with the oracle's slot writer."""
+    rng = np.random.default_rng(group * 1000 + group_size * 10 + bs + max_sfx)
+    prefix = [0, 16 * bs // 16 * 1, 400 // bs * bs, 1024]
+    suffix = rng.integers(0, max_sfx + 1, size=len(prefix) * group_size)
+    suffix[0] = 0                # a member with neither prefix nor suffix (group 0 has no prefix)
+    suffix[-1] = max_sfx         # a full suffix
+    w = wl.shared_groups(prefix, list(suffix), group_size, 2 * group, 2, 128, bs, seed=int(rng.integers(1 << 30)))
+    c = Case(w)
+    plan = designed_plan(w, group_size)
+    new_kv = None
+    if append:   # each member with a suffix stores its last token; the oracle's writer does the same
+        sel = np.asarray(plan["suffix_lens"])[w.new_seq_idx] > 0
+        slots = c.orc.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size)
+        c.orc.reshape_and_cache(c.pool_ref, c.geom, bits(c.cpu["new_k"]), bits(c.cpu["new_v"]),
+                                np.where(sel, slots, -1))
+        full_k = torch.zeros((w.batch, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16)
+        full_v = torch.zeros_like(full_k)
+        full_k[w.new_seq_idx] = c.cpu["new_k"]
+        full_v[w.new_seq_idx] = c.cpu["new_v"]
+        new_kv = (full_k.to(c.dev), full_v.to(c.dev))
+    out = grouped_call(pa, c, plan, group_size, max_suffix=max_sfx, new_kv=new_kv)
+    if append:
+        assert np.array_equal(bits(c.pool), c.pool_ref), "the stored new tokens differ from the slot writer's"
+    ref = oracle_full(c)
+    assert_close(out, ref, f"grouped G={group} n={group_size} b={bs} append={append}")
+    assert w.seq_lens[0] == 0 and not out[0].float().abs().sum().item()   # no keys at all: zeros
+
+
+def test_grouped_full_size_beams_repeatable(pa):
+    """The beam batch (32 groups of 4 after copy-on-write) through one
+    pa_decode_grouped call that also stores every beam's new token: every
+    row against the oracle, then eight more calls (every other one under a
+    concurrent copy on a second stream) bit-identical to the first."""
+    w = wl.beam_fork()
+    c = Case(w)
+    pa.copy_blocks(c.pool, torch.as_tensor(w.copy_pairs, device=c.dev))
+    c.orc.copy_blocks(c.pool_ref, c.geom, w.copy_pairs)
+    plan = pa.cascade_plan(w.tables, w.seq_lens, 4, w.block_size)
+    assert int(plan["suffix_lens"].max()) <= 16
+    first = grouped_call(pa, c, plan, 4, new_kv=(c.new_k, c.new_v))
+    c.orc.reshape_and_cache(c.pool_ref, c.geom, bits(c.cpu["new_k"]), bits(c.cpu["new_v"]),
+                            c.orc.slot_mapping(w.tables, w.new_seq_idx, w.new_positions, w.block_size))
+    assert np.array_equal(bits(c.pool), c.pool_ref), "the stored new tokens differ from the slot writer's"
+    assert_close(first, oracle_full(c), "grouped beams")
+    side = torch.cuda.Stream()
+    src = torch.empty(1 << 30, dtype=torch.uint8, device=c.dev)
+    dst = torch.empty_like(src)
+    for rep in range(8):
+        if rep % 2:
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    dst.copy_(src)
+        again = grouped_call(pa, c, plan, 4, new_kv=(c.new_k, c.new_v))
+        assert torch.equal(again, first), f"grouped output differs at run {rep}"
+
+
+def test_grouped_refuses_long_suffixes(pa):
+    """Suffixes that do not fit one 128-key tile for the M-tile's members are
+    refused on the host (the two-call cascade serves them)."""
+    c = grouped_case(8, 4, [256, 64], seed=5)
+    plan = pa.cascade_plan(c.w.tables, c.w.seq_lens, 4, c.w.block_size)
+    with pytest.raises(pa.PagedAttentionError) as e:
+        grouped_call(pa, c, plan, 4)
+    assert e.value.status == 2
