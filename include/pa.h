@@ -477,6 +477,23 @@ pa_status pa_check_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
 pa_status pa_set_stream_k_ctas(int32_t ctas);
 
 /*
+ * Testing hook: the number of persistent CTAs of the tensor-core kernel
+ * behind pa_prefill_chunk, pa_prefix_attention and pa_decode_grouped.  That
+ * kernel splits its work into units of one (M-tile, kv-head, sequence) each and
+ * runs one CTA per SM by default, each CTA walking its share of the units (in
+ * rounds of alternating direction) with its copy and tensor-core pipeline
+ * running on from one unit into the next.  ctas > 0 fixes the grid for every
+ * later call in the process (still at most one CTA per unit, and at least
+ * enough CTAs that none holds more than 256 units); 0 restores the default.
+ * Which units share a CTA, and so every hand-over of the pipeline from one
+ * unit to the next, follows from this number: sweeping it exercises them on one
+ * GPU, whatever its SM count.  The results do not depend on it.  Not for
+ * production use: the setting is process-wide.  Negative values give
+ * PA_ERR_INVALID_ARG.  The pages have no counterpart to this call.
+ */
+pa_status pa_set_prefill_ctas(int32_t ctas);
+
+/*
  * Reads (and, if clear != 0, resets) the current device's error word after
  * synchronising `stream`.  Returns PA_ERR_DEVICE when the word is non-zero.
  */

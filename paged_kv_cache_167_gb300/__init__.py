@@ -8,11 +8,11 @@ from .binding import (PA_DECODE_EARLY_METADATA, PA_SWAP_IN, PA_SWAP_OUT, PagedAt
                       capacity_estimate, cascade_plan, check_wait_timeout, copy_blocks, decode, decode_cascade,
                       decode_grouped, decode_host, decode_host_staging_size, decode_noalloc, decode_partition_tokens,
                       decode_workspace_size, get_device_error, lib, pool_desc, prefill_chunk, prefix_attention,
-                      reshape_and_cache, set_stream_k_ctas, slot_mapping, swap_blocks)
+                      reshape_and_cache, set_prefill_ctas, set_stream_k_ctas, slot_mapping, swap_blocks)
 from .block_manager import BlockManager
 
 __all__ = ["PagedAttentionError", "BlockManager", "PA_DECODE_EARLY_METADATA", "PA_SWAP_IN", "PA_SWAP_OUT",
            "block_layout", "capacity_estimate", "cascade_plan", "check_wait_timeout", "copy_blocks", "decode",
            "decode_cascade", "decode_grouped", "decode_host", "decode_host_staging_size", "decode_noalloc", "decode_partition_tokens",
            "decode_workspace_size", "get_device_error", "lib", "pool_desc", "prefill_chunk", "prefix_attention",
-           "reshape_and_cache", "set_stream_k_ctas", "slot_mapping", "swap_blocks"]
+           "reshape_and_cache", "set_prefill_ctas", "set_stream_k_ctas", "slot_mapping", "swap_blocks"]

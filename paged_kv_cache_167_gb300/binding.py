@@ -71,6 +71,7 @@ SIGNATURES = {
     "pa_get_device_error": (_I32, [ctypes.POINTER(_U32), _I32, _P]),
     "pa_check_wait_timeout": (_I32, [ctypes.c_uint64, _P]),
     "pa_set_stream_k_ctas": (_I32, [_I32]),
+    "pa_set_prefill_ctas": (_I32, [_I32]),
     "pa_block_layout": (_I32, [_I64, _I32, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "pa_slot_mapping": (_I32, [_P, _P, _I32, _I32, _P, _P, _I64, _I32, _I64]),
     "pa_bm_create": (_I32, [ctypes.POINTER(_P), _I64, _I32]),
@@ -464,6 +465,13 @@ def set_stream_k_ctas(ctas: int) -> None:
     """pa_set_stream_k_ctas (testing hook): fix the balanced decode grid at
     ``ctas`` CTAs for later calls in this process; 0 restores the default."""
     _check(lib().pa_set_stream_k_ctas(int(ctas)), "pa_set_stream_k_ctas")
+
+
+def set_prefill_ctas(ctas: int) -> None:
+    """pa_set_prefill_ctas (testing hook): fix the persistent grid of the
+    tensor-core prefill / prefix / grouped kernel at `ctas` CTAs (0 restores
+    one per SM)."""
+    _check(lib().pa_set_prefill_ctas(int(ctas)), "pa_set_prefill_ctas")
 
 
 def get_device_error(clear: bool = True, stream=None) -> int:

@@ -434,6 +434,12 @@ pa_status pa_set_stream_k_ctas(int32_t ctas) {
     return PA_OK;
 }
 
+pa_status pa_set_prefill_ctas(int32_t ctas) {
+    if (ctas < 0) return PA_ERR_INVALID_ARG;
+    set_prefill_ctas(ctas);
+    return PA_OK;
+}
+
 pa_status pa_get_device_error(uint32_t *err_out, int32_t clear, cudaStream_t stream) {
     if (!err_out) return PA_ERR_INVALID_ARG;
     unsigned int *word = device_error_word();

@@ -113,5 +113,6 @@ struct PrefillArgs {
 };
 bool prefill_supported(int head_dim, int group, int block_size);
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+void set_prefill_ctas(int32_t ctas);   // 0: one CTA per SM
 
 }  // namespace pa

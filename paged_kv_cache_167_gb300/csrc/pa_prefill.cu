@@ -57,6 +57,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
 #include <type_traits>
 
 #include "pa_device.cuh"
@@ -79,15 +82,19 @@ constexpr int kKeys = 128;                  // N tile of Q.K (keys per iteration
 constexpr int kD = 128;                     // head_dim
 constexpr uint32_t kHalf = 128u * 128u;     // one [128 rows][64 bf16] swizzled half tile, bytes
 constexpr uint32_t kTile = 2u * kHalf;      // [2 halves][128 rows][128 B]
-constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffQ = 0;               // two Q buffers (a unit's Q lands while the previous one finishes)
 #ifndef PA_PREFILL_KV_STAGES
 #define PA_PREFILL_KV_STAGES 2
 #endif
 constexpr int kKV = PA_PREFILL_KV_STAGES;    // K and V ring depth (2 and 3 measured alike)
-constexpr uint32_t kOffK = kOffQ + kTile;   // kKV stages, [half][128 keys][128 B]
+constexpr uint32_t kOffK = kOffQ + 2 * kTile;   // kKV stages, [half][128 keys][128 B]
 constexpr uint32_t kOffV = kOffK + kKV * kTile; // kKV stages, [block][half][16 keys][128 B]
 constexpr uint32_t kOffBar = kOffV + kKV * kTile;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // + alignment slack
+constexpr uint32_t kBarBytes = 256;
+constexpr uint32_t kOffX = kOffBar + kBarBytes;   // epilogue: each part's (m, l, done) per row
+constexpr int kMaxUnits = 256;                    // units per CTA (the launcher adds CTAs beyond)
+constexpr uint32_t kOffUnits = kOffX + (uint32_t)kParts * 128u * 12u;
+constexpr uint32_t kSmemBytes = kOffUnits + kMaxUnits * 8 + 1024;   // + alignment slack
 constexpr int kSBufs = 2;                   // S accumulators in tensor memory
 constexpr uint32_t kTmemCols = 512;         // S0, S1, O0, O1 (128 columns each)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -113,7 +120,10 @@ struct Params {
     int32_t causal;              // 0: every query of sequence s sees keys 0 .. ctx_lens[s] - 1
     float *o_part;               // non-null: fp32 output normalised by l, [B][C][Hq][D], instead of out
     float *lse;                  // with o_part: [B][C][Hq] natural-log sum of exp(scale * q.k)
-    const int32_t *order;        // non-null: CTA z processes sequence order[z] (a permutation of 0 .. B-1)
+    const int32_t *order;        // non-null: sequence slot z holds sequence order[z] (a permutation of 0 .. B-1)
+    int32_t num_mt;              // M-tiles per sequence
+    int32_t num_kv;              // kv-heads
+    int32_t num_seqs;            // sequences (B)
     // Grouped decode (sfx_tables non-null): sequence s stands for a group of
     // `chunk` members that share its ctx_lens[s] prefix tokens; after the
     // prefix tiles one more tile holds every member's own suffix blocks (member
@@ -133,18 +143,6 @@ struct Params {
     int64_t kv_stride;
 };
 
-// Suffix length of member sequence `seq`, clipped to [0, its bound] (an
-// out-of-range length is reported and clipped).
-template <int BS>
-__device__ __forceinline__ int suffix_len(const Params &p, int seq, bool report) {
-    int L = __ldg(p.sfx_lens + seq);
-    const int cap = min(p.max_sfx_len, min(p.sfx_max_blocks, p.sfx_nb) * BS);
-    if (L < 0 || L > cap) {
-        if (report) raise_error(p.err, PA_DEVERR_SEQ_LEN);
-        L = L < 0 ? 0 : cap;
-    }
-    return L;
-}
 
 // ---- PTX wrappers -----------------------------------------------------------
 
@@ -238,7 +236,9 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[32]) {   // r[0..15]
+template <int N>
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[N]) {   // r[0..15]
+    static_assert(N >= 16, "16 words");
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
         "%14, %15, %16};" ::"r"(taddr),
@@ -289,16 +289,31 @@ __device__ __forceinline__ float max_tree64(const uint32_t (&a)[32], const uint3
     return m[0];
 }
 
-// Timeline of tile t (kKV = kSBufs = 3):
-//   K warp   : K(t) -> K slot t % 3 once Q.K(t-3) has completed
-//   V warp   : V(t) -> V slot t % 3 once P.V(t-3) has completed
-//   Q.K lane : Q.K(t) -> S[t%3] once K(t) has landed and P.V(t-3) has completed
-//   P.V lane : P.V(t) once P(t) and V(t) are in place
-//   softmax  : S[t%3] -> registers ; row max over both halves ; P(t) into S[t%3] ;
-//              O rescale when the reference moved ; signal P(t)
-// Barriers: S ready (MMA commit), S free (256 arrivals), P ready (256 arrivals),
-// P.V done per P buffer and per S buffer (MMA commit), K / V / Q landed (TMA),
-// one drain per MMA lane (MMA commit, used once).
+// Work units: one (M-tile mt, kv-head g, sequence slot z) each, numbered
+// u = mt + num_mt * (g + num_kv * z).  The grid is persistent (one CTA per SM
+// at most): CTA c takes units k * C + c for even rounds k and k * C + C - 1 - c
+// for odd ones, so when the caller orders the sequences longest first a CTA
+// that drew a long unit in one round draws a short one in the next.  Each
+// role walks the same unit list; the CTA's tiles are numbered T = 0, 1, ...
+// across its units, and every ring (K / V slots, S buffers, P and P.V
+// barriers) is indexed by T, so the next unit's copies stream while the
+// current one finishes.
+//
+// Timeline of tile T (kKV = kSBufs = 2):
+//   K warp   : Q of unit k -> Q buffer k % 2 once the Q.K of unit k - 2 are done;
+//              K(T) -> K slot T % 2 once Q.K(T - 2) has completed
+//   V warp   : V(T) -> V slot T % 2 once P.V(T - 2) has completed
+//   Q.K lane : Q.K(T) -> S[T % 2] once K(T) and the unit's Q have landed and
+//              P.V(T - 2) has completed
+//   P.V lane : P.V(T) once P(T) and V(T) are in place (a unit's first once the
+//              previous unit's epilogue has read O)
+//   softmax  : S[T % 2] -> registers ; P(T) into S[T % 2] ; O rescale when the
+//              reference moved ; signal P(T) ; after a unit's last tile its
+//              epilogue, then O is released to the next unit
+// Barriers: Q landed / Q free per buffer, K / V landed (TMA), S ready, P.V done
+// per P buffer and per S buffer, K / V slot free (MMA commit), P ready and O
+// read (256 arrivals), unit's P.V done, suffix tile's V ready (grouped), one
+// drain per MMA lane (MMA commit, used once).
 // A parity wait is exact only while the barrier's previous phase is known to
 // have completed; each wait below names the completion that guarantees it.
 template <int G, int BS, bool kGrouped>
@@ -314,19 +329,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char *gbase = smem_raw + (base - smem_addr(smem_raw));
     const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
     const uint32_t barQ = base + kOffBar;
-    // barriers: Q | K[kKV] | V[kKV] | S[3] | S free[3] | P[2] | P.V done[2] | drain (P.V, Q.K issuers) |
-    // P.V done per S buffer[3] | K slot free[kKV] | V slot free[kKV]
-    const uint32_t barK = barQ + 8, barV = barK + 8 * kKV, barS = barV + 8 * kKV, barSfree = barS + 24,
-                   barP = barSfree + 24, barOP = barP + 16, barEnd = barOP + 16, barEndQk = barEnd + 8,
-                   barSdone = barEndQk + 8, barKfree = barSdone + 24, barVfree = barKfree + 8 * kKV;
-    constexpr int kNumBars = 1 + 2 * kKV + 3 + 3 + 2 + 2 + 2 + 3 + 2 * kKV;
+    // barriers: Q landed[2] | K[kKV] | V[kKV] | S[2] | P[2] | P.V done[2] | P.V done per S buffer[2] |
+    // K slot free[kKV] | V slot free[kKV] | Q free[2] | unit's P.V done | O read | suffix V ready |
+    // drain (P.V, Q.K issuers)
+    const uint32_t barK = barQ + 16, barV = barK + 8 * kKV, barS = barV + 8 * kKV, barP = barS + 16,
+                   barOP = barP + 16, barSdone = barOP + 16, barKfree = barSdone + 16, barVfree = barKfree + 8 * kKV,
+                   barQfree = barVfree + 8 * kKV, barUnit = barQfree + 16, barOfree = barUnit + 8,
+                   barVsfx = barOfree + 8, barEnd = barVsfx + 8, barEndQk = barEnd + 8;
+    constexpr int kNumBars = 2 + 2 * kKV + 2 + 2 + 2 + 2 + 2 * kKV + 2 + 1 + 1 + 1 + 2;
+    static_assert(8 * kNumBars + 8 <= kBarBytes, "barrier area");
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 8 * kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffBar + 8 * kNumBars + 4);
+    int2 *utab = reinterpret_cast<int2 *>(gbase + kOffUnits);   // this CTA's units: (sequence, context length)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int mt = blockIdx.x, g = blockIdx.y;
-    int s = blockIdx.z;   // replaced by order[z] once the inputs may be read
-    const int j0 = mt * QPT;
 
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -337,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             const uint32_t b = barQ + 8 * i;
-            const bool softmax_arrivals = (b >= barSfree && b < barOP);   // S free[3] and P[2]: the softmax threads
+            const bool softmax_arrivals = (b >= barP && b < barOP) || b == barOfree;   // P[2], O read
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b),
                          "r"(softmax_arrivals ? (uint32_t)(kSoftWarps * 32) : 1u)
                          : "memory");
@@ -345,159 +361,288 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_barrier_init();
     }
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // ---- this CTA's units, read once into shared memory
+    const int C = (int)gridDim.x, cta = (int)blockIdx.x;
+    const int per_seq = p.num_mt * p.num_kv;
+    const int n_units = per_seq * p.num_seqs;
+    auto unit_index = [&](int k) { return k * C + ((k & 1) ? C - 1 - cta : cta); };
+    const int rounds = (n_units + C - 1) / C;
+    int my_units = rounds > 0 ? rounds - 1 + (unit_index(rounds - 1) < n_units ? 1 : 0) : 0;
+    if (my_units > kMaxUnits) {   // the launcher sizes the grid so that this cannot happen
+        if (tid == 0) raise_error(p.err, PA_DEVERR_SEQ_LEN);
+        my_units = kMaxUnits;
+    }
+    for (int k = tid; k < my_units; k += kThreads) {
+        const int z = unit_index(k) / per_seq;
+        int s = z;
+        if (p.order != nullptr) {   // the caller's order: units start in it, so the longest work can go first
+            const int o = __ldg(p.order + z);
+            if (o >= 0 && o < p.num_seqs) s = o;
+            else raise_error(p.err, PA_DEVERR_ORDER);
+        }
+        int ctx = __ldg(p.ctx_lens + s);
+        if (ctx < 0 || ctx > p.max_ctx_len) {
+            raise_error(p.err, PA_DEVERR_SEQ_LEN);
+            ctx = ctx < 0 ? 0 : p.max_ctx_len;
+        }
+        utab[k] = make_int2(s, ctx);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tO = tmem + kSBufs * 128;
 
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-
-    if (p.order != nullptr) {   // the caller's order: CTAs start in it, so the longest work can go first
-        const int o = __ldg(p.order + blockIdx.z);
-        if (o >= 0 && o < (int)gridDim.z)
-            s = o;
-        else if (tid == 0 && mt == 0 && g == 0)
-            raise_error(p.err, PA_DEVERR_ORDER);
-    }
-    int ctx = __ldg(p.ctx_lens + s);
-    if (ctx < 0 || ctx > p.max_ctx_len) {
-        if (tid == 0 && mt == 0 && g == 0) raise_error(p.err, PA_DEVERR_SEQ_LEN);
-        ctx = ctx < 0 ? 0 : p.max_ctx_len;
-    }
-    // causal: keys 0 .. ctx + C - 1 exist and query j sees 0 .. ctx + j;
-    // otherwise keys 0 .. ctx - 1 exist and every query sees all of them
-    const int seq_end = p.causal ? ctx + p.chunk : ctx;
-    const int nblk_seq = (seq_end + BS - 1) / BS;
-    const int last_q = min(j0 + QPT, p.chunk) - 1;             // last valid query of this tile
-    const int n_pre = ((p.causal ? ctx + last_q + 1 : ctx) + kKeys - 1) / kKeys;   // 0 only without causal
     // grouped decode is a separate instantiation: its code in the plain
     // kernel, even when idle, cost the causal prefill 20% (1.18 against 0.98 ms)
     const bool grouped = kGrouped && p.sfx_tables != nullptr && p.sfx_nb > 0;
-    const int n_tiles = n_pre + (grouped ? 1 : 0);   // grouped: the members' suffix tile last
-    // members of this M-tile (grouped): queries j0 .. j0 + members - 1
-    const int members = max(0, min(QPT, p.chunk - j0));
-    // Grouped rows that may see fewer than kPreciseKeys keys carry each
-    // probability as two bf16 terms, hi = bf16(p) and lo = bf16(p - hi), and
-    // P.V runs once for each: with few keys a single rounding of p (relative
-    // error 2^-9) does not average down (one output of an eight-key beam row
-    // moved by 1.0% of its value); with many it does, and one term is kept.
-    // The plain kernel has no second term at all: even idle, it cost the
-    // causal prefill 13% (1.09 against 0.96 ms).
-    const bool precise = kGrouped && ctx + p.max_sfx_len < kPreciseKeys;
+    struct Unit {
+        int s, g, j0, ctx, seq_end, nblk_seq, n_pre, n_tiles, members;
+        bool precise;
+    };
+    auto unit = [&](int k) {
+        Unit U;
+        const int u = unit_index(k);
+        const int2 e = utab[k];
+        U.s = e.x;
+        U.ctx = e.y;
+        U.g = (u / p.num_mt) % p.num_kv;
+        U.j0 = (u % p.num_mt) * QPT;
+        // causal: keys 0 .. ctx + C - 1 exist and query j sees 0 .. ctx + j;
+        // otherwise keys 0 .. ctx - 1 exist and every query sees all of them
+        U.seq_end = p.causal ? U.ctx + p.chunk : U.ctx;
+        U.nblk_seq = (U.seq_end + BS - 1) / BS;
+        const int last_q = min(U.j0 + QPT, p.chunk) - 1;   // last valid query of the M-tile
+        U.n_pre = ((p.causal ? U.ctx + last_q + 1 : U.ctx) + kKeys - 1) / kKeys;   // 0 only without causal
+        U.n_tiles = U.n_pre + (grouped ? 1 : 0);   // grouped: the members' suffix tile last
+        // members of the M-tile (grouped): queries j0 .. j0 + members - 1
+        U.members = max(0, min(QPT, p.chunk - U.j0));
+        // Grouped rows that may see fewer than kPreciseKeys keys carry each
+        // probability as two bf16 terms, hi = bf16(p) and lo = bf16(p - hi), and
+        // P.V runs once for each: with few keys a single rounding of p (relative
+        // error 2^-9) does not average down (one output of an eight-key beam row
+        // moved by 1.0% of its value); with many it does, and one term is kept.
+        // The plain kernel has no second term at all: even idle, it cost the
+        // causal prefill 13% (1.09 against 0.96 ms).
+        U.precise = kGrouped && U.ctx + p.max_sfx_len < kPreciseKeys;
+        return U;
+    };
     constexpr uint32_t idesc_qk = idesc_bf16(kRows, kKeys, false);
     constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, true);
 
     if (warp == kKWarp || warp == kVWarp) {
         // ---- copy warps: a lane per box.  Block ids sit in registers: one
         // load of the 32 lanes holds blocks c * 32 + lane, i.e. tiles c * TPC ..
-        // c * TPC + TPC - 1, and the next load is issued a whole load ahead,
-        // so no copy waits on a table read (a dependent read per tile held the
-        // copies ~1,800 cycles apart, slower than the MMAs consume tiles).
+        // c * TPC + TPC - 1, and the next load is issued a whole load ahead (the
+        // next unit's first two at the start of this one), so no copy waits on
+        // a table read (a dependent read per tile held the copies ~1,800 cycles
+        // apart, slower than the MMAs consume tiles).  An id is checked when its
+        // load becomes the current one.
         constexpr int TPC = 32 / NBT;
         const bool is_k = warp == kKWarp;
-        const int32_t *table_row = p.tables + (size_t)s * p.max_blocks;
         const uint32_t bar0 = is_k ? barK : barV;
         const uint32_t slot0 = is_k ? sK : sV;
-        if (is_k) {
-            if (lane == 0) mbar_expect(barQ, kTile);
-            __syncwarp();
-            if (lane < 2) tma_load_4d(sQ + lane * kHalf, &tmap_q, lane * 64, 0, g, s * p.chunk + j0, barQ);
-        }
-        int tail_id = (int)p.num_blocks;   // grouped: this lane's block of the suffix tile (out of bounds: zeros)
-        if (grouped) {
-            // each member's new token first (K warp: K rows, V warp: V rows), 16
-            // bytes a lane, then a proxy fence: this warp's tensor copy of the
-            // suffix tile is issued after it in program order
-            if (p.new_k != nullptr) {
-                for (int m = 0; m < members; ++m) {
-                    const int seq = s * p.chunk + j0 + m;
-                    const int L = suffix_len<BS>(p, seq, is_k && lane == 0 && g == 0);
-                    if (L <= 0 || lane >= kD / 8) continue;
-                    const int blk = __ldg(p.sfx_tables + (size_t)seq * p.sfx_max_blocks + (L - 1) / BS);
-                    if (blk < 0 || blk >= p.num_blocks) continue;   // reported with the tile's ids below
-                    const __nv_bfloat16 *src = (is_k ? p.new_k : p.new_v) + ((size_t)seq * gridDim.y + g) * kD + lane * 8;
-                    __nv_bfloat16 *dst = p.pool + (size_t)blk * p.block_stride + (is_k ? 0 : p.kv_stride) +
-                                         ((size_t)g * BS + (L - 1) % BS) * kD + lane * 8;
-                    *reinterpret_cast<uint4 *>(dst) = __ldg(reinterpret_cast<const uint4 *>(src));
-                }
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-                __syncwarp();
-            }
-            if (lane < NBT) {
-                const int m = lane / p.sfx_nb, b = lane % p.sfx_nb;
-                if (m < members) {
-                    const int seq = s * p.chunk + j0 + m;
-                    if (b * BS < suffix_len<BS>(p, seq, false)) {
-                        const int v = __ldg(p.sfx_tables + (size_t)seq * p.sfx_max_blocks + b);
-                        if (v < 0 || v >= p.num_blocks) raise_error(p.err, PA_DEVERR_BLOCK_ID);
-                        else tail_id = v;
-                    }
-                }
-            }
-        }
-        auto load_ids = [&](int c) -> int {
+        auto ids_load = [&](const Unit &U, int c) -> int {
             const int bi = c * 32 + lane;
-            int id = (int)p.num_blocks;   // out-of-bounds coordinate: zero fill
-            if (bi < nblk_seq && bi < n_pre * NBT) {
-                const int v = __ldg(table_row + bi);
-                if (v < 0 || v >= p.num_blocks) raise_error(p.err, PA_DEVERR_BLOCK_ID);
-                else id = v;
-            }
-            return id;
+            int v = 0;
+            if (bi < U.nblk_seq && bi < U.n_pre * NBT) v = __ldg(p.tables + (size_t)U.s * p.max_blocks + bi);
+            return v;
         };
-        int ids_cur = load_ids(0), ids_next = load_ids(1);
-        int issued = 0;
-        bool ok = true;
-        for (int t = 0; t < n_tiles; ++t) {
-            if (*abort_flag) break;
-            const int st = t % kKV;
-            if (t > 0 && t % TPC == 0) {
-                ids_cur = ids_next;
-                ids_next = load_ids(t / TPC + 1);
+        auto ids_check = [&](int v, const Unit &U, int c) -> int {   // out-of-bounds coordinate: zero fill
+            const int bi = c * 32 + lane;
+            if (!(bi < U.nblk_seq && bi < U.n_pre * NBT)) return (int)p.num_blocks;
+            if (v < 0 || v >= p.num_blocks) {
+                raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                return (int)p.num_blocks;
             }
-            const int tb = (t % TPC) * NBT;   // the tile's first block in the loaded ids
-            const bool tail = grouped && t == n_pre;   // the members' suffix tile
-            const int id = tail ? tail_id : __shfl_sync(0xffffffffu, ids_cur, (tb + lane) & 31);
-            if (t >= kKV) {   // the slot's previous tile has been consumed by its MMAs
-                // (Q.K for a K slot, P.V for a V slot, each committing to the slot's
-                // own barrier; its next completion needs the copy issued below, so
-                // its phase cannot be lapped)
-                const int tp = t - kKV;
-                const uint32_t free_bar = (is_k ? barKfree : barVfree) + 8 * (tp % kKV);
-                ok = __all_sync(0xffffffffu, mbar_wait(free_bar, (uint32_t)((tp / kKV) & 1), p.err));
+            return v;
+        };
+        bool ok = true;
+        int T = 0;                 // tiles issued so far
+        Unit U;
+        int raw_cur = 0, raw_next = 0;
+        if (my_units > 0) {
+            U = unit(0);
+            raw_cur = ids_load(U, 0);
+            raw_next = ids_load(U, 1);
+        }
+        for (int k = 0; k < my_units && ok; ++k) {
+            Unit N = U;            // the next unit, and its first ids
+            int nraw_cur = 0, nraw_next = 0;
+            if (k + 1 < my_units) {
+                N = unit(k + 1);
+                nraw_cur = ids_load(N, 0);
+                nraw_next = ids_load(N, 1);
+            }
+            if (is_k) {
+                // Q buffer k % 2 held unit k - 2's Q: its Q.K must have completed
+                // (the phase before, unit k - 4's, was waited for here two units ago)
+                const int qb = k & 1;
+                if (k >= 2) ok = __all_sync(0xffffffffu, mbar_wait(barQfree + 8 * qb, (uint32_t)(((k >> 1) - 1) & 1), p.err));
                 if (!ok) {
                     *abort_flag = 1;
                     break;
                 }
+                if (lane == 0) mbar_expect(barQ + 8 * qb, kTile);
+                __syncwarp();
+                if (lane < 2)
+                    tma_load_4d(sQ + qb * kTile + lane * kHalf, &tmap_q, lane * 64, 0, U.g, U.s * p.chunk + U.j0,
+                                barQ + 8 * qb);
             }
-            if (lane == 0) mbar_expect(bar0 + 8 * st, kTile);
-            __syncwarp();
-            const uint32_t dst = slot0 + st * kTile;
-            if (is_k) {
-                const int blk = tail ? __shfl_sync(0xffffffffu, tail_id, lane >> 1)
-                                     : __shfl_sync(0xffffffffu, ids_cur, (tb + (lane >> 1)) & 31);
-                if (lane < 2 * NBT)
-                    tma_load_5d(dst + (lane & 1) * kHalf + (lane >> 1) * (BS * 128), &tmap_k, (lane & 1) * 64, 0, g, 0,
-                                blk, bar0 + 8 * st);
-            } else if (lane < NBT) {
-                tma_load_5d(dst + lane * kVBlock, &tmap_v, 0, 0, 0, g, id, bar0 + 8 * st);
+            int ids_cur = ids_check(raw_cur, U, 0);
+            int tail_id = (int)p.num_blocks;   // grouped: this lane's block of the suffix tile (out of bounds: zeros)
+            // grouped: lane m < members holds member m's suffix length, loaded here
+            // and first used once the unit's first tiles are in flight (members <=
+            // NBT: each member owns at least one block of the suffix tile)
+            int len_m = 0;
+            if (grouped && lane < U.members) len_m = __ldg(p.sfx_lens + U.s * p.chunk + U.j0 + lane);
+            // Each member's new token goes into the pool (K warp: K rows, V warp: V
+            // rows), then a proxy fence: this warp's tensor copy of the suffix tile
+            // is issued after it in program order.  The work runs in three stages,
+            // one before each of three consecutive slot waits once the unit's first
+            // tiles are in flight, each only issuing the reads the next one
+            // consumes, so the chain of dependent reads (length, block, token)
+            // overlaps waits the warp makes anyway; stages not yet run by the
+            // suffix tile run there.
+            constexpr int kPass = (NBT + 1) / 2;   // two members a pass: 16 lanes x 16 B = one row of d = 128
+            int L = 0, nblk = -1, tv = 0;
+            bool tv_read = false;   // this lane read a block of the suffix tile into tv
+            uint4 tok[kPass];
+            auto prep_lengths = [&]() {   // clip the lengths; read each token's block and this lane's tail block
+                const int cap = min(p.max_sfx_len, min(p.sfx_max_blocks, p.sfx_nb) * BS);
+                L = len_m;
+                if (lane < U.members && (L < 0 || L > cap)) {
+                    if (is_k && U.g == 0) raise_error(p.err, PA_DEVERR_SEQ_LEN);
+                    L = L < 0 ? 0 : cap;
+                }
+                if (p.new_k != nullptr && lane < U.members && L > 0)
+                    nblk = __ldg(p.sfx_tables + (size_t)(U.s * p.chunk + U.j0 + lane) * p.sfx_max_blocks + (L - 1) / BS);
+                // this lane's block of the suffix tile: member lane / sfx_nb, its block lane % sfx_nb
+                const int mt_ = lane / p.sfx_nb, bt = lane % p.sfx_nb;
+                const int Lt = __shfl_sync(0xffffffffu, L, mt_ & 31);
+                tv_read = lane < NBT && mt_ < U.members && bt * BS < Lt;
+                if (tv_read) tv = __ldg(p.sfx_tables + (size_t)(U.s * p.chunk + U.j0 + mt_) * p.sfx_max_blocks + bt);
+            };
+            auto prep_tokens = [&]() {    // check the tail blocks; read the tokens
+                if (tv_read) {
+                    if (tv < 0 || tv >= p.num_blocks) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                    else tail_id = tv;
+                }
+                if (p.new_k == nullptr) return;
+#pragma unroll
+                for (int ps = 0; ps < kPass; ++ps) {
+                    const int m = ps * 2 + (lane >> 4), c16 = lane & 15;
+                    const int bm = __shfl_sync(0xffffffffu, nblk, m & 31), Lm = __shfl_sync(0xffffffffu, L, m & 31);
+                    tok[ps] = make_uint4(0u, 0u, 0u, 0u);
+                    if (m < U.members && Lm > 0 && bm >= 0 && bm < p.num_blocks) {   // a bad id is reported above
+                        const size_t seq = (size_t)U.s * p.chunk + U.j0 + m;
+                        tok[ps] = __ldg(reinterpret_cast<const uint4 *>((is_k ? p.new_k : p.new_v) +
+                                                                        (seq * p.num_kv + U.g) * kD + c16 * 8));
+                    }
+                }
+            };
+            auto prep_store = [&]() {     // store the tokens, then the proxy fence
+                if (p.new_k == nullptr) return;
+#pragma unroll
+                for (int ps = 0; ps < kPass; ++ps) {
+                    const int m = ps * 2 + (lane >> 4), c16 = lane & 15;
+                    const int bm = __shfl_sync(0xffffffffu, nblk, m & 31), Lm = __shfl_sync(0xffffffffu, L, m & 31);
+                    if (m < U.members && Lm > 0 && bm >= 0 && bm < p.num_blocks)
+                        *reinterpret_cast<uint4 *>(p.pool + (size_t)bm * p.block_stride + (is_k ? 0 : p.kv_stride) +
+                                                   ((size_t)U.g * BS + (Lm - 1) % BS) * kD + c16 * 8) = tok[ps];
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __syncwarp();
+            };
+            const int prep0 = min(U.n_pre, kKV);   // the first stage's tile
+            for (int t = 0; t < U.n_tiles; ++t) {
+                if (*abort_flag) {
+                    ok = false;
+                    break;
+                }
+                const int st = T % kKV;
+                if (t > 0 && t % TPC == 0) {
+                    ids_cur = ids_check(raw_next, U, t / TPC);
+                    raw_next = ids_load(U, t / TPC + 1);
+                }
+                if (grouped) {   // before the slot wait below; all three by the suffix tile
+                    if (t == prep0) prep_lengths();
+                    if (t == min(prep0 + 1, U.n_pre)) prep_tokens();
+                    if (t == min(prep0 + 2, U.n_pre)) prep_store();
+                }
+                const int tb = (t % TPC) * NBT;   // the tile's first block in the loaded ids
+                const bool tail = grouped && t == U.n_pre;   // the members' suffix tile
+                const int id = tail ? tail_id : __shfl_sync(0xffffffffu, ids_cur, (tb + lane) & 31);
+                if (T >= kKV) {   // the slot's previous tile has been consumed by its MMAs
+                    // (Q.K for a K slot, P.V for a V slot, each committing to the slot's
+                    // own barrier; its next completion needs the copy issued below, so
+                    // its phase cannot be lapped)
+                    const int tp = T - kKV;
+                    const uint32_t free_bar = (is_k ? barKfree : barVfree) + 8 * (tp % kKV);
+                    ok = __all_sync(0xffffffffu, mbar_wait(free_bar, (uint32_t)((tp / kKV) & 1), p.err));
+                    if (!ok) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
+                if (lane == 0) mbar_expect(bar0 + 8 * st, kTile);
+                __syncwarp();
+                const uint32_t dst = slot0 + st * kTile;
+                if (is_k) {
+                    const int blk = tail ? __shfl_sync(0xffffffffu, tail_id, lane >> 1)
+                                         : __shfl_sync(0xffffffffu, ids_cur, (tb + (lane >> 1)) & 31);
+                    if (lane < 2 * NBT)
+                        tma_load_5d(dst + (lane & 1) * kHalf + (lane >> 1) * (BS * 128), &tmap_k, (lane & 1) * 64, 0,
+                                    U.g, 0, blk, bar0 + 8 * st);
+                } else if (lane < NBT) {
+                    tma_load_5d(dst + lane * kVBlock, &tmap_v, 0, 0, 0, U.g, id, bar0 + 8 * st);
+                }
+                ++T;
             }
-            issued = t + 1;
+            if (!ok) break;
+            if (grouped && !is_k) {
+                // suffix tile (this unit's last, T - 1): zero each member's V slots
+                // past its length (p is 0 there, but the slots may hold non-finite
+                // junk), then hand the tile to its P.V.  The wait is exact: this warp
+                // issued the copy only after the slot's previous tile (its previous
+                // phase) had been consumed.
+                const int Ts = T - 1, sv = Ts % kKV;
+                mbar_wait(barV + 8 * sv, (uint32_t)((Ts / kKV) & 1), p.err);
+                for (int m = 0; m < U.members; ++m) {
+                    const int r0 = m * p.sfx_nb * BS + __shfl_sync(0xffffffffu, L, m & 31);
+                    const int r1 = (m + 1) * p.sfx_nb * BS;
+                    for (int idx = lane; idx < (r1 - r0) * 2 * 8; idx += 32) {
+                        const int rr = r0 + idx / 16, h = (idx / 8) & 1, c16 = idx & 7;
+                        const uint32_t addr = sV + sv * kTile + (uint32_t)(rr / BS) * kVBlock + h * (kVBlock / 2) +
+                                              (uint32_t)(rr % BS) * 128u + (uint32_t)c16 * 16u;
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                    }
+                }
+                // the zeros (generic proxy) before the P.V that reads them (async proxy)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive_u32(barVsfx);
+            }
+            U = N;
+            raw_cur = nraw_cur;
+            raw_next = nraw_next;
         }
         if (!ok || *abort_flag) {
             // wait (bounded) for this warp's copies still in flight before the memory is released
-            for (int t = max(0, issued - kKV); t < issued; ++t)
+            for (int t = max(0, T - kKV); t < T; ++t)
                 mbar_wait(bar0 + 8 * (t % kKV), (uint32_t)((t / kKV) & 1), p.err);
+            if (grouped && !is_k && lane == 0) mbar_arrive_u32(barVsfx);   // a waiting P.V lane gives up sooner
         }
         __syncwarp();
     } else if (warp == kMmaWarp || warp == kQkWarp) {
         // Two issuing lanes in two warps keep the tensor pipe's queue fed: one
-        // issues Q.K(t) as soon as K(t) has landed and S buffer t % 3 is free
-        // (P.V(t - 3), which read P(t - 3) from it, has completed; a barrier per
-        // S buffer tracks that), the other
-        // P.V(t) as soon as P(t) and V(t) are in place.  Each commits and drains
-        // only its own MMAs.
+        // issues Q.K(T) as soon as K(T) has landed and S buffer T % 2 is free
+        // (P.V(T - 2), which read P(T - 2) from it, has completed; a barrier per
+        // S buffer tracks that), the other P.V(T) as soon as P(T) and V(T) are in
+        // place.  Each commits and drains only its own MMAs.
         if (lane == 0) {
             const bool is_qk = warp == kQkWarp;
             bool ok = true;
@@ -508,57 +653,82 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return ok;
             };
-            if (is_qk) {
-                if (wait(barQ, 0)) {
-                    for (int t = 0; t < n_tiles && ok && !*abort_flag; ++t) {
-                        const int st = t % kKV, sb = t % kSBufs;
-                        if (!wait(barK + 8 * st, (uint32_t)((t / kKV) & 1))) break;
-                        // S buffer sb held P(t - 3): its P.V must have completed (P.V(t)
+            int T = 0;
+            for (int k = 0; k < my_units && ok && !*abort_flag; ++k) {
+                const Unit U = unit(k);
+                if (is_qk) {
+                    // unit k's Q (the phase before, unit k - 2's, was waited for here)
+                    const int qb = k & 1;
+                    if (!wait(barQ + 8 * qb, (uint32_t)((k >> 1) & 1))) break;
+                    const uint32_t sQb = sQ + qb * kTile;
+                    for (int t = 0; t < U.n_tiles; ++t, ++T) {
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        const int st = T % kKV, sb = T % kSBufs;
+                        if (!wait(barK + 8 * st, (uint32_t)((T / kKV) & 1))) break;
+                        // S buffer sb held P(T - 2): its P.V must have completed (P.V(T)
                         // cannot complete before this Q.K, so the phase cannot be lapped)
-                        if (t >= kSBufs && !wait(barSdone + 8 * sb, (uint32_t)(((t - kSBufs) / kSBufs) & 1))) break;
+                        if (T >= kSBufs && !wait(barSdone + 8 * sb, (uint32_t)(((T - kSBufs) / kSBufs) & 1))) break;
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < kD / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                            umma(tmem + sb * 128, smem_desc(sQ + off, 16, 1024),
+                            umma(tmem + sb * 128, smem_desc(sQb + off, 16, 1024),
                                  smem_desc(sK + st * kTile + off, 16, 1024), idesc_qk, kk > 0);
                         }
                         umma_commit(barS + 8 * sb);
                         umma_commit(barKfree + 8 * st);   // K slot st is free again
                     }
-                }
-            } else {
-                for (int t = 0; t < n_tiles && ok && !*abort_flag; ++t) {
-                    const int st = t % kKV;
-                    if (!wait(barP + 8 * (t & 1), (uint32_t)((t >> 1) & 1))) break;
-                    if (!wait(barV + 8 * st, (uint32_t)((t / kKV) & 1))) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int term = 0; term < (precise ? 2 : 1); ++term) {   // hi, then lo (precise rows)
-#pragma unroll
-                        for (int kk = 0; kk < kKeys / 16; ++kk) {
-                            // 16 keys of the V tile: within one block for b >= 16 (8-key groups
-                            // 1024 B apart), or two whole blocks for b = 8 (groups one block apart)
-                            const uint32_t v_off =
-                                (uint32_t)(kk * 16 / BS) * kVBlock + (uint32_t)((kk * 16) % BS) * 128u;
-                            // keys of the first half accumulate into O0, of the second into O1
-                            umma_ts(tO + (uint32_t)(kk / (kKeys / 32)) * 128u,
-                                    tmem + p_col(t % kSBufs, kk) + (uint32_t)(term * (kPK / 2)),
-                                    smem_desc(sV + st * kTile + v_off, BS * 128, BS >= 16 ? 1024 : kVBlock),
-                                    idesc_pv, (t > 0 || term > 0 || kk % (kKeys / 32) > 0) ? 1u : 0u);
+                    if (!ok) break;
+                    umma_commit(barQfree + 8 * qb);        // Q buffer qb is free again
+                } else {
+                    // O is overwritten by this unit's first P.V: the previous unit's
+                    // epilogue must have read it (its phase before, unit k - 2's, was
+                    // waited for here)
+                    if (k > 0 && !wait(barOfree, (uint32_t)((k - 1) & 1))) break;
+                    for (int t = 0; t < U.n_tiles; ++t, ++T) {
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
                         }
+                        const int st = T % kKV;
+                        if (!wait(barP + 8 * (T & 1), (uint32_t)((T >> 1) & 1))) break;
+                        // the suffix tile's V once the V warp has zeroed its unused
+                        // slots (one such tile per unit)
+                        const bool vsfx = grouped && t == U.n_pre;
+                        if (!wait(vsfx ? barVsfx : barV + 8 * st, vsfx ? (uint32_t)(k & 1) : (uint32_t)((T / kKV) & 1)))
+                            break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int term = 0; term < (U.precise ? 2 : 1); ++term) {   // hi, then lo (precise rows)
+#pragma unroll
+                            for (int kk = 0; kk < kKeys / 16; ++kk) {
+                                // 16 keys of the V tile: within one block for b >= 16 (8-key groups
+                                // 1024 B apart), or two whole blocks for b = 8 (groups one block apart)
+                                const uint32_t v_off =
+                                    (uint32_t)(kk * 16 / BS) * kVBlock + (uint32_t)((kk * 16) % BS) * 128u;
+                                // keys of the first half accumulate into O0, of the second into O1
+                                umma_ts(tO + (uint32_t)(kk / (kKeys / 32)) * 128u,
+                                        tmem + p_col(T % kSBufs, kk) + (uint32_t)(term * (kPK / 2)),
+                                        smem_desc(sV + st * kTile + v_off, BS * 128, BS >= 16 ? 1024 : kVBlock),
+                                        idesc_pv, (t > 0 || term > 0 || kk % (kKeys / 32) > 0) ? 1u : 0u);
+                            }
+                        }
+                        umma_commit(barOP + 8 * (T & 1));
+                        umma_commit(barSdone + 8 * (T % kSBufs));
+                        umma_commit(barVfree + 8 * st);   // V slot st is free again
                     }
-                    umma_commit(barOP + 8 * (t & 1));
-                    umma_commit(barSdone + 8 * (t % kSBufs));
-                    umma_commit(barVfree + 8 * st);   // V slot st is free again
+                    if (!ok) break;
+                    umma_commit(barUnit);   // every P.V of the unit has completed
                 }
             }
             // One more commit, on a barrier used once, tracks every MMA this lane
             // issued; its phase-0 wait is exact.  (Waiting on the last P.V's own
-            // barrier is not: the two P.V barriers alternate, and when P.V(t - 2)
-            // has not completed either, a parity wait for P.V(t) cannot tell the
-            // two apart and returns early.)  The softmax epilogue waits on the
-            // P.V lane's drain barrier before it reads O.
+            // barrier is not: the two P.V barriers alternate, and when P.V(T - 2)
+            // has not completed either, a parity wait for P.V(T) cannot tell the
+            // two apart and returns early.)
             if (!ok || *abort_flag) *abort_flag = 1;   // give up: drain what was issued
             const uint32_t end = is_qk ? barEndQk : barEnd;
             umma_commit(end);
@@ -569,230 +739,246 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- softmax warps: row r, key part pt (scale_log2 > 0: maxima of raw scores)
         const int r = (warp & 3) * 32 + lane, pt = warp >> 2;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const int jr = j0 + r / G;
-        const int pos = p.causal ? min(ctx + jr, seq_end - 1) : seq_end - 1;   // last key this row may attend
-        // grouped: this row's keys in the suffix tile, [sfx_lo, sfx_hi)
-        const int sfx_lo = (r / G) * p.sfx_nb * BS;
-        const int sfx_hi = grouped && jr < p.chunk ? sfx_lo + suffix_len<BS>(p, s * p.chunk + jr, false) : sfx_lo;
         const float c = p.scale_log2;
-        float m_ref = -INFINITY;                       // reference maximum, log2 domain
-        float2 l2 = make_float2(0.f, 0.f);
-        int done = 0;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int st = t & 1, sb = t % kSBufs;   // st: P barrier of this tile
-            bool ok = mbar_wait(barS + 8 * sb, (uint32_t)((t / kSBufs) & 1), p.err);
-            uint32_t sr[kPC][32];
-            if (__all_sync(0xffffffffu, ok)) {
-                tc_fence_after();
-#pragma unroll
-                for (int cc = 0; cc < kPC; ++cc) tmem_ld32(tmem + sb * 128 + lane_off + pt * kPK + cc * 32, sr[cc]);
-                tmem_ld_wait();
-            } else {
-                ok = false;
+        float *mx = reinterpret_cast<float *>(gbase + kOffX);   // the halves' (m, l, ok) of each row
+        float *lx = mx + kParts * 128;
+        int *okx = reinterpret_cast<int *>(lx + kParts * 128);
+        // grouped: the row's member's suffix length, read a unit ahead
+        auto sfx_load = [&](int k) -> int {
+            const Unit N = unit(k);
+            const int j = N.j0 + r / G;
+            return j < p.chunk ? __ldg(p.sfx_lens + N.s * p.chunk + j) : 0;
+        };
+        int sfx_next = grouped && my_units > 0 ? sfx_load(0) : 0;
+        int T = 0;
+        for (int k = 0; k < my_units; ++k) {
+            const Unit U = unit(k);
+            const int jr = U.j0 + r / G;
+            const int pos = p.causal ? min(U.ctx + jr, U.seq_end - 1) : U.seq_end - 1;   // last key this row may attend
+            // grouped: this row's keys in the suffix tile, [sfx_lo, sfx_hi) (a bad
+            // length is clipped here and reported by the copy warps)
+            const int sfx_lo = (r / G) * p.sfx_nb * BS;
+            int sfx_hi = sfx_lo;
+            if (grouped) {
+                const int cap = min(p.max_sfx_len, min(p.sfx_max_blocks, p.sfx_nb) * BS);
+                sfx_hi = jr < p.chunk ? sfx_lo + min(max(sfx_next, 0), cap) : sfx_lo;
+                if (k + 1 < my_units) sfx_next = sfx_load(k + 1);
             }
-            tc_fence_before();
-            mbar_arrive_u32(barSfree + 8 * sb);
-            const int key0 = t * kKeys + pt * kPK;
-            if (grouped && t == n_pre) {   // suffix tile: the row's own member's keys only
+            float m_ref = -INFINITY;                       // reference maximum, log2 domain
+            float2 l2 = make_float2(0.f, 0.f);
+            int done = 0;
+            for (int t = 0; t < U.n_tiles; ++t, ++T) {
+                const int st = T & 1, sb = T % kSBufs;   // st: P barrier of this tile
+                bool ok = mbar_wait(barS + 8 * sb, (uint32_t)((T / kSBufs) & 1), p.err);
+                uint32_t sr[kPC][32];
+                if (__all_sync(0xffffffffu, ok)) {
+                    tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < kPC; ++cc)
+                    for (int cc = 0; cc < kPC; ++cc) tmem_ld32(tmem + sb * 128 + lane_off + pt * kPK + cc * 32, sr[cc]);
+                    tmem_ld_wait();
+                } else {
+                    ok = false;
+                }
+                const int key0 = t * kKeys + pt * kPK;
+                if (grouped && t == U.n_pre) {   // suffix tile: the row's own member's keys only
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int k = pt * kPK + cc * 32 + i;
-                        if (k < sfx_lo || k >= sfx_hi) sr[cc][i] = __float_as_uint(-INFINITY);
-                    }
-            } else if (!__all_sync(0xffffffffu, key0 + kPK - 1 <= pos)) {   // tile crosses some row's causal edge
+                    for (int cc = 0; cc < kPC; ++cc)
 #pragma unroll
-                for (int cc = 0; cc < kPC; ++cc)
+                        for (int i = 0; i < 32; ++i) {
+                            const int kx = pt * kPK + cc * 32 + i;
+                            if (kx < sfx_lo || kx >= sfx_hi) sr[cc][i] = __float_as_uint(-INFINITY);
+                        }
+                } else if (!__all_sync(0xffffffffu, key0 + kPK - 1 <= pos)) {   // tile crosses some row's causal edge
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (key0 + cc * 32 + i > pos) sr[cc][i] = __float_as_uint(-INFINITY);
-            }
-            float mh;
-            if constexpr (kPC == 2) mh = max_tree64(sr[0], sr[1]);
-            else mh = max_tree32(sr[0]);
-            if (__any_sync(0xffffffffu, !ok || *abort_flag)) {   // give up
-                *abort_flag = 1;
-                mbar_arrive_u32(barP + 8 * st);   // keep the arrival count balanced
-                break;
-            }
-            // this half's own reference: it moves only when the tile maximum
-            // exceeds it by more than kRescaleThreshold; the halves' sums meet in
-            // the epilogue, so the halves never wait for each other here
-            const float mrow = mh;
-            const float mt_ = mrow * c;
-            float alpha = 1.f;
-            if (mt_ > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt_ != -INFINITY)) {
-                alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - mt_);
-                m_ref = mt_;
-            }
-            const float2 c2 = make_float2(c, c);
-            const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
-            const float2 nm2 = make_float2(nm, nm);
-            // P goes back into this part's S columns (read above), two bf16 per
-            // column; Q.K(t + 3) overwrites them only after P.V(t) has read them
-            float2 ps2 = make_float2(0.f, 0.f);
-            uint32_t pw[32];
-            // term 0: hi = bf16(p) into the first half of this part's S columns;
-            // term 1 (precise rows): lo = bf16(p - hi) into the second half
-#pragma unroll 1
-            for (int term = 0; term < (precise ? 2 : 1); ++term) {
+                    for (int cc = 0; cc < kPC; ++cc)
 #pragma unroll
-                for (int cc = 0; cc < kPC; ++cc) {
+                        for (int i = 0; i < 32; ++i)
+                            if (key0 + cc * 32 + i > pos) sr[cc][i] = __float_as_uint(-INFINITY);
+                }
+                float mh;
+                if constexpr (kPC == 2) mh = max_tree64(sr[0], sr[1]);
+                else mh = max_tree32(sr[0]);
+                if (__any_sync(0xffffffffu, !ok || *abort_flag)) {   // give up
+                    *abort_flag = 1;
+                    mbar_arrive_u32(barP + 8 * st);   // keep the arrival count balanced
+                    break;
+                }
+                // this half's own reference: it moves only when the tile maximum
+                // exceeds it by more than kRescaleThreshold; the halves' sums meet in
+                // the epilogue, so the halves never wait for each other here
+                const float mt_ = mh * c;
+                float alpha = 1.f;
+                if (mt_ > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt_ != -INFINITY)) {
+                    alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - mt_);
+                    m_ref = mt_;
+                }
+                const float2 c2 = make_float2(c, c);
+                const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
+                const float2 nm2 = make_float2(nm, nm);
+                // P goes back into this part's S columns (read above), two bf16 per
+                // column; Q.K(T + 2) overwrites them only after P.V(T) has read them
+                float2 ps2 = make_float2(0.f, 0.f);
+                uint32_t pw[32];
+                if (!U.precise) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cc][2 * e]),
-                                                                __uint_as_float(sr[cc][2 * e + 1])),
-                                                    c2, nm2);
-                        const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                        if (term == 0) {
+                    for (int cc = 0; cc < kPC; ++cc) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cc][2 * e]),
+                                                                    __uint_as_float(sr[cc][2 * e + 1])),
+                                                        c2, nm2);
+                            const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
                             ps2 = __fadd2_rn(ps2, pe);
                             pw[cc * 16 + e] = pack_bf16x2(pe.x, pe.y);
-                        } else {
-                            const float2 hi = bf16x2_to_float2(pack_bf16x2(pe.x, pe.y));
-                            pw[cc * 16 + e] = pack_bf16x2(pe.x - hi.x, pe.y - hi.y);
                         }
                     }
-                }
-                if constexpr (kPC == 2) tmem_st32(tmem + sb * 128 + lane_off + pt * kPK + term * (kPK / 2), pw);
-                else tmem_st16(tmem + sb * 128 + lane_off + pt * kPK + term * (kPK / 2), pw);
-            }
-            tmem_st_wait();
-            l2.x = l2.x * alpha + (ps2.x + ps2.y);
-            // rescale this half's accumulator (all of d) once P.V(t-1) has completed
-            // (the barrier's previous phase, P.V(t-3), completed before Q.K(t - 1)
-            // was issued, which S(t - 1), read before this tile, needed)
-            if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                const int tp = t - 1;
-                mbar_wait(barOP + 8 * (tp & 1), (uint32_t)((tp >> 1) & 1), p.err);
-                tc_fence_after();
+                    if constexpr (kPC == 2) tmem_st32(tmem + sb * 128 + lane_off + pt * kPK, pw);
+                    else tmem_st16(tmem + sb * 128 + lane_off + pt * kPK, pw);
+                } else {
+                    // hi = bf16(p) into the first half of this part's S columns, lo =
+                    // bf16(p - hi) into the second, 32 scores at a time: a whole part's
+                    // hi and lo words at once spilled registers
 #pragma unroll
-                for (int cc = 0; cc < kD / 32; ++cc) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + pt * 128 + lane_off + cc * 32, o);
-                    tmem_ld_wait();
+                    for (int cc = 0; cc < kPC; ++cc) {
+                        uint32_t ph[16], pl[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(tO + pt * 128 + lane_off + cc * 32, o);
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cc][2 * e]),
+                                                                    __uint_as_float(sr[cc][2 * e + 1])),
+                                                        c2, nm2);
+                            const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                            ps2 = __fadd2_rn(ps2, pe);
+                            ph[e] = pack_bf16x2(pe.x, pe.y);
+                            const float2 hi = bf16x2_to_float2(ph[e]);
+                            pl[e] = pack_bf16x2(pe.x - hi.x, pe.y - hi.y);
+                        }
+                        tmem_st16(tmem + sb * 128 + lane_off + pt * kPK + cc * 16, ph);
+                        tmem_st16(tmem + sb * 128 + lane_off + pt * kPK + kPK / 2 + cc * 16, pl);
+                    }
                 }
                 tmem_st_wait();
-            }
-            // keys past the sequence end inside its last block: zero their V rows
-            // (their p is 0, but the slots may hold non-finite junk)
-            const int tile0 = t * kKeys;
-            const int tail_lo = seq_end - tile0, blk_end = ((seq_end + BS - 1) / BS) * BS - tile0;
-            const bool zero_tail = tail_lo > 0 && tail_lo < kKeys && (seq_end % BS) != 0;
-            if (zero_tail) {
-                const int sv = t % kKV;   // V ring slot of this tile
-                mbar_wait(barV + 8 * sv, (uint32_t)((t / kKV) & 1), p.err);
-                const int nrows = min(blk_end, kKeys) - tail_lo;
-                for (int idx = tid; idx < nrows * 2 * 8; idx += kSoftWarps * 32) {
-                    const int rr = tail_lo + idx / 16, h = (idx / 8) & 1, c16 = idx & 7;
-                    const uint32_t addr = sV + sv * kTile + (uint32_t)(rr / BS) * kVBlock + h * (kVBlock / 2) +
-                                          (uint32_t)(rr % BS) * 128u + (uint32_t)c16 * 16u;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                l2.x = l2.x * alpha + (ps2.x + ps2.y);
+                // rescale this half's accumulator (all of d) once P.V(T - 1) has
+                // completed (the barrier's previous phase, P.V(T - 3), completed before
+                // Q.K(T - 1) was issued, which S(T - 1), read before this tile, needed)
+                if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    const int tp = T - 1;
+                    mbar_wait(barOP + 8 * (tp & 1), (uint32_t)((tp >> 1) & 1), p.err);
+                    tc_fence_after();
+#pragma unroll
+                    for (int cc = 0; cc < kD / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + pt * 128 + lane_off + cc * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + pt * 128 + lane_off + cc * 32, o);
+                    }
+                    tmem_st_wait();
                 }
-            }
-            const bool zero_sfx = grouped && t == n_pre;   // suffix tile: each member's slots past its length
-            if (zero_sfx) {
-                const int sv = t % kKV;
-                mbar_wait(barV + 8 * sv, (uint32_t)((t / kKV) & 1), p.err);
-                for (int m = 0; m < members; ++m) {
-                    const int r0 = m * p.sfx_nb * BS + suffix_len<BS>(p, s * p.chunk + j0 + m, false);
-                    const int r1 = (m + 1) * p.sfx_nb * BS;
-                    for (int idx = tid; idx < (r1 - r0) * 2 * 8; idx += kSoftWarps * 32) {
-                        const int rr = r0 + idx / 16, h = (idx / 8) & 1, c16 = idx & 7;
+                // keys past the sequence end inside its last block: zero their V rows
+                // (their p is 0, but the slots may hold non-finite junk).  The wait is
+                // exact: S(T) needed Q.K(T), issued after P.V(T - 2), which needed
+                // V(T - 2), had completed.
+                const int tile0 = t * kKeys;
+                const int tail_lo = U.seq_end - tile0, blk_end = ((U.seq_end + BS - 1) / BS) * BS - tile0;
+                const bool zero_tail = tail_lo > 0 && tail_lo < kKeys && (U.seq_end % BS) != 0;
+                if (zero_tail) {
+                    const int sv = T % kKV;   // V ring slot of this tile
+                    mbar_wait(barV + 8 * sv, (uint32_t)((T / kKV) & 1), p.err);
+                    const int nrows = min(blk_end, kKeys) - tail_lo;
+                    for (int idx = tid; idx < nrows * 2 * 8; idx += kSoftWarps * 32) {
+                        const int rr = tail_lo + idx / 16, h = (idx / 8) & 1, c16 = idx & 7;
                         const uint32_t addr = sV + sv * kTile + (uint32_t)(rr / BS) * kVBlock + h * (kVBlock / 2) +
                                               (uint32_t)(rr % BS) * 128u + (uint32_t)c16 * 16u;
                         asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
                     }
+                    // the zeroed V rows (generic proxy) before the P.V that reads them (async proxy)
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
+                tc_fence_before();
+                mbar_arrive_u32(barP + 8 * st);
+                done = t + 1;
             }
-            // the zeroed V rows (generic proxy) before the P.V that reads them (async proxy)
-            if (zero_tail || zero_sfx) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            tc_fence_before();
-            mbar_arrive_u32(barP + 8 * st);
-            done = t + 1;
-        }
-        // ---- epilogue: the row's two halves merged by their references (O0 f0 +
-        // O1 f1) / (l0 f0 + l1 f1), f_h = 2^(m_h - max(m0, m1)); this thread
-        // writes half of d: bf16, or fp32 with the row's log-sum-exp.  The
-        // halves' (m, l) meet in the Q tile, free once every Q.K has completed
-        // (each did before its S was read).
-        const float l = l2.x;
-        const bool empty = n_tiles == 0;   // no keys: O = 0, lse = -inf, tensor memory never written
-        // every P.V has completed once the P.V lane's drain commit has arrived
-        const bool fin = empty || (done == n_tiles && !*abort_flag && mbar_wait(barEnd, 0, p.err));
-        float mh2[kParts], lh2[kParts];
-#pragma unroll
-        for (int q = 0; q < kParts; ++q) {
-            mh2[q] = -INFINITY;
-            lh2[q] = 0.f;
-        }
-        if (!empty) {   // (with no keys the Q copy may still be landing; O and l are zero anyway)
-            float *mx = reinterpret_cast<float *>(gbase + kOffQ);
-            float *lx = mx + kParts * 128;
+            // ---- epilogue: the row's two halves merged by their references (O0 f0 +
+            // O1 f1) / (l0 f0 + l1 f1), f_h = 2^(m_h - max(m0, m1)); this thread
+            // writes half of d: bf16, or fp32 with the row's log-sum-exp.  The
+            // unit's P.V have all completed once the P.V lane's unit commit has
+            // arrived (the phase before, the previous unit's, was waited for here).
+            const bool empty = U.n_tiles == 0;   // no keys: O = 0, lse = -inf, tensor memory never written
+            const bool fin = done == U.n_tiles && !*abort_flag && mbar_wait(barUnit, (uint32_t)(k & 1), p.err);
             mx[pt * 128 + r] = m_ref;
-            lx[pt * 128 + r] = l;
+            lx[pt * 128 + r] = l2.x;
+            okx[pt * 128 + r] = fin ? 1 : 0;
             part_sync(warp);
+            float mh2[kParts], lh2[kParts];
+            bool row_fin = true;
 #pragma unroll
             for (int q = 0; q < kParts; ++q) {
                 mh2[q] = mx[q * 128 + r];
                 lh2[q] = lx[q * 128 + r];
+                row_fin = row_fin && okx[q * 128 + r] != 0;
             }
-        }
-        float M = -INFINITY;
+            part_sync(warp);   // the next unit's epilogue writes these again
+            // one decision for the warp and its partner (both hold the same rows)
+            const bool all_fin = __all_sync(0xffffffffu, row_fin);
+            float M = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < kParts; ++q) M = fmaxf(M, mh2[q]);
-        float f[kParts], lt = 0.f;
+            for (int q = 0; q < kParts; ++q) M = fmaxf(M, mh2[q]);
+            float f[kParts], lt = 0.f;
 #pragma unroll
-        for (int q = 0; q < kParts; ++q) {
-            f[q] = mh2[q] == -INFINITY ? 0.f : fast_exp2(mh2[q] - M);
-            lt += lh2[q] * f[q];
-        }
-        tc_fence_after();
-        if (__all_sync(0xffffffffu, fin)) {
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            const bool row_ok = jr < p.chunk;
-            const size_t row = ((size_t)s * p.chunk + jr) * p.num_q_heads + (size_t)g * G + (r % G);
+            for (int q = 0; q < kParts; ++q) {
+                f[q] = mh2[q] == -INFINITY ? 0.f : fast_exp2(mh2[q] - M);
+                lt += lh2[q] * f[q];
+            }
+            tc_fence_after();
+            if (all_fin) {
+                const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                const bool row_ok = jr < p.chunk;
+                const size_t row = ((size_t)U.s * p.chunk + jr) * p.num_q_heads + (size_t)U.g * G + (r % G);
 #pragma unroll
-            for (int cc = 0; cc < kD / kParts / 32; ++cc) {
-                const int d0 = pt * (kD / kParts) + cc * 32;   // this chunk's first dim
-                float o[32];
+                for (int cc = 0; cc < kD / kParts / 32; ++cc) {
+                    const int d0 = pt * (kD / kParts) + cc * 32;   // this chunk's first dim
+                    float o[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = 0.f;
-                if (!empty) {
+                    for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                    if (!empty) {
 #pragma unroll
-                    for (int q = 0; q < kParts; ++q) {
-                        uint32_t oq[32];
-                        tmem_ld32(tO + q * 128 + lane_off + d0, oq);
-                        tmem_ld_wait();
+                        for (int q = 0; q < kParts; ++q) {
+                            uint32_t oq[32];
+                            tmem_ld32(tO + q * 128 + lane_off + d0, oq);
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] += __uint_as_float(oq[i]) * f[q];
+                            for (int i = 0; i < 32; ++i) o[i] += __uint_as_float(oq[i]) * f[q];
+                        }
+                    }
+                    if (row_ok && p.o_part != nullptr) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.o_part + row * kD + d0);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            dst[q4] = make_float4(o[q4 * 4 + 0] * inv, o[q4 * 4 + 1] * inv, o[q4 * 4 + 2] * inv,
+                                                  o[q4 * 4 + 3] * inv);
+                    } else if (row_ok) {
+                        __nv_bfloat16 *dst = p.out + row * kD + d0;
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 v;
+                            v.x = pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+                            v.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+                            v.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+                            v.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
+                            *reinterpret_cast<uint4 *>(dst + q4 * 8) = v;
+                        }
                     }
                 }
-                if (row_ok && p.o_part != nullptr) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + row * kD + d0);
-#pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4)
-                        dst[q4] = make_float4(o[q4 * 4 + 0] * inv, o[q4 * 4 + 1] * inv, o[q4 * 4 + 2] * inv,
-                                              o[q4 * 4 + 3] * inv);
-                } else if (row_ok) {
-                    __nv_bfloat16 *dst = p.out + row * kD + d0;
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 v;
-                        v.x = pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
-                        v.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
-                        v.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
-                        v.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
-                        *reinterpret_cast<uint4 *>(dst + q4 * 8) = v;
-                    }
-                }
+                // sum of exp2(s * scale * log2 e) over the row's keys is lt * 2^M
+                if (row_ok && p.o_part != nullptr && pt == 0)
+                    p.lse[row] = lt > 0.f ? (M + log2f(lt)) * kLn2 : -INFINITY;
             }
-            // sum of exp2(s * scale * log2 e) over the row's keys is lt * 2^M
-            if (row_ok && p.o_part != nullptr && pt == 0)
-                p.lse[row] = lt > 0.f ? (M + log2f(lt)) * kLn2 : -INFINITY;
+            // O has been read: the next unit's first P.V may overwrite it
+            tc_fence_before();
+            mbar_arrive_u32(barOfree);
+            if (!all_fin) break;   // gave up (the partner warp decides alike)
         }
     }
     tc_fence_before();
@@ -804,6 +990,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---- host side --------------------------------------------------------------
+
+// pa_set_prefill_ctas: a fixed persistent grid size (0: one CTA per SM).
+std::atomic<int32_t> g_prefill_ctas{0};
 
 template <int G, int BS, bool kGrouped>
 cudaError_t launch_kernel(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mkv, const CUtensorMap &mv,
@@ -817,10 +1006,17 @@ cudaError_t launch_kernel(const PrefillArgs &a, const CUtensorMap &mq, const CUt
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    constexpr int QPT = kRows / G;
-    dim3 grid((a.chunk_len + QPT - 1) / QPT, a.pool.num_kv_heads, a.num_seqs);
+    // persistent grid: one CTA per SM (or the set count), and enough CTAs that
+    // none holds more than kMaxUnits units
+    const int64_t n_units = (int64_t)prm.num_mt * prm.num_kv * prm.num_seqs;
+    if (n_units == 0) return cudaSuccess;
+    int64_t ctas = g_prefill_ctas.load(std::memory_order_relaxed);
+    if (ctas <= 0) ctas = device_sm_count();
+    if (ctas <= 0) return cudaErrorUnknown;
+    ctas = std::max<int64_t>(std::min<int64_t>(ctas, n_units), (n_units + kMaxUnits - 1) / kMaxUnits);
+    if (ctas > INT32_MAX) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
+    cfg.gridDim = dim3((unsigned)ctas);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
@@ -841,6 +1037,8 @@ cudaError_t launch_group(const PrefillArgs &a, const CUtensorMap &mq, const CUte
 
 }  // namespace prefill
 
+void set_prefill_ctas(int32_t ctas) { prefill::g_prefill_ctas.store(ctas, std::memory_order_relaxed); }
+
 bool prefill_supported(int head_dim, int group, int block_size) {
     return head_dim == prefill::kD &&
            (block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64) &&
@@ -854,6 +1052,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     auto encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const int G = a.num_q_heads / a.pool.num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return cudaErrorInvalidValue;
     const int Hkv = a.pool.num_kv_heads;
 
     // q viewed as (d, head in group, kv-head, row = s * C + j); box 64 x G x 1 x (128 / G)
@@ -899,6 +1098,9 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     prm.o_part = a.o_part;
     prm.lse = a.lse;
     prm.order = a.order;
+    prm.num_mt = (a.chunk_len + kRows / G - 1) / (kRows / G);
+    prm.num_kv = Hkv;
+    prm.num_seqs = a.num_seqs;
     prm.sfx_tables = a.sfx_tables;
     prm.sfx_max_blocks = a.sfx_max_blocks;
     prm.sfx_lens = a.sfx_lens;

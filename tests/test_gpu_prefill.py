@@ -131,3 +131,32 @@ def test_prefill_repeatable_under_contention(pa):
         torch.cuda.synchronize()
         assert pa.get_device_error() == 0
         assert torch.equal(out, first), f"prefill output differs at run {rep}"
+
+
+@pytest.mark.parametrize("group,hkv,ctx,chunk", [
+    (4, 2, [0, 300, 1000], 70),      # 3 M-tiles x 2 heads x 3 sequences = 18 units, one of them empty of context
+    (8, 2, [40] * 10, 256),          # 320 units: one CTA may hold at most 256, so a grid of 1 becomes 2
+])
+def test_prefill_persistent_grid_sweep(pa, group, hkv, ctx, chunk):
+    """The persistent grid walks its units in rounds and hands the copy and
+    tensor-core pipeline from one unit to the next inside a CTA.  Every grid
+    size from one CTA (every unit in one CTA) to one per unit gives the same
+    output bit for bit, and the default grid matches the oracle."""
+    w = wl.prefill_chunk(batch=len(ctx), ctx=ctx, chunk=chunk, num_blocks=1024, num_q_heads=group * hkv,
+                         num_kv_heads=hkv, seed=900 + group + chunk)
+    c = Case(w)
+    base = run_prefill(pa, c)
+    if len(ctx) <= 3:
+        assert_close(base, oracle_prefill(c), f"G={group} ctx={ctx} C={chunk}")
+    ctxd = torch.as_tensor(w.ctx_lens, device=c.dev)
+    n_units = -(-chunk // (128 // group)) * hkv * len(ctx)
+    try:
+        for ctas in (1, 2, 3, 5, 7, 17, n_units - 1, n_units, n_units + 5):
+            pa.set_prefill_ctas(ctas)
+            out = torch.full_like(c.q, float("nan"))
+            pa.prefill_chunk(out, c.q, c.pool, c.tables, ctxd, int(w.ctx_lens.max()), w.scale)
+            torch.cuda.synchronize()
+            assert pa.get_device_error() == 0
+            assert torch.equal(out, base), f"{ctas} CTAs: output differs from the default grid's"
+    finally:
+        pa.set_prefill_ctas(0)

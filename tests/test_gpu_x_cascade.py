@@ -362,6 +362,29 @@ def test_grouped_full_size_beams_repeatable(pa):
         assert torch.equal(again, first), f"grouped output differs at run {rep}"
 
 
+def test_grouped_persistent_grid_sweep(pa):
+    """Grouped decode (6 groups of 4 beams, 2 kv-heads: 12 units) with every
+    grid size from one CTA (all units in one CTA, the pipeline handed from
+    unit to unit, each unit's suffix tile zeroed and released in turn) to more
+    CTAs than units: outputs bit for bit alike, the default grid's against
+    the oracle."""
+    rng = np.random.default_rng(41)
+    prefix = [0, 160, 400, 1024, 48, 704]
+    suffix = rng.integers(0, 33, size=len(prefix) * 4)
+    w = wl.shared_groups(prefix, list(suffix), 4, 16, 2, 128, 16, seed=41)
+    c = Case(w)
+    plan = designed_plan(w, 4)
+    base = grouped_call(pa, c, plan, 4)
+    assert_close(base, oracle_full(c), "grouped sweep")
+    try:
+        for ctas in (1, 2, 3, 5, 11, 12, 13):
+            pa.set_prefill_ctas(ctas)
+            out = grouped_call(pa, c, plan, 4)
+            assert torch.equal(out, base), f"{ctas} CTAs: output differs from the default grid's"
+    finally:
+        pa.set_prefill_ctas(0)
+
+
 def test_grouped_refuses_long_suffixes(pa):
     """Suffixes that do not fit one 128-key tile for the M-tile's members are
     refused on the host (the two-call cascade serves them)."""
