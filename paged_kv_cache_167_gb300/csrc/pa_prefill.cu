@@ -155,6 +155,18 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Shared -> global copy of one box of a 4-D tensor map at (c0 .. c3), in this
+// thread's current bulk group (coordinates >= 0, c0 * 2 B a multiple of 16 B).
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, int c0, int c1, int c2, int c3, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(map),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk stores have finished reading shared memory / have completed
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
                                             int c4, uint32_t bar) {
     asm volatile(
@@ -267,6 +279,10 @@ __device__ __forceinline__ void part_sync(int warp) {   // warps w, w + 4, ... o
     asm volatile("bar.sync %0, %1;" ::"r"(1 + (warp & 3)), "r"(kParts * 32) : "memory");
 }
 
+__device__ __forceinline__ void soft_sync() {   // all softmax warps
+    asm volatile("bar.sync 5, %0;" ::"n"(kSoftWarps * 32) : "memory");
+}
+
 __device__ __forceinline__ float max_tree32(const uint32_t (&a)[32]) {
     float m[16];
 #pragma unroll
@@ -319,7 +335,8 @@ __device__ __forceinline__ float max_tree64(const uint32_t (&a)[32], const uint3
 template <int G, int BS, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+                   const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
+                   const Params p) {
     constexpr int QPT = kRows / G;   // queries per M-tile
     constexpr int NBT = kKeys / BS;  // blocks per 128-key tile
     constexpr uint32_t kVBlock = 2u * BS * 128u;   // one block's V box: [half][BS keys][128 B]
@@ -354,8 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kNumBars; ++i) {
             const uint32_t b = barQ + 8 * i;
             const bool softmax_arrivals = (b >= barP && b < barOP) || b == barOfree;   // P[2], O read
+            // Q free: the Q.K lane's commit and the softmax's release of the
+            // buffer, which may stage the unit's output tile for a tensor store
+            const bool q_free = b >= barQfree && b < barQfree + 16;
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b),
-                         "r"(softmax_arrivals ? (uint32_t)(kSoftWarps * 32) : 1u)
+                         "r"(softmax_arrivals ? (uint32_t)(kSoftWarps * 32) : (q_free ? 2u : 1u))
                          : "memory");
         }
         *abort_flag = 0;
@@ -479,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (is_k) {
                 // Q buffer k % 2 held unit k - 2's Q: its Q.K must have completed
+                // and the store of the output tile staged there must have read it
                 // (the phase before, unit k - 4's, was waited for here two units ago)
                 const int qb = k & 1;
                 if (k >= 2) ok = __all_sync(0xffffffffu, mbar_wait(barQfree + 8 * qb, (uint32_t)(((k >> 1) - 1) & 1), p.err));
@@ -743,6 +764,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *mx = reinterpret_cast<float *>(gbase + kOffX);   // the halves' (m, l, ok) of each row
         float *lx = mx + kParts * 128;
         int *okx = reinterpret_cast<int *>(lx + kParts * 128);
+        // thread 0: the Q buffer whose release it owes once the tensor store of
+        // the output tile staged there has read it (-1: none)
+        int q_owed = -1;
+        auto release = [&]() {
+            bulk_wait_read();
+            mbar_arrive_u32(barQfree + 8 * q_owed);
+            q_owed = -1;
+        };
         // grouped: the row's member's suffix length, read a unit ahead
         auto sfx_load = [&](int k) -> int {
             const Unit N = unit(k);
@@ -770,6 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < U.n_tiles; ++t, ++T) {
                 const int st = T & 1, sb = T % kSBufs;   // st: P barrier of this tile
                 bool ok = mbar_wait(barS + 8 * sb, (uint32_t)((T / kSBufs) & 1), p.err);
+                if (t == 1 && tid == 0 && q_owed >= 0) release();   // the previous unit's store was issued a tile ago
                 uint32_t sr[kPC][32];
                 if (__all_sync(0xffffffffu, ok)) {
                     tc_fence_after();
@@ -906,6 +936,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // unit's P.V have all completed once the P.V lane's unit commit has
             // arrived (the phase before, the previous unit's, was waited for here).
             const bool empty = U.n_tiles == 0;   // no keys: O = 0, lse = -inf, tensor memory never written
+            if (tid == 0 && q_owed >= 0) release();   // (units of fewer than two tiles)
+            // A full M-tile of bf16 rows is staged in the unit's Q buffer (every Q.K
+            // of the unit has completed) in the Q tile's layout and written by two
+            // tensor stores: rows written straight from registers leave each warp
+            // store 32 lines apart, and those stores held the epilogue ~1 us.
+            const bool tma_out = p.o_part == nullptr && !empty && U.j0 + QPT <= p.chunk;
+            const uint32_t sOut = sQ + (uint32_t)(k & 1) * kTile;
             const bool fin = done == U.n_tiles && !*abort_flag && mbar_wait(barUnit, (uint32_t)(k & 1), p.err);
             mx[pt * 128 + r] = m_ref;
             lx[pt * 128 + r] = l2.x;
@@ -960,6 +997,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   o[q4 * 4 + 3] * inv);
                     } else if (row_ok) {
                         __nv_bfloat16 *dst = p.out + row * kD + d0;
+                        // 16-byte chunk c of the row's half goes to chunk c ^ (r % 8) of its
+                        // 128-byte line: the Q tile's swizzle, which the tensor store undoes
+                        const uint32_t line = sOut + (uint32_t)pt * kHalf + (uint32_t)r * 128u;
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             uint4 v;
@@ -967,7 +1007,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
                             v.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
                             v.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
-                            *reinterpret_cast<uint4 *>(dst + q4 * 8) = v;
+                            if (tma_out) {
+                                const uint32_t c16 = (uint32_t)(cc * 4 + q4);
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                                 line + ((c16 ^ ((uint32_t)r & 7u)) << 4)),
+                                             "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                             : "memory");
+                            } else {
+                                *reinterpret_cast<uint4 *>(dst + q4 * 8) = v;
+                            }
                         }
                     }
                 }
@@ -975,10 +1023,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (row_ok && p.o_part != nullptr && pt == 0)
                     p.lse[row] = lt > 0.f ? (M + log2f(lt)) * kLn2 : -INFINITY;
             }
+            if (tma_out) {
+                // both halves by one tensor store each, once every softmax thread has
+                // written its rows (generic writes, then reads by the async proxy)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                soft_sync();
+                if (tid == 0) {
+                    if (all_fin) {
+                        tma_store_4d(&tmap_o, 0, 0, U.g, U.s * p.chunk + U.j0, sOut);
+                        tma_store_4d(&tmap_o, 64, 0, U.g, U.s * p.chunk + U.j0, sOut + kHalf);
+                        bulk_commit();
+                    }
+                    q_owed = k & 1;   // released once the stores have read it
+                }
+            } else if (tid == 0) {
+                mbar_arrive_u32(barQfree + 8 * (k & 1));   // nothing staged in the unit's Q buffer
+            }
             // O has been read: the next unit's first P.V may overwrite it
             tc_fence_before();
             mbar_arrive_u32(barOfree);
             if (!all_fin) break;   // gave up (the partner warp decides alike)
+        }
+        if (tid == 0) {   // no store may still read shared memory, or be in flight, when the CTA ends
+            if (q_owed >= 0) release();
+            bulk_wait_all();
         }
     }
     tc_fence_before();
@@ -996,7 +1064,7 @@ std::atomic<int32_t> g_prefill_ctas{0};
 
 template <int G, int BS, bool kGrouped>
 cudaError_t launch_kernel(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mkv, const CUtensorMap &mv,
-                         const Params &prm, cudaStream_t stream) {
+                         const CUtensorMap &mo, const Params &prm, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1025,14 +1093,14 @@ cudaError_t launch_kernel(const PrefillArgs &a, const CUtensorMap &mq, const CUt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<G, BS, kGrouped>, mq, mkv, mv, prm);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<G, BS, kGrouped>, mq, mkv, mv, mo, prm);
 }
 
 template <int G, int BS>
 cudaError_t launch_group(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mkv, const CUtensorMap &mv,
-                         const Params &prm, cudaStream_t stream) {
-    return a.sfx_tables != nullptr ? launch_kernel<G, BS, true>(a, mq, mkv, mv, prm, stream)
-                                   : launch_kernel<G, BS, false>(a, mq, mkv, mv, prm, stream);
+                         const CUtensorMap &mo, const Params &prm, cudaStream_t stream) {
+    return a.sfx_tables != nullptr ? launch_kernel<G, BS, true>(a, mq, mkv, mv, mo, prm, stream)
+                                   : launch_kernel<G, BS, false>(a, mq, mkv, mv, mo, prm, stream);
 }
 
 }  // namespace prefill
@@ -1055,15 +1123,17 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     if (G != 1 && G != 2 && G != 4 && G != 8) return cudaErrorInvalidValue;
     const int Hkv = a.pool.num_kv_heads;
 
-    // q viewed as (d, head in group, kv-head, row = s * C + j); box 64 x G x 1 x (128 / G)
-    CUtensorMap mq, mkv;
-    {
+    // q viewed as (d, head in group, kv-head, row = s * C + j); box 64 x G x 1 x (128 / G).
+    // The bf16 output, of q's shape, the same way (tensor stores of full M-tiles).
+    CUtensorMap mq, mo, mkv;
+    for (int which = 0; which < 2; ++which) {
         cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)G, (cuuint64_t)Hkv,
                               (cuuint64_t)a.num_seqs * (cuuint64_t)a.chunk_len};
         cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)G * kD * 2, (cuuint64_t)a.num_q_heads * kD * 2};
         cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)(kRows / G)};
         cuuint32_t estr[4] = {1, 1, 1, 1};
-        if (encode(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(a.q), dims, strides, box, estr,
+        void *base = which == 0 || a.out == nullptr ? const_cast<void *>(a.q) : a.out;   // no bf16 output: unused
+        if (encode(which == 0 ? &mq : &mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
@@ -1114,10 +1184,10 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     auto by_block = [&](auto gtag) -> cudaError_t {
         constexpr int GG = decltype(gtag)::value;
         switch (a.pool.block_size) {
-            case 8: return launch_group<GG, 8>(a, mq, mkv, mv, prm, stream);
-            case 16: return launch_group<GG, 16>(a, mq, mkv, mv, prm, stream);
-            case 32: return launch_group<GG, 32>(a, mq, mkv, mv, prm, stream);
-            case 64: return launch_group<GG, 64>(a, mq, mkv, mv, prm, stream);
+            case 8: return launch_group<GG, 8>(a, mq, mkv, mv, mo, prm, stream);
+            case 16: return launch_group<GG, 16>(a, mq, mkv, mv, mo, prm, stream);
+            case 32: return launch_group<GG, 32>(a, mq, mkv, mv, mo, prm, stream);
+            case 64: return launch_group<GG, 64>(a, mq, mkv, mv, mo, prm, stream);
             default: return cudaErrorInvalidValue;
         }
     };
