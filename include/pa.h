@@ -438,6 +438,12 @@ pa_status pa_decode_cascade(void *out, const void *q, const pa_kv_pool *pool,
  *   new_k, new_v   device, [num_groups * group_size][Hkv][d] bf16 or both NULL:
  *                  each member's new token, stored at its last suffix position
  *                  (as pa_decode_ex stores it) before it is attended
+ *   flags          0 or PA_DECODE_EARLY_METADATA: the caller promises that
+ *                  group_order, prefix_lens and prefix_tables are not written by
+ *                  the kernel this call immediately follows in `stream`; they
+ *                  are then read while that kernel still runs (q, the pool and
+ *                  the suffix arrays still wait for it).  Results are identical
+ *                  with and without it; other bits give PA_ERR_INVALID_ARG.
  * Supported when the members of one M-tile (min(group_size, 128 / (num_q_heads
  * / Hkv))) times ceil(max_suffix_len / block_size) blocks fit one 128-key
  * tile; otherwise PA_ERR_UNSUPPORTED (use pa_prefix_attention and
@@ -449,7 +455,7 @@ pa_status pa_decode_grouped(void *out, const void *q, const pa_kv_pool *pool, co
                             const int32_t *suffix_tables, int32_t max_suffix_blocks, const int32_t *suffix_lens,
                             int32_t num_groups, int32_t group_size, int32_t num_q_heads, int32_t max_prefix_len,
                             int32_t max_suffix_len, float scale, const void *new_k, const void *new_v,
-                            cudaStream_t stream);
+                            uint32_t flags, cudaStream_t stream);
 
 /*
  * Check of the bounded waits: launches one CTA whose wait on a shared-memory

@@ -67,7 +67,7 @@ SIGNATURES = {
                                  _U32, _P]),
     "pa_cascade_plan": (_I32, [_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "pa_decode_grouped": (_I32, [_P, _P, _POOL, _P, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _F,
-                                 _P, _P, _P]),
+                                 _P, _P, _U32, _P]),
     "pa_get_device_error": (_I32, [ctypes.POINTER(_U32), _I32, _P]),
     "pa_check_wait_timeout": (_I32, [ctypes.c_uint64, _P]),
     "pa_set_stream_k_ctas": (_I32, [_I32]),
@@ -399,9 +399,11 @@ def decode_grouped(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, prefi
                    prefix_lens: torch.Tensor, suffix_tables: torch.Tensor, suffix_lens: torch.Tensor, group_size: int,
                    max_prefix_len: int, max_suffix_len: int, scale: float,
                    group_order: Optional[torch.Tensor] = None, new_k: Optional[torch.Tensor] = None,
-                   new_v: Optional[torch.Tensor] = None, layer: Optional[int] = None, stream=None) -> None:
+                   new_v: Optional[torch.Tensor] = None, layer: Optional[int] = None, flags: int = 0,
+                   stream=None) -> None:
     """pa_decode_grouped: each group's queries over its shared prefix and each
-    member's own suffix in one call (the cascade fused, for short suffixes)."""
+    member's own suffix in one call (the cascade fused, for short suffixes).
+    flags: 0 or PA_DECODE_EARLY_METADATA."""
     desc = pool_desc(pool, layer)
     B, Hq, _ = q.shape
     if group_size <= 0 or B % group_size != 0:
@@ -426,7 +428,8 @@ def decode_grouped(out: torch.Tensor, q: torch.Tensor, pool: torch.Tensor, prefi
                                    prefix_tables.shape[1], _dev(prefix_lens, torch.int32, "prefix_lens"), order,
                                    _dev(suffix_tables, torch.int32, "suffix_tables"), suffix_tables.shape[1],
                                    _dev(suffix_lens, torch.int32, "suffix_lens"), G, int(group_size), Hq,
-                                   int(max_prefix_len), int(max_suffix_len), float(scale), nk, nv, _stream(stream)),
+                                   int(max_prefix_len), int(max_suffix_len), float(scale), nk, nv, int(flags),
+                                   _stream(stream)),
            "pa_decode_grouped")
 
 

@@ -376,12 +376,13 @@ pa_status pa_decode_grouped(void *out, const void *q, const pa_kv_pool *pool, co
                             const int32_t *suffix_tables, int32_t max_suffix_blocks, const int32_t *suffix_lens,
                             int32_t num_groups, int32_t group_size, int32_t num_q_heads, int32_t max_prefix_len,
                             int32_t max_suffix_len, float scale, const void *new_k, const void *new_v,
-                            cudaStream_t stream) {
+                            uint32_t flags, cudaStream_t stream) {
     PoolView view;
     pa_status st = resolve_pool(pool, &view);
     if (st != PA_OK) return st;
     if (num_groups < 0 || group_size < 0 || num_q_heads <= 0 || max_prefix_len < 0 || max_suffix_len < 0)
         return PA_ERR_INVALID_ARG;
+    if (flags & ~PA_DECODE_EARLY_METADATA) return PA_ERR_INVALID_ARG;
     if (num_q_heads % view.num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     const int group = num_q_heads / view.num_kv_heads;
     if (!prefill_supported(view.head_dim, group, view.block_size)) return PA_ERR_UNSUPPORTED;
@@ -420,6 +421,7 @@ pa_status pa_decode_grouped(void *out, const void *q, const pa_kv_pool *pool, co
     a.max_sfx_len = max_suffix_len;
     a.new_k = new_k;
     a.new_v = new_v;
+    a.early_meta = (flags & PA_DECODE_EARLY_METADATA) != 0;
     return launch_prefill(a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

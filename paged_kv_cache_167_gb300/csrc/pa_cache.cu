@@ -70,8 +70,12 @@ struct CacheParams {
 
 // One thread per 16-B vector of a (token, K/V, head) row.
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheParams p) {
-    asm volatile("griddepcontrol.launch_dependents;");   // the next kernel still waits for this grid to finish
-    asm volatile("griddepcontrol.wait;" ::: "memory");   // inputs may come from the previous kernel
+    // inputs may come from the previous kernel; the next one may be scheduled
+    // once this CTA has passed that wait (so every kernel before this one has
+    // finished: a caller's promise about the kernel immediately before the
+    // next call holds), and still waits for this grid to finish
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int64_t per_token = 2ll * p.num_kv_heads * p.row_vecs;
     const int64_t total = p.num_tokens * per_token;
     const int64_t slot_limit = p.num_blocks * p.block_size;
@@ -253,8 +257,8 @@ struct AppendParams {
 };
 
 __global__ void __launch_bounds__(256) append_last_kernel(const AppendParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // as in the slot writer
     asm volatile("griddepcontrol.launch_dependents;");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t per_seq = 2ll * p.num_kv_heads * p.row_vecs;
     const int64_t total = (int64_t)p.num_seqs * per_seq;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;

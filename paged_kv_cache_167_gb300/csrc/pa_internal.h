@@ -110,6 +110,7 @@ struct PrefillArgs {
     int32_t max_sfx_len = 0;
     const void *new_k = nullptr;
     const void *new_v = nullptr;
+    bool early_meta = false;   // order, ctx_lens and tables are not written by the kernel before
 };
 bool prefill_supported(int head_dim, int group, int block_size);
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);

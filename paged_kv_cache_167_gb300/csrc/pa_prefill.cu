@@ -124,6 +124,7 @@ struct Params {
     int32_t num_mt;              // M-tiles per sequence
     int32_t num_kv;              // kv-heads
     int32_t num_seqs;            // sequences (B)
+    int32_t early_meta;          // order, ctx_lens and tables are not written by the kernel before
     // Grouped decode (sfx_tables non-null): sequence s stands for a group of
     // `chunk` members that share its ctx_lens[s] prefix tokens; after the
     // prefix tiles one more tile holds every member's own suffix blocks (member
@@ -381,8 +382,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_barrier_init();
     }
+    __syncthreads();   // the barriers, before unit 0's Q copy below
 
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The kernel is launched with programmatic stream serialisation: what it
+    // reads waits for the kernel before it to finish here, except, when the
+    // caller promises that kernel does not write them, the sequence order,
+    // context lengths and tables, read below while it still runs.  Each CTA
+    // lets the kernel after this one be scheduled once it has passed that
+    // wait (so every kernel before this one has finished, and every CTA of
+    // this grid has started): that kernel's CTAs set up on the SMs this grid's
+    // CTAs leave as they finish, and wait for the whole grid before they read
+    // what it wrote.
+    if (!p.early_meta) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
 
     // ---- this CTA's units, read once into shared memory
     const int C = (int)gridDim.x, cta = (int)blockIdx.x;
@@ -394,6 +408,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (my_units > kMaxUnits) {   // the launcher sizes the grid so that this cannot happen
         if (tid == 0) raise_error(p.err, PA_DEVERR_SEQ_LEN);
         my_units = kMaxUnits;
+    }
+    // Copy warps: unit 0's sequence and its first 64 block ids, read beside the
+    // table below instead of after it (an id is checked against the unit's
+    // blocks when first used, so the ids need not wait for the context
+    // length); the K warp copies unit 0's Q as soon as its sequence is known.
+    int ids0_a = 0, ids0_b = 0, s0 = 0;
+    if ((warp == kKWarp || warp == kVWarp) && my_units > 0) {
+        const int z0 = unit_index(0) / per_seq;
+        s0 = z0;
+        if (p.order != nullptr) {   // a bad entry is reported by the table fill
+            const int o = __ldg(p.order + z0);
+            if (o >= 0 && o < p.num_seqs) s0 = o;
+        }
+        const int32_t *row0 = p.tables + (size_t)s0 * p.max_blocks;
+        if (lane < p.max_blocks) ids0_a = __ldg(row0 + lane);
+        if (32 + lane < p.max_blocks) ids0_b = __ldg(row0 + 32 + lane);
+        if (warp == kKWarp && !p.early_meta) {
+            const int u0 = unit_index(0);
+            if (lane == 0) mbar_expect(barQ, kTile);
+            __syncwarp();
+            if (lane < 2)
+                tma_load_4d(sQ + lane * kHalf, &tmap_q, lane * 64, 0, (u0 / p.num_mt) % p.num_kv,
+                            s0 * p.chunk + (u0 % p.num_mt) * QPT, barQ);
+        }
     }
     for (int k = tid; k < my_units; k += kThreads) {
         const int z = unit_index(k) / per_seq;
@@ -409,6 +447,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ctx = ctx < 0 ? 0 : p.max_ctx_len;
         }
         utab[k] = make_int2(s, ctx);
+    }
+    if (p.early_meta) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (warp == kKWarp && my_units > 0) {   // q may come from the kernel before
+            const int u0 = unit_index(0);
+            if (lane == 0) mbar_expect(barQ, kTile);
+            __syncwarp();
+            if (lane < 2)
+                tma_load_4d(sQ + lane * kHalf, &tmap_q, lane * 64, 0, (u0 / p.num_mt) % p.num_kv,
+                            s0 * p.chunk + (u0 % p.num_mt) * QPT, barQ);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -483,12 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int T = 0;                 // tiles issued so far
         Unit U;
-        int raw_cur = 0, raw_next = 0;
-        if (my_units > 0) {
-            U = unit(0);
-            raw_cur = ids_load(U, 0);
-            raw_next = ids_load(U, 1);
-        }
+        int raw_cur = ids0_a, raw_next = ids0_b;   // unit 0's, read above
+        if (my_units > 0) U = unit(0);
         for (int k = 0; k < my_units && ok; ++k) {
             Unit N = U;            // the next unit, and its first ids
             int nraw_cur = 0, nraw_next = 0;
@@ -497,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 nraw_cur = ids_load(N, 0);
                 nraw_next = ids_load(N, 1);
             }
-            if (is_k) {
+            if (is_k && k > 0) {   // (unit 0's Q was copied above)
                 // Q buffer k % 2 held unit k - 2's Q: its Q.K must have completed
                 // and the store of the output tile staged there must have read it
                 // (the phase before, unit k - 4's, was waited for here two units ago)
@@ -1171,6 +1217,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     prm.num_mt = (a.chunk_len + kRows / G - 1) / (kRows / G);
     prm.num_kv = Hkv;
     prm.num_seqs = a.num_seqs;
+    prm.early_meta = a.early_meta ? 1 : 0;
     prm.sfx_tables = a.sfx_tables;
     prm.sfx_max_blocks = a.sfx_max_blocks;
     prm.sfx_lens = a.sfx_lens;

@@ -205,11 +205,14 @@ def test_grouped_decode_validation(B):
     good = _pool(B, nb=64, hkv=8, b=16, d=128)
     ok_ptr = P(0x20000)
 
-    def call(out=ok_ptr, pool=good, gsz=4, groups=2, hq=64, max_pre=64, max_sfx=32, scale=0.1, nk=P(0), nv=P(0)):
+    def call(out=ok_ptr, pool=good, gsz=4, groups=2, hq=64, max_pre=64, max_sfx=32, scale=0.1, nk=P(0), nv=P(0),
+             flags=0):
         return L.pa_decode_grouped(out, ok_ptr, ctypes.byref(pool), ok_ptr, 8, ok_ptr, P(0), ok_ptr, 4, ok_ptr,
-                                   groups, gsz, hq, max_pre, max_sfx, scale, nk, nv, P(0))
+                                   groups, gsz, hq, max_pre, max_sfx, scale, nk, nv, flags, P(0))
 
     assert call(groups=0) == 0                         # nothing to do
+    assert call(groups=0, flags=1) == 0                # PA_DECODE_EARLY_METADATA is accepted
+    assert call(flags=2) == 1                          # an unknown flag bit
     assert call(max_sfx=33) == 2                       # 4 members x 3 blocks > 128 keys
     assert call(gsz=16, max_sfx=16) == 2               # 16 members (of G = 8) x 1 block > 128 keys
     assert call(pool=_pool(B, d=64)) == 2              # head_dim 64 not built for the tensor-core path

@@ -279,7 +279,7 @@ def test_beam_cascade_grid_sweep(pa, ctas):
     assert_close(out, oracle_full(c), f"beam cascade ctas={ctas}")
 
 
-def grouped_call(pa, c: Case, plan, group_size, max_suffix=None, new_kv=None, order="plan"):
+def grouped_call(pa, c: Case, plan, group_size, max_suffix=None, new_kv=None, order="plan", flags=0):
     w, dev = c.w, c.dev
     out = torch.full_like(c.q, float("nan"))
     if isinstance(order, str):
@@ -291,7 +291,8 @@ def grouped_call(pa, c: Case, plan, group_size, max_suffix=None, new_kv=None, or
                       torch.as_tensor(plan["suffix_tables"], device=dev),
                       torch.as_tensor(plan["suffix_lens"], device=dev), group_size,
                       int(plan["prefix_lens"].max()), ms, w.scale,
-                      group_order=None if order is None else torch.as_tensor(order, device=dev), new_k=nk, new_v=nv)
+                      group_order=None if order is None else torch.as_tensor(order, device=dev), new_k=nk, new_v=nv,
+                      flags=flags)
     torch.cuda.synchronize()
     assert pa.get_device_error() == 0
     return out
@@ -338,7 +339,8 @@ def test_grouped_full_size_beams_repeatable(pa):
     """The beam batch (32 groups of 4 after copy-on-write) through one
     pa_decode_grouped call that also stores every beam's new token: every
     row against the oracle, then eight more calls (every other one under a
-    concurrent copy on a second stream) bit-identical to the first."""
+    concurrent copy on a second stream, half of them reading the tables
+    before the previous kernel has finished) bit-identical to the first."""
     w = wl.beam_fork()
     c = Case(w)
     pa.copy_blocks(c.pool, torch.as_tensor(w.copy_pairs, device=c.dev))
@@ -358,7 +360,8 @@ def test_grouped_full_size_beams_repeatable(pa):
             with torch.cuda.stream(side):
                 for _ in range(3):
                     dst.copy_(src)
-        again = grouped_call(pa, c, plan, 4, new_kv=(c.new_k, c.new_v))
+        again = grouped_call(pa, c, plan, 4, new_kv=(c.new_k, c.new_v),
+                             flags=pa.PA_DECODE_EARLY_METADATA if rep % 4 >= 2 else 0)
         assert torch.equal(again, first), f"grouped output differs at run {rep}"
 
 
@@ -379,8 +382,9 @@ def test_grouped_persistent_grid_sweep(pa):
     try:
         for ctas in (1, 2, 3, 5, 11, 12, 13):
             pa.set_prefill_ctas(ctas)
-            out = grouped_call(pa, c, plan, 4)
-            assert torch.equal(out, base), f"{ctas} CTAs: output differs from the default grid's"
+            for flags in (0, pa.PA_DECODE_EARLY_METADATA):   # the tables read before or after the wait
+                out = grouped_call(pa, c, plan, 4, flags=flags)
+                assert torch.equal(out, base), f"{ctas} CTAs, flags {flags}: output differs from the default grid's"
     finally:
         pa.set_prefill_ctas(0)
 
