@@ -295,15 +295,32 @@ __device__ __forceinline__ float max_tree32(const uint32_t (&a)[32]) {
     return m[0];
 }
 
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Maximum of 64 values by three-input steps: 64 -> 22 -> 8 -> 4 -> 2 -> 1
+// (32 instructions, five deep, against 63 and six with two-input steps).
 __device__ __forceinline__ float max_tree64(const uint32_t (&a)[32], const uint32_t (&b)[32]) {
-    float m[32];
+    float v[64];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) m[i] = fmaxf(__uint_as_float(a[i]), __uint_as_float(b[i]));
+    for (int i = 0; i < 32; ++i) {
+        v[i] = __uint_as_float(a[i]);
+        v[32 + i] = __uint_as_float(b[i]);
+    }
+    float m1[22];
 #pragma unroll
-    for (int w = 16; w >= 1; w >>= 1)
+    for (int i = 0; i < 21; ++i) m1[i] = max3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+    m1[21] = v[63];
+    float m2[8];
 #pragma unroll
-        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
-    return m[0];
+    for (int i = 0; i < 7; ++i) m2[i] = max3(m1[3 * i], m1[3 * i + 1], m1[3 * i + 2]);
+    m2[7] = m1[21];
+    const float x = max3(m2[0], m2[1], m2[2]), y = max3(m2[3], m2[4], m2[5]);
+    return fmaxf(max3(x, y, m2[6]), m2[7]);
 }
 
 // Work units: one (M-tile mt, kv-head g, sequence slot z) each, numbered
@@ -894,6 +911,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // P goes back into this part's S columns (read above), two bf16 per
                 // column; Q.K(T + 2) overwrites them only after P.V(T) has read them
                 float2 ps2 = make_float2(0.f, 0.f);
+                float2 ps2b = make_float2(0.f, 0.f);   // a second chain: the sums are 16 adds deep, not 32
                 uint32_t pw[32];
                 if (!U.precise) {
 #pragma unroll
@@ -904,7 +922,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                     __uint_as_float(sr[cc][2 * e + 1])),
                                                         c2, nm2);
                             const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                            ps2 = __fadd2_rn(ps2, pe);
+                            if (e & 1) ps2b = __fadd2_rn(ps2b, pe);
+                            else ps2 = __fadd2_rn(ps2, pe);
                             pw[cc * 16 + e] = pack_bf16x2(pe.x, pe.y);
                         }
                     }
@@ -933,6 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tmem_st_wait();
+                ps2 = __fadd2_rn(ps2, ps2b);
                 l2.x = l2.x * alpha + (ps2.x + ps2.y);
                 // rescale this half's accumulator (all of d) once P.V(T - 1) has
                 // completed (the barrier's previous phase, P.V(T - 3), completed before
@@ -987,7 +1007,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // of the unit has completed) in the Q tile's layout and written by two
             // tensor stores: rows written straight from registers leave each warp
             // store 32 lines apart, and those stores held the epilogue ~1 us.
-            const bool tma_out = p.o_part == nullptr && !empty && U.j0 + QPT <= p.chunk;
+            // (with fewer queries than an M-tile holds, every tile has all `chunk` of
+            // them and the output map's box is that high)
+            const bool tma_out = p.o_part == nullptr && !empty && U.j0 + min(QPT, p.chunk) <= p.chunk;
             const uint32_t sOut = sQ + (uint32_t)(k & 1) * kTile;
             const bool fin = done == U.n_tiles && !*abort_flag && mbar_wait(barUnit, (uint32_t)(k & 1), p.err);
             mx[pt * 128 + r] = m_ref;
@@ -1176,7 +1198,9 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
         cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)G, (cuuint64_t)Hkv,
                               (cuuint64_t)a.num_seqs * (cuuint64_t)a.chunk_len};
         cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)G * kD * 2, (cuuint64_t)a.num_q_heads * kD * 2};
-        cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)(kRows / G)};
+        // the output's box: a whole M-tile of queries, or all of them when fewer
+        const int qrows = which == 0 ? kRows / G : std::max(1, std::min(kRows / G, a.chunk_len));
+        cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)qrows};
         cuuint32_t estr[4] = {1, 1, 1, 1};
         void *base = which == 0 || a.out == nullptr ? const_cast<void *>(a.q) : a.out;   // no bf16 output: unused
         if (encode(which == 0 ? &mq : &mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
