@@ -168,6 +168,14 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Hint: bring one box of a 4-D tensor map at (c0 .. c3) into L2 (changes no
+// data and orders nothing, so it may run before the data's writer finishes).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(map), "r"(c0),
+                 "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
                                             int c4, uint32_t bar) {
     asm volatile(
@@ -441,6 +449,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t *row0 = p.tables + (size_t)s0 * p.max_blocks;
         if (lane < p.max_blocks) ids0_a = __ldg(row0 + lane);
         if (32 + lane < p.max_blocks) ids0_b = __ldg(row0 + 32 + lane);
+        if (p.early_meta) {
+            // While the kernel before still runs: unit 0's Q and first two K/V
+            // tiles into L2 (hints; an id past the unit's blocks only warms an
+            // unused block, one out of range is skipped)
+            const int u0 = unit_index(0);
+            if (warp == kKWarp && lane < 2)
+                tma_prefetch_4d(&tmap_q, lane * 64, 0, (u0 / p.num_mt) % p.num_kv, s0 * p.chunk + (u0 % p.num_mt) * QPT);
+            if (lane < kKV * NBT && ids0_a >= 0 && ids0_a < p.num_blocks) {
+                const int g0 = (u0 / p.num_mt) % p.num_kv;
+                if (warp == kKWarp) {
+                    tensor_prefetch_l2_5d(&tmap_k, 0, 0, g0, 0, ids0_a);
+                    tensor_prefetch_l2_5d(&tmap_k, 64, 0, g0, 0, ids0_a);
+                } else {
+                    tensor_prefetch_l2_5d(&tmap_v, 0, 0, 0, g0, ids0_a);
+                }
+            }
+        }
         if (warp == kKWarp && !p.early_meta) {
             const int u0 = unit_index(0);
             if (lane == 0) mbar_expect(barQ, kTile);
