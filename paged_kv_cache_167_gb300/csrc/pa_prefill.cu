@@ -373,13 +373,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
     const uint32_t barQ = base + kOffBar;
     // barriers: Q landed[2] | K[kKV] | V[kKV] | S[2] | P[2] | P.V done[2] | P.V done per S buffer[2] |
-    // K slot free[kKV] | V slot free[kKV] | Q free[2] | unit's P.V done | O read | suffix V ready |
+    // K slot free[kKV] | V slot free[kKV] | Q free[2] | unit's P.V done | O read | suffix V ready[2] |
     // drain (P.V, Q.K issuers)
     const uint32_t barK = barQ + 16, barV = barK + 8 * kKV, barS = barV + 8 * kKV, barP = barS + 16,
                    barOP = barP + 16, barSdone = barOP + 16, barKfree = barSdone + 16, barVfree = barKfree + 8 * kKV,
                    barQfree = barVfree + 8 * kKV, barUnit = barQfree + 16, barOfree = barUnit + 8,
-                   barVsfx = barOfree + 8, barEnd = barVsfx + 8, barEndQk = barEnd + 8;
-    constexpr int kNumBars = 2 + 2 * kKV + 2 + 2 + 2 + 2 + 2 * kKV + 2 + 1 + 1 + 1 + 2;
+                   barVsfx = barOfree + 8, barEnd = barVsfx + 16, barEndQk = barEnd + 8;
+    constexpr int kNumBars = 2 + 2 * kKV + 2 + 2 + 2 + 2 + 2 * kKV + 2 + 1 + 1 + 2 + 2;
     static_assert(8 * kNumBars + 8 <= kBarBytes, "barrier area");
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + 8 * kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffBar + 8 * kNumBars + 4);
@@ -730,10 +730,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
                     }
                 }
-                // the zeros (generic proxy) before the P.V that reads them (async proxy)
+                // the zeros (generic proxy) before the P.V that reads them (async proxy).
+                // Units alternate between two barriers: with one, a run of one-tile
+                // units let this warp release two units' tiles before the P.V lane
+                // waited for the first, and that wait then saw the phase after
+                // (released, unit k + 2's tile needs V slot reuse, which waits for
+                // unit k's P.V, so neither barrier is lapped).
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive_u32(barVsfx);
+                if (lane == 0) mbar_arrive_u32(barVsfx + 8 * (k & 1));
             }
             U = N;
             raw_cur = nraw_cur;
@@ -743,7 +748,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // wait (bounded) for this warp's copies still in flight before the memory is released
             for (int t = max(0, T - kKV); t < T; ++t)
                 mbar_wait(bar0 + 8 * (t % kKV), (uint32_t)((t / kKV) & 1), p.err);
-            if (grouped && !is_k && lane == 0) mbar_arrive_u32(barVsfx);   // a waiting P.V lane gives up sooner
+            if (grouped && !is_k && lane == 0) {   // a waiting P.V lane gives up sooner
+                mbar_arrive_u32(barVsfx);
+                mbar_arrive_u32(barVsfx + 8);
+            }
         }
         __syncwarp();
     } else if (warp == kMmaWarp || warp == kQkWarp) {
@@ -805,9 +813,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int st = T % kKV;
                         if (!wait(barP + 8 * (T & 1), (uint32_t)((T >> 1) & 1))) break;
                         // the suffix tile's V once the V warp has zeroed its unused
-                        // slots (one such tile per unit)
+                        // slots (one such tile per unit, units alternating barriers)
                         const bool vsfx = grouped && t == U.n_pre;
-                        if (!wait(vsfx ? barVsfx : barV + 8 * st, vsfx ? (uint32_t)(k & 1) : (uint32_t)((T / kKV) & 1)))
+                        if (!wait(vsfx ? barVsfx + 8 * (k & 1) : barV + 8 * st,
+                                  vsfx ? (uint32_t)((k >> 1) & 1) : (uint32_t)((T / kKV) & 1)))
                             break;
                         tc_fence_after();
 #pragma unroll

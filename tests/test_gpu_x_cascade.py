@@ -366,13 +366,16 @@ def test_grouped_full_size_beams_repeatable(pa):
 
 
 def test_grouped_persistent_grid_sweep(pa):
-    """Grouped decode (6 groups of 4 beams, 2 kv-heads: 12 units) with every
+    """Grouped decode (7 groups of 4 beams, 2 kv-heads: 14 units) with every
     grid size from one CTA (all units in one CTA, the pipeline handed from
     unit to unit, each unit's suffix tile zeroed and released in turn) to more
     CTAs than units: outputs bit for bit alike, the default grid's against
-    the oracle."""
+    the oracle.  The groups without a prefix make runs of one-tile units, in
+    which the V warp can release two units' suffix tiles before the P.V lane
+    waits for the first (with a single barrier for them, that wait saw the
+    later phase and the CTA stalled)."""
     rng = np.random.default_rng(41)
-    prefix = [0, 160, 400, 1024, 48, 704]
+    prefix = [0, 160, 0, 400, 1024, 48, 704]
     suffix = rng.integers(0, 33, size=len(prefix) * 4)
     w = wl.shared_groups(prefix, list(suffix), 4, 16, 2, 128, 16, seed=41)
     c = Case(w)
@@ -380,7 +383,7 @@ def test_grouped_persistent_grid_sweep(pa):
     base = grouped_call(pa, c, plan, 4)
     assert_close(base, oracle_full(c), "grouped sweep")
     try:
-        for ctas in (1, 2, 3, 5, 11, 12, 13):
+        for ctas in (1, 2, 3, 5, 13, 14, 15):
             pa.set_prefill_ctas(ctas)
             for flags in (0, pa.PA_DECODE_EARLY_METADATA):   # the tables read before or after the wait
                 out = grouped_call(pa, c, plan, 4, flags=flags)
