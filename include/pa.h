@@ -344,13 +344,15 @@ pa_status pa_prefill_chunk(void *out, const void *q, const pa_kv_pool *pool,
  *                 shared blocks
  *   prefix_lens   device, [num_groups] int32, each in [0, max_prefix_len]
  *   group_order   device, [num_groups] int32, a permutation of the groups, or
- *                 NULL: the order in which the groups' CTAs start (longest
- *                 prefix first balances the GPU's waves; pa_cascade_plan
- *                 writes that order).  It changes no result.  An entry outside
- *                 [0, num_groups) raises PA_DEVERR_ORDER and that CTA works on
- *                 its own index instead (some group is then done twice and
- *                 another not at all); a repeated entry is not detected and
- *                 leaves the rows of a missing group unwritten.
+ *                 NULL: the order in which the groups' units are dealt to the
+ *                 persistent CTAs (in rounds of alternating direction, so with
+ *                 the longest prefix first a CTA that draws a long unit draws
+ *                 a short one next; pa_cascade_plan writes that order).  It
+ *                 changes no result.  An entry outside [0, num_groups) raises
+ *                 PA_DEVERR_ORDER and that slot takes its own index instead
+ *                 (some group is then done twice and another not at all); a
+ *                 repeated entry is not detected and leaves the rows of a
+ *                 missing group unwritten.
  *   max_prefix_len host bound, <= max_prefix_blocks * block_size
  *   scale         as pa_prefill_chunk
  * Every query of group i attends all prefix_lens[i] keys (no causal mask: the
