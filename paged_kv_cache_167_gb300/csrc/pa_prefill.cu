@@ -18,13 +18,16 @@
 // log-sum-exp, which the decode of the private suffixes folds in.
 //
 // Design:
-//  * One CTA per 128-row M-tile of one (sequence, kv-head): row r is query
-//    j0 + r / G of head g*G + r % G, so every K/V tile staged in shared memory
-//    serves the whole query group.  Eleven warps: eight softmax warps in two
-//    warpgroups each own 64 of a row's 128 keys (tensor-memory lanes follow
-//    warp % 4); lane 0 of one warp issues the Q.K MMAs and lane 0 of another
-//    the P.V MMAs, so each runs ahead as far as its own inputs allow; a K warp
-//    and a V warp issue the tensor copies, one lane per box.
+//  * Work comes in units of one 128-row M-tile of one (sequence, kv-head): row
+//    r is query j0 + r / G of head g*G + r % G, so every K/V tile staged in
+//    shared memory serves the whole query group.  The grid is persistent (one
+//    CTA per SM); each CTA walks its units in rounds of alternating direction,
+//    its copy and tensor-core pipeline running on from one unit into the next.
+//  * Twelve warps: eight softmax warps in two warpgroups each own 64 of a
+//    row's 128 keys (tensor-memory lanes follow warp % 4); lane 0 of one warp
+//    issues the Q.K MMAs and lane 0 of another the P.V MMAs, so each runs
+//    ahead as far as its own inputs allow; a K warp and a V warp issue the
+//    tensor copies, one lane per box.
 //  * TMA (cp.async.bulk.tensor, 128-byte swizzle) brings Q and the K/V tiles.
 //    A K tile of 128 keys is 8 blocks x 2 halves of d, one box of 16 rows x
 //    64 dims per (block, half) through a 5-D tensor map of the pool's
@@ -36,22 +39,20 @@
 //    which TMA fills with zeros.  No multicast.
 //  * S = Q.K^T and O += P.V are tcgen05.mma kind::f16 (bf16 in, fp32 out)
 //    with M = N = 128, K = 16 per instruction, accumulators in tensor memory
-//    (three S buffers in columns 0..383, O in 384..511), tracked with
-//    tcgen05.commit on mbarriers.  Q.K runs up to three tiles ahead of P.V,
-//    so the tensor pipe works on later tiles while the softmax warps process
-//    this one.
-//  * Softmax: each thread owns half of one row.  It reads S with tcgen05.ld,
-//    applies the causal mask, agrees with the other half on the tile maximum
-//    through shared memory, keeps a reference maximum in the log2 domain that
-//    only moves when a tile's maximum exceeds it by more than 8 (so p <= 2^8
-//    and O needs rescaling rarely; the result is exact because l and O share
-//    the reference), writes P as bf16 back into the first half of the S
-//    columns it read (tcgen05.st, two bf16 per column), from where P.V takes
-//    its A operand, and sums the fp32 probabilities into l.  The S buffer is
-//    written again only by Q.K(t + 3), which the MMA lane issues after P.V(t).
-//  * K and V rings of three stages each (Q and six 32 KiB tiles fill 224 KiB
-//    of shared memory); a K slot is refilled once its Q.K MMA has completed,
-//    a V slot once its P.V MMA has.
+//    (two S buffers, and one O accumulator per key half: 512 columns),
+//    tracked with tcgen05.commit on mbarriers.  Q.K runs up to two tiles ahead
+//    of P.V.
+//  * Softmax: each thread owns half of one row's keys and its own accumulator.
+//    It reads S with tcgen05.ld, applies the mask, keeps its own reference
+//    maximum in the log2 domain that only moves when a tile's maximum exceeds
+//    it by more than 8 (so p <= 2^8 and O needs rescaling rarely), writes P as
+//    bf16 back into the first half of the S columns it read (tcgen05.st, two
+//    bf16 per column), from where P.V takes its A operand, and sums the fp32
+//    probabilities into its l.  The two halves meet once, in the epilogue:
+//    (O0 f0 + O1 f1) / (l0 f0 + l1 f1), f = 2^(m - max(m0, m1)).
+//  * Two Q buffers, two-stage K and V rings; a K slot is refilled once its Q.K
+//    has completed, a V slot once its P.V has.  A full M-tile of bf16 output is
+//    staged in its unit's Q buffer and leaves by tensor stores.
 //  * Every wait is bounded; on expiry the kernel records PA_DEVERR_TIMEOUT,
 //    waits (bounded) for its outstanding work and frees its tensor memory.
 #include <cuda.h>
